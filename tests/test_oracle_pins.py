@@ -1,0 +1,358 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix:
+hand-worked examples (tests/golden), closed forms, brute force on tiny inputs,
+invariants and special cases that reduce to a dense MLP.  Each pin is chosen so
+that a plausible mistake in the oracle (a dropped term, a wrong sign, swapped
+gate/up halves, a transposed operand, weights from the shifted scores, the
+route scale on the shared expert) fails at least one of them."""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- scores
+
+def test_softmax_closed_form():
+    s = O.score(np.log([[1.0, 2.0, 3.0, 4.0]]), O.SCORE_SOFTMAX)
+    np.testing.assert_allclose(s, [[0.1, 0.2, 0.3, 0.4]], rtol=0, atol=1e-15)
+    # shift invariance of softmax
+    s2 = O.score(np.log([[1.0, 2.0, 3.0, 4.0]]) + 123.0, O.SCORE_SOFTMAX)
+    np.testing.assert_allclose(s2, s, rtol=0, atol=1e-14)
+
+
+def test_sigmoid_closed_form():
+    s = O.score(np.array([[0.0, math.log(3.0), -math.log(3.0), -800.0, 800.0]]), O.SCORE_SIGMOID)
+    np.testing.assert_allclose(s, [[0.5, 0.75, 0.25, 0.0, 1.0]], rtol=0, atol=1e-15)
+
+
+def test_sqrtsoftplus_closed_form():
+    l = np.array([[0.0, math.log(3.0), 40.0, -40.0]])
+    s = O.score(l, O.SCORE_SQRTSOFTPLUS)
+    expect = [math.sqrt(math.log(2.0)), math.sqrt(math.log(4.0)),
+              math.sqrt(40.0 + math.log1p(math.exp(-40.0))), math.sqrt(math.log1p(math.exp(-40.0)))]
+    np.testing.assert_allclose(s[0], expect, rtol=1e-15, atol=0)
+    assert abs(s[0, 3] - math.exp(-20.0)) < 1e-24
+
+
+# ---------------------------------------------------------------- golden, hand worked
+
+def test_golden_softmax_top2_and_expert_bias():
+    g = _golden("router_softmax_top2_hand.json")
+    r = O.Recipe(num_experts=4, top_k=g["top_k"], score_fn=g["score_fn"], route_scale=g["route_scale"])
+    s, idx, w, _ = O.route_from_logits(np.array(g["logits"]), r)
+    np.testing.assert_allclose(s, g["expected_scores"], atol=1e-15)
+    assert idx.tolist() == g["expected_idx"]
+    np.testing.assert_allclose(w, g["expected_weights"], atol=1e-15)
+    s_b, idx_b, w_b, _ = O.route_from_logits(np.array(g["logits"]), r, np.array(g["expert_bias"]))
+    assert idx_b.tolist() == g["expected_idx_biased"]
+    np.testing.assert_allclose(w_b, g["expected_weights_biased"], atol=1e-15)
+    np.testing.assert_array_equal(s_b, s)  # the bias never touches the scores
+
+
+def test_golden_sigmoid_group_limited():
+    g = _golden("router_sigmoid_grouped_hand.json")
+    p = np.array([g["p"]])
+    logits = np.log(p / (1.0 - p))
+    r = O.Recipe(num_experts=8, top_k=g["top_k"], score_fn=g["score_fn"], n_group=g["n_group"],
+                 topk_group=g["topk_group"], route_scale=g["route_scale"])
+    s, idx, w, c = O.route_from_logits(logits, r)
+    np.testing.assert_allclose(O.group_scores(c, 4, 2), g["expected_group_scores"], atol=1e-14)
+    assert idx.tolist() == g["expected_idx"]
+    np.testing.assert_allclose(w, g["expected_weights"], atol=1e-14)
+    plain = O.Recipe(num_experts=8, top_k=2, score_fn=O.SCORE_SIGMOID, route_scale=2.5)
+    assert O.route_from_logits(logits, plain)[1].tolist() == g["expected_idx_plain"]
+
+
+def test_golden_swiglu_clamp():
+    g = _golden("swiglu_clamp_hand.json")
+    x = np.array(g["x"])
+    wgu = np.array(g["w_gate_up"])
+    wd = np.array(g["w_down"])
+    y_c = O.expert_forward(x, wgu, wd, g["limit"])
+    y_u = O.expert_forward(x, wgu, wd, 0.0)
+    assert abs(y_c[0, 0] - g["expected_y_clamped"]) < 1e-12
+    assert abs(y_u[0, 0] - g["expected_y_unclamped"]) < 1e-12
+
+
+# ---------------------------------------------------------------- selection: brute force
+
+def _ref_topk(c_row, k):
+    return sorted(range(len(c_row)), key=lambda e: (-c_row[e], e))[:k]
+
+
+def test_topk_equals_full_sort_with_ties():
+    rng = np.random.default_rng(7)
+    for e in (1, 2, 3, 5, 8, 13, 16):
+        for _ in range(40):
+            # values from a small set force exact ties
+            c = rng.integers(0, 4, size=(6, e)).astype(np.float64) * 0.25
+            for k in range(1, e + 1):
+                got = O.select_topk(c, k)
+                for t in range(c.shape[0]):
+                    assert got[t].tolist() == _ref_topk(c[t].tolist(), k)
+
+
+def _ref_group_limited(c_row, k, n_group, topk_group, topn):
+    e = len(c_row)
+    gsz = e // n_group
+    gscore = [sum(sorted(c_row[g * gsz:(g + 1) * gsz], reverse=True)[:topn]) for g in range(n_group)]
+    # brute force over every set of topk_group groups: the kept set is the one
+    # whose sorted (-score, index) keys are lexicographically smallest
+    best = None
+    for combo in itertools.combinations(range(n_group), topk_group):
+        key = sorted((-gscore[g], g) for g in combo)
+        if best is None or key < best[0]:
+            best = (key, combo)
+    keep = set(best[1])
+    eligible = [j for j in range(e) if j // gsz in keep]
+    return sorted(eligible, key=lambda j: (-c_row[j], j))[:k]
+
+
+def test_group_limited_brute_force():
+    rng = np.random.default_rng(11)
+    for (e, n_group) in ((8, 4), (8, 2), (12, 3), (16, 4), (16, 8)):
+        for topk_group in range(1, n_group + 1):
+            gsz = e // n_group
+            for k in range(1, topk_group * gsz + 1):
+                c = rng.integers(0, 5, size=(5, e)).astype(np.float64) * 0.125
+                got = O.select_group_limited(c, k, n_group, topk_group, 2 if gsz >= 2 else 1)
+                for t in range(c.shape[0]):
+                    ref = _ref_group_limited(c[t].tolist(), k, n_group, topk_group, 2 if gsz >= 2 else 1)
+                    assert got[t].tolist() == ref, (e, n_group, topk_group, k, c[t])
+
+
+def test_group_limited_all_groups_is_plain_topk():
+    rng = np.random.default_rng(3)
+    for seed in range(20):
+        c = rng.normal(size=(9, 32))
+        for k in (1, 4, 8):
+            np.testing.assert_array_equal(O.select_group_limited(c, k, 8, 8, 2), O.select_topk(c, k))
+
+
+def test_selection_order_descending():
+    rng = np.random.default_rng(5)
+    c = rng.normal(size=(50, 64))
+    idx = O.select_topk(c, 10)
+    picked = np.take_along_axis(c, idx, 1)
+    assert np.all(np.diff(picked, axis=1) <= 0)
+
+
+# ---------------------------------------------------------------- routing weights
+
+@pytest.mark.parametrize("fn", [O.SCORE_SOFTMAX, O.SCORE_SIGMOID, O.SCORE_SQRTSOFTPLUS])
+def test_renormalised_weights_sum_to_route_scale(fn):
+    rng = np.random.default_rng(fn)
+    logits = rng.normal(size=(40, 64)) * 2
+    r = O.Recipe(num_experts=64, top_k=6, score_fn=fn, route_scale=1.5)
+    _, _, w, _ = O.route_from_logits(logits, r)
+    np.testing.assert_allclose(w.sum(axis=1), 1.5, rtol=1e-12)
+
+
+def test_weights_without_renorm_are_scaled_scores():
+    rng = np.random.default_rng(9)
+    logits = rng.normal(size=(10, 16))
+    r = O.Recipe(num_experts=16, top_k=3, score_fn=O.SCORE_SIGMOID, norm_topk_prob=False, route_scale=2.0)
+    s, idx, w, _ = O.route_from_logits(logits, r)
+    np.testing.assert_array_equal(w, np.take_along_axis(s, idx, 1) * 2.0)
+
+
+def test_epsilon_is_bitwise_noop_for_softmax():
+    """Sum of the K largest of E softmax probabilities >= K/E >= 1/512, whose
+    half-ulp exceeds 1e-20 in fp64 and in fp32."""
+    rng = np.random.default_rng(1)
+    for e, k in ((8, 1), (8, 2), (512, 10), (256, 8)):
+        logits = rng.normal(size=(64, e)) * 3
+        a = O.route_from_logits(logits, O.Recipe(e, k, norm_eps=1e-20))[2]
+        b = O.route_from_logits(logits, O.Recipe(e, k, norm_eps=0.0))[2]
+        np.testing.assert_array_equal(a, b)
+        # the same in fp32 arithmetic
+        s = O.score(logits, O.SCORE_SOFTMAX).astype(np.float32)
+        idx = O.select_topk(s.astype(np.float64), k)
+        g = np.take_along_axis(s, idx, 1)
+        tot = g.sum(axis=1, keepdims=True, dtype=np.float32)
+        np.testing.assert_array_equal(g / (tot + np.float32(1e-20)), g / tot)
+
+
+def test_epsilon_guards_sigmoid_underflow():
+    logits = np.full((1, 4), -800.0)  # every sigmoid underflows to 0
+    w = O.route_from_logits(logits, O.Recipe(4, 2, score_fn=O.SCORE_SIGMOID))[2]
+    assert np.all(np.isfinite(w)) and np.all(w == 0.0)
+
+
+def test_top1_renorm_weight_is_route_scale():
+    rng = np.random.default_rng(2)
+    logits = rng.normal(size=(72, 8)) * 2
+    for scale in (1.0, 2.5):
+        w = O.route_from_logits(logits, O.Recipe(8, 1, route_scale=scale))[2]
+        np.testing.assert_array_equal(w, np.full((72, 1), scale))
+
+
+def test_route_scale_scales_weights_exactly():
+    rng = np.random.default_rng(4)
+    logits = rng.normal(size=(30, 32))
+    w1 = O.route_from_logits(logits, O.Recipe(32, 4, score_fn=O.SCORE_SIGMOID))[2]
+    w25 = O.route_from_logits(logits, O.Recipe(32, 4, score_fn=O.SCORE_SIGMOID, route_scale=2.5))[2]
+    np.testing.assert_array_equal(w25, w1 * 2.5)
+
+
+def test_expert_bias_moves_indices_not_weights():
+    rng = np.random.default_rng(6)
+    logits = rng.normal(size=(20, 16))
+    r = O.Recipe(16, 4, score_fn=O.SCORE_SIGMOID, route_scale=1.0)
+    s, idx0, w0, _ = O.route_from_logits(logits, r)
+    bias = np.zeros(16)
+    bias[15] = 10.0  # promotes expert 15 everywhere
+    s1, idx1, w1, _ = O.route_from_logits(logits, r, bias)
+    assert np.all(idx1[:, 0] == 15)
+    assert not np.array_equal(idx0, idx1)
+    gathered = np.take_along_axis(s, idx1, 1)
+    np.testing.assert_allclose(w1, gathered / gathered.sum(1, keepdims=True), rtol=1e-15)
+
+
+def test_router_bias_moves_weights():
+    rng = np.random.default_rng(8)
+    x = rng.normal(size=(5, 12))
+    gate = rng.normal(size=(6, 12)) * 0.1
+    rb = rng.normal(size=6)
+    l0 = O.router_logits(x, gate)
+    l1 = O.router_logits(x, gate, rb)
+    for t in range(5):
+        for e in range(6):
+            ref = sum(x[t, h] * gate[e, h] for h in range(12)) + rb[e]
+            assert abs(l1[t, e] - ref) < 1e-12
+    w0 = O.route_from_logits(l0, O.Recipe(6, 2))[2]
+    w1 = O.route_from_logits(l1, O.Recipe(6, 2))[2]
+    assert not np.allclose(w0, w1)
+
+
+def test_selection_margin_constructed():
+    c = np.array([[0.9, 0.5, 0.49, 0.1]])
+    idx = O.select_topk(c, 2)
+    m = O.selection_margin(c, idx, O.Recipe(4, 2))
+    assert abs(m[0] - 0.01) < 1e-12
+
+
+# ---------------------------------------------------------------- experts and combine
+
+def _dense_swiglu_loops(x, wgu, wd, limit=0.0):
+    """Textbook SwiGLU MLP in pure Python loops: gate rows [0, I), up rows
+    [I, 2I), down [H, I]."""
+    T, H = len(x), len(x[0])
+    I = len(wgu) // 2
+    out = []
+    for t in range(T):
+        h = []
+        for i in range(I):
+            g = sum(wgu[i][j] * x[t][j] for j in range(H))
+            u = sum(wgu[I + i][j] * x[t][j] for j in range(H))
+            if limit > 0:
+                g = min(g, limit)
+                u = max(-limit, min(u, limit))
+            h.append(g / (1.0 + math.exp(-g)) * u)
+        out.append([sum(wd[r][i] * h[i] for i in range(I)) for r in range(H)])
+    return out
+
+
+@pytest.mark.parametrize("limit", [0.0, 0.05])
+def test_single_expert_top1_is_dense_mlp(limit):
+    rng = np.random.default_rng(12)
+    T, H, I = 3, 8, 4
+    x = rng.normal(size=(T, H))
+    gate = rng.normal(size=(1, H))
+    wgu = rng.normal(size=(1, 2 * I, H)) * 0.3
+    wd = rng.normal(size=(1, H, I)) * 0.3
+    for scale in (1.0, 2.5):
+        r = O.Recipe(1, 1, route_scale=scale, swiglu_limit=limit)
+        out = O.moe_layer(x, gate, wgu, wd, r)
+        np.testing.assert_array_equal(out["weights"], np.full((T, 1), scale))
+        ref = np.array(_dense_swiglu_loops(x.tolist(), wgu[0].tolist(), wd[0].tolist(), limit)) * scale
+        np.testing.assert_allclose(out["y"], ref, rtol=1e-12, atol=1e-14)
+
+
+def test_gate_up_halves_not_interchangeable():
+    """Swapping the gate and up halves changes the output (silu is not odd),
+    so the dense-MLP pin above fixes the order."""
+    rng = np.random.default_rng(13)
+    x = rng.normal(size=(2, 6))
+    wgu = rng.normal(size=(8, 6))
+    wd = rng.normal(size=(6, 4))
+    a = O.expert_forward(x, wgu, wd, 0.0)
+    b = O.expert_forward(x, np.concatenate([wgu[4:], wgu[:4]]), wd, 0.0)
+    assert not np.allclose(a, b)
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_shared_expert_gate_and_no_route_scale(gated):
+    rng = np.random.default_rng(14)
+    T, H, I, Is = 4, 6, 3, 5
+    x = rng.normal(size=(T, H))
+    gate = rng.normal(size=(1, H))
+    wgu = rng.normal(size=(1, 2 * I, H)) * 0.4
+    wd = rng.normal(size=(1, H, I)) * 0.4
+    sgu = rng.normal(size=(2 * Is, H)) * 0.4
+    sd = rng.normal(size=(H, Is)) * 0.4
+    sg = rng.normal(size=H) if gated else None
+    r = O.Recipe(1, 1, route_scale=2.5)
+    y = O.moe_layer(x, gate, wgu, wd, r, sh_gate_up=sgu, sh_down=sd, sh_gate=sg)["y"]
+    routed = np.array(_dense_swiglu_loops(x.tolist(), wgu[0].tolist(), wd[0].tolist()))
+    shared = np.array(_dense_swiglu_loops(x.tolist(), sgu.tolist(), sd.tolist()))
+    if gated:
+        gz = np.array([1.0 / (1.0 + math.exp(-sum(x[t, h] * sg[h] for h in range(H)))) for t in range(T)])
+    else:
+        gz = np.ones(T)
+    np.testing.assert_allclose(y, 2.5 * routed + gz[:, None] * shared, rtol=1e-12, atol=1e-13)
+
+
+def test_topk_combine_against_loops():
+    """K = 2 of E = 4: y_t = sum_k w_tk * Expert_{i_tk}(x_t), each expert by loops."""
+    rng = np.random.default_rng(15)
+    T, H, I, E = 5, 6, 3, 4
+    x = rng.normal(size=(T, H))
+    gate = rng.normal(size=(E, H))
+    wgu = rng.normal(size=(E, 2 * I, H)) * 0.5
+    wd = rng.normal(size=(E, H, I)) * 0.5
+    out = O.moe_layer(x, gate, wgu, wd, O.Recipe(E, 2))
+    for t in range(T):
+        ref = np.zeros(H)
+        for k in range(2):
+            e = out["idx"][t, k]
+            ref += out["weights"][t, k] * np.array(
+                _dense_swiglu_loops([x[t].tolist()], wgu[e].tolist(), wd[e].tolist())[0])
+        np.testing.assert_allclose(out["y"][t], ref, rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- permutation
+
+def test_permute_invariants():
+    rng = np.random.default_rng(16)
+    for (T, K, E) in ((16, 2, 8), (72, 10, 512), (9, 6, 256), (1, 1, 1), (33, 3, 5)):
+        idx = np.stack([rng.choice(E, size=K, replace=False) for _ in range(T)])
+        counts, offsets, sp, pp = O.permute(idx, E)
+        assert counts.sum() == T * K
+        np.testing.assert_array_equal(np.sort(sp), np.arange(T * K))
+        np.testing.assert_array_equal(pp[sp], np.arange(T * K))
+        flat = idx.reshape(-1)
+        for e in range(E):
+            seg = sp[offsets[e]:offsets[e + 1]]
+            assert np.all(flat[seg] == e)
+            assert np.all(np.diff(seg) > 0)
+            assert len(seg) == (flat == e).sum()
+
+
+def test_empty_input_routes_empty():
+    out = O.moe_layer(np.zeros((0, 8)), np.ones((4, 8)), np.ones((4, 6, 8)), np.ones((4, 8, 3)),
+                      O.Recipe(4, 2))
+    assert out["idx"].shape == (0, 2) and out["y"].shape == (0, 8)
+    assert out["counts"].tolist() == [0, 0, 0, 0]
