@@ -1,0 +1,190 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) MoE-FFN layer forward used by
+ * DFlash / DSpark block-diffusion draft models.
+ *
+ * The layer (sources are web pages, cited by title and section):
+ *   1. Router, the score -> select -> routing_weights template of SpecForge
+ *      PR #1033 "MoE FFN for DFlash-family drafts: the module", section
+ *      "Router": fp32 logits of a linear gate (sglang PR #48763 "[Feat]
+ *      dflash: Serve MoE FFN drafts for DFlash and DSpark", commit note
+ *      "Router logits go to TopK in fp32"), optionally with a folded router
+ *      bias added to the logits (SpecForge PR #941 "SGLang draft classes for
+ *      the Qwen3.8-27B DSpark MoE drafter", section "What"); softmax, sigmoid
+ *      or sqrt(softplus) scores; a selection-only expert bias (SpecForge PR
+ *      #1073 "MoE drafts: DeepSeek-V4.1's own DSpark draft", expert-bias
+ *      commit note); plain or group-limited top-k; weights gathered from the
+ *      unshifted scores, renormalised with +1e-20 and times route_scale.
+ *   2. Token-to-expert grouped SwiGLU experts (fused gate_up_proj [E,2I,H],
+ *      down_proj [E,H,I]; PR #1073 commit note on the fused expert layout),
+ *      with DeepSeek's optional clamp (PR #941 follow-up comment).
+ *   3. An optional shared expert, sigmoid-gated (Qwen, PR #941 "What") or
+ *      ungated (DeepSeek), added to the weighted combine of the routed
+ *      experts (PR #48763 commit note on DraftMoE forward).
+ *
+ * Conventions (every entry point):
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; tensors are
+ *     contiguous, row-major.  bf16 tensors are passed as raw 16-bit words.
+ *     Indices are int32 (PR #48763: "int32 ids, as the fused routers emit").
+ *   - Calls are asynchronous on `stream` and never synchronise the host, so a
+ *     sequence of them can be captured in a CUDA graph.  The library performs
+ *     no device allocation; scratch space is the caller's workspace.
+ *   - Argument errors are returned synchronously, before any launch.  Errors
+ *     found on the device (a bounded wait that ran out) are recorded in the
+ *     workspace's status word and read with moe_get_device_status().
+ *   - T == 0 returns MOE_OK and launches nothing (PR #48763: a rank with no
+ *     tokens routes an empty top-k output).
+ *   - x is only read; y must not alias x (PR #48763 fix: the shared expert
+ *     must read x before in-place experts overwrite it).
+ *   - Requested features are never silently dropped (PR #48763: dropped expert
+ *     bias, unapplied routed_scaling_factor): what the kernels cannot do is
+ *     refused with MOE_ERR_UNSUPPORTED.
+ *   - Limits: 1 <= E <= 1024, 1 <= K <= min(E, 32), H and I multiples of 8,
+ *     8 <= H <= 65536, 8 <= I <= 16384, T <= 65536, n_group <= 32 and
+ *     divides E, K <= topk_group * (E / n_group).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16; /* raw bfloat16 bits */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,    /* null required pointer, negative size, ...  */
+  MOE_ERR_UNSUPPORTED = 2,    /* well-formed but outside the kernels' limits */
+  MOE_ERR_WORKSPACE = 3,      /* workspace missing, too small or misaligned  */
+  MOE_ERR_CUDA = 4,           /* a CUDA runtime call failed                  */
+  MOE_ERR_DEVICE_TIMEOUT = 5  /* a bounded device-side wait ran out          */
+} moe_status;
+
+typedef enum {
+  MOE_SCORE_SOFTMAX = 0,
+  MOE_SCORE_SIGMOID = 1,
+  MOE_SCORE_SQRTSOFTPLUS = 2
+} moe_score_fn;
+
+/* The routing recipe (PR #1033 "Router" table; the HF keys num_experts,
+ * num_experts_per_tok, scoring_func, n_group / topk_group, norm_topk_prob,
+ * routed_scaling_factor, swiglu_limit map onto these fields). */
+typedef struct {
+  int32_t num_experts;    /* E                                                  */
+  int32_t top_k;          /* K                                                  */
+  int32_t score_fn;       /* moe_score_fn                                       */
+  int32_t n_group;        /* 1 = plain top-k; > 1 = group-limited select        */
+  int32_t topk_group;     /* groups kept by group-limited select                */
+  int32_t group_topn;     /* a group's score = sum of its group_topn best (2)   */
+  int32_t norm_topk_prob; /* 1: renormalise the K gathered scores               */
+  float norm_eps;         /* added to the renormalisation sum (1e-20)           */
+  float route_scale;      /* route_scale == routed_scaling_factor (routed only) */
+  float swiglu_limit;     /* > 0: clamped SwiGLU (routed and shared experts)    */
+} moe_recipe;
+
+/* Human-readable name of a status code (static storage). */
+MOE_API const char* moe_status_string(moe_status s);
+
+/* Bytes of workspace moe_route() needs for T tokens and E experts (token-block
+ * completion counters and, when logits_out is NULL, the [T,E] fp32 logits). */
+MOE_API size_t moe_route_workspace_bytes(int T, int E);
+
+/* Router: logits = x . gate^T (+ router_bias), fp32 accumulation of the exact
+ * bf16 products; scores; select over scores + expert_bias; weights.
+ *   x           [T,H] bf16            gate        [E,H] bf16
+ *   router_bias [E] fp32 or NULL      added to the logits (moves weights too)
+ *   expert_bias [E] fp32 or NULL      added to the scores for selection only
+ *   logits_out  [T,E] fp32 or NULL    the fp32 logits
+ *   topk_idx    [T,K] int32           descending shifted score, ties -> lower e
+ *   topk_w      [T,K] fp32            routing weights
+ *   ws          workspace of >= moe_route_workspace_bytes(T, E) bytes,
+ *               256-byte aligned, zero-filled before its first use (the
+ *               library leaves its counters at zero after every call).
+ */
+MOE_API moe_status moe_route(const moe_bf16* x, int T, int H, const moe_bf16* gate,
+                     const float* router_bias, const float* expert_bias,
+                     const moe_recipe* recipe, float* logits_out,
+                     int32_t* topk_idx, float* topk_w,
+                     void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Router steps score -> select -> routing_weights on given fp32 logits [T,E]
+ * (the same logits fed to another implementation give the same selection).
+ * Needs no workspace. */
+MOE_API moe_status moe_route_from_logits(const float* logits, int T,
+                                 const float* expert_bias,
+                                 const moe_recipe* recipe,
+                                 int32_t* topk_idx, float* topk_w,
+                                 cudaStream_t stream);
+
+/* Token-to-expert grouping (SpecForge grouped_mm experts, PR #1033; the
+ * tokens_per_expert counts of PR #1073):
+ *   counts[e]   = #{(t,k) : topk_idx[t,k] == e}                 [E]   int32
+ *   offsets     = exclusive prefix sum of counts                [E+1] int32
+ *   sorted_pair = pairs p = t*K + k, stably sorted by expert   [T*K] int32
+ *   pair_pos    = inverse permutation of sorted_pair            [T*K] int32
+ * Needs no workspace (ws may be NULL). */
+MOE_API moe_status moe_permute(const int32_t* topk_idx, int T, int K, int E,
+                       int32_t* counts, int32_t* offsets,
+                       int32_t* sorted_pair, int32_t* pair_pos,
+                       void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Workspace bytes for moe_ffn_forward() on the CURRENT device (the size
+ * depends on its SM count).  Is = 0 means no shared expert.  Returns 0 for an
+ * invalid recipe. */
+MOE_API size_t moe_ffn_workspace_bytes(int T, int H, int I, int Is, const moe_recipe* recipe);
+
+/* Zero-fill a workspace (required once before its first use). */
+MOE_API moe_status moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* The whole layer: y = sum_k w_tk * Expert_{idx_tk}(x_t) + g_t * Shared(x_t).
+ *   x          [T,H] bf16
+ *   gate       [E,H] bf16; router_bias, expert_bias as in moe_route()
+ *   w_gate_up  [E,2I,H] bf16: rows [0,I) gate (w1), rows [I,2I) up (w3)
+ *   w_down     [E,H,I] bf16
+ *   sh_gate_up [2Is,H] bf16 or NULL (no shared expert; then Is must be 0)
+ *   sh_down    [H,Is] bf16
+ *   sh_gate    [H] bf16 or NULL: g_t = sigmoid(x_t . sh_gate), else g_t = 1
+ *   ws         >= moe_ffn_workspace_bytes(T,H,I,Is,recipe) bytes, 256-byte
+ *              aligned, zero-filled before its first use; one workspace must
+ *              not be used by two calls that may overlap on the GPU.
+ *   y          [T,H] bf16 output (round to nearest even from fp32)
+ *   topk_idx_out [T,K] int32, topk_w_out [T,K] fp32, counts_out [E] int32:
+ *              optional copies of the routing (each may be NULL).
+ */
+MOE_API moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I,
+                           const moe_bf16* gate, const float* router_bias,
+                           const float* expert_bias,
+                           const moe_bf16* w_gate_up, const moe_bf16* w_down,
+                           const moe_bf16* sh_gate_up, const moe_bf16* sh_down,
+                           int Is, const moe_bf16* sh_gate,
+                           const moe_recipe* recipe, void* ws, size_t ws_bytes,
+                           moe_bf16* y, int32_t* topk_idx_out, float* topk_w_out,
+                           int32_t* counts_out, cudaStream_t stream);
+
+/* Synchronises `stream`, reads the device status word of a workspace used by
+ * moe_route() or moe_ffn_forward(), and clears it.  Returns MOE_OK or the
+ * first device-side error recorded (MOE_ERR_DEVICE_TIMEOUT); *info_out (if
+ * not NULL) receives the kernel-specific detail word. */
+MOE_API moe_status moe_get_device_status(void* ws, cudaStream_t stream, int32_t* info_out);
+
+/* Profiling hook: when `events` is not NULL, moe_ffn_forward() records
+ * events[2*i] / events[2*i+1] (cudaEvent_t) around its i-th kernel launch,
+ * for i < n_pairs, on its stream.  Per calling thread; NULL turns it off.
+ * The launch order is: router, gate_up GEMM, down GEMM, combine (the last is
+ * skipped when K == 1 and there is no shared expert). */
+MOE_API void moe_set_profile_events(void* const* events, int n_pairs);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

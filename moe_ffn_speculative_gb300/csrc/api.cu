@@ -1,0 +1,401 @@
+// C ABI of libmoe_gb300.so: argument validation, workspace layout, TMA
+// descriptors and the launch sequence of the MoE-FFN layer forward.  The
+// contract of every entry point is documented in include/moe.h.
+#include <string.h>
+
+#include <mutex>
+
+#include "moe.h"
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kAlign = 256;
+constexpr int kSmemLimit = 232448;  // 227 KB of dynamic shared memory per CTA
+constexpr int kCtrlBytes = 256 + 256 * 8;
+
+int g_sms[kMaxDevices];
+
+thread_local void* const* t_events = nullptr;
+thread_local int t_nev = 0;
+
+int device_sms() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return 0;
+  if (g_sms[d] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return 0;
+    g_sms[d] = n;
+  }
+  return g_sms[d];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor [d2][d1][d0] (d0 contiguous), loaded in boxes of 64 x 128 x 1
+// with the 128-byte swizzle; out-of-range elements read as zero.
+bool encode_weights_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kBlockK), static_cast<cuuint32_t>(kHalfRows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_recipe(const moe_recipe* r) {
+  if (!r) return MOE_ERR_INVALID_ARG;
+  const int E = r->num_experts, K = r->top_k;
+  if (E < 1 || K < 1) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || K > 32 || K > E) return MOE_ERR_UNSUPPORTED;
+  if (r->score_fn < 0 || r->score_fn > 2) return MOE_ERR_INVALID_ARG;
+  if (r->n_group < 1) return MOE_ERR_INVALID_ARG;
+  if (r->n_group > 1) {
+    if (r->n_group > 32 || E % r->n_group != 0) return MOE_ERR_UNSUPPORTED;
+    const int gsz = E / r->n_group;
+    if (r->topk_group < 1 || r->topk_group > r->n_group) return MOE_ERR_INVALID_ARG;
+    if (r->group_topn < 1 || r->group_topn > gsz) return MOE_ERR_INVALID_ARG;
+    if (K > r->topk_group * gsz) return MOE_ERR_UNSUPPORTED;
+  }
+  if (!(r->norm_eps >= 0.f) || !(r->route_scale == r->route_scale) || !(r->swiglu_limit == r->swiglu_limit))
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+struct RouterGeom {
+  int tb, quads, hsplit, n_eb, n_tb;
+};
+
+RouterGeom router_geometry(int T, int E_tot, int sms) {
+  RouterGeom g;
+  const int qn = ceil_div(E_tot, 4);
+  g.quads = 1;
+  while (g.quads < qn && g.quads < 8) g.quads <<= 1;
+  g.hsplit = 8 / g.quads;
+  g.n_eb = ceil_div(qn, g.quads);
+  g.tb = 8;
+  if (static_cast<long long>(ceil_div(T, 8)) * g.n_eb < sms) g.tb = 4;
+  g.n_tb = ceil_div(T, g.tb);
+  return g;
+}
+
+struct Layout {
+  RouterGeom rg;
+  int n_max, stages, nbuf, grid, I_ld;
+  uint32_t tmem_cols;
+  size_t smem;
+  int max_gu_tiles, max_dn_tiles, g_max;
+  bool need_out;
+  size_t o_status, o_cnt, o_tiles, o_logits, o_shl, o_shw, o_idx, o_w, o_counts, o_offsets, o_sp, o_pp, o_groups,
+      o_header, o_partials, o_h, o_out, total;
+};
+
+Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sms) {
+  Layout L;
+  L.rg = router_geometry(T, E + (gated ? 1 : 0), sms);
+  int nm = ((T + 15) / 16) * 16;
+  L.n_max = nm < 16 ? 16 : (nm > 256 ? 256 : nm);
+  L.nbuf = (4 * L.n_max <= 512) ? 2 : 1;
+  uint32_t cols = 32;
+  while (cols < static_cast<uint32_t>(L.nbuf * 2 * L.n_max)) cols <<= 1;
+  L.tmem_cols = cols;
+  const int stage_bytes = 2 * kTileBytesA + L.n_max * 128;
+  L.stages = (kSmemLimit - 1024 - kCtrlBytes) / stage_bytes;
+  if (L.stages > kMaxStages) L.stages = kMaxStages;
+  L.smem = 1024 + static_cast<size_t>(L.stages) * stage_bytes + kCtrlBytes;
+  L.grid = sms;
+  const int Imax = Is > I ? Is : I;
+  L.I_ld = ((Imax + 7) / 8) * 8;
+  const long long TK = static_cast<long long>(T) * K;
+  const long long u_max = TK < E ? TK : E;
+  const long long nb_sum = u_max + TK / L.n_max;
+  long long gu = ceil_div(I, kHalfRows) * nb_sum, dn = ceil_div(H, 2 * kHalfRows) * nb_sum;
+  if (Is > 0) {
+    gu += static_cast<long long>(ceil_div(Is, kHalfRows)) * ceil_div(T, L.n_max);
+    dn += static_cast<long long>(ceil_div(H, 2 * kHalfRows)) * ceil_div(T, L.n_max);
+  }
+  L.max_gu_tiles = static_cast<int>(gu);
+  L.max_dn_tiles = static_cast<int>(dn);
+  L.g_max = static_cast<int>(u_max) + (Is > 0 ? 1 : 0);
+  L.need_out = (K > 1 || Is > 0);
+  const size_t rows = static_cast<size_t>(TK) + T;
+  size_t o = 0;
+  L.o_status = o; o += kAlign;
+  L.o_cnt = o; o = align_up(o + 4 * (L.rg.n_tb + 1));
+  L.o_tiles = o; o = align_up(o + 4 * static_cast<size_t>(L.max_gu_tiles + L.max_dn_tiles));
+  L.o_logits = o; o = align_up(o + 4 * static_cast<size_t>(T) * E);
+  L.o_shl = o; o = align_up(o + 4 * static_cast<size_t>(T));
+  L.o_shw = o; o = align_up(o + 4 * static_cast<size_t>(T));
+  L.o_idx = o; o = align_up(o + 4 * static_cast<size_t>(TK));
+  L.o_w = o; o = align_up(o + 4 * static_cast<size_t>(TK));
+  L.o_counts = o; o = align_up(o + 4 * static_cast<size_t>(E));
+  L.o_offsets = o; o = align_up(o + 4 * static_cast<size_t>(E + 1));
+  L.o_sp = o; o = align_up(o + 4 * static_cast<size_t>(TK));
+  L.o_pp = o; o = align_up(o + 4 * static_cast<size_t>(TK));
+  L.o_groups = o; o = align_up(o + sizeof(GroupEntry) * static_cast<size_t>(L.g_max + 1));
+  L.o_header = o; o = align_up(o + sizeof(GemmHeader));
+  L.o_partials = o; o = align_up(o + 4 * static_cast<size_t>(L.grid) * 2 * 2 * L.n_max * 128);
+  L.o_h = o; o = align_up(o + 2 * rows * L.I_ld);
+  L.o_out = o;
+  if (L.need_out) o = align_up(o + 4 * rows * H);
+  L.total = o;
+  return L;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+void record_event_on(int i, cudaStream_t s) {
+  if (t_events && i < 2 * t_nev && t_events[i]) cudaEventRecord(static_cast<cudaEvent_t>(t_events[i]), s);
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+size_t moe_route_workspace_bytes(int T, int E) {
+  if (T < 0 || E < 1) return 0;
+  const int n_tb = ceil_div(T, 4);  // the smallest token block the router uses
+  return kAlign + align_up(4 * static_cast<size_t>(n_tb + 1)) + align_up(4 * static_cast<size_t>(T) * E);
+}
+
+moe_status moe_route(const moe_bf16* x, int T, int H, const moe_bf16* gate, const float* router_bias,
+                     const float* expert_bias, const moe_recipe* recipe, float* logits_out, int32_t* topk_idx,
+                     float* topk_w, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  moe_status st = check_recipe(recipe);
+  if (st != MOE_OK) return st;
+  if (T < 0 || H < 8 || H % 8 != 0) return H % 8 != 0 && H >= 8 ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
+  if (H > 65536 || T > 65536) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x || !gate || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(gate)) return MOE_ERR_INVALID_ARG;
+  const int E = recipe->num_experts;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0 || ws_bytes < moe_route_workspace_bytes(T, E))
+    return MOE_ERR_WORKSPACE;
+  const int sms = device_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const RouterGeom rg = router_geometry(T, E, sms);
+  char* w = static_cast<char*>(ws);
+  const size_t o_cnt = kAlign;
+  const size_t o_logits = o_cnt + align_up(4 * static_cast<size_t>(ceil_div(T, 4) + 1));
+  RouteParams p;
+  memset(&p, 0, sizeof(p));
+  p.x = x; p.gate = gate; p.router_bias = router_bias; p.expert_bias = expert_bias; p.sh_gate = nullptr;
+  p.T = T; p.H = H; p.E = E; p.K = recipe->top_k;
+  p.score_fn = recipe->score_fn; p.n_group = recipe->n_group; p.topk_group = recipe->topk_group;
+  p.group_topn = recipe->group_topn; p.renorm = recipe->norm_topk_prob; p.eps = recipe->norm_eps;
+  p.scale = recipe->route_scale;
+  p.quads = rg.quads; p.hsplit = rg.hsplit; p.n_eb = rg.n_eb; p.n_tb = rg.n_tb;
+  p.logits = logits_out ? logits_out : reinterpret_cast<float*>(w + o_logits);
+  p.idx = topk_idx; p.w = topk_w;
+  p.tb_counter = reinterpret_cast<int32_t*>(w + o_cnt);
+  p.glob_counter = p.tb_counter + ceil_div(T, 4);
+  p.do_permute = 0;
+  return cuda_status(launch_route(p, rg.tb, stream));
+}
+
+moe_status moe_route_from_logits(const float* logits, int T, const float* expert_bias, const moe_recipe* recipe,
+                                 int32_t* topk_idx, float* topk_w, cudaStream_t stream) {
+  moe_status st = check_recipe(recipe);
+  if (st != MOE_OK) return st;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T > 65536) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_select_from_logits(logits, T, recipe->num_experts, recipe->top_k, expert_bias,
+                                               recipe->score_fn, recipe->n_group, recipe->topk_group,
+                                               recipe->group_topn, recipe->norm_topk_prob, recipe->norm_eps,
+                                               recipe->route_scale, topk_idx, topk_w, stream));
+}
+
+moe_status moe_permute(const int32_t* topk_idx, int T, int K, int E, int32_t* counts, int32_t* offsets,
+                       int32_t* sorted_pair, int32_t* pair_pos, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (T < 0 || K < 1 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || K > E || T > 65536) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_idx || !sorted_pair || !pair_pos)) return MOE_ERR_INVALID_ARG;
+  // T == 0 still defines counts and offsets (all zero)
+  return cuda_status(launch_permute(topk_idx, T, K, E, counts, offsets, sorted_pair, pair_pos, stream));
+}
+
+size_t moe_ffn_workspace_bytes(int T, int H, int I, int Is, const moe_recipe* recipe) {
+  if (check_recipe(recipe) != MOE_OK || T < 0 || H < 8 || I < 8 || Is < 0) return 0;
+  const int sms = device_sms();
+  if (sms <= 0) return 0;
+  // the gated/ungated choice changes only the router's geometry: size for the larger
+  const Layout a = make_layout(T, H, I, Is, recipe->num_experts, recipe->top_k, false, sms);
+  const Layout b = make_layout(T, H, I, Is, recipe->num_experts, recipe->top_k, true, sms);
+  return a.total > b.total ? a.total : b.total;
+}
+
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, stream));
+}
+
+moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf16* gate, const float* router_bias,
+                           const float* expert_bias, const moe_bf16* w_gate_up, const moe_bf16* w_down,
+                           const moe_bf16* sh_gate_up, const moe_bf16* sh_down, int Is, const moe_bf16* sh_gate,
+                           const moe_recipe* recipe, void* ws, size_t ws_bytes, moe_bf16* y,
+                           int32_t* topk_idx_out, float* topk_w_out, int32_t* counts_out, cudaStream_t stream) {
+  moe_status st = check_recipe(recipe);
+  if (st != MOE_OK) return st;
+  if (T < 0 || H < 8 || I < 8 || Is < 0) return MOE_ERR_INVALID_ARG;
+  if (H % 8 != 0 || I % 8 != 0 || Is % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (H > 65536 || I > 16384 || Is > 16384 || T > 65536) return MOE_ERR_UNSUPPORTED;
+  if ((sh_gate_up == nullptr) != (Is == 0) || (Is > 0 && sh_down == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (sh_gate && Is == 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !gate || !w_gate_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(gate) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(y) ||
+      (sh_gate_up && !aligned16(sh_gate_up)) || (sh_down && !aligned16(sh_down)))
+    return MOE_ERR_INVALID_ARG;
+  const size_t xy_bytes = static_cast<size_t>(T) * H * 2;
+  if (overlaps(x, xy_bytes, y, xy_bytes)) return MOE_ERR_INVALID_ARG;
+  const int E = recipe->num_experts, K = recipe->top_k;
+  const int sms = device_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const Layout L = make_layout(T, H, I, Is, E, K, sh_gate != nullptr, sms);
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0 || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  char* w = static_cast<char*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(w + L.o_status);
+  int32_t* idx = topk_idx_out ? topk_idx_out : reinterpret_cast<int32_t*>(w + L.o_idx);
+  float* wts = topk_w_out ? topk_w_out : reinterpret_cast<float*>(w + L.o_w);
+  int32_t* counts = counts_out ? counts_out : reinterpret_cast<int32_t*>(w + L.o_counts);
+  int32_t* sorted_pair = reinterpret_cast<int32_t*>(w + L.o_sp);
+  int32_t* pair_pos = reinterpret_cast<int32_t*>(w + L.o_pp);
+  float* sh_w = reinterpret_cast<float*>(w + L.o_shw);
+  GroupEntry* groups = reinterpret_cast<GroupEntry*>(w + L.o_groups);
+  GemmHeader* header = reinterpret_cast<GemmHeader*>(w + L.o_header);
+  int32_t* tiles = reinterpret_cast<int32_t*>(w + L.o_tiles);
+  uint16_t* h = reinterpret_cast<uint16_t*>(w + L.o_h);
+  float* out_ws = reinterpret_cast<float*>(w + L.o_out);
+
+  // ---- 1. router + permutation + work list
+  RouteParams rp;
+  memset(&rp, 0, sizeof(rp));
+  rp.x = x; rp.gate = gate; rp.router_bias = router_bias; rp.expert_bias = expert_bias; rp.sh_gate = sh_gate;
+  rp.T = T; rp.H = H; rp.E = E; rp.K = K;
+  rp.score_fn = recipe->score_fn; rp.n_group = recipe->n_group; rp.topk_group = recipe->topk_group;
+  rp.group_topn = recipe->group_topn; rp.renorm = recipe->norm_topk_prob; rp.eps = recipe->norm_eps;
+  rp.scale = recipe->route_scale;
+  rp.quads = L.rg.quads; rp.hsplit = L.rg.hsplit; rp.n_eb = L.rg.n_eb; rp.n_tb = L.rg.n_tb;
+  rp.logits = reinterpret_cast<float*>(w + L.o_logits);
+  rp.sh_logit = reinterpret_cast<float*>(w + L.o_shl);
+  rp.idx = idx; rp.w = wts; rp.sh_w = Is > 0 ? sh_w : nullptr;
+  rp.tb_counter = reinterpret_cast<int32_t*>(w + L.o_cnt);
+  rp.glob_counter = rp.tb_counter + L.rg.n_tb;
+  rp.do_permute = 1;
+  rp.counts = counts; rp.offsets = reinterpret_cast<int32_t*>(w + L.o_offsets);
+  rp.sorted_pair = sorted_pair; rp.pair_pos = pair_pos;
+  rp.groups = groups; rp.header = header;
+  rp.I = I; rp.Is = Is; rp.n_max = L.n_max;
+  rp.zero_ptr = tiles; rp.zero_count = L.max_gu_tiles + L.max_dn_tiles;
+  record_event_on(0, stream);
+  cudaError_t e = launch_route(rp, L.rg.tb, stream);
+  record_event_on(1, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  // ---- 2./3. grouped GEMMs
+  CUtensorMap tm_gu, tm_gu_sh, tm_dn, tm_dn_sh;
+  if (!encode_weights_3d(&tm_gu, w_gate_up, H, I, 2ull * E) || !encode_weights_3d(&tm_dn, w_down, I, H, E))
+    return MOE_ERR_CUDA;
+  if (Is > 0) {
+    if (!encode_weights_3d(&tm_gu_sh, sh_gate_up, H, Is, 2) || !encode_weights_3d(&tm_dn_sh, sh_down, Is, H, 1))
+      return MOE_ERR_CUDA;
+  } else {
+    tm_gu_sh = tm_gu;
+    tm_dn_sh = tm_dn;
+  }
+  GemmParams gp;
+  memset(&gp, 0, sizeof(gp));
+  gp.groups = groups; gp.header = header; gp.sorted_pair = sorted_pair;
+  gp.T = T; gp.K = K; gp.TK = T * K; gp.H = H; gp.I_ld = L.I_ld;
+  gp.n_max = L.n_max; gp.stages = L.stages; gp.nbuf = L.nbuf; gp.tmem_cols = L.tmem_cols;
+  gp.swiglu_limit = recipe->swiglu_limit;
+  gp.h = h; gp.out_ws = out_ws; gp.y = y; gp.direct_y = L.need_out ? 0 : 1;
+  gp.topk_w = wts; gp.sh_w = (Is > 0 && sh_gate) ? sh_w : nullptr;
+  gp.partials = reinterpret_cast<float*>(w + L.o_partials);
+  gp.status = status;
+  gp.bsrc = x;
+  gp.tile_counters = tiles;
+  record_event_on(2, stream);
+  e = launch_gemm(0, tm_gu, tm_gu_sh, gp, L.grid, L.smem, stream);
+  record_event_on(3, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  gp.bsrc = h;
+  gp.tile_counters = tiles + L.max_gu_tiles;
+  record_event_on(4, stream);
+  e = launch_gemm(1, tm_dn, tm_dn_sh, gp, L.grid, L.smem, stream);
+  record_event_on(5, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  // ---- 4. weighted combine (+ shared expert)
+  if (L.need_out) {
+    record_event_on(6, stream);
+    e = launch_combine(out_ws, pair_pos, T, K, H, Is > 0 ? 1 : 0, y, stream);
+    record_event_on(7, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_get_device_status(void* ws, cudaStream_t stream, int32_t* info_out) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t words[2] = {0, 0};
+  if (cudaMemcpy(words, ws, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (info_out) *info_out = words[1];
+  if (words[0] != 0 && cudaMemset(ws, 0, sizeof(words)) != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status>(words[0]);
+}
+
+void moe_set_profile_events(void* const* events, int n_pairs) {
+  t_events = events;
+  t_nev = events ? n_pairs : 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,277 @@
+// Internal declarations shared by the kernels and the host layer of
+// libmoe_gb300.so: work-list structures, launch parameter blocks and the
+// inline-PTX wrappers for sm_103a (mbarrier, TMA, cp.async, tcgen05/TMEM).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ----------------------------------------------------------------------------
+// status word (first 8 bytes of every workspace): {code, info}
+// ----------------------------------------------------------------------------
+enum : int32_t { kStatusTimeout = 5 };
+// info values: which wait ran out
+enum : int32_t {
+  kInfoEmpty = 1, kInfoFull = 2, kInfoAccFull = 3, kInfoAccEmpty = 4,
+  kInfoGatherEmpty = 5, kInfoDrain = 6
+};
+
+// ----------------------------------------------------------------------------
+// Expert-group work list written by the router's last CTA and read by the
+// grouped GEMMs.  Group g is one touched expert (expert >= 0, in expert
+// order) or the shared expert (expert == -1, always last).  Its rows are the
+// sorted (token, slot) pairs [row_base, row_base + count) of the expert, or
+// for the shared expert the T tokens in order at row_base = T*K.
+// ----------------------------------------------------------------------------
+struct GroupEntry {
+  int32_t expert;
+  int32_t row_base;
+  int32_t count;
+  int32_t idim;     // I of this expert (I or Is)
+  int32_t gu_tile;  // first tile index of the group in the gate_up GEMM
+  int32_t dn_tile;  // first tile index of the group in the down GEMM
+  int32_t pad0, pad1;
+  int64_t gu_iter;  // first k-block iteration of the group (gate_up)
+  int64_t dn_iter;  // first k-block iteration of the group (down)
+};
+static_assert(sizeof(GroupEntry) == 48, "group entry layout");
+
+struct GemmHeader {
+  int32_t ngroups;
+  int32_t gu_tiles;
+  int32_t dn_tiles;
+  int32_t pad;
+  int64_t gu_iters;
+  int64_t dn_iters;
+};
+
+// Tile geometry.  A "tile" is 256 weight rows (two 128-row MMA halves) by up
+// to n_max tokens; one k-block is 64 elements of the reduction dimension.
+//   gate_up: half 0 = gate rows [m*128, m*128+128), half 1 = the matching up
+//            rows; m-blocks = ceil(I/128); K = H.
+//   down:    half 0 = output rows [m*256, m*256+128), half 1 = the next 128;
+//            m-blocks = ceil(H/256); K = I.
+constexpr int kBlockK = 64;
+constexpr int kHalfRows = 128;
+constexpr int kTileBytesA = kHalfRows * kBlockK * 2;  // one half, bf16: 16 KB
+constexpr int kGemmThreads = 224;                     // 7 warps
+constexpr int kMaxStages = 8;
+constexpr int kGatherLag = 2;                         // cp.async groups in flight
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+__host__ __device__ inline void group_geometry(int phase, int count, int idim, int H, int n_max,
+                                               int& mb, int& nb, int& kb) {
+  nb = ceil_div(count, n_max);
+  if (phase == 0) { mb = ceil_div(idim, kHalfRows); kb = ceil_div(H, kBlockK); }
+  else            { mb = ceil_div(H, 2 * kHalfRows); kb = ceil_div(idim, kBlockK); }
+}
+
+struct GemmParams {
+  const GroupEntry* groups;
+  const GemmHeader* header;
+  const uint16_t* bsrc;        // gate_up: x [T,H]; down: h [rows, I_ld]
+  const int32_t* sorted_pair;  // [T*K]
+  int T, K, TK, H, I_ld;
+  int n_max;                   // token tile width, multiple of 16, <= 256
+  int stages;
+  int nbuf;                    // TMEM accumulator buffers (1 or 2)
+  uint32_t tmem_cols;
+  float swiglu_limit;
+  uint16_t* h;                 // gate_up output [T*K + T, I_ld] bf16
+  float* out_ws;               // down output [T*K + T, H] fp32 (weighted)
+  uint16_t* y;                 // down output when direct_y: [T, H] bf16
+  int direct_y;
+  const float* topk_w;         // [T*K]
+  const float* sh_w;           // [T] shared-expert gate (nullable = 1)
+  float* partials;             // [grid, 2 slots, 2 halves, n_max, 128] fp32
+  int32_t* tile_counters;      // [tiles]
+  int32_t* status;
+};
+
+struct RouteParams {
+  const uint16_t* x;
+  const uint16_t* gate;
+  const float* router_bias;
+  const float* expert_bias;
+  const uint16_t* sh_gate;
+  int T, H, E, K;
+  int score_fn, n_group, topk_group, group_topn, renorm;
+  float eps, scale;
+  int quads, hsplit, n_eb, n_tb;
+  float* logits;               // [T, E]
+  float* sh_logit;             // [T] (when sh_gate)
+  int32_t* idx;                // [T*K]
+  float* w;                    // [T*K]
+  float* sh_w;                 // [T] (nullable)
+  int32_t* tb_counter;         // [n_tb]
+  int32_t* glob_counter;       // [1]
+  // optional permutation and GEMM work list (do_permute)
+  int do_permute;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_pair;
+  int32_t* pair_pos;
+  GroupEntry* groups;          // nullable
+  GemmHeader* header;
+  int I, Is, n_max;
+  int32_t* zero_ptr;           // GEMM tile counters cleared by this launch
+  int zero_count;
+};
+
+// launchers (route.cu, gemm.cu, combine.cu); return cudaError_t
+cudaError_t launch_route(const RouteParams& p, int tb, cudaStream_t s);
+cudaError_t launch_select_from_logits(const float* logits, int T, int E, int K, const float* expert_bias,
+                                      int score_fn, int n_group, int topk_group, int group_topn,
+                                      int renorm, float eps, float scale, int32_t* idx, float* w,
+                                      cudaStream_t s);
+cudaError_t launch_permute(const int32_t* idx, int T, int K, int E, int32_t* counts, int32_t* offsets,
+                           int32_t* sorted_pair, int32_t* pair_pos, cudaStream_t s);
+cudaError_t launch_gemm(int phase, const CUtensorMap& tm_routed, const CUtensorMap& tm_shared,
+                        const GemmParams& p, int grid, size_t smem_bytes, cudaStream_t s);
+cudaError_t launch_combine(const float* out_ws, const int32_t* pair_pos, int T, int K, int H,
+                           int has_shared, uint16_t* y, cudaStream_t s);
+
+// ----------------------------------------------------------------------------
+// inline PTX (device only)
+// ----------------------------------------------------------------------------
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// A bounded wait gives up after this many SM clock cycles (about 1 s).
+constexpr long long kWaitLimitCycles = 2000000000ll;
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                   smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase of `parity` to complete; returns false if the CTA's
+// abort flag (when given) is raised or the wait runs past kWaitLimitCycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// TMA: 3-D tiled load into shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// cp.async (16 bytes, L2 only); src_bytes == 0 zero-fills the destination.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// tcgen05 / TMEM
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrives once on `bar` when every tcgen05.mma issued so far by this thread is complete.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major tile with 128-byte swizzle:
+// rows of 128 bytes (64 bf16), 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset: 8 rows x 128 B
+  d |= static_cast<uint64_t>(1) << 46;                  // descriptor version for tcgen05
+  d |= static_cast<uint64_t>(2) << 61;                  // 128-byte swizzle
+  return d;
+}
+#endif  // __CUDACC__
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A
+// and B, both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+}  // namespace moe

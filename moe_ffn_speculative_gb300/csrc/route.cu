@@ -1,0 +1,512 @@
+// Router of the MoE-FFN layer: fp32 gate logits on CUDA cores, score ->
+// select -> routing_weights per token, and the token-to-expert permutation
+// plus the grouped-GEMM work list.
+//
+// Sources (web pages): SpecForge PR #1033 "MoE FFN for DFlash-family drafts:
+// the module", section "Router" (the score -> select -> routing_weights
+// template; weights gathered from the unshifted scores, renormalised with
+// DeepSeek's 1e-20, times route_scale); sglang PR #48763 "[Feat] dflash: Serve
+// MoE FFN drafts for DFlash and DSpark" (fp32 router logits, int32 ids);
+// SpecForge PR #941 (folded router bias on the logits; DeepSeek-V4 follow-up:
+// sqrtsoftplus, selection-only bias, groups); SpecForge PR #1073 "MoE drafts:
+// DeepSeek-V4.1's own DSpark draft" (the expert bias shifts the picks, never
+// the weights; select sees the shifted scores; tokens_per_expert counts).
+#include <float.h>
+#include <math.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRouteThreads = 256;
+constexpr int kMaxExperts = 1024;
+constexpr float kNegInf = -INFINITY;
+
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// acc += sum_i a_i * b_i over 8 bf16 pairs, one fused multiply-add at a time
+// (bf16 x bf16 products are exact in fp32).
+__device__ __forceinline__ float dot8(const uint4& a, const uint4& b, float acc) {
+  acc = fmaf(bf_lo(a.x), bf_lo(b.x), acc);
+  acc = fmaf(bf_hi(a.x), bf_hi(b.x), acc);
+  acc = fmaf(bf_lo(a.y), bf_lo(b.y), acc);
+  acc = fmaf(bf_hi(a.y), bf_hi(b.y), acc);
+  acc = fmaf(bf_lo(a.z), bf_lo(b.z), acc);
+  acc = fmaf(bf_hi(a.z), bf_hi(b.z), acc);
+  acc = fmaf(bf_lo(a.w), bf_lo(b.w), acc);
+  acc = fmaf(bf_hi(a.w), bf_hi(b.w), acc);
+  return acc;
+}
+
+__device__ __forceinline__ uint4 ldg128(const uint16_t* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// (value, index) maximum over the warp; ties go to the lower index.  The
+// order is total, so every lane ends with the same winner.
+__device__ __forceinline__ void warp_argmax(float& v, int& ix, float& carry) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, ix, off);
+    const float oc = __shfl_xor_sync(0xffffffffu, carry, off);
+    if (ov > v || (ov == v && oi < ix)) { v = ov; ix = oi; carry = oc; }
+  }
+}
+
+struct SelCfg {
+  int E, K, score_fn, n_group, topk_group, group_topn, renorm;
+  float eps, scale;
+  const float* expert_bias;
+};
+
+// score -> select -> routing_weights for one token, by one warp.  Lane l
+// holds experts l, l+32, ..., (NJ per lane).  Writes idx_out[0..K) and
+// w_out[0..K).
+template <int NJ>
+__device__ void select_token(const float* lrow, const SelCfg& c, int32_t* idx_out, float* w_out) {
+  const int lane = threadIdx.x & 31;
+  float l[NJ], s[NJ], key[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int e = lane + 32 * j;
+    l[j] = e < c.E ? __ldcg(lrow + e) : kNegInf;
+  }
+  // ---- score (fp32)
+  if (c.score_fn == 0) {  // softmax
+    float m = kNegInf;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) m = fmaxf(m, l[j]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      s[j] = (lane + 32 * j < c.E) ? expf(l[j] - m) : 0.f;
+      sum += s[j];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) s[j] = s[j] / sum;
+  } else if (c.score_fn == 1) {  // sigmoid
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) s[j] = (lane + 32 * j < c.E) ? 1.f / (1.f + expf(-l[j])) : 0.f;
+  } else {  // sqrt(softplus)
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+      s[j] = (lane + 32 * j < c.E) ? sqrtf(fmaxf(l[j], 0.f) + log1pf(expf(-fabsf(l[j])))) : 0.f;
+  }
+  // ---- selection key.  All three scores are strictly increasing in the
+  // logit, so without an expert bias and without groups the selection is
+  // made on the fp32 logits themselves (the exact order of the scores).
+  // A NaN key becomes the lowest finite value, so every pick stays a valid
+  // expert id (-inf marks only experts that may not be picked).
+  const bool on_logits = (c.expert_bias == nullptr && c.n_group == 1);
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int e = lane + 32 * j;
+    float v;
+    if (e >= c.E) v = kNegInf;
+    else if (on_logits) v = l[j];
+    else v = c.expert_bias ? s[j] + __ldg(c.expert_bias + e) : s[j];
+    key[j] = (v != v) ? -FLT_MAX : v;
+  }
+  // ---- group-limited select: keep the topk_group groups with the best sum
+  // of their group_topn largest keys; the other experts become unselectable.
+  if (c.n_group > 1) {
+    const int gsz = c.E / c.n_group;
+    float my_gs = kNegInf;
+    for (int g = 0; g < c.n_group; ++g) {
+      float tmp[NJ];
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        const int e = lane + 32 * j;
+        tmp[j] = (e < c.E && e / gsz == g) ? key[j] : kNegInf;
+      }
+      float gsum = 0.f;
+      for (int r = 0; r < c.group_topn; ++r) {
+        float bv = kNegInf;
+        int bj = -1;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j)
+          if (tmp[j] > bv) { bv = tmp[j]; bj = j; }
+        int ix = bj >= 0 ? lane + 32 * bj : 0x7fffffff;
+        float dummy = 0.f;
+        warp_argmax(bv, ix, dummy);
+        gsum = (r == 0) ? bv : gsum + bv;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j)
+          if (lane + 32 * j == ix) tmp[j] = kNegInf;
+      }
+      if (lane == g) my_gs = gsum;
+    }
+    uint32_t keep = 0;
+    float gv = my_gs;
+    for (int r = 0; r < c.topk_group; ++r) {
+      float v = gv;
+      int ix = lane < c.n_group ? lane : 0x7fffffff;
+      float dummy = 0.f;
+      warp_argmax(v, ix, dummy);
+      keep |= 1u << ix;
+      if (lane == ix) gv = kNegInf;
+    }
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int e = lane + 32 * j;
+      if (e < c.E && !((keep >> (e / gsz)) & 1u)) key[j] = kNegInf;
+    }
+  }
+  // ---- K rounds of warp argmax; lane k keeps the k-th pick and its score.
+  int my_e = -1;
+  float my_s = 0.f;
+  for (int k = 0; k < c.K; ++k) {
+    float bv = kNegInf, bs = 0.f;
+    int bj = -1;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+      if (key[j] > bv) { bv = key[j]; bj = j; bs = s[j]; }
+    int ix = bj >= 0 ? lane + 32 * bj : 0x7fffffff;
+    warp_argmax(bv, ix, bs);
+    if (lane == k) { my_e = ix; my_s = bs; }
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+      if (lane + 32 * j == ix) key[j] = kNegInf;
+  }
+  // ---- routing weights from the unshifted scores
+  float sum = 0.f;
+  for (int k = 0; k < c.K; ++k) sum += __shfl_sync(0xffffffffu, my_s, k);
+  if (lane < c.K) {
+    float wv = my_s;
+    if (c.renorm) wv = wv / (sum + c.eps);
+    wv = wv * c.scale;
+    idx_out[lane] = my_e;
+    w_out[lane] = wv;
+  }
+}
+
+// Counting-sort permutation of the (token, slot) pairs by expert, stable in
+// the pair index p = t*K + k, and (optionally) the grouped-GEMM work list.
+// Run by one whole CTA.
+__device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* counts, int32_t* offsets,
+                              int32_t* sorted_pair, int32_t* pair_pos, GroupEntry* groups, GemmHeader* header,
+                              int H, int I, int Is, int n_max, int* s_cnt, int* s_cur) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int TK = T * K;
+  for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  // ids outside [0, E) are not counted and get no row
+  for (int p = tid; p < TK; p += blockDim.x) {
+    const int e = __ldcg(idx + p);
+    if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int v = e < E ? s_cnt[e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += n;
+      }
+      if (e < E) s_cur[e] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    __syncwarp();
+    for (int base = 0; base < TK; base += 32) {
+      const int p = base + lane;
+      const int ev = p < TK ? __ldcg(idx + p) : -1;
+      const bool act = static_cast<unsigned>(ev) < static_cast<unsigned>(E);
+      const int e = act ? ev : -1 - lane;
+      const uint32_t peers = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int leader = __ffs(peers) - 1;
+      int bpos = (act && lane == leader) ? s_cur[e] : 0;
+      bpos = __shfl_sync(0xffffffffu, bpos, leader);
+      if (act) {
+        sorted_pair[bpos + rank] = p;
+        pair_pos[p] = bpos + rank;
+      }
+      __syncwarp();
+      if (act && lane == leader) s_cur[e] = bpos + __popc(peers);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  // s_cur[e] now holds the end of expert e's rows
+  for (int e = tid; e < E; e += blockDim.x) {
+    if (counts) counts[e] = s_cnt[e];
+    if (offsets) offsets[e + 1] = s_cur[e];
+  }
+  if (tid == 0 && offsets) offsets[0] = 0;
+  if (groups == nullptr || warp != 0) return;
+  int g = 0, gu_t = 0, dn_t = 0;
+  long long gu_i = 0, dn_i = 0;
+  for (int base = 0; base < E; base += 32) {
+    const int e = base + lane;
+    const int c = e < E ? s_cnt[e] : 0;
+    const bool touched = c > 0;
+    const uint32_t m = __ballot_sync(0xffffffffu, touched);
+    int gut = 0, dnt = 0;
+    long long gui = 0, dni = 0;
+    if (touched) {
+      int mb, nb, kb;
+      group_geometry(0, c, I, H, n_max, mb, nb, kb);
+      gut = mb * nb;
+      gui = static_cast<long long>(gut) * kb;
+      group_geometry(1, c, I, H, n_max, mb, nb, kb);
+      dnt = mb * nb;
+      dni = static_cast<long long>(dnt) * kb;
+    }
+    int a = gut, b = dnt;
+    long long ci = gui, di = dni;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int na = __shfl_up_sync(0xffffffffu, a, off);
+      const int nb2 = __shfl_up_sync(0xffffffffu, b, off);
+      const long long nci = __shfl_up_sync(0xffffffffu, ci, off);
+      const long long ndi = __shfl_up_sync(0xffffffffu, di, off);
+      if (lane >= off) { a += na; b += nb2; ci += nci; di += ndi; }
+    }
+    if (touched) {
+      GroupEntry ge;
+      ge.expert = e;
+      ge.row_base = s_cur[e] - c;
+      ge.count = c;
+      ge.idim = I;
+      ge.gu_tile = gu_t + a - gut;
+      ge.dn_tile = dn_t + b - dnt;
+      ge.gu_iter = gu_i + ci - gui;
+      ge.dn_iter = dn_i + di - dni;
+      groups[g + __popc(m & ((1u << lane) - 1u))] = ge;
+    }
+    g += __popc(m);
+    gu_t += __shfl_sync(0xffffffffu, a, 31);
+    dn_t += __shfl_sync(0xffffffffu, b, 31);
+    gu_i += __shfl_sync(0xffffffffu, ci, 31);
+    dn_i += __shfl_sync(0xffffffffu, di, 31);
+  }
+  if (lane == 0) {
+    if (Is > 0) {
+      GroupEntry ge;
+      int mb, nb, kb;
+      ge.expert = -1;
+      ge.row_base = TK;
+      ge.count = T;
+      ge.idim = Is;
+      ge.gu_tile = gu_t;
+      ge.dn_tile = dn_t;
+      ge.gu_iter = gu_i;
+      ge.dn_iter = dn_i;
+      groups[g] = ge;
+      group_geometry(0, T, Is, H, n_max, mb, nb, kb);
+      gu_t += mb * nb;
+      gu_i += static_cast<long long>(mb * nb) * kb;
+      group_geometry(1, T, Is, H, n_max, mb, nb, kb);
+      dn_t += mb * nb;
+      dn_i += static_cast<long long>(mb * nb) * kb;
+      ++g;
+    }
+    GemmHeader hd;
+    hd.ngroups = g;
+    hd.gu_tiles = gu_t;
+    hd.dn_tiles = dn_t;
+    hd.pad = 0;
+    hd.gu_iters = gu_i;
+    hd.dn_iters = dn_i;
+    *header = hd;
+  }
+}
+
+// One launch: every CTA computes a TB-token x (4*quads)-row block of the fp32
+// logits (row E is the shared-expert gate when present); the last CTA of a
+// token block selects its tokens; the last token block builds the
+// permutation and the work list.
+template <int TB, int NJ>
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams p) {
+  __shared__ float red[8][TB][4];
+  __shared__ int s_flag;
+  __shared__ int s_cnt[kMaxExperts];
+  __shared__ int s_cur[kMaxExperts];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tbi = blockIdx.x, ebi = blockIdx.y;
+  const int E_tot = p.E + (p.sh_gate ? 1 : 0);
+  {  // clear the GEMM tile counters for this forward
+    const int nthr = gridDim.x * gridDim.y * kRouteThreads;
+    const int gid = (blockIdx.y * gridDim.x + blockIdx.x) * kRouteThreads + threadIdx.x;
+    for (int i = gid; i < p.zero_count; i += nthr) p.zero_ptr[i] = 0;
+  }
+  // ---- logits block
+  const int quad = warp / p.hsplit, hs = warp % p.hsplit;
+  const int e0 = (ebi * p.quads + quad) * 4;
+  const uint16_t* rows[4];
+  bool ev[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int e = e0 + q;
+    ev[q] = quad < p.quads && e < E_tot;
+    rows[q] = e < p.E ? p.gate + static_cast<size_t>(e) * p.H : p.sh_gate;
+  }
+  const int t0 = tbi * TB;
+  const int hs_len = ceil_div(ceil_div(p.H, p.hsplit), 8) * 8;
+  const int h_lo = hs * hs_len;
+  const int h_hi = min(p.H, h_lo + hs_len);
+  float acc[TB][4];
+#pragma unroll
+  for (int t = 0; t < TB; ++t)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[t][q] = 0.f;
+  for (int c = h_lo + lane * 8; c < h_hi; c += 256) {
+    uint4 gv[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) gv[q] = ev[q] ? ldg128(rows[q] + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int t = 0; t < TB; ++t) {
+      if (t0 + t < p.T) {
+        const uint4 xv = ldg128(p.x + static_cast<size_t>(t0 + t) * p.H + c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[t][q] = dot8(xv, gv[q], acc[t][q]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TB; ++t)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float v = acc[t][q];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      acc[t][q] = v;
+    }
+  if (lane == 0) {
+#pragma unroll
+    for (int t = 0; t < TB; ++t)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) red[warp][t][q] = acc[t][q];
+  }
+  __syncthreads();
+  for (int o = threadIdx.x; o < p.quads * 4 * TB; o += kRouteThreads) {
+    const int qd = o / (4 * TB), rem = o % (4 * TB), t = rem / 4, q = rem % 4;
+    const int e = (ebi * p.quads + qd) * 4 + q, tok = t0 + t;
+    if (e < E_tot && tok < p.T) {
+      float v = red[qd * p.hsplit][t][q];
+      for (int h2 = 1; h2 < p.hsplit; ++h2) v += red[qd * p.hsplit + h2][t][q];
+      if (e < p.E) {
+        if (p.router_bias) v += __ldg(p.router_bias + e);
+        p.logits[static_cast<size_t>(tok) * p.E + e] = v;
+      } else {
+        p.sh_logit[tok] = v;
+      }
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int old = atomicAdd(&p.tb_counter[tbi], 1);
+    const int last = (old == p.n_eb - 1);
+    if (last) p.tb_counter[tbi] = 0;
+    s_flag = last;
+  }
+  __syncthreads();
+  if (!s_flag) return;
+  __threadfence();
+  // ---- selection: warp w routes token t0 + w
+  if (warp < TB && t0 + warp < p.T) {
+    const int tok = t0 + warp;
+    SelCfg c{p.E, p.K, p.score_fn, p.n_group, p.topk_group, p.group_topn, p.renorm, p.eps, p.scale,
+             p.expert_bias};
+    select_token<NJ>(p.logits + static_cast<size_t>(tok) * p.E, c, p.idx + static_cast<size_t>(tok) * p.K,
+                     p.w + static_cast<size_t>(tok) * p.K);
+    if (lane == 0 && p.sh_w) p.sh_w[tok] = p.sh_gate ? 1.f / (1.f + expf(-__ldcg(p.sh_logit + tok))) : 1.f;
+  }
+  if (!p.do_permute) return;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int old = atomicAdd(p.glob_counter, 1);
+    const int last = (old == p.n_tb - 1);
+    if (last) *p.glob_counter = 0;
+    s_flag = last;
+  }
+  __syncthreads();
+  if (!s_flag) return;
+  __threadfence();
+  permute_block(p.idx, p.T, p.K, p.E, p.counts, p.offsets, p.sorted_pair, p.pair_pos, p.groups, p.header, p.H,
+                p.I, p.Is, p.n_max, s_cnt, s_cur);
+}
+
+template <int NJ>
+__global__ void __launch_bounds__(kRouteThreads) select_kernel(const float* logits, int T, SelCfg c, int32_t* idx,
+                                                               float* w) {
+  const int tok = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (tok >= T) return;
+  select_token<NJ>(logits + static_cast<size_t>(tok) * c.E, c, idx + static_cast<size_t>(tok) * c.K,
+                   w + static_cast<size_t>(tok) * c.K);
+}
+
+__global__ void __launch_bounds__(kRouteThreads) permute_kernel(const int32_t* idx, int T, int K, int E,
+                                                                int32_t* counts, int32_t* offsets,
+                                                                int32_t* sorted_pair, int32_t* pair_pos) {
+  __shared__ int s_cnt[kMaxExperts];
+  __shared__ int s_cur[kMaxExperts];
+  permute_block(idx, T, K, E, counts, offsets, sorted_pair, pair_pos, nullptr, nullptr, 0, 0, 0, 1, s_cnt, s_cur);
+}
+
+int nj_for(int E) {
+  const int nj = ceil_div(E, 32);
+  if (nj <= 1) return 1;
+  if (nj <= 2) return 2;
+  if (nj <= 4) return 4;
+  if (nj <= 8) return 8;
+  if (nj <= 16) return 16;
+  return 32;
+}
+
+template <int TB>
+cudaError_t launch_route_tb(const RouteParams& p, cudaStream_t s) {
+  dim3 grid(p.n_tb, p.n_eb);
+  switch (nj_for(p.E)) {
+    case 1: route_kernel<TB, 1><<<grid, kRouteThreads, 0, s>>>(p); break;
+    case 2: route_kernel<TB, 2><<<grid, kRouteThreads, 0, s>>>(p); break;
+    case 4: route_kernel<TB, 4><<<grid, kRouteThreads, 0, s>>>(p); break;
+    case 8: route_kernel<TB, 8><<<grid, kRouteThreads, 0, s>>>(p); break;
+    case 16: route_kernel<TB, 16><<<grid, kRouteThreads, 0, s>>>(p); break;
+    default: route_kernel<TB, 32><<<grid, kRouteThreads, 0, s>>>(p); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_route(const RouteParams& p, int tb, cudaStream_t s) {
+  return tb == 4 ? launch_route_tb<4>(p, s) : launch_route_tb<8>(p, s);
+}
+
+cudaError_t launch_select_from_logits(const float* logits, int T, int E, int K, const float* expert_bias,
+                                      int score_fn, int n_group, int topk_group, int group_topn, int renorm,
+                                      float eps, float scale, int32_t* idx, float* w, cudaStream_t s) {
+  SelCfg c{E, K, score_fn, n_group, topk_group, group_topn, renorm, eps, scale, expert_bias};
+  const int grid = ceil_div(T, 8);
+  switch (nj_for(E)) {
+    case 1: select_kernel<1><<<grid, kRouteThreads, 0, s>>>(logits, T, c, idx, w); break;
+    case 2: select_kernel<2><<<grid, kRouteThreads, 0, s>>>(logits, T, c, idx, w); break;
+    case 4: select_kernel<4><<<grid, kRouteThreads, 0, s>>>(logits, T, c, idx, w); break;
+    case 8: select_kernel<8><<<grid, kRouteThreads, 0, s>>>(logits, T, c, idx, w); break;
+    case 16: select_kernel<16><<<grid, kRouteThreads, 0, s>>>(logits, T, c, idx, w); break;
+    default: select_kernel<32><<<grid, kRouteThreads, 0, s>>>(logits, T, c, idx, w); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const int32_t* idx, int T, int K, int E, int32_t* counts, int32_t* offsets,
+                           int32_t* sorted_pair, int32_t* pair_pos, cudaStream_t s) {
+  permute_kernel<<<1, kRouteThreads, 0, s>>>(idx, T, K, E, counts, offsets, sorted_pair, pair_pos);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,262 @@
+"""Python binding of libmoe_gb300.so (ctypes).
+
+Argument marshalling only: torch supplies device memory and the stream, every
+step of the layer runs in the library's CUDA kernels.  There is no fallback:
+when the library is missing or the device is not a CUDA GPU the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "moe.h")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT = range(6)
+SCORE_SOFTMAX, SCORE_SIGMOID, SCORE_SQRTSOFTPLUS = 0, 1, 2
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+class Recipe(ctypes.Structure):
+    """Mirror of ``moe_recipe`` in include/moe.h."""
+
+    _fields_ = [
+        ("num_experts", ctypes.c_int32),
+        ("top_k", ctypes.c_int32),
+        ("score_fn", ctypes.c_int32),
+        ("n_group", ctypes.c_int32),
+        ("topk_group", ctypes.c_int32),
+        ("group_topn", ctypes.c_int32),
+        ("norm_topk_prob", ctypes.c_int32),
+        ("norm_eps", ctypes.c_float),
+        ("route_scale", ctypes.c_float),
+        ("swiglu_limit", ctypes.c_float),
+    ]
+
+    @classmethod
+    def make(cls, num_experts, top_k, score_fn=SCORE_SOFTMAX, n_group=1, topk_group=1, group_topn=2,
+             norm_topk_prob=True, norm_eps=1e-20, route_scale=1.0, swiglu_limit=0.0) -> "Recipe":
+        return cls(num_experts, top_k, score_fn, n_group, topk_group if n_group > 1 else 1, group_topn,
+                   1 if norm_topk_prob else 0, norm_eps, route_scale, swiglu_limit)
+
+    @classmethod
+    def from_config(cls, cfg) -> "Recipe":
+        """From a ``synthetic.LayerConfig``."""
+        return cls.make(cfg.E, cfg.K, cfg.score_fn, cfg.n_group, cfg.topk_group, cfg.group_topn,
+                        cfg.norm_topk_prob, cfg.norm_eps, cfg.route_scale, cfg.swiglu_limit)
+
+
+_lib_handle: Optional[ctypes.CDLL] = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+_SIGS = {
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_route_workspace_bytes": (_SZ, [_I, _I]),
+    "moe_route": (_I, [_P, _I, _I, _P, _P, _P, ctypes.POINTER(Recipe), _P, _P, _P, _P, _SZ, _P]),
+    "moe_route_from_logits": (_I, [_P, _I, _P, ctypes.POINTER(Recipe), _P, _P, _P]),
+    "moe_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_ffn_workspace_bytes": (_SZ, [_I, _I, _I, _I, ctypes.POINTER(Recipe)]),
+    "moe_workspace_init": (_I, [_P, _SZ, _P]),
+    "moe_ffn_forward": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, ctypes.POINTER(Recipe),
+                             _P, _SZ, _P, _P, _P, _P, _P]),
+    "moe_get_device_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
+    "moe_set_profile_events": (None, [_P, _I]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with moe_ffn_speculative_gb300.build.build()")
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(h, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib_handle = h
+    return _lib_handle
+
+
+def header_functions():
+    """Names of the functions include/moe.h declares."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    return re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text)
+
+
+def status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("tensor is not on a CUDA device")
+            if not t.is_contiguous():
+                raise ValueError("tensor is not contiguous")
+
+
+def _u16(t: torch.Tensor) -> torch.Tensor:
+    if t.dtype != torch.bfloat16:
+        raise TypeError("expected a bfloat16 tensor")
+    return t
+
+
+# --------------------------------------------------------------------------- workspaces
+
+class Workspace:
+    """A zero-filled device workspace owned by torch's allocator."""
+
+    def __init__(self, nbytes: int, device=None):
+        self.nbytes = int(nbytes)
+        self.buf = torch.zeros(max(self.nbytes, 256), dtype=torch.uint8,
+                               device=device or torch.device("cuda", torch.cuda.current_device()))
+
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    def device_status(self, stream=None) -> Tuple[int, int]:
+        info = ctypes.c_int32(0)
+        st = lib().moe_get_device_status(self.ptr(), _stream(stream), ctypes.byref(info))
+        return st, info.value
+
+
+def ffn_workspace_bytes(T: int, H: int, I: int, Is: int, recipe: Recipe) -> int:
+    n = lib().moe_ffn_workspace_bytes(T, H, I, Is, ctypes.byref(recipe))
+    if n == 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "moe_ffn_workspace_bytes")
+    return n
+
+
+# --------------------------------------------------------------------------- entry points
+
+def moe_route(x, gate, recipe: Recipe, router_bias=None, expert_bias=None, ws: Workspace = None,
+              want_logits=True, stream=None):
+    """-> (topk_idx int32 [T,K], topk_w fp32 [T,K], logits fp32 [T,E] or None)."""
+    _need_cuda(x, gate, router_bias, expert_bias)
+    T, H = x.shape
+    E, K = recipe.num_experts, recipe.top_k
+    dev = x.device
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    w = torch.empty((T, K), dtype=torch.float32, device=dev)
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev) if want_logits else None
+    if ws is None:
+        ws = Workspace(lib().moe_route_workspace_bytes(T, E), dev)
+    _check(lib().moe_route(_ptr(_u16(x)), T, H, _ptr(_u16(gate)), _ptr(router_bias), _ptr(expert_bias),
+                           ctypes.byref(recipe), _ptr(logits), _ptr(idx), _ptr(w), ws.ptr(), ws.nbytes,
+                           _stream(stream)), "moe_route")
+    return idx, w, logits
+
+
+def moe_route_from_logits(logits, recipe: Recipe, expert_bias=None, stream=None):
+    """-> (topk_idx int32 [T,K], topk_w fp32 [T,K])."""
+    _need_cuda(logits, expert_bias)
+    T = logits.shape[0]
+    K = recipe.top_k
+    idx = torch.empty((T, K), dtype=torch.int32, device=logits.device)
+    w = torch.empty((T, K), dtype=torch.float32, device=logits.device)
+    _check(lib().moe_route_from_logits(_ptr(logits), T, _ptr(expert_bias), ctypes.byref(recipe), _ptr(idx),
+                                       _ptr(w), _stream(stream)), "moe_route_from_logits")
+    return idx, w
+
+
+def moe_permute(topk_idx, num_experts: int, stream=None):
+    """-> (counts [E], offsets [E+1], sorted_pair [T*K], pair_pos [T*K]), int32."""
+    _need_cuda(topk_idx)
+    T, K = topk_idx.shape
+    dev = topk_idx.device
+    counts = torch.empty(num_experts, dtype=torch.int32, device=dev)
+    offsets = torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+    sp = torch.empty(T * K, dtype=torch.int32, device=dev)
+    pp = torch.empty(T * K, dtype=torch.int32, device=dev)
+    _check(lib().moe_permute(_ptr(topk_idx), T, K, num_experts, _ptr(counts), _ptr(offsets), _ptr(sp), _ptr(pp),
+                             None, 0, _stream(stream)), "moe_permute")
+    return counts, offsets, sp, pp
+
+
+def moe_ffn_forward(x, gate, w_gate_up, w_down, recipe: Recipe, ws: Workspace, router_bias=None,
+                    expert_bias=None, sh_gate_up=None, sh_down=None, sh_gate=None, y=None,
+                    topk_idx_out=None, topk_w_out=None, counts_out=None, stream=None):
+    """The whole layer; returns y [T,H] bf16."""
+    _need_cuda(x, gate, w_gate_up, w_down, router_bias, expert_bias, sh_gate_up, sh_down, sh_gate, y,
+               topk_idx_out, topk_w_out, counts_out)
+    T, H = x.shape
+    I = w_down.shape[2]
+    Is = 0 if sh_gate_up is None else sh_down.shape[1]
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _check(lib().moe_ffn_forward(
+        _ptr(_u16(x)), T, H, I, _ptr(_u16(gate)), _ptr(router_bias), _ptr(expert_bias), _ptr(_u16(w_gate_up)),
+        _ptr(_u16(w_down)), _ptr(sh_gate_up), _ptr(sh_down), Is, _ptr(sh_gate), ctypes.byref(recipe), ws.ptr(),
+        ws.nbytes, _ptr(y), _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(counts_out), _stream(stream)),
+        "moe_ffn_forward")
+    return y
+
+
+def set_profile_events(events) -> None:
+    """events: a list of torch.cuda.Event (pairs around each launch) or None."""
+    global _profile_keepalive
+    if not events:
+        lib().moe_set_profile_events(None, 0)
+        _profile_keepalive = None
+        return
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _profile_keepalive = arr
+    lib().moe_set_profile_events(ctypes.cast(arr, ctypes.c_void_p), len(events) // 2)
+
+
+_profile_keepalive = None
+
+
+class MoELayer:
+    """Weights of one layer plus its workspace; ``forward(x)`` runs the layer."""
+
+    def __init__(self, tensors: dict, recipe: Recipe, max_tokens: int):
+        self.t = tensors
+        self.recipe = recipe
+        self.H = tensors["w_down"].shape[1]
+        self.I = tensors["w_down"].shape[2]
+        self.Is = 0 if tensors.get("sh_gate_up") is None else tensors["sh_down"].shape[1]
+        self.max_tokens = max_tokens
+        self.ws = Workspace(ffn_workspace_bytes(max_tokens, self.H, self.I, self.Is, recipe),
+                            tensors["w_down"].device)
+
+    def forward(self, x, y=None, topk_idx_out=None, topk_w_out=None, counts_out=None, stream=None):
+        if x.shape[0] > self.max_tokens:
+            raise ValueError("more tokens than the workspace was sized for")
+        t = self.t
+        return moe_ffn_forward(x, t["gate"], t["w_gate_up"], t["w_down"], self.recipe, self.ws,
+                               router_bias=t.get("router_bias"), expert_bias=t.get("expert_bias"),
+                               sh_gate_up=t.get("sh_gate_up"), sh_down=t.get("sh_down"), sh_gate=t.get("sh_gate"),
+                               y=y, topk_idx_out=topk_idx_out, topk_w_out=topk_w_out, counts_out=counts_out,
+                               stream=stream)

@@ -1,0 +1,290 @@
+"""GPU parity: the CUDA library through its C ABI against the fp64 oracle on
+the same seeded inputs.
+
+Bars (from the routing/equivalence requirements of the MoE-FFN layer):
+* routing from identical fp32 logits: indices bit-exact (ambiguity rule only
+  where fp32 and fp64 shifted scores tie within MARGIN_TOL), weights within
+  1e-6 absolute;
+* permutation: counts, offsets, sorted pairs and positions bit-exact;
+* layer output: max |y - y_oracle| / RMS(y_oracle) <= 2e-2;
+* end-to-end routing (GPU fp32 logits vs exact logits): logits within 3e-5
+  (about 6x the fp32 accumulation error u*sqrt(H)*|logit| at H <= 7168,
+  |logit| <= ~10), no index mismatch with a margin above 1e-4, weights within
+  1e-5.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from moe_ffn_speculative_gb300 import ops
+from moe_ffn_speculative_gb300 import synthetic as S
+from moe_ffn_speculative_gb300.build import build
+from parity_util import (MARGIN_TOL, W_ABS_TOL, Y_REL_RMS_TOL, compare_routing, np64, oracle_recipe,
+                         oracle_rows, rel_rms_error)
+
+pytestmark = pytest.mark.gpu
+
+LOGIT_TOL = 3e-5
+E2E_MARGIN_TOL = 1e-4
+E2E_W_TOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    build()
+    ops.lib()
+    torch.cuda.init()
+
+
+def _gen(seed):
+    g = torch.Generator()
+    g.manual_seed(seed)
+    return g
+
+
+# =========================================================================== routing from logits
+
+ROUTE_CASES = {
+    "softmax_E8_K2": dict(E=8, K=2),
+    "softmax_E8_K1": dict(E=8, K=1),
+    "softmax_E512_K10": dict(E=512, K=10),
+    "softmax_E1024_K32": dict(E=1024, K=32),
+    "softmax_E1_K1": dict(E=1, K=1),
+    "softmax_E8_K2_bias": dict(E=8, K=2, bias=0.05),
+    "sigmoid_E256_K8_grouped": dict(E=256, K=8, score_fn=1, n_group=8, topk_group=4, route_scale=2.5, bias=0.05),
+    "sigmoid_E33_K5_grouped3": dict(E=33, K=5, score_fn=1, n_group=3, topk_group=2),
+    "sigmoid_E64_K4_unnormalised": dict(E=64, K=4, score_fn=1, renorm=False, route_scale=2.0),
+    "sqrtsoftplus_E256_K6": dict(E=256, K=6, score_fn=2, route_scale=1.5, bias=0.05),
+    "softmax_E16_K4_grouped_all": dict(E=16, K=4, n_group=4, topk_group=4),
+}
+
+
+def _route_case(name, T, seed, tie_every=0):
+    c = ROUTE_CASES[name]
+    E, K = c["E"], c["K"]
+    logits = S.make_logits(T, E, std=2.0, seed=seed, tie_every=tie_every)
+    bias = None
+    if c.get("bias"):
+        bias = torch.randn(E, generator=_gen(seed + 1000)) * c["bias"]
+    kw = dict(score_fn=c.get("score_fn", 0), n_group=c.get("n_group", 1), topk_group=c.get("topk_group", 1),
+              norm_topk_prob=c.get("renorm", True), route_scale=c.get("route_scale", 1.0))
+    rec = ops.Recipe.make(E, K, **kw)
+    orec = O.Recipe(E, K, **kw)
+    return logits, bias, rec, orec
+
+
+@pytest.mark.parametrize("T", [1, 72, 1000])
+@pytest.mark.parametrize("name", list(ROUTE_CASES))
+def test_route_from_logits(name, T):
+    logits, bias, rec, orec = _route_case(name, T, seed=T)
+    idx, w = ops.moe_route_from_logits(logits.cuda(), rec, None if bias is None else bias.cuda())
+    torch.cuda.synchronize()
+    _, oidx, ow, c = O.route_from_logits(np64(logits), orec, np64(bias))
+    margin = O.selection_margin(c, oidx, orec)
+    n_amb, _ = compare_routing(idx, w, oidx, ow, margin)
+    assert n_amb == 0, f"{n_amb} ambiguous rows"
+    if orec.norm_topk_prob:
+        np.testing.assert_allclose(w.sum(1).cpu().numpy(), orec.route_scale, rtol=2e-6)
+
+
+@pytest.mark.parametrize("name", ["softmax_E8_K2", "softmax_E512_K10", "softmax_E1024_K32"])
+def test_route_from_logits_exact_ties(name):
+    """Exact fp32 ties (every 3rd expert copies its neighbour): both sides pick
+    the lower expert id first, so the indices match bit for bit."""
+    logits, bias, rec, orec = _route_case(name, 200, seed=5, tie_every=3)
+    idx, w = ops.moe_route_from_logits(logits.cuda(), rec)
+    _, oidx, ow, _ = O.route_from_logits(np64(logits), orec)
+    np.testing.assert_array_equal(idx.cpu().numpy(), oidx)
+    assert np.abs(w.cpu().numpy() - ow).max() <= W_ABS_TOL
+
+
+def test_expert_bias_changes_picks_not_weights():
+    """The expert bias shifts the selection only (regression of a dropped bias)."""
+    logits = S.make_logits(64, 16, seed=3).cuda()
+    rec = ops.Recipe.make(16, 4, score_fn=1)
+    bias = torch.zeros(16, device="cuda")
+    bias[15] = 10.0
+    i0, w0 = ops.moe_route_from_logits(logits, rec)
+    i1, w1 = ops.moe_route_from_logits(logits, rec, bias)
+    assert (i1[:, 0] == 15).all()
+    assert not torch.equal(i0, i1)
+    s = torch.sigmoid(logits.double())
+    g = torch.gather(s, 1, i1.long())
+    ref = (g / g.sum(1, keepdim=True)).float()
+    assert (w1 - ref).abs().max().item() <= 1e-6
+
+
+def test_route_scale_applied_exactly():
+    """route_scale multiplies the weights (regression of an unapplied
+    routed_scaling_factor): bitwise w(2.5) == fp32(w(1) * 2.5)."""
+    logits = S.make_logits(72, 256, seed=4).cuda()
+    a = ops.moe_route_from_logits(logits, ops.Recipe.make(256, 8, score_fn=1, n_group=8, topk_group=4))[1]
+    b = ops.moe_route_from_logits(logits, ops.Recipe.make(256, 8, score_fn=1, n_group=8, topk_group=4,
+                                                          route_scale=2.5))[1]
+    assert torch.equal(b, a * 2.5)
+
+
+@pytest.mark.parametrize("E,K", [(8, 2), (512, 10), (256, 8)])
+def test_softmax_epsilon_bitwise_noop(E, K):
+    logits = S.make_logits(128, E, std=3.0, seed=E).cuda()
+    a = ops.moe_route_from_logits(logits, ops.Recipe.make(E, K, norm_eps=1e-20))[1]
+    b = ops.moe_route_from_logits(logits, ops.Recipe.make(E, K, norm_eps=0.0))[1]
+    assert torch.equal(a, b)
+
+
+# =========================================================================== permutation
+
+@pytest.mark.parametrize("T,K,E", [(0, 2, 8), (1, 1, 1), (16, 2, 8), (72, 10, 512), (600, 1, 2), (4096, 6, 256),
+                                   (4096, 32, 1024)])
+def test_permute_bitexact(T, K, E):
+    g = _gen(T * 31 + K)
+    idx = (torch.stack([torch.randperm(E, generator=g)[:K] for _ in range(T)]) if T else
+           torch.empty((0, K), dtype=torch.int64)).to(torch.int32)
+    counts, offsets, sp, pp = ops.moe_permute(idx.cuda(), E)
+    oc, oo, osp, opp = O.permute(idx.numpy().astype(np.int64), E)
+    np.testing.assert_array_equal(counts.cpu().numpy(), oc)
+    np.testing.assert_array_equal(offsets.cpu().numpy(), oo)
+    np.testing.assert_array_equal(sp.cpu().numpy(), osp)
+    np.testing.assert_array_equal(pp.cpu().numpy(), opp)
+
+
+# =========================================================================== whole layer, small
+
+SMALL = {
+    "tiny": S.CONFIGS["tiny"],
+    "ragged_gated_shared_router_bias": S.LayerConfig("r1", T=37, H=264, E=4, I=200, K=2, router_bias_std=0.1,
+                                                     shared_I=136, shared_gated=True, seed=5),
+    "ragged_sigmoid_groups_clamp": S.LayerConfig("r2", T=50, H=192, E=16, I=96, K=3, score_fn=1, n_group=4,
+                                                 topk_group=2, expert_bias_std=0.05, route_scale=2.5,
+                                                 swiglu_limit=0.25, shared_I=64, seed=6, w_std=0.03),
+    "more_tokens_than_a_tile": S.LayerConfig("r3", T=600, H=128, E=2, I=64, K=1, seed=7),
+    "top1_direct_store": S.LayerConfig("r4", T=72, H=512, E=8, I=384, K=1, seed=8),
+    "sqrtsoftplus_clamp_shared": S.LayerConfig("r5", T=9, H=256, E=32, I=128, K=6, score_fn=2,
+                                               expert_bias_std=0.05, route_scale=1.5, swiglu_limit=7.0,
+                                               shared_I=128, seed=9),
+    "single_expert_dense": S.LayerConfig("r6", T=20, H=128, E=1, I=64, K=1, route_scale=2.0, seed=10),
+    "one_token": S.LayerConfig("r7", T=1, H=64, E=8, I=32, K=2, shared_I=32, seed=11),
+    "wide_tokens_K8": S.LayerConfig("r8", T=300, H=320, E=64, I=160, K=8, score_fn=1, n_group=8, topk_group=4,
+                                    expert_bias_std=0.05, shared_I=96, seed=12),
+}
+
+
+def _run_layer(cfg, d, stream=None):
+    rec = ops.Recipe.from_config(cfg)
+    layer = ops.MoELayer(d, rec, cfg.T)
+    idx = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device="cuda")
+    w = torch.empty((cfg.T, cfg.K), dtype=torch.float32, device="cuda")
+    counts = torch.empty(cfg.E, dtype=torch.int32, device="cuda")
+    y = layer.forward(d["x"], topk_idx_out=idx, topk_w_out=w, counts_out=counts, stream=stream)
+    torch.cuda.synchronize()
+    return layer, y, idx, w, counts
+
+
+def _oracle_routing(cfg, d):
+    orec = oracle_recipe(cfg)
+    x64, gate64 = np64(d["x"]), np64(d["gate"])
+    logits = O.router_logits(x64, gate64, np64(d["router_bias"]))
+    _, oidx, ow, c = O.route_from_logits(logits, orec, np64(d["expert_bias"]))
+    return orec, logits, oidx, ow, O.selection_margin(c, oidx, orec)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_layer_small(name):
+    cfg = SMALL[name]
+    d = S.make_inputs(cfg, device="cpu")
+    d = {k: (None if v is None else v.cuda()) for k, v in d.items()}
+    x_before = d["x"].clone()
+    layer, y, idx, w, counts = _run_layer(cfg, d)
+    assert torch.equal(d["x"], x_before), "x was modified"
+    orec, _, oidx, ow, margin = _oracle_routing(cfg, d)
+    n_amb, same = compare_routing(idx, w, oidx, ow, margin, w_tol=E2E_W_TOL, margin_tol=E2E_MARGIN_TOL)
+    assert n_amb == 0
+    np.testing.assert_array_equal(counts.cpu().numpy(), np.bincount(oidx.reshape(-1), minlength=cfg.E))
+    rows = np.arange(cfg.T)
+    y_ref = oracle_rows(d, cfg, rows, oidx, ow)
+    err = rel_rms_error(y, y_ref)
+    assert err <= Y_REL_RMS_TOL, f"rel-RMS error {err}"
+    st, info = layer.ws.device_status()
+    assert st == 0, (st, info)
+
+
+def test_layer_deterministic_and_repeatable():
+    cfg = SMALL["wide_tokens_K8"]
+    d = {k: (None if v is None else v.cuda()) for k, v in S.make_inputs(cfg).items()}
+    layer, y1, *_ = _run_layer(cfg, d)
+    y2 = layer.forward(d["x"])
+    y3 = layer.forward(d["x"])
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2) and torch.equal(y2, y3)
+
+
+def test_layer_zero_tokens():
+    cfg = S.CONFIGS["tiny"]
+    d = {k: (None if v is None else v.cuda()) for k, v in S.make_inputs(cfg).items()}
+    rec = ops.Recipe.from_config(cfg)
+    ws = ops.Workspace(ops.ffn_workspace_bytes(16, cfg.H, cfg.I, 0, rec))
+    y = ops.moe_ffn_forward(d["x"][:0], d["gate"], d["w_gate_up"], d["w_down"], rec, ws)
+    torch.cuda.synchronize()
+    assert y.shape == (0, cfg.H)
+
+
+def test_layer_refuses_in_place_output():
+    cfg = S.CONFIGS["tiny"]
+    d = {k: (None if v is None else v.cuda()) for k, v in S.make_inputs(cfg).items()}
+    rec = ops.Recipe.from_config(cfg)
+    ws = ops.Workspace(ops.ffn_workspace_bytes(cfg.T, cfg.H, cfg.I, 0, rec))
+    with pytest.raises(ops.MoeError) as e:
+        ops.moe_ffn_forward(d["x"], d["gate"], d["w_gate_up"], d["w_down"], rec, ws, y=d["x"])
+    assert e.value.status == ops.MOE_ERR_INVALID_ARG
+
+
+def test_cuda_graph_replay():
+    cfg = SMALL["ragged_gated_shared_router_bias"]
+    d = {k: (None if v is None else v.cuda()) for k, v in S.make_inputs(cfg).items()}
+    layer, y_ref, *_ = _run_layer(cfg, d)
+    s = torch.cuda.Stream()
+    y = torch.empty_like(y_ref)
+    with torch.cuda.stream(s):
+        layer.forward(d["x"], y=y, stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer.forward(d["x"], y=y, stream=s)
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_ref)
+
+
+# =========================================================================== whole layer, full sizes
+
+FULL = [("qwen3_8b_dspark", 72), ("qwen38_27b_dspark", 72), ("dsv3_style", 72), ("dsv4_style", 9),
+        ("dsv4_style", 72), ("dsv4_style", 576), ("dsv4_style", 4096)]
+
+
+@pytest.mark.parametrize("name,T", FULL)
+def test_layer_full_size_sampled(name, T):
+    cfg = S.CONFIGS[name].with_(T=T)
+    d = S.make_inputs(cfg, device="cuda")
+    layer, y, idx, w, counts = _run_layer(cfg, d)
+    orec, logits, oidx, ow, margin = _oracle_routing(cfg, d)
+    # GPU fp32 logits (same router kernel, standalone entry point) against exact logits
+    rec = ops.Recipe.from_config(cfg)
+    _, _, glog = ops.moe_route(d["x"], d["gate"], rec, router_bias=d["router_bias"],
+                               expert_bias=d["expert_bias"])
+    lerr = np.abs(glog.cpu().numpy().astype(np.float64) - logits).max()
+    assert lerr <= LOGIT_TOL, f"logit error {lerr}"
+    n_amb, same = compare_routing(idx, w, oidx, ow, margin, w_tol=E2E_W_TOL, margin_tol=E2E_MARGIN_TOL)
+    assert n_amb == 0, f"{n_amb} ambiguous rows"
+    np.testing.assert_array_equal(counts.cpu().numpy(), np.bincount(oidx.reshape(-1), minlength=cfg.E))
+    n_s = 4 if name == "dsv3_style" else 8
+    rows = np.unique(np.linspace(0, T - 1, n_s).round().astype(int))
+    y_ref = oracle_rows(d, cfg, rows, oidx[rows], ow[rows])
+    err = rel_rms_error(y[torch.as_tensor(rows, device="cuda")], y_ref)
+    assert err <= Y_REL_RMS_TOL, f"rel-RMS error {err}"
+    y2 = layer.forward(d["x"])
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2), "not deterministic"
+    st, info = layer.ws.device_status()
+    assert st == 0, (st, info)
