@@ -106,9 +106,9 @@ RouterGeom router_geometry(int T, int E_tot, int sms) {
 
 struct Layout {
   RouterGeom rg;
-  int n_max, stages, nbuf, grid, I_ld;
+  int n_max, stages[2], nbuf, grid, I_ld;
   uint32_t tmem_cols;
-  size_t smem;
+  size_t smem[2];
   int max_gu_tiles, max_dn_tiles, g_max;
   bool need_out;
   size_t o_status, o_cnt, o_tiles, o_logits, o_shl, o_shw, o_idx, o_w, o_counts, o_offsets, o_sp, o_pp, o_groups,
@@ -124,10 +124,12 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(L.nbuf * 2 * L.n_max)) cols <<= 1;
   L.tmem_cols = cols;
-  const int stage_bytes = 2 * kTileBytesA + L.n_max * 128;
-  L.stages = (kSmemLimit - 1024 - kCtrlBytes) / stage_bytes;
-  if (L.stages > kMaxStages) L.stages = kMaxStages;
-  L.smem = 1024 + static_cast<size_t>(L.stages) * stage_bytes + kCtrlBytes;
+  for (int ph = 0; ph < 2; ++ph) {  // the down GEMM stages two token tiles (h hi and lo)
+    const int stage_bytes = 2 * kTileBytesA + (ph + 1) * L.n_max * 128;
+    L.stages[ph] = (kSmemLimit - 1024 - kCtrlBytes) / stage_bytes;
+    if (L.stages[ph] > kMaxStages) L.stages[ph] = kMaxStages;
+    L.smem[ph] = 1024 + static_cast<size_t>(L.stages[ph]) * stage_bytes + kCtrlBytes;
+  }
   L.grid = sms;
   const int Imax = Is > I ? Is : I;
   L.I_ld = ((Imax + 7) / 8) * 8;
@@ -160,7 +162,7 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   L.o_groups = o; o = align_up(o + sizeof(GroupEntry) * static_cast<size_t>(L.g_max + 1));
   L.o_header = o; o = align_up(o + sizeof(GemmHeader));
   L.o_partials = o; o = align_up(o + 4 * static_cast<size_t>(L.grid) * 2 * 2 * L.n_max * 128);
-  L.o_h = o; o = align_up(o + 2 * rows * L.I_ld);
+  L.o_h = o; o = align_up(o + 2 * 2 * rows * L.I_ld);
   L.o_out = o;
   if (L.need_out) o = align_up(o + 4 * rows * H);
   L.total = o;
@@ -354,7 +356,7 @@ moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf1
   memset(&gp, 0, sizeof(gp));
   gp.groups = groups; gp.header = header; gp.sorted_pair = sorted_pair;
   gp.T = T; gp.K = K; gp.TK = T * K; gp.H = H; gp.I_ld = L.I_ld;
-  gp.n_max = L.n_max; gp.stages = L.stages; gp.nbuf = L.nbuf; gp.tmem_cols = L.tmem_cols;
+  gp.n_max = L.n_max; gp.stages = L.stages[0]; gp.nbuf = L.nbuf; gp.tmem_cols = L.tmem_cols;
   gp.swiglu_limit = recipe->swiglu_limit;
   gp.h = h; gp.out_ws = out_ws; gp.y = y; gp.direct_y = L.need_out ? 0 : 1;
   gp.topk_w = wts; gp.sh_w = (Is > 0 && sh_gate) ? sh_w : nullptr;
@@ -363,13 +365,14 @@ moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf1
   gp.bsrc = x;
   gp.tile_counters = tiles;
   record_event_on(2, stream);
-  e = launch_gemm(0, tm_gu, tm_gu_sh, gp, L.grid, L.smem, stream);
+  e = launch_gemm(0, tm_gu, tm_gu_sh, gp, L.grid, L.smem[0], stream);
   record_event_on(3, stream);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   gp.bsrc = h;
+  gp.stages = L.stages[1];
   gp.tile_counters = tiles + L.max_gu_tiles;
   record_event_on(4, stream);
-  e = launch_gemm(1, tm_dn, tm_dn_sh, gp, L.grid, L.smem, stream);
+  e = launch_gemm(1, tm_dn, tm_dn_sh, gp, L.grid, L.smem[1], stream);
   record_event_on(5, stream);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 

@@ -113,7 +113,9 @@ __device__ __forceinline__ void finish_chunk(const GemmParams& p, const Seg& sg,
     // SwiGLU: h = silu(gate) * up, with the clamp when a limit is set
     const int row = sg.m * kHalfRows + r;
     if (row >= sg.idim) return;
-    uint16_t* hp = p.h + static_cast<size_t>(sg.row_base + sg.n * p.n_max) * p.I_ld + row;
+    // h is kept as a compensated pair hi + lo of bf16 (about 16 significant
+    // bits): row r holds hi in [0, I_ld) and lo in [I_ld, 2*I_ld)
+    uint16_t* hp = p.h + static_cast<size_t>(sg.row_base + sg.n * p.n_max) * (2 * p.I_ld) + row;
     const float lim = p.swiglu_limit;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -125,7 +127,10 @@ __device__ __forceinline__ void finish_chunk(const GemmParams& p, const Seg& sg,
           u = fminf(fmaxf(u, -lim), lim);
         }
         const float hv = g / (1.f + expf(-g)) * u;
-        hp[static_cast<size_t>(j) * p.I_ld] = f2bf(hv);
+        const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
+        const float lo = hv - __bfloat162float(hi);
+        hp[static_cast<size_t>(j) * (2 * p.I_ld)] = __bfloat16_as_ushort(hi);
+        hp[static_cast<size_t>(j) * (2 * p.I_ld) + p.I_ld] = f2bf(lo);
       }
     }
   } else {
@@ -173,7 +178,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int S = p.stages;
-  const uint32_t stage_bytes = 2 * kTileBytesA + p.n_max * 128;
+  constexpr int kBTiles = PHASE == 0 ? 1 : 2;  // down: B = h_hi and h_lo
+  const uint32_t b_bytes = p.n_max * 128;
+  const uint32_t stage_bytes = 2 * kTileBytesA + kBTiles * b_bytes;
   uint8_t* ctrl = smem + S * stage_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + kMaxStages;
@@ -290,8 +297,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int ks = 0; ks < kBlockK / 16; ++ks) {
             const uint32_t acc = (kk > 0 || ks > 0) ? 1u : 0u;
             const uint64_t bd = sw128_desc(bb + ks * 32);
-            mma_bf16(d0, sw128_desc(a0 + ks * 32), bd, idesc, acc);
-            mma_bf16(d1, sw128_desc(a1 + ks * 32), bd, idesc, acc);
+            const uint64_t ad0 = sw128_desc(a0 + ks * 32), ad1 = sw128_desc(a1 + ks * 32);
+            mma_bf16(d0, ad0, bd, idesc, acc);
+            mma_bf16(d1, ad1, bd, idesc, acc);
+            if (PHASE == 1) {  // + W * h_lo
+              const uint64_t bl = sw128_desc(bb + b_bytes + ks * 32);
+              mma_bf16(d0, ad0, bl, idesc, 1u);
+              mma_bf16(d1, ad1, bl, idesc, 1u);
+            }
           }
           mma_commit(&empty[stage]);
           if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -310,6 +323,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t phase = 0;
     bool ok = true;
     const int K = p.K, H = p.H;
+    // copies kept in flight before arriving; below the stage count, so the
+    // stage this warp waits to refill never depends on an arrival it holds
+    const int lag = kGatherLag < S - 1 ? kGatherLag : S - 1;
     while (ok && sc.next(sg)) {
       const int nrows = max(16, (sg.n_cnt + 15) & ~15);
       const int kdim = PHASE == 0 ? H : sg.idim;
@@ -322,7 +338,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int tok = sg.expert >= 0 ? __ldg(p.sorted_pair + sg.row_base + r) / K : r;
             off = static_cast<long long>(tok) * H;
           } else {
-            off = static_cast<long long>(sg.row_base + r) * p.I_ld;
+            off = static_cast<long long>(sg.row_base + r) * (2 * p.I_ld);
           }
         }
         rowoff[j] = off;
@@ -337,18 +353,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         const uint32_t bbase = smem_u32(smem + stage * stage_bytes) + 2 * kTileBytesA;
-        for (int q = lane; q < nrows * 8; q += 32) {
-          const int j = q >> 3, c = q & 7;
+        for (int q = lane; q < nrows * 8 * kBTiles; q += 32) {
+          const int t = (kBTiles == 2 && q >= nrows * 8) ? 1 : 0;  // 0: x or h_hi, 1: h_lo
+          const int qq = q - t * nrows * 8;
+          const int j = qq >> 3, c = qq & 7;
           const long long off = rowoff[j];
           const int col = kx + c * 8;
           const bool valid = off >= 0 && col < kdim;
-          const uint16_t* src = valid ? p.bsrc + off + col : p.bsrc;
-          cp_async_16(bbase + j * 128 + ((c ^ (j & 7)) << 4), src, valid ? 16u : 0u);
+          const uint16_t* src = valid ? p.bsrc + off + t * p.I_ld + col : p.bsrc;
+          cp_async_16(bbase + t * b_bytes + j * 128 + ((c ^ (j & 7)) << 4), src, valid ? 16u : 0u);
         }
         cp_async_commit();
         ++pending;
-        if (pending > kGatherLag) {
-          cp_async_wait<kGatherLag>();
+        if (pending > lag) {
+          if (lag >= 2) cp_async_wait<2>(); else cp_async_wait<1>();
           fence_proxy_async();
           mbar_arrive(&full[arr_stage]);
           if (++arr_stage == S) arr_stage = 0;

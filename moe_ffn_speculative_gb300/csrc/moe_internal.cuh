@@ -59,7 +59,7 @@ constexpr int kHalfRows = 128;
 constexpr int kTileBytesA = kHalfRows * kBlockK * 2;  // one half, bf16: 16 KB
 constexpr int kGemmThreads = 224;                     // 7 warps
 constexpr int kMaxStages = 8;
-constexpr int kGatherLag = 2;                         // cp.async groups in flight
+constexpr int kGatherLag = 2;                         // cp.async groups in flight (<= stages - 1)
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -73,7 +73,7 @@ __host__ __device__ inline void group_geometry(int phase, int count, int idim, i
 struct GemmParams {
   const GroupEntry* groups;
   const GemmHeader* header;
-  const uint16_t* bsrc;        // gate_up: x [T,H]; down: h [rows, I_ld]
+  const uint16_t* bsrc;        // gate_up: x [T,H]; down: h [rows, 2*I_ld] (hi, lo)
   const int32_t* sorted_pair;  // [T*K]
   int T, K, TK, H, I_ld;
   int n_max;                   // token tile width, multiple of 16, <= 256
@@ -81,7 +81,7 @@ struct GemmParams {
   int nbuf;                    // TMEM accumulator buffers (1 or 2)
   uint32_t tmem_cols;
   float swiglu_limit;
-  uint16_t* h;                 // gate_up output [T*K + T, I_ld] bf16
+  uint16_t* h;                 // gate_up output [T*K + T, 2*I_ld] bf16 hi | lo
   float* out_ws;               // down output [T*K + T, H] fp32 (weighted)
   uint16_t* y;                 // down output when direct_y: [T, H] bf16
   int direct_y;

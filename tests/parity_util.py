@@ -75,3 +75,53 @@ def logits_bound(x64, gate64):
     accumulated in fp32: H * 2^-24 * sum_h |x_h g_h| (per token, expert)."""
     H = x64.shape[1]
     return H * 2.0 ** -24 * (np.abs(x64) @ np.abs(gate64).T)
+
+
+def bf(a):
+    """Round to bf16 (nearest even) and back to float64."""
+    return torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def bf_pair(a):
+    """The compensated pair hi + lo of bf16 that carries h between the GEMMs."""
+    hi = bf(a)
+    return hi + bf(a - hi)
+
+
+def output_rounding_error(y_ref):
+    """rel-RMS error of rounding the exact output to bf16 alone."""
+    return float(np.abs(bf(y_ref) - y_ref).max() / np.sqrt(np.mean(y_ref ** 2)))
+
+
+def report(**kw):
+    """Append one parity record to $MOE_PARITY_REPORT (a JSON-lines file)."""
+    import json
+    import os
+    path = os.environ.get("MOE_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(kw) + "\n")
+
+
+def bf16_floor_error(d, cfg: LayerConfig, rows, idx_rows, w_rows, y_ref):
+    """rel-RMS error that the roundings the path prescribes -- h carried as a
+    bf16 hi + lo pair between the GEMMs, the output y in bf16 -- produce on
+    their own (everything else exact, fp64)."""
+
+    x = np64(d["x"][rows])
+    ye = np.zeros_like(y_ref)
+    for e in np.unique(idx_rows):
+        wgu, wd = np64(d["w_gate_up"][int(e)]), np64(d["w_down"][int(e)])
+        rr, kk = np.nonzero(idx_rows == e)
+        gu = x[rr] @ wgu.T
+        i = wgu.shape[0] // 2
+        h = bf_pair(O.swiglu(gu[:, :i], gu[:, i:], cfg.swiglu_limit))
+        ye[rr] += w_rows[rr, kk][:, None] * (h @ wd.T)
+    if d.get("sh_gate_up") is not None:
+        sgu, sd = np64(d["sh_gate_up"]), np64(d["sh_down"])
+        gu = x @ sgu.T
+        i = sgu.shape[0] // 2
+        hs = bf_pair(O.swiglu(gu[:, :i], gu[:, i:], cfg.swiglu_limit))
+        ye += O.shared_gate(x, np64(d.get("sh_gate")))[:, None] * (hs @ sd.T)
+    ye = bf(ye)
+    return float(np.abs(ye - y_ref).max() / np.sqrt(np.mean(y_ref ** 2)))
