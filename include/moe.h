@@ -117,6 +117,31 @@ MOE_API moe_status moe_route(const moe_bf16* x, int T, int H, const moe_bf16* ga
                      int32_t* topk_idx, float* topk_w,
                      void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* moe_route() without a workspace, for callers that cannot allocate device
+ * memory when they call it (a serving engine whose pool has reserved the whole
+ * device up front, code that must not re-enter its allocator, a plain C
+ * caller with no device allocator).  The pages have no counterpart: this is a
+ * packaging variant of moe_route().
+ *   Same arguments and results as moe_route() minus ws / ws_bytes.
+ *   Scratch: one file-scope device array of about 1.1 MB inside the library
+ *     (token-block counters and the [T,E] fp32 logits), held on every GPU that
+ *     loads the library until the process exits.  No cudaMalloc / cudaFree or
+ *     other allocating call is made.
+ *   Limits: T <= MOE_NOALLOC_MAX_TOKENS and T*E <= MOE_NOALLOC_MAX_LOGITS,
+ *     else MOE_ERR_UNSUPPORTED before anything runs.
+ *   The first call on each device looks the array's device address up
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   Every call shares the one array: the call clears its counters (they must
+ *     start at zero) on `stream`, and two calls that may overlap on the GPU
+ *     (other streams, other host threads) race on it. */
+#define MOE_NOALLOC_MAX_TOKENS 4096
+#define MOE_NOALLOC_MAX_LOGITS 262144
+MOE_API moe_status moe_route_noalloc(const moe_bf16* x, int T, int H, const moe_bf16* gate,
+                                     const float* router_bias, const float* expert_bias,
+                                     const moe_recipe* recipe, float* logits_out,
+                                     int32_t* topk_idx, float* topk_w, cudaStream_t stream);
+
 /* Router steps score -> select -> routing_weights on given fp32 logits [T,E]
  * (the same logits fed to another implementation give the same selection).
  * Needs no workspace. */

@@ -65,6 +65,7 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_route_workspace_bytes": (_SZ, [_I, _I]),
     "moe_route": (_I, [_P, _I, _I, _P, _P, _P, ctypes.POINTER(Recipe), _P, _P, _P, _P, _SZ, _P]),
+    "moe_route_noalloc": (_I, [_P, _I, _I, _P, _P, _P, ctypes.POINTER(Recipe), _P, _P, _P, _P]),
     "moe_route_from_logits": (_I, [_P, _I, _P, ctypes.POINTER(Recipe), _P, _P, _P]),
     "moe_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_ffn_workspace_bytes": (_SZ, [_I, _I, _I, _I, ctypes.POINTER(Recipe)]),
@@ -175,6 +176,23 @@ def moe_route(x, gate, recipe: Recipe, router_bias=None, expert_bias=None, ws: W
     _check(lib().moe_route(_ptr(_u16(x)), T, H, _ptr(_u16(gate)), _ptr(router_bias), _ptr(expert_bias),
                            ctypes.byref(recipe), _ptr(logits), _ptr(idx), _ptr(w), ws.ptr(), ws.nbytes,
                            _stream(stream)), "moe_route")
+    return idx, w, logits
+
+
+def moe_route_noalloc(x, gate, recipe: Recipe, router_bias=None, expert_bias=None, want_logits=True,
+                      stream=None):
+    """moe_route with the library's fixed scratch array instead of a workspace.
+    -> (topk_idx int32 [T,K], topk_w fp32 [T,K], logits fp32 [T,E] or None)."""
+    _need_cuda(x, gate, router_bias, expert_bias)
+    T, H = x.shape
+    E, K = recipe.num_experts, recipe.top_k
+    dev = x.device
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    w = torch.empty((T, K), dtype=torch.float32, device=dev)
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev) if want_logits else None
+    _check(lib().moe_route_noalloc(_ptr(_u16(x)), T, H, _ptr(_u16(gate)), _ptr(router_bias), _ptr(expert_bias),
+                                   ctypes.byref(recipe), _ptr(logits), _ptr(idx), _ptr(w), _stream(stream)),
+           "moe_route_noalloc")
     return idx, w, logits
 
 
