@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", default="qwen3_8b_dspark", choices=list(S.CONFIGS))
     ap.add_argument("--tokens", type=int, default=None, help="override T of the workload")
+    ap.add_argument("--experts", type=int, default=None, help="override E (small profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -133,8 +134,8 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- roofline helpers
 
 def algorithmic(cfg, counts_u: int):
-    """Bytes and FLOPs of one layer forward and of its gate_up GEMM, counting
-    only the touched experts' weights (each read once)."""
+    """Bytes and FLOPs of one layer forward and of its expert-GEMM launch,
+    counting only the touched experts' weights (each read once)."""
     T, H, I, E, K, Is = cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.shared_I
     gu_w = counts_u * 2 * I * H * 2 + 2 * Is * H * 2
     dn_w = counts_u * H * I * 2 + H * Is * 2
@@ -142,10 +143,13 @@ def algorithmic(cfg, counts_u: int):
     gate = E * H * 2 + (H * 2 if cfg.shared_gated else 0)
     biases = E * 4 * ((cfg.router_bias_std > 0) + (cfg.expert_bias_std > 0))
     layer_bytes = gu_w + dn_w + act + gate + biases
-    gu_bytes = gu_w + T * H * 2 + (T * K + (T if Is else 0)) * max(I, Is) * 2
+    rows = T * K + (T if Is else 0)
+    # experts launch: both projections' weights once, x gathered, h (hi and lo)
+    # written and read back, the weighted outputs written (fp32 rows, or bf16 y)
+    out = rows * H * 4 if (K > 1 or Is) else T * H * 2
+    ex_bytes = gu_w + dn_w + T * H * 2 + 2 * rows * max(I, Is) * 2 * 2 + out
     flops = T * K * 6 * H * I + (T * 6 * H * Is if Is else 0) + 2 * T * H * E
-    gu_flops = T * K * 4 * H * I + (T * 4 * H * Is if Is else 0)
-    return layer_bytes, gu_bytes, flops, gu_flops
+    return layer_bytes, ex_bytes, flops
 
 
 def measured_peaks():
@@ -158,9 +162,9 @@ def measured_peaks():
 
 
 def ncu_traffic(workload: str):
-    """Per-launch DRAM traffic of the gate_up GEMM from the committed ncu
+    """Per-launch DRAM traffic of the expert-GEMM kernel from the committed ncu
     summary, or None when the kernel source changed since the capture."""
-    path = os.path.join(ROOT, "profiles", f"gate_up_gemm_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"experts_kernel_{workload}.md")
     if not os.path.exists(path):
         return None
     with open(path) as f:
@@ -329,7 +333,7 @@ def run_gpu(args, cfg, rank, world):
 
     # per-kernel durations (eager launches, events around every kernel)
     n_prof = min(K, 400)
-    n_k = 4
+    n_k = 3
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * n_k)] for _ in range(n_prof)]
     for row in evs:  # torch creates the CUDA event on its first record
         for e in row:
@@ -341,8 +345,8 @@ def run_gpu(args, cfg, rank, world):
             fwd(i)
     ops.set_profile_events(None)
     torch.cuda.synchronize()
-    names = ["router", "gate_up_gemm", "down_gemm", "combine"]
-    launched = 4 if (cfg.K > 1 or cfg.shared_I > 0) else 3
+    names = ["router", "experts", "combine"]
+    launched = 3 if (cfg.K > 1 or cfg.shared_I > 0) else 2
     per_kernel = {}
     for k in range(launched):
         per_kernel[names[k]] = float(np.mean([e[2 * k].elapsed_time(e[2 * k + 1]) for e in evs])) * 1e3  # us
@@ -373,12 +377,13 @@ def run_gpu(args, cfg, rank, world):
         raise SystemExit(f"device status {st} ({info}) after the timed region")
 
     hbm, tflops, peak_src = measured_peaks()
-    layer_bytes, gu_bytes, flops, gu_flops = algorithmic(cfg, u)
-    t_gu = per_kernel["gate_up_gemm"] * 1e-6
-    achieved = gu_bytes / t_gu / 1e9
+    layer_bytes, ex_bytes, flops = algorithmic(cfg, u)
+    t_ex = per_kernel["experts"] * 1e-6
+    achieved = ex_bytes / t_ex / 1e9
     layer_gbs = layer_bytes / (ms_step * 1e-3) / 1e9
     roof_layer_us = max(layer_bytes / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
-    traffic = ncu_traffic(cfg.name if args.tokens is None else f"{cfg.name}_T{cfg.T}")
+    traffic = ncu_traffic(cfg.name if args.tokens is None and args.experts is None else
+                          f"{cfg.name}_T{cfg.T}_E{cfg.E}")
 
     if rank != 0:
         return
@@ -391,9 +396,9 @@ def run_gpu(args, cfg, rank, world):
                    "shared_I": cfg.shared_I, "touched_experts": u, "launch": "cuda_graph_replay",
                    "l2": f"weights rotate over {n_copies} copies ({n_copies * cfg.weight_bytes / 1e9:.2f} GB) > L2",
                    "parallelism": "replicas" if world > 1 else "single_gpu"},
-        "roofline": {"bound": "hbm", "kernel": "gate_up_gemm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": traffic, "peak_source": peak_src,
-                     "algorithmic_bytes_per_launch": gu_bytes},
+        "roofline": {"bound": "hbm", "kernel": "moe_experts_kernel", "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic, "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": ex_bytes},
         "layer_roofline": {"bytes": layer_bytes, "flops": flops, "roofline_us": roof_layer_us,
                            "achieved_gbs": layer_gbs, "frac": roof_layer_us / (ms_step * 1e3)},
         "kernel_us": per_kernel,
@@ -412,6 +417,8 @@ def main():
     cfg = S.CONFIGS[args.config]
     if args.tokens is not None:
         cfg = cfg.with_(T=args.tokens)
+    if args.experts is not None:
+        cfg = cfg.with_(E=args.experts)
     rank, world = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, cfg, rank, world)

@@ -205,8 +205,9 @@ MOE_API moe_status moe_get_device_status(void* ws, cudaStream_t stream, int32_t*
 /* Profiling hook: when `events` is not NULL, moe_ffn_forward() records
  * events[2*i] / events[2*i+1] (cudaEvent_t) around its i-th kernel launch,
  * for i < n_pairs, on its stream.  Per calling thread; NULL turns it off.
- * The launch order is: router, gate_up GEMM, down GEMM, combine (the last is
- * skipped when K == 1 and there is no shared expert). */
+ * The launch order is: router, expert GEMMs (gate_up and down in one
+ * persistent launch), combine (skipped when K == 1 and there is no shared
+ * expert). */
 MOE_API void moe_set_profile_events(void* const* events, int n_pairs);
 
 #ifdef __cplusplus

@@ -106,9 +106,9 @@ RouterGeom router_geometry(int T, int E_tot, int sms) {
 
 struct Layout {
   RouterGeom rg;
-  int n_max, stages[2], nbuf, grid, I_ld;
+  int n_max, stages, nbuf, grid, I_ld;
   uint32_t tmem_cols;
-  size_t smem[2];
+  size_t smem;
   int max_gu_tiles, max_dn_tiles, g_max;
   bool need_out;
   size_t o_status, o_cnt, o_tiles, o_logits, o_shl, o_shw, o_idx, o_w, o_counts, o_offsets, o_sp, o_pp, o_groups,
@@ -124,12 +124,12 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(L.nbuf * 2 * L.n_max)) cols <<= 1;
   L.tmem_cols = cols;
-  for (int ph = 0; ph < 2; ++ph) {  // the down GEMM stages two token tiles (h hi and lo)
-    const int stage_bytes = 2 * kTileBytesA + (ph + 1) * L.n_max * 128;
-    L.stages[ph] = (kSmemLimit - 1024 - kCtrlBytes) / stage_bytes;
-    if (L.stages[ph] > kMaxStages) L.stages[ph] = kMaxStages;
-    L.smem[ph] = 1024 + static_cast<size_t>(L.stages[ph]) * stage_bytes + kCtrlBytes;
-  }
+  // a stage holds two 16 KB weight halves and two token tiles (the down GEMM
+  // reads h as hi and lo)
+  const int stage_bytes = 2 * kTileBytesA + 2 * L.n_max * 128;
+  L.stages = (kSmemLimit - 1024 - kCtrlBytes) / stage_bytes;
+  if (L.stages > kMaxStages) L.stages = kMaxStages;
+  L.smem = 1024 + static_cast<size_t>(L.stages) * stage_bytes + kCtrlBytes;
   L.grid = sms;
   const int Imax = Is > I ? Is : I;
   L.I_ld = ((Imax + 7) / 8) * 8;
@@ -149,7 +149,8 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   size_t o = 0;
   L.o_status = o; o += kAlign;
   L.o_cnt = o; o = align_up(o + 4 * (L.rg.n_tb + 1));
-  L.o_tiles = o; o = align_up(o + 4 * static_cast<size_t>(L.max_gu_tiles + L.max_dn_tiles));
+  // stream-K arrival counters (gate_up, down) and gate_up readiness counters
+  L.o_tiles = o; o = align_up(o + 4 * static_cast<size_t>(2 * L.max_gu_tiles + L.max_dn_tiles));
   L.o_logits = o; o = align_up(o + 4 * static_cast<size_t>(T) * E);
   L.o_shl = o; o = align_up(o + 4 * static_cast<size_t>(T));
   L.o_shw = o; o = align_up(o + 4 * static_cast<size_t>(T));
@@ -161,7 +162,7 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   L.o_pp = o; o = align_up(o + 4 * static_cast<size_t>(TK));
   L.o_groups = o; o = align_up(o + sizeof(GroupEntry) * static_cast<size_t>(L.g_max + 1));
   L.o_header = o; o = align_up(o + sizeof(GemmHeader));
-  L.o_partials = o; o = align_up(o + 4 * static_cast<size_t>(L.grid) * 2 * 2 * L.n_max * 128);
+  L.o_partials = o; o = align_up(o + 4 * static_cast<size_t>(L.grid) * 4 * 2 * L.n_max * 128);
   L.o_h = o; o = align_up(o + 2 * 2 * rows * L.I_ld);
   L.o_out = o;
   if (L.need_out) o = align_up(o + 4 * rows * H);
@@ -335,13 +336,13 @@ moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf1
   rp.sorted_pair = sorted_pair; rp.pair_pos = pair_pos;
   rp.groups = groups; rp.header = header;
   rp.I = I; rp.Is = Is; rp.n_max = L.n_max;
-  rp.zero_ptr = tiles; rp.zero_count = L.max_gu_tiles + L.max_dn_tiles;
+  rp.zero_ptr = tiles; rp.zero_count = 2 * L.max_gu_tiles + L.max_dn_tiles;
   record_event_on(0, stream);
   cudaError_t e = launch_route(rp, L.rg.tb, stream);
   record_event_on(1, stream);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-  // ---- 2./3. grouped GEMMs
+  // ---- 2. both grouped GEMMs, one persistent cooperative launch
   CUtensorMap tm_gu, tm_gu_sh, tm_dn, tm_dn_sh;
   if (!encode_weights_3d(&tm_gu, w_gate_up, H, I, 2ull * E) || !encode_weights_3d(&tm_dn, w_down, I, H, E))
     return MOE_ERR_CUDA;
@@ -355,32 +356,27 @@ moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf1
   GemmParams gp;
   memset(&gp, 0, sizeof(gp));
   gp.groups = groups; gp.header = header; gp.sorted_pair = sorted_pair;
+  gp.x = x; gp.h = h;
   gp.T = T; gp.K = K; gp.TK = T * K; gp.H = H; gp.I_ld = L.I_ld;
-  gp.n_max = L.n_max; gp.stages = L.stages[0]; gp.nbuf = L.nbuf; gp.tmem_cols = L.tmem_cols;
+  gp.n_max = L.n_max; gp.stages = L.stages; gp.nbuf = L.nbuf; gp.tmem_cols = L.tmem_cols;
   gp.swiglu_limit = recipe->swiglu_limit;
-  gp.h = h; gp.out_ws = out_ws; gp.y = y; gp.direct_y = L.need_out ? 0 : 1;
+  gp.out_ws = out_ws; gp.y = y; gp.direct_y = L.need_out ? 0 : 1;
   gp.topk_w = wts; gp.sh_w = (Is > 0 && sh_gate) ? sh_w : nullptr;
   gp.partials = reinterpret_cast<float*>(w + L.o_partials);
   gp.status = status;
-  gp.bsrc = x;
-  gp.tile_counters = tiles;
+  gp.tile_counters_gu = tiles;
+  gp.tile_counters_dn = tiles + L.max_gu_tiles;
+  gp.ready = tiles + L.max_gu_tiles + L.max_dn_tiles;
   record_event_on(2, stream);
-  e = launch_gemm(0, tm_gu, tm_gu_sh, gp, L.grid, L.smem[0], stream);
+  e = launch_experts(tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, gp, L.grid, L.smem, stream);
   record_event_on(3, stream);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  gp.bsrc = h;
-  gp.stages = L.stages[1];
-  gp.tile_counters = tiles + L.max_gu_tiles;
-  record_event_on(4, stream);
-  e = launch_gemm(1, tm_dn, tm_dn_sh, gp, L.grid, L.smem[1], stream);
-  record_event_on(5, stream);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   // ---- 4. weighted combine (+ shared expert)
   if (L.need_out) {
-    record_event_on(6, stream);
+    record_event_on(4, stream);
     e = launch_combine(out_ws, pair_pos, T, K, H, Is > 0 ? 1 : 0, y, stream);
-    record_event_on(7, stream);
+    record_event_on(5, stream);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   return MOE_OK;

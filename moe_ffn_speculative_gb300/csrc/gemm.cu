@@ -18,6 +18,10 @@
 // A tile cut by a CTA boundary is finished by whichever of its CTAs arrives
 // last, which sums the partial accumulators in CTA order (deterministic).
 //
+// Both GEMMs run in one persistent launch: each CTA streams its share of the
+// gate_up iterations, then its share of the down iterations; a down tile's
+// token rows are gathered once the gate_up tiles that write them signal.
+//
 // Warp roles (224 threads): warp 0 issues the weight TMA loads, warp 1
 // allocates TMEM and issues the MMAs, warp 2 gathers the token rows with
 // cp.async into the 128-byte-swizzled B tile, warps 3..6 drain TMEM in the
@@ -41,6 +45,7 @@ __device__ __forceinline__ void record_failure(int32_t* status, volatile int* ab
 struct Seg {
   int expert, row_base, count, idim;
   int m, n, k0, len, kb, tile, n_cnt;
+  int ready_idx;  // readiness counter of (expert group, token block) = its first gate_up tile + n
   long long tile_iter0;
 };
 
@@ -89,6 +94,7 @@ struct Sched {
     s.tile = (phase == 0 ? ge.gu_tile : ge.dn_tile) + tile_in;
     s.tile_iter0 = start + static_cast<long long>(tile_in) * kb;
     s.n_cnt = min(n_max, ge.count - s.n * n_max);
+    s.ready_idx = ge.gu_tile + s.n;
     it += len;
     return true;
   }
@@ -171,47 +177,405 @@ __device__ __forceinline__ void u32_to_f32(const uint32_t (&u)[16], float (&f)[1
   for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(u[i]);
 }
 
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Position in the ring of shared-memory stages (each role keeps its own).
+struct Ring {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ void next(int S) {
+    if (++stage == S) { stage = 0; phase ^= 1u; }
+  }
+};
+
+// The CTA's shared memory: S stages of [A gate|A up or two 128-row output
+// halves (16 KB each) | B tile (n_max x 64 bf16) | second B tile (h_lo)],
+// then barriers and small control words.
+struct Smem {
+  uint8_t* base;
+  uint32_t stage_bytes, b_bytes;
+  int S;
+  uint64_t *full, *empty, *accf, *acce, *drain;
+  volatile int* abort_flag;
+  int* bcast;
+  int* s_ok;
+  long long* rowoff;
+};
+
+// ---------------------------------------------------------------- TMA producer (weights)
+// One CTA's weight k-blocks in the order it consumes them: its gate_up span,
+// then its down span.
+struct WeightCursor {
+  Sched sc0, sc1;
+  Seg sg;
+  int ph, kk;
+  bool valid;
+
+  __device__ void init(const GemmParams& p, int ngroups, long long b0, long long e0, long long b1, long long e1) {
+    sc0.init(p.groups, ngroups, 0, p.H, p.n_max, b0, e0);
+    sc1.init(p.groups, ngroups, 1, p.H, p.n_max, b1, e1);
+    ph = 0;
+    kk = 0;
+    valid = false;
+    next_segment();
+  }
+  __device__ void next_segment() {
+    while (ph < 2) {
+      if (ph == 0 ? sc0.next(sg) : sc1.next(sg)) {
+        kk = 0;
+        valid = true;
+        return;
+      }
+      ++ph;
+    }
+    valid = false;
+  }
+  __device__ void step() {
+    if (++kk >= sg.len) next_segment();
+  }
+  // tensor map and box coordinates of half h of the current k-block
+  __device__ const CUtensorMap* box(const CUtensorMap* tm_gu, const CUtensorMap* tm_gu_sh, const CUtensorMap* tm_dn,
+                                    const CUtensorMap* tm_dn_sh, int h, int& c0, int& c1, int& c2) const {
+    const int plane = sg.expert >= 0 ? sg.expert : 0;
+    c0 = (sg.k0 + kk) * kBlockK;
+    if (ph == 0) {
+      c1 = sg.m * kHalfRows;
+      c2 = 2 * plane + h;
+    } else {
+      c1 = sg.m * 2 * kHalfRows + h * kHalfRows;
+      c2 = plane;
+    }
+    if (ph == 0) return sg.expert >= 0 ? tm_gu : tm_gu_sh;
+    return sg.expert >= 0 ? tm_dn : tm_dn_sh;
+  }
+};
+
+__device__ bool produce(const Smem& sm, const GemmParams& p, int ngroups, long long b0, long long e0, long long b1,
+                        long long e1, const CUtensorMap* tm_gu, const CUtensorMap* tm_gu_sh,
+                        const CUtensorMap* tm_dn, const CUtensorMap* tm_dn_sh, Ring& ring, int32_t* status) {
+  WeightCursor ld;
+  ld.init(p, ngroups, b0, e0, b1, e1);
+  while (ld.valid) {
+    if (!mbar_wait(&sm.empty[ring.stage], ring.phase ^ 1u, sm.abort_flag)) {
+      record_failure(status, sm.abort_flag, kInfoEmpty);
+      return false;
+    }
+    uint8_t* a0 = sm.base + ring.stage * sm.stage_bytes;
+    uint64_t* bar = &sm.full[ring.stage];
+    mbar_arrive_expect_tx(bar, 2 * kTileBytesA);
+    int c0, c1, c2;
+    for (int h = 0; h < 2; ++h) {
+      const CUtensorMap* tm = ld.box(tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, h, c0, c1, c2);
+      tma_load_3d(a0 + h * kTileBytesA, tm, bar, c0, c1, c2);
+    }
+    ld.step();
+    ring.next(sm.S);
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- MMA issuer (one thread)
 template <int PHASE>
+__device__ bool issue_mma(const Smem& sm, const GemmParams& p, int ngroups, long long begin, long long end,
+                          uint32_t tmem_base, Ring& ring, int& seg_i, int32_t* status) {
+  Sched sc;
+  sc.init(p.groups, ngroups, PHASE, p.H, p.n_max, begin, end);
+  Seg sg;
+  while (sc.next(sg)) {
+    const int buf = seg_i % p.nbuf;
+    const uint32_t use = static_cast<uint32_t>(seg_i / p.nbuf);
+    if (!mbar_wait(&sm.acce[buf], (use & 1u) ^ 1u, sm.abort_flag)) {
+      record_failure(status, sm.abort_flag, kInfoAccEmpty);
+      return false;
+    }
+    tc_fence_after();
+    const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * 2 * p.n_max);
+    const uint32_t d1 = d0 + static_cast<uint32_t>(p.n_max);
+    const int nmma = max(16, (sg.n_cnt + 15) & ~15);
+    const uint32_t idesc = idesc_bf16(kHalfRows, nmma);
+    for (int kk = 0; kk < sg.len; ++kk) {
+      if (!mbar_wait(&sm.full[ring.stage], ring.phase, sm.abort_flag)) {
+        record_failure(status, sm.abort_flag, kInfoFull);
+        return false;
+      }
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(sm.base + ring.stage * sm.stage_bytes);
+      const uint32_t a1 = a0 + kTileBytesA;
+      const uint32_t bb = a0 + 2 * kTileBytesA;
+#pragma unroll
+      for (int ks = 0; ks < kBlockK / 16; ++ks) {
+        const uint32_t acc = (kk > 0 || ks > 0) ? 1u : 0u;
+        const uint64_t bd = sw128_desc(bb + ks * 32);
+        const uint64_t ad0 = sw128_desc(a0 + ks * 32), ad1 = sw128_desc(a1 + ks * 32);
+        mma_bf16(d0, ad0, bd, idesc, acc);
+        mma_bf16(d1, ad1, bd, idesc, acc);
+        if (PHASE == 1) {  // + W * h_lo
+          const uint64_t bl = sw128_desc(bb + sm.b_bytes + ks * 32);
+          mma_bf16(d0, ad0, bl, idesc, 1u);
+          mma_bf16(d1, ad1, bl, idesc, 1u);
+        }
+      }
+      mma_commit(&sm.empty[ring.stage]);
+      ring.next(sm.S);
+    }
+    mma_commit(&sm.accf[buf]);
+    ++seg_i;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- token-row gather (B), one warp
+// gate_up: rows of x for the expert's tokens; down: the expert's h rows (hi and
+// lo), after the gate_up tiles that write them have signalled.
+template <int PHASE>
+__device__ bool gather(const Smem& sm, const GemmParams& p, int ngroups, long long begin, long long end, Ring& ring,
+                       int& pending, int& arr_stage, int lag, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  Sched sc;
+  sc.init(p.groups, ngroups, PHASE, p.H, p.n_max, begin, end);
+  constexpr int kBTiles = PHASE == 0 ? 1 : 2;
+  const uint16_t* bsrc = PHASE == 0 ? p.x : p.h;
+  Seg sg;
+  while (sc.next(sg)) {
+    const int nrows = max(16, (sg.n_cnt + 15) & ~15);
+    const int kdim = PHASE == 0 ? p.H : sg.idim;
+    __syncwarp();
+    for (int j = lane; j < nrows; j += 32) {
+      long long off = -1;
+      if (j < sg.n_cnt) {
+        const int r = sg.n * p.n_max + j;
+        if (PHASE == 0) {
+          const int tok = sg.expert >= 0 ? __ldg(p.sorted_pair + sg.row_base + r) / p.K : r;
+          off = static_cast<long long>(tok) * p.H;
+        } else {
+          off = static_cast<long long>(sg.row_base + r) * (2 * p.I_ld);
+        }
+      }
+      sm.rowoff[j] = off;
+    }
+    if (PHASE == 1) {
+      // h of this (expert, token block) is complete once every gate_up tile
+      // of it has signalled
+      const int target = ceil_div(sg.idim, kHalfRows);
+      const int32_t* rp = p.ready + sg.ready_idx;
+      int ready = lane == 0 ? (ld_acquire_gpu(rp) >= target) : 0;
+      ready = __shfl_sync(0xffffffffu, ready, 0);
+      if (!ready) {
+        // Release every stage this warp still holds first: the missing tiles
+        // may be this CTA's own last gate_up tiles, whose MMAs wait on them.
+        cp_async_wait<0>();
+        fence_proxy_async();
+        while (pending > 0) {
+          mbar_arrive(&sm.full[arr_stage]);
+          if (++arr_stage == sm.S) arr_stage = 0;
+          --pending;
+        }
+        int okr = 1;
+        if (lane == 0) {
+          const long long t0 = clock64();
+          while (ld_acquire_gpu(rp) < target) {
+            if (*sm.abort_flag || clock64() - t0 > kWaitLimitCycles) { okr = 0; break; }
+            __nanosleep(64);
+          }
+        }
+        okr = __shfl_sync(0xffffffffu, okr, 0);
+        if (!okr) {
+          if (lane == 0) record_failure(status, sm.abort_flag, kInfoReady);
+          return false;
+        }
+      }
+    }
+    __syncwarp();
+    for (int kk = 0; kk < sg.len; ++kk) {
+      const int kx = (sg.k0 + kk) * kBlockK;
+      const bool got = mbar_wait(&sm.empty[ring.stage], ring.phase ^ 1u, sm.abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) record_failure(status, sm.abort_flag, kInfoGatherEmpty);
+        return false;
+      }
+      const uint32_t bbase = smem_u32(sm.base + ring.stage * sm.stage_bytes) + 2 * kTileBytesA;
+      for (int q = lane; q < nrows * 8 * kBTiles; q += 32) {
+        const int t = (kBTiles == 2 && q >= nrows * 8) ? 1 : 0;  // 0: x or h_hi, 1: h_lo
+        const int qq = q - t * nrows * 8;
+        const int j = qq >> 3, c = qq & 7;
+        const long long off = sm.rowoff[j];
+        const int col = kx + c * 8;
+        const bool valid = off >= 0 && col < kdim;
+        const uint16_t* src = valid ? bsrc + off + t * p.I_ld + col : bsrc;
+        cp_async_16(bbase + t * sm.b_bytes + j * 128 + ((c ^ (j & 7)) << 4), src, valid ? 16u : 0u);
+      }
+      cp_async_commit();
+      ++pending;
+      if (pending > lag) {
+        if (lag >= 2) cp_async_wait<2>(); else cp_async_wait<1>();
+        fence_proxy_async();
+        mbar_arrive(&sm.full[arr_stage]);
+        if (++arr_stage == sm.S) arr_stage = 0;
+        --pending;
+      }
+      ring.next(sm.S);
+    }
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- epilogue (4 warps)
+template <int PHASE>
+__device__ bool epilogue(const Smem& sm, const GemmParams& p, int ngroups, long long begin, long long end,
+                         long long total, uint32_t tmem_base, int& seg_i, int32_t* tile_counters, int32_t* status) {
+  Sched sc;
+  sc.init(p.groups, ngroups, PHASE, p.H, p.n_max, begin, end);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = warp & 3;
+  const int r = quad * 32 + lane;  // accumulator row = TMEM lane
+  const bool leader = (warp == 3 && lane == 0);
+  const long long grid = gridDim.x;
+  Seg sg;
+  while (sc.next(sg)) {
+    const int buf = seg_i % p.nbuf;
+    const uint32_t use = static_cast<uint32_t>(seg_i / p.nbuf);
+    // one thread waits, the four warps leave or go on together
+    if (leader) {
+      const bool got = mbar_wait(&sm.accf[buf], use & 1u, sm.abort_flag);
+      if (!got) record_failure(status, sm.abort_flag, kInfoAccFull);
+      *sm.s_ok = got ? 1 : 0;
+    }
+    epi_sync();
+    if (!*reinterpret_cast<volatile int*>(sm.s_ok)) return false;
+    tc_fence_after();
+    const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                          static_cast<uint32_t>(buf * 2 * p.n_max);
+    const bool whole = (sg.k0 == 0 && sg.len == sg.kb);
+    bool done = false;  // this CTA finished the tile's output
+    uint32_t ua[16], ub[16];
+    float fa[16], fb[16];
+    if (whole) {
+      for (int j0 = 0; j0 < sg.n_cnt; j0 += 16) {
+        tmem_ld16(tacc + j0, ua);
+        tmem_ld16(tacc + p.n_max + j0, ub);
+        tmem_ld_wait();
+        u32_to_f32(ua, fa);
+        u32_to_f32(ub, fb);
+        finish_chunk<PHASE>(p, sg, r, j0, fa, fb);
+      }
+      tc_fence_before();
+      mbar_arrive(&sm.acce[buf]);
+      done = true;
+    } else {
+      const int slot = PHASE * 2 + ((begin >= sg.tile_iter0) ? 0 : 1);
+      float* mine = p.partials + static_cast<size_t>(blockIdx.x * 4 + slot) * 2 * p.n_max * 128;
+      for (int j0 = 0; j0 < sg.n_cnt; j0 += 16) {
+        tmem_ld16(tacc + j0, ua);
+        tmem_ld16(tacc + p.n_max + j0, ub);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (j0 + i < sg.n_cnt) {
+            __stcg(mine + static_cast<size_t>(j0 + i) * 128 + r, __uint_as_float(ua[i]));
+            __stcg(mine + static_cast<size_t>(p.n_max + j0 + i) * 128 + r, __uint_as_float(ub[i]));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sm.acce[buf]);
+      __threadfence();
+      epi_sync();
+      if (leader) {
+        const int old = atomicAdd(tile_counters + sg.tile, sg.len);
+        const int last = (old + sg.len == sg.kb);
+        if (last) atomicExch(tile_counters + sg.tile, 0);
+        *sm.bcast = last;
+      }
+      epi_sync();
+      if (*reinterpret_cast<volatile int*>(sm.bcast)) {
+        __threadfence();
+        const int c0 = cta_of(sg.tile_iter0, total, grid);
+        const int c1 = cta_of(sg.tile_iter0 + sg.kb - 1, total, grid);
+        for (int j0 = 0; j0 < sg.n_cnt; j0 += 16) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) { fa[i] = 0.f; fb[i] = 0.f; }
+          for (int c = c0; c <= c1; ++c) {
+            const long long bc = cta_begin(c, total, grid);
+            if (bc == cta_begin(c + 1, total, grid)) continue;  // CTA with an empty range
+            const int sl = PHASE * 2 + ((bc >= sg.tile_iter0) ? 0 : 1);
+            const float* pp = p.partials + static_cast<size_t>(c * 4 + sl) * 2 * p.n_max * 128;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              if (j0 + i < sg.n_cnt) {
+                fa[i] += __ldcg(pp + static_cast<size_t>(j0 + i) * 128 + r);
+                fb[i] += __ldcg(pp + static_cast<size_t>(p.n_max + j0 + i) * 128 + r);
+              }
+            }
+          }
+          finish_chunk<PHASE>(p, sg, r, j0, fa, fb);
+        }
+        done = true;
+      }
+    }
+    if (PHASE == 0 && done) {
+      // this gate_up tile's h rows are written: count it towards its
+      // (expert, token block)
+      __threadfence();
+      epi_sync();
+      if (leader) atomicAdd(p.ready + sg.ready_idx, 1);
+    }
+    epi_sync();
+    ++seg_i;
+  }
+  return true;
+}
+
+// One persistent CTA per SM runs the gate_up GEMM over its share of the
+// gate_up k-block iterations, then the down GEMM over its share of the down
+// iterations.  The launch is cooperative (every CTA resident), so the down
+// phase's bounded waits on the gate_up tiles of other CTAs always resolve.
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_routed, const __grid_constant__ CUtensorMap tm_shared,
-                    const GemmParams p) {
+    moe_experts_kernel(const __grid_constant__ CUtensorMap tm_gu, const __grid_constant__ CUtensorMap tm_gu_sh,
+                       const __grid_constant__ CUtensorMap tm_dn, const __grid_constant__ CUtensorMap tm_dn_sh,
+                       const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const int S = p.stages;
-  constexpr int kBTiles = PHASE == 0 ? 1 : 2;  // down: B = h_hi and h_lo
-  const uint32_t b_bytes = p.n_max * 128;
-  const uint32_t stage_bytes = 2 * kTileBytesA + kBTiles * b_bytes;
-  uint8_t* ctrl = smem + S * stage_bytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
-  uint64_t* empty = full + kMaxStages;
-  uint64_t* accf = empty + kMaxStages;
-  uint64_t* acce = accf + 2;
-  uint64_t* drain = acce + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* bcast = reinterpret_cast<int*>(tmem_slot + 2);
-  int* s_ok = reinterpret_cast<int*>(tmem_slot + 3);
-  long long* rowoff = reinterpret_cast<long long*>(ctrl + 256);
+  Smem sm;
+  sm.base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  sm.S = p.stages;
+  sm.b_bytes = p.n_max * 128;
+  sm.stage_bytes = 2 * kTileBytesA + 2 * sm.b_bytes;
+  uint8_t* ctrl = sm.base + sm.S * sm.stage_bytes;
+  sm.full = reinterpret_cast<uint64_t*>(ctrl);
+  sm.empty = sm.full + kMaxStages;
+  sm.accf = sm.empty + kMaxStages;
+  sm.acce = sm.accf + 2;
+  sm.drain = sm.acce + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm.drain + 1);
+  sm.abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  sm.bcast = reinterpret_cast<int*>(tmem_slot + 2);
+  sm.s_ok = reinterpret_cast<int*>(tmem_slot + 3);
+  sm.rowoff = reinterpret_cast<long long*>(ctrl + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1 + 32);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < sm.S; ++s) {
+      mbar_init(&sm.full[s], 1 + 32);
+      mbar_init(&sm.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&accf[b], 1);
-      mbar_init(&acce[b], 128);
+      mbar_init(&sm.accf[b], 1);
+      mbar_init(&sm.acce[b], 128);
     }
-    mbar_init(drain, 1);
-    *abort_flag = 0;
-    *bcast = 0;
+    mbar_init(sm.drain, 1);
+    *sm.abort_flag = 0;
+    *sm.bcast = 0;
     fence_barrier_init();
     fence_proxy_async();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_routed);
-    tma_prefetch_desc(&tm_shared);
+    tma_prefetch_desc(&tm_gu);
+    tma_prefetch_desc(&tm_gu_sh);
+    tma_prefetch_desc(&tm_dn);
+    tma_prefetch_desc(&tm_dn_sh);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, p.tmem_cols);
@@ -223,42 +587,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const GemmHeader hd = *p.header;
-  const long long total = PHASE == 0 ? hd.gu_iters : hd.dn_iters;
   const long long grid = gridDim.x;
-  const long long begin = cta_begin(blockIdx.x, total, grid);
-  const long long end = cta_begin(blockIdx.x + 1, total, grid);
-  Sched sc;
-  sc.init(p.groups, hd.ngroups, PHASE, p.H, p.n_max, begin, end);
-  Seg sg;
+  const long long b0 = cta_begin(blockIdx.x, hd.gu_iters, grid), e0 = cta_begin(blockIdx.x + 1, hd.gu_iters, grid);
+  const long long b1 = cta_begin(blockIdx.x, hd.dn_iters, grid), e1 = cta_begin(blockIdx.x + 1, hd.dn_iters, grid);
+  const int ng = hd.ngroups;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer (weights)
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      while (ok && sc.next(sg)) {
-        const CUtensorMap* tm = sg.expert >= 0 ? &tm_routed : &tm_shared;
-        const int plane = sg.expert >= 0 ? sg.expert : 0;
-        for (int kk = 0; kk < sg.len; ++kk) {
-          const int kx = (sg.k0 + kk) * kBlockK;
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
-            record_failure(p.status, abort_flag, kInfoEmpty);
-            ok = false;
-            break;
-          }
-          uint8_t* a0 = smem + stage * stage_bytes;
-          mbar_arrive_expect_tx(&full[stage], 2 * kTileBytesA);
-          if (PHASE == 0) {
-            tma_load_3d(a0, tm, &full[stage], kx, sg.m * kHalfRows, 2 * plane);
-            tma_load_3d(a0 + kTileBytesA, tm, &full[stage], kx, sg.m * kHalfRows, 2 * plane + 1);
-          } else {
-            tma_load_3d(a0, tm, &full[stage], kx, sg.m * 2 * kHalfRows, plane);
-            tma_load_3d(a0 + kTileBytesA, tm, &full[stage], kx, sg.m * 2 * kHalfRows + kHalfRows, plane);
-          }
-          if (++stage == S) { stage = 0; phase ^= 1u; }
-        }
-      }
+      Ring ring;
+      const bool ok = produce(sm, p, ng, b0, e0, b1, e1, &tm_gu, &tm_gu_sh, &tm_dn, &tm_dn_sh, ring, p.status);
       if (!ok) {
         // let the loads already issued land before the CTA can exit
         const long long t0 = clock64();
@@ -266,210 +603,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int stage = 0, seg_i = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      while (ok && sc.next(sg)) {
-        const int buf = seg_i % p.nbuf;
-        const uint32_t use = static_cast<uint32_t>(seg_i / p.nbuf);
-        if (!mbar_wait(&acce[buf], (use & 1u) ^ 1u, abort_flag)) {
-          record_failure(p.status, abort_flag, kInfoAccEmpty);
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * 2 * p.n_max);
-        const uint32_t d1 = d0 + static_cast<uint32_t>(p.n_max);
-        const int nmma = max(16, (sg.n_cnt + 15) & ~15);
-        const uint32_t idesc = idesc_bf16(kHalfRows, nmma);
-        for (int kk = 0; kk < sg.len; ++kk) {
-          if (!mbar_wait(&full[stage], phase, abort_flag)) {
-            record_failure(p.status, abort_flag, kInfoFull);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + stage * stage_bytes);
-          const uint32_t a1 = a0 + kTileBytesA;
-          const uint32_t bb = a0 + 2 * kTileBytesA;
-#pragma unroll
-          for (int ks = 0; ks < kBlockK / 16; ++ks) {
-            const uint32_t acc = (kk > 0 || ks > 0) ? 1u : 0u;
-            const uint64_t bd = sw128_desc(bb + ks * 32);
-            const uint64_t ad0 = sw128_desc(a0 + ks * 32), ad1 = sw128_desc(a1 + ks * 32);
-            mma_bf16(d0, ad0, bd, idesc, acc);
-            mma_bf16(d1, ad1, bd, idesc, acc);
-            if (PHASE == 1) {  // + W * h_lo
-              const uint64_t bl = sw128_desc(bb + b_bytes + ks * 32);
-              mma_bf16(d0, ad0, bl, idesc, 1u);
-              mma_bf16(d1, ad1, bl, idesc, 1u);
-            }
-          }
-          mma_commit(&empty[stage]);
-          if (++stage == S) { stage = 0; phase ^= 1u; }
-        }
-        if (!ok) break;
-        mma_commit(&accf[buf]);
-        ++seg_i;
-      }
+      Ring ring;
+      int seg_i = 0;
+      if (issue_mma<0>(sm, p, ng, b0, e0, tmem_base, ring, seg_i, p.status))
+        issue_mma<1>(sm, p, ng, b1, e1, tmem_base, ring, seg_i, p.status);
       // every MMA issued above has completed once `drain` flips
-      mma_commit(drain);
-      if (!mbar_wait(drain, 0, nullptr)) record_failure(p.status, abort_flag, kInfoDrain);
+      mma_commit(sm.drain);
+      if (!mbar_wait(sm.drain, 0, nullptr)) record_failure(p.status, sm.abort_flag, kInfoDrain);
     }
   } else if (warp == 2) {
-    // ------------------------------------------------ token-row gather (B)
-    int stage = 0, arr_stage = 0, pending = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    const int K = p.K, H = p.H;
+    Ring ring;
+    int pending = 0, arr_stage = 0;
     // copies kept in flight before arriving; below the stage count, so the
     // stage this warp waits to refill never depends on an arrival it holds
-    const int lag = kGatherLag < S - 1 ? kGatherLag : S - 1;
-    while (ok && sc.next(sg)) {
-      const int nrows = max(16, (sg.n_cnt + 15) & ~15);
-      const int kdim = PHASE == 0 ? H : sg.idim;
-      __syncwarp();
-      for (int j = lane; j < nrows; j += 32) {
-        long long off = -1;
-        if (j < sg.n_cnt) {
-          const int r = sg.n * p.n_max + j;
-          if (PHASE == 0) {
-            const int tok = sg.expert >= 0 ? __ldg(p.sorted_pair + sg.row_base + r) / K : r;
-            off = static_cast<long long>(tok) * H;
-          } else {
-            off = static_cast<long long>(sg.row_base + r) * (2 * p.I_ld);
-          }
-        }
-        rowoff[j] = off;
-      }
-      __syncwarp();
-      for (int kk = 0; kk < sg.len; ++kk) {
-        const int kx = (sg.k0 + kk) * kBlockK;
-        const bool got = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
-        if (!__all_sync(0xffffffffu, got)) {
-          if (lane == 0) record_failure(p.status, abort_flag, kInfoGatherEmpty);
-          ok = false;
-          break;
-        }
-        const uint32_t bbase = smem_u32(smem + stage * stage_bytes) + 2 * kTileBytesA;
-        for (int q = lane; q < nrows * 8 * kBTiles; q += 32) {
-          const int t = (kBTiles == 2 && q >= nrows * 8) ? 1 : 0;  // 0: x or h_hi, 1: h_lo
-          const int qq = q - t * nrows * 8;
-          const int j = qq >> 3, c = qq & 7;
-          const long long off = rowoff[j];
-          const int col = kx + c * 8;
-          const bool valid = off >= 0 && col < kdim;
-          const uint16_t* src = valid ? p.bsrc + off + t * p.I_ld + col : p.bsrc;
-          cp_async_16(bbase + t * b_bytes + j * 128 + ((c ^ (j & 7)) << 4), src, valid ? 16u : 0u);
-        }
-        cp_async_commit();
-        ++pending;
-        if (pending > lag) {
-          if (lag >= 2) cp_async_wait<2>(); else cp_async_wait<1>();
-          fence_proxy_async();
-          mbar_arrive(&full[arr_stage]);
-          if (++arr_stage == S) arr_stage = 0;
-          --pending;
-        }
-        if (++stage == S) { stage = 0; phase ^= 1u; }
-      }
-    }
+    const int lag = kGatherLag < sm.S - 1 ? kGatherLag : sm.S - 1;
+    if (gather<0>(sm, p, ng, b0, e0, ring, pending, arr_stage, lag, p.status))
+      gather<1>(sm, p, ng, b1, e1, ring, pending, arr_stage, lag, p.status);
     cp_async_wait<0>();
     fence_proxy_async();
     while (pending > 0) {
-      mbar_arrive(&full[arr_stage]);
-      if (++arr_stage == S) arr_stage = 0;
+      mbar_arrive(&sm.full[arr_stage]);
+      if (++arr_stage == sm.S) arr_stage = 0;
       --pending;
     }
   } else {
-    // ------------------------------------------------ epilogue (warps 3..6)
-    const int quad = warp & 3;
-    const int r = quad * 32 + lane;  // accumulator row = TMEM lane
-    const bool leader = (warp == 3 && lane == 0);
     int seg_i = 0;
-    while (sc.next(sg)) {
-      const int buf = seg_i % p.nbuf;
-      const uint32_t use = static_cast<uint32_t>(seg_i / p.nbuf);
-      // one thread waits, the four warps leave or go on together
-      if (leader) {
-        const bool got = mbar_wait(&accf[buf], use & 1u, abort_flag);
-        if (!got) record_failure(p.status, abort_flag, kInfoAccFull);
-        *s_ok = got ? 1 : 0;
-      }
-      epi_sync();
-      if (!*reinterpret_cast<volatile int*>(s_ok)) break;
-      tc_fence_after();
-      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                            static_cast<uint32_t>(buf * 2 * p.n_max);
-      const bool whole = (sg.k0 == 0 && sg.len == sg.kb);
-      uint32_t ua[16], ub[16];
-      float fa[16], fb[16];
-      if (whole) {
-        for (int j0 = 0; j0 < sg.n_cnt; j0 += 16) {
-          tmem_ld16(tacc + j0, ua);
-          tmem_ld16(tacc + p.n_max + j0, ub);
-          tmem_ld_wait();
-          u32_to_f32(ua, fa);
-          u32_to_f32(ub, fb);
-          finish_chunk<PHASE>(p, sg, r, j0, fa, fb);
-        }
-        tc_fence_before();
-        mbar_arrive(&acce[buf]);
-      } else {
-        const int slot = (begin >= sg.tile_iter0) ? 0 : 1;
-        float* mine = p.partials + static_cast<size_t>(blockIdx.x * 2 + slot) * 2 * p.n_max * 128;
-        for (int j0 = 0; j0 < sg.n_cnt; j0 += 16) {
-          tmem_ld16(tacc + j0, ua);
-          tmem_ld16(tacc + p.n_max + j0, ub);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            if (j0 + i < sg.n_cnt) {
-              __stcg(mine + static_cast<size_t>(j0 + i) * 128 + r, __uint_as_float(ua[i]));
-              __stcg(mine + static_cast<size_t>(p.n_max + j0 + i) * 128 + r, __uint_as_float(ub[i]));
-            }
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(&acce[buf]);
-        __threadfence();
-        epi_sync();
-        if (leader) {
-          const int old = atomicAdd(p.tile_counters + sg.tile, sg.len);
-          const int last = (old + sg.len == sg.kb);
-          if (last) atomicExch(p.tile_counters + sg.tile, 0);
-          *bcast = last;
-        }
-        epi_sync();
-        const int last = *reinterpret_cast<volatile int*>(bcast);
-        if (last) {
-          __threadfence();
-          const int c0 = cta_of(sg.tile_iter0, total, grid);
-          const int c1 = cta_of(sg.tile_iter0 + sg.kb - 1, total, grid);
-          for (int j0 = 0; j0 < sg.n_cnt; j0 += 16) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) { fa[i] = 0.f; fb[i] = 0.f; }
-            for (int c = c0; c <= c1; ++c) {
-              const long long bc = cta_begin(c, total, grid);
-              if (bc == cta_begin(c + 1, total, grid)) continue;  // CTA with an empty range
-              const int sl = (bc >= sg.tile_iter0) ? 0 : 1;
-              const float* pp = p.partials + static_cast<size_t>(c * 2 + sl) * 2 * p.n_max * 128;
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                if (j0 + i < sg.n_cnt) {
-                  fa[i] += __ldcg(pp + static_cast<size_t>(j0 + i) * 128 + r);
-                  fb[i] += __ldcg(pp + static_cast<size_t>(p.n_max + j0 + i) * 128 + r);
-                }
-              }
-            }
-            finish_chunk<PHASE>(p, sg, r, j0, fa, fb);
-          }
-        }
-      }
-      epi_sync();
-      ++seg_i;
-    }
+    if (epilogue<0>(sm, p, ng, b0, e0, hd.gu_iters, tmem_base, seg_i, p.tile_counters_gu, p.status))
+      epilogue<1>(sm, p, ng, b1, e1, hd.dn_iters, tmem_base, seg_i, p.tile_counters_dn, p.status);
   }
 
   tc_fence_before();
@@ -505,20 +666,23 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 
 }  // namespace
 
-cudaError_t launch_gemm(int phase, const CUtensorMap& tm_routed, const CUtensorMap& tm_shared, const GemmParams& p,
-                        int grid, size_t smem_bytes, cudaStream_t s) {
-  if (phase == 0) {
-    cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes));
-    if (e != cudaSuccess) return e;
-    moe_gemm_kernel<0><<<grid, kGemmThreads, smem_bytes, s>>>(tm_routed, tm_shared, p);
-  } else {
-    cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes));
-    if (e != cudaSuccess) return e;
-    moe_gemm_kernel<1><<<grid, kGemmThreads, smem_bytes, s>>>(tm_routed, tm_shared, p);
-  }
-  return cudaGetLastError();
+cudaError_t launch_experts(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, const CUtensorMap& tm_dn,
+                           const CUtensorMap& tm_dn_sh, const GemmParams& p, int grid, size_t smem_bytes,
+                           cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(moe_experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem_bytes));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, moe_experts_kernel, tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, p);
 }
 
 cudaError_t launch_combine(const float* out_ws, const int32_t* pair_pos, int T, int K, int H, int has_shared,

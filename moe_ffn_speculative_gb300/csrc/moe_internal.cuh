@@ -16,7 +16,7 @@ enum : int32_t { kStatusTimeout = 5 };
 // info values: which wait ran out
 enum : int32_t {
   kInfoEmpty = 1, kInfoFull = 2, kInfoAccFull = 3, kInfoAccEmpty = 4,
-  kInfoGatherEmpty = 5, kInfoDrain = 6
+  kInfoGatherEmpty = 5, kInfoDrain = 6, kInfoReady = 7
 };
 
 // ----------------------------------------------------------------------------
@@ -73,7 +73,7 @@ __host__ __device__ inline void group_geometry(int phase, int count, int idim, i
 struct GemmParams {
   const GroupEntry* groups;
   const GemmHeader* header;
-  const uint16_t* bsrc;        // gate_up: x [T,H]; down: h [rows, 2*I_ld] (hi, lo)
+  const uint16_t* x;           // [T,H] (gate_up token rows)
   const int32_t* sorted_pair;  // [T*K]
   int T, K, TK, H, I_ld;
   int n_max;                   // token tile width, multiple of 16, <= 256
@@ -81,14 +81,16 @@ struct GemmParams {
   int nbuf;                    // TMEM accumulator buffers (1 or 2)
   uint32_t tmem_cols;
   float swiglu_limit;
-  uint16_t* h;                 // gate_up output [T*K + T, 2*I_ld] bf16 hi | lo
+  uint16_t* h;                 // gate_up output / down input [T*K + T, 2*I_ld] bf16 hi | lo
   float* out_ws;               // down output [T*K + T, H] fp32 (weighted)
   uint16_t* y;                 // down output when direct_y: [T, H] bf16
   int direct_y;
   const float* topk_w;         // [T*K]
   const float* sh_w;           // [T] shared-expert gate (nullable = 1)
-  float* partials;             // [grid, 2 slots, 2 halves, n_max, 128] fp32
-  int32_t* tile_counters;      // [tiles]
+  float* partials;             // [grid, 2 phases x 2 slots, 2 halves, n_max, 128] fp32
+  int32_t* tile_counters_gu;   // [gate_up tiles] stream-K arrivals
+  int32_t* tile_counters_dn;   // [down tiles]
+  int32_t* ready;              // [gate_up tiles] finished gate_up tiles per (group, token block)
   int32_t* status;
 };
 
@@ -130,8 +132,9 @@ cudaError_t launch_select_from_logits(const float* logits, int T, int E, int K, 
                                       cudaStream_t s);
 cudaError_t launch_permute(const int32_t* idx, int T, int K, int E, int32_t* counts, int32_t* offsets,
                            int32_t* sorted_pair, int32_t* pair_pos, cudaStream_t s);
-cudaError_t launch_gemm(int phase, const CUtensorMap& tm_routed, const CUtensorMap& tm_shared,
-                        const GemmParams& p, int grid, size_t smem_bytes, cudaStream_t s);
+cudaError_t launch_experts(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, const CUtensorMap& tm_dn,
+                           const CUtensorMap& tm_dn_sh, const GemmParams& p, int grid, size_t smem_bytes,
+                           cudaStream_t s);
 cudaError_t launch_combine(const float* out_ws, const int32_t* pair_pos, int T, int K, int H,
                            int has_shared, uint16_t* y, cudaStream_t s);
 

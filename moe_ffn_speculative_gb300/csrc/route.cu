@@ -65,14 +65,14 @@ struct SelCfg {
 // score -> select -> routing_weights for one token, by one warp.  Lane l
 // holds experts l, l+32, ..., (NJ per lane).  Writes idx_out[0..K) and
 // w_out[0..K).
-template <int NJ>
+template <int NJ, bool kShared>
 __device__ void select_token(const float* lrow, const SelCfg& c, int32_t* idx_out, float* w_out) {
   const int lane = threadIdx.x & 31;
   float l[NJ], s[NJ], key[NJ];
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
     const int e = lane + 32 * j;
-    l[j] = e < c.E ? __ldcg(lrow + e) : kNegInf;
+    l[j] = e < c.E ? (kShared ? lrow[e] : __ldcg(lrow + e)) : kNegInf;
   }
   // ---- score (fp32)
   if (c.score_fn == 0) {  // softmax
@@ -189,17 +189,23 @@ __device__ void select_token(const float* lrow, const SelCfg& c, int32_t* idx_ou
 
 // Counting-sort permutation of the (token, slot) pairs by expert, stable in
 // the pair index p = t*K + k, and (optionally) the grouped-GEMM work list.
-// Run by one whole CTA.
+// Run by one whole CTA.  Up to kPermStaged ids are first copied to shared
+// memory in one parallel pass, so the serial scatter reads them from there.
+constexpr int kPermStaged = 4096;
+
 __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* counts, int32_t* offsets,
                               int32_t* sorted_pair, int32_t* pair_pos, GroupEntry* groups, GemmHeader* header,
-                              int H, int I, int Is, int n_max, int* s_cnt, int* s_cur) {
+                              int H, int I, int Is, int n_max, int* s_cnt, int* s_cur, int* s_idx) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int TK = T * K;
+  const bool staged = TK <= kPermStaged;
   for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
+  if (staged)
+    for (int p = tid; p < TK; p += blockDim.x) s_idx[p] = __ldcg(idx + p);
   __syncthreads();
   // ids outside [0, E) are not counted and get no row
   for (int p = tid; p < TK; p += blockDim.x) {
-    const int e = __ldcg(idx + p);
+    const int e = staged ? s_idx[p] : __ldcg(idx + p);
     if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicAdd(&s_cnt[e], 1);
   }
   __syncthreads();
@@ -220,7 +226,7 @@ __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* 
     __syncwarp();
     for (int base = 0; base < TK; base += 32) {
       const int p = base + lane;
-      const int ev = p < TK ? __ldcg(idx + p) : -1;
+      const int ev = p < TK ? (staged ? s_idx[p] : __ldcg(idx + p)) : -1;
       const bool act = static_cast<unsigned>(ev) < static_cast<unsigned>(E);
       const int e = act ? ev : -1 - lane;
       const uint32_t peers = __match_any_sync(0xffffffffu, e);
@@ -330,9 +336,11 @@ __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* 
 template <int TB, int NJ>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams p) {
   __shared__ float red[8][TB][4];
+  __shared__ float s_log[TB][33];  // the block's logits when it covers every expert (E <= 32)
   __shared__ int s_flag;
   __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_cur[kMaxExperts];
+  __shared__ int s_idx[kPermStaged];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tbi = blockIdx.x, ebi = blockIdx.y;
   const int E_tot = p.E + (p.sh_gate ? 1 : 0);
@@ -361,18 +369,32 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
   for (int t = 0; t < TB; ++t)
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[t][q] = 0.f;
-  for (int c = h_lo + lane * 8; c < h_hi; c += 256) {
-    uint4 gv[4];
+  // one step of loads stays in flight while the previous step is multiplied
+  uint4 gv[4], xv[TB];
+  auto load_step = [&](int c, uint4 (&g)[4], uint4 (&xx)[TB]) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) gv[q] = ev[q] ? ldg128(rows[q] + c) : make_uint4(0, 0, 0, 0);
+    for (int q = 0; q < 4; ++q) g[q] = ev[q] ? ldg128(rows[q] + c) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int t = 0; t < TB; ++t) {
-      if (t0 + t < p.T) {
-        const uint4 xv = ldg128(p.x + static_cast<size_t>(t0 + t) * p.H + c);
+    for (int t = 0; t < TB; ++t)
+      xx[t] = (t0 + t < p.T) ? ldg128(p.x + static_cast<size_t>(t0 + t) * p.H + c) : make_uint4(0, 0, 0, 0);
+  };
+  int c = h_lo + lane * 8;
+  if (c < h_hi) load_step(c, gv, xv);
+  while (c < h_hi) {
+    const int cn = c + 256;
+    uint4 gn[4], xn[TB];
+    if (cn < h_hi) load_step(cn, gn, xn);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[t][q] = dot8(xv, gv[q], acc[t][q]);
-      }
+    for (int t = 0; t < TB; ++t)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[t][q] = dot8(xv[t], gv[q], acc[t][q]);
+    if (cn < h_hi) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) gv[q] = gn[q];
+#pragma unroll
+      for (int t = 0; t < TB; ++t) xv[t] = xn[t];
     }
+    c = cn;
   }
 #pragma unroll
   for (int t = 0; t < TB; ++t)
@@ -402,27 +424,40 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
       } else {
         p.sh_logit[tok] = v;
       }
+      if (p.n_eb == 1) s_log[t][e] = v;
     }
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int old = atomicAdd(&p.tb_counter[tbi], 1);
-    const int last = (old == p.n_eb - 1);
-    if (last) p.tb_counter[tbi] = 0;
-    s_flag = last;
-  }
-  __syncthreads();
-  if (!s_flag) return;
-  __threadfence();
-  // ---- selection: warp w routes token t0 + w
-  if (warp < TB && t0 + warp < p.T) {
-    const int tok = t0 + warp;
-    SelCfg c{p.E, p.K, p.score_fn, p.n_group, p.topk_group, p.group_topn, p.renorm, p.eps, p.scale,
-             p.expert_bias};
-    select_token<NJ>(p.logits + static_cast<size_t>(tok) * p.E, c, p.idx + static_cast<size_t>(tok) * p.K,
-                     p.w + static_cast<size_t>(tok) * p.K);
-    if (lane == 0 && p.sh_w) p.sh_w[tok] = p.sh_gate ? 1.f / (1.f + expf(-__ldcg(p.sh_logit + tok))) : 1.f;
+  const SelCfg sel{p.E, p.K, p.score_fn, p.n_group, p.topk_group, p.group_topn, p.renorm, p.eps, p.scale,
+                   p.expert_bias};
+  if (p.n_eb == 1) {
+    // this block holds every expert's logit of its tokens: select from shared memory
+    __syncthreads();
+    if (warp < TB && t0 + warp < p.T) {
+      const int tok = t0 + warp;
+      if (NJ == 1)
+        select_token<1, true>(s_log[warp], sel, p.idx + static_cast<size_t>(tok) * p.K,
+                              p.w + static_cast<size_t>(tok) * p.K);
+      if (lane == 0 && p.sh_w) p.sh_w[tok] = p.sh_gate ? 1.f / (1.f + expf(-s_log[warp][p.E])) : 1.f;
+    }
+  } else {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int old = atomicAdd(&p.tb_counter[tbi], 1);
+      const int last = (old == p.n_eb - 1);
+      if (last) p.tb_counter[tbi] = 0;
+      s_flag = last;
+    }
+    __syncthreads();
+    if (!s_flag) return;
+    __threadfence();
+    // ---- selection: warp w routes token t0 + w
+    if (warp < TB && t0 + warp < p.T) {
+      const int tok = t0 + warp;
+      select_token<NJ, false>(p.logits + static_cast<size_t>(tok) * p.E, sel,
+                              p.idx + static_cast<size_t>(tok) * p.K, p.w + static_cast<size_t>(tok) * p.K);
+      if (lane == 0 && p.sh_w) p.sh_w[tok] = p.sh_gate ? 1.f / (1.f + expf(-__ldcg(p.sh_logit + tok))) : 1.f;
+    }
   }
   if (!p.do_permute) return;
   __threadfence();
@@ -437,7 +472,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
   if (!s_flag) return;
   __threadfence();
   permute_block(p.idx, p.T, p.K, p.E, p.counts, p.offsets, p.sorted_pair, p.pair_pos, p.groups, p.header, p.H,
-                p.I, p.Is, p.n_max, s_cnt, s_cur);
+                p.I, p.Is, p.n_max, s_cnt, s_cur, s_idx);
 }
 
 template <int NJ>
@@ -445,8 +480,8 @@ __global__ void __launch_bounds__(kRouteThreads) select_kernel(const float* logi
                                                                float* w) {
   const int tok = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (tok >= T) return;
-  select_token<NJ>(logits + static_cast<size_t>(tok) * c.E, c, idx + static_cast<size_t>(tok) * c.K,
-                   w + static_cast<size_t>(tok) * c.K);
+  select_token<NJ, false>(logits + static_cast<size_t>(tok) * c.E, c, idx + static_cast<size_t>(tok) * c.K,
+                          w + static_cast<size_t>(tok) * c.K);
 }
 
 __global__ void __launch_bounds__(kRouteThreads) permute_kernel(const int32_t* idx, int T, int K, int E,
@@ -454,7 +489,9 @@ __global__ void __launch_bounds__(kRouteThreads) permute_kernel(const int32_t* i
                                                                 int32_t* sorted_pair, int32_t* pair_pos) {
   __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_cur[kMaxExperts];
-  permute_block(idx, T, K, E, counts, offsets, sorted_pair, pair_pos, nullptr, nullptr, 0, 0, 0, 1, s_cnt, s_cur);
+  __shared__ int s_idx[kPermStaged];
+  permute_block(idx, T, K, E, counts, offsets, sorted_pair, pair_pos, nullptr, nullptr, 0, 0, 0, 1, s_cnt, s_cur,
+                s_idx);
 }
 
 int nj_for(int E) {
