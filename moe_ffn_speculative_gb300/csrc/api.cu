@@ -112,7 +112,7 @@ struct Layout {
   int max_gu_tiles, max_dn_tiles, g_max;
   bool need_out;
   size_t o_status, o_cnt, o_tiles, o_logits, o_shl, o_shw, o_idx, o_w, o_counts, o_offsets, o_sp, o_pp, o_groups,
-      o_header, o_partials, o_h, o_out, total;
+      o_header, o_spans, o_span_groups, o_partials, o_h, o_out, total;
 };
 
 Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sms) {
@@ -162,6 +162,8 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   L.o_pp = o; o = align_up(o + 4 * static_cast<size_t>(TK));
   L.o_groups = o; o = align_up(o + sizeof(GroupEntry) * static_cast<size_t>(L.g_max + 1));
   L.o_header = o; o = align_up(o + sizeof(GemmHeader));
+  L.o_spans = o; o = align_up(o + 8 * 2 * static_cast<size_t>(L.grid + 1));
+  L.o_span_groups = o; o = align_up(o + 4 * 2 * static_cast<size_t>(L.grid + 1));
   L.o_partials = o; o = align_up(o + 4 * static_cast<size_t>(L.grid) * 4 * 2 * L.n_max * 128);
   L.o_h = o; o = align_up(o + 2 * 2 * rows * L.I_ld);
   L.o_out = o;
@@ -335,6 +337,9 @@ moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf1
   rp.counts = counts; rp.offsets = reinterpret_cast<int32_t*>(w + L.o_offsets);
   rp.sorted_pair = sorted_pair; rp.pair_pos = pair_pos;
   rp.groups = groups; rp.header = header;
+  rp.spans = reinterpret_cast<int64_t*>(w + L.o_spans);
+  rp.span_groups = reinterpret_cast<int32_t*>(w + L.o_span_groups);
+  rp.grid = L.grid;
   rp.I = I; rp.Is = Is; rp.n_max = L.n_max;
   rp.zero_ptr = tiles; rp.zero_count = 2 * L.max_gu_tiles + L.max_dn_tiles;
   record_event_on(0, stream);
@@ -356,6 +361,7 @@ moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf1
   GemmParams gp;
   memset(&gp, 0, sizeof(gp));
   gp.groups = groups; gp.header = header; gp.sorted_pair = sorted_pair;
+  gp.spans = rp.spans; gp.span_groups = rp.span_groups;
   gp.x = x; gp.h = h;
   gp.T = T; gp.K = K; gp.TK = T * K; gp.H = H; gp.I_ld = L.I_ld;
   gp.n_max = L.n_max; gp.stages = L.stages; gp.nbuf = L.nbuf; gp.tmem_cols = L.tmem_cols;

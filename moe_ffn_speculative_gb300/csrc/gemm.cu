@@ -58,16 +58,9 @@ struct Sched {
 
   __device__ long long iter_of(int gi) const { return phase == 0 ? groups[gi].gu_iter : groups[gi].dn_iter; }
 
-  __device__ void init(const GroupEntry* gs, int ng, int ph, int H_, int nmax, long long b, long long e) {
-    groups = gs; ngroups = ng; phase = ph; H = H_; n_max = nmax; it = b; end = e; g = 0;
-    if (b < e) {
-      int lo = 0, hi = ng - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (iter_of(mid) <= b) lo = mid; else hi = mid - 1;
-      }
-      g = lo;
-    }
+  // [b, e): the CTA's iterations; g0: the group holding iteration b
+  __device__ void init(const GroupEntry* gs, int ng, int ph, int H_, int nmax, long long b, long long e, int g0) {
+    groups = gs; ngroups = ng; phase = ph; H = H_; n_max = nmax; it = b; end = e; g = g0;
   }
 
   __device__ bool next(Seg& s) {
@@ -100,12 +93,14 @@ struct Sched {
   }
 };
 
-__device__ __forceinline__ long long cta_begin(long long c, long long total, long long grid) {
-  return c * total / grid;
-}
-// The CTA whose iteration range holds iteration i.
-__device__ __forceinline__ int cta_of(long long i, long long total, long long grid) {
-  return static_cast<int>(((i + 1) * grid + total - 1) / total - 1);
+// The CTA whose iteration range [span[c], span[c+1]) holds iteration i.
+__device__ __forceinline__ int cta_of(const int64_t* span, int grid, long long i) {
+  int lo = 0, hi = grid - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(span + mid) <= i) lo = mid; else hi = mid - 1;
+  }
+  return lo;
 }
 
 // --------------------------------------------------------------------------
@@ -215,9 +210,10 @@ struct WeightCursor {
   int ph, kk;
   bool valid;
 
-  __device__ void init(const GemmParams& p, int ngroups, long long b0, long long e0, long long b1, long long e1) {
-    sc0.init(p.groups, ngroups, 0, p.H, p.n_max, b0, e0);
-    sc1.init(p.groups, ngroups, 1, p.H, p.n_max, b1, e1);
+  __device__ void init(const GemmParams& p, int ngroups, const long long (&b)[2], const long long (&e)[2],
+                       const int (&g)[2]) {
+    sc0.init(p.groups, ngroups, 0, p.H, p.n_max, b[0], e[0], g[0]);
+    sc1.init(p.groups, ngroups, 1, p.H, p.n_max, b[1], e[1], g[1]);
     ph = 0;
     kk = 0;
     valid = false;
@@ -254,11 +250,12 @@ struct WeightCursor {
   }
 };
 
-__device__ bool produce(const Smem& sm, const GemmParams& p, int ngroups, long long b0, long long e0, long long b1,
-                        long long e1, const CUtensorMap* tm_gu, const CUtensorMap* tm_gu_sh,
-                        const CUtensorMap* tm_dn, const CUtensorMap* tm_dn_sh, Ring& ring, int32_t* status) {
+__device__ bool produce(const Smem& sm, const GemmParams& p, int ngroups, const long long (&b)[2],
+                        const long long (&e)[2], const int (&g)[2], const CUtensorMap* tm_gu,
+                        const CUtensorMap* tm_gu_sh, const CUtensorMap* tm_dn, const CUtensorMap* tm_dn_sh,
+                        Ring& ring, int32_t* status) {
   WeightCursor ld;
-  ld.init(p, ngroups, b0, e0, b1, e1);
+  ld.init(p, ngroups, b, e, g);
   while (ld.valid) {
     if (!mbar_wait(&sm.empty[ring.stage], ring.phase ^ 1u, sm.abort_flag)) {
       record_failure(status, sm.abort_flag, kInfoEmpty);
@@ -280,10 +277,10 @@ __device__ bool produce(const Smem& sm, const GemmParams& p, int ngroups, long l
 
 // ---------------------------------------------------------------- MMA issuer (one thread)
 template <int PHASE>
-__device__ bool issue_mma(const Smem& sm, const GemmParams& p, int ngroups, long long begin, long long end,
+__device__ bool issue_mma(const Smem& sm, const GemmParams& p, int ngroups, long long begin, long long end, int g0,
                           uint32_t tmem_base, Ring& ring, int& seg_i, int32_t* status) {
   Sched sc;
-  sc.init(p.groups, ngroups, PHASE, p.H, p.n_max, begin, end);
+  sc.init(p.groups, ngroups, PHASE, p.H, p.n_max, begin, end, g0);
   Seg sg;
   while (sc.next(sg)) {
     const int buf = seg_i % p.nbuf;
@@ -332,11 +329,11 @@ __device__ bool issue_mma(const Smem& sm, const GemmParams& p, int ngroups, long
 // gate_up: rows of x for the expert's tokens; down: the expert's h rows (hi and
 // lo), after the gate_up tiles that write them have signalled.
 template <int PHASE>
-__device__ bool gather(const Smem& sm, const GemmParams& p, int ngroups, long long begin, long long end, Ring& ring,
-                       int& pending, int& arr_stage, int lag, int32_t* status) {
+__device__ bool gather(const Smem& sm, const GemmParams& p, int ngroups, long long begin, long long end, int g0,
+                       Ring& ring, int& pending, int& arr_stage, int lag, int32_t* status) {
   const int lane = threadIdx.x & 31;
   Sched sc;
-  sc.init(p.groups, ngroups, PHASE, p.H, p.n_max, begin, end);
+  sc.init(p.groups, ngroups, PHASE, p.H, p.n_max, begin, end, g0);
   constexpr int kBTiles = PHASE == 0 ? 1 : 2;
   const uint16_t* bsrc = PHASE == 0 ? p.x : p.h;
   Seg sg;
@@ -425,15 +422,16 @@ __device__ bool gather(const Smem& sm, const GemmParams& p, int ngroups, long lo
 
 // ---------------------------------------------------------------- epilogue (4 warps)
 template <int PHASE>
-__device__ bool epilogue(const Smem& sm, const GemmParams& p, int ngroups, long long begin, long long end,
-                         long long total, uint32_t tmem_base, int& seg_i, int32_t* tile_counters, int32_t* status) {
+__device__ bool epilogue(const Smem& sm, const GemmParams& p, int ngroups, long long begin, long long end, int g0,
+                         uint32_t tmem_base, int& seg_i, int32_t* tile_counters, int32_t* status) {
   Sched sc;
-  sc.init(p.groups, ngroups, PHASE, p.H, p.n_max, begin, end);
+  sc.init(p.groups, ngroups, PHASE, p.H, p.n_max, begin, end, g0);
+  const int64_t* span = p.spans + PHASE * (gridDim.x + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
   const int r = quad * 32 + lane;  // accumulator row = TMEM lane
   const bool leader = (warp == 3 && lane == 0);
-  const long long grid = gridDim.x;
+  const int grid = gridDim.x;
   Seg sg;
   while (sc.next(sg)) {
     const int buf = seg_i % p.nbuf;
@@ -493,14 +491,14 @@ __device__ bool epilogue(const Smem& sm, const GemmParams& p, int ngroups, long 
       epi_sync();
       if (*reinterpret_cast<volatile int*>(sm.bcast)) {
         __threadfence();
-        const int c0 = cta_of(sg.tile_iter0, total, grid);
-        const int c1 = cta_of(sg.tile_iter0 + sg.kb - 1, total, grid);
+        const int c0 = cta_of(span, grid, sg.tile_iter0);
+        const int c1 = cta_of(span, grid, sg.tile_iter0 + sg.kb - 1);
         for (int j0 = 0; j0 < sg.n_cnt; j0 += 16) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) { fa[i] = 0.f; fb[i] = 0.f; }
           for (int c = c0; c <= c1; ++c) {
-            const long long bc = cta_begin(c, total, grid);
-            if (bc == cta_begin(c + 1, total, grid)) continue;  // CTA with an empty range
+            const long long bc = __ldg(span + c);
+            if (bc == __ldg(span + c + 1)) continue;  // CTA with an empty range
             const int sl = PHASE * 2 + ((bc >= sg.tile_iter0) ? 0 : 1);
             const float* pp = p.partials + static_cast<size_t>(c * 4 + sl) * 2 * p.n_max * 128;
 #pragma unroll
@@ -586,16 +584,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const GemmHeader hd = *p.header;
-  const long long grid = gridDim.x;
-  const long long b0 = cta_begin(blockIdx.x, hd.gu_iters, grid), e0 = cta_begin(blockIdx.x + 1, hd.gu_iters, grid);
-  const long long b1 = cta_begin(blockIdx.x, hd.dn_iters, grid), e1 = cta_begin(blockIdx.x + 1, hd.dn_iters, grid);
-  const int ng = hd.ngroups;
+  const int ng = p.header->ngroups;
+  // this CTA's cost-balanced spans of the gate_up and down iterations
+  const int G1 = gridDim.x + 1;
+  const long long bs[2] = {p.spans[blockIdx.x], p.spans[G1 + blockIdx.x]};
+  const long long es[2] = {p.spans[blockIdx.x + 1], p.spans[G1 + blockIdx.x + 1]};
+  const int gs[2] = {p.span_groups[blockIdx.x], p.span_groups[G1 + blockIdx.x]};
 
   if (warp == 0) {
     if (lane == 0) {
       Ring ring;
-      const bool ok = produce(sm, p, ng, b0, e0, b1, e1, &tm_gu, &tm_gu_sh, &tm_dn, &tm_dn_sh, ring, p.status);
+      const bool ok = produce(sm, p, ng, bs, es, gs, &tm_gu, &tm_gu_sh, &tm_dn, &tm_dn_sh, ring, p.status);
       if (!ok) {
         // let the loads already issued land before the CTA can exit
         const long long t0 = clock64();
@@ -606,8 +605,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       Ring ring;
       int seg_i = 0;
-      if (issue_mma<0>(sm, p, ng, b0, e0, tmem_base, ring, seg_i, p.status))
-        issue_mma<1>(sm, p, ng, b1, e1, tmem_base, ring, seg_i, p.status);
+      if (issue_mma<0>(sm, p, ng, bs[0], es[0], gs[0], tmem_base, ring, seg_i, p.status))
+        issue_mma<1>(sm, p, ng, bs[1], es[1], gs[1], tmem_base, ring, seg_i, p.status);
       // every MMA issued above has completed once `drain` flips
       mma_commit(sm.drain);
       if (!mbar_wait(sm.drain, 0, nullptr)) record_failure(p.status, sm.abort_flag, kInfoDrain);
@@ -618,8 +617,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // copies kept in flight before arriving; below the stage count, so the
     // stage this warp waits to refill never depends on an arrival it holds
     const int lag = kGatherLag < sm.S - 1 ? kGatherLag : sm.S - 1;
-    if (gather<0>(sm, p, ng, b0, e0, ring, pending, arr_stage, lag, p.status))
-      gather<1>(sm, p, ng, b1, e1, ring, pending, arr_stage, lag, p.status);
+    if (gather<0>(sm, p, ng, bs[0], es[0], gs[0], ring, pending, arr_stage, lag, p.status))
+      gather<1>(sm, p, ng, bs[1], es[1], gs[1], ring, pending, arr_stage, lag, p.status);
     cp_async_wait<0>();
     fence_proxy_async();
     while (pending > 0) {
@@ -629,8 +628,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     int seg_i = 0;
-    if (epilogue<0>(sm, p, ng, b0, e0, hd.gu_iters, tmem_base, seg_i, p.tile_counters_gu, p.status))
-      epilogue<1>(sm, p, ng, b1, e1, hd.dn_iters, tmem_base, seg_i, p.tile_counters_dn, p.status);
+    if (epilogue<0>(sm, p, ng, bs[0], es[0], gs[0], tmem_base, seg_i, p.tile_counters_gu, p.status))
+      epilogue<1>(sm, p, ng, bs[1], es[1], gs[1], tmem_base, seg_i, p.tile_counters_dn, p.status);
   }
 
   tc_fence_before();

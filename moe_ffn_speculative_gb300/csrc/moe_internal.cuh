@@ -33,7 +33,8 @@ struct GroupEntry {
   int32_t idim;     // I of this expert (I or Is)
   int32_t gu_tile;  // first tile index of the group in the gate_up GEMM
   int32_t dn_tile;  // first tile index of the group in the down GEMM
-  int32_t pad0, pad1;
+  int32_t gu_w;     // cost of one gate_up k-block of this group (quarter k-blocks)
+  int32_t dn_w;     // cost of one down k-block
   int64_t gu_iter;  // first k-block iteration of the group (gate_up)
   int64_t dn_iter;  // first k-block iteration of the group (down)
 };
@@ -63,6 +64,16 @@ constexpr int kGatherLag = 2;                         // cp.async groups in flig
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Relative cost of one k-block of a group whose tiles carry `nmma` token
+// columns, in quarters of a weight-streaming k-block: up to 16 columns a
+// k-block costs what its 32 KB of weights take to stream; wider tiles
+// (the shared expert, large token counts) add MMA, gather and epilogue
+// work, more in the down GEMM (h as hi and lo doubles its MMAs and gathers).
+// The slopes are fitted to per-CTA timings of 16- and 80-column tiles.
+__host__ __device__ inline int kblock_cost(int phase, int nmma) {
+  return phase == 0 ? 4 + ((nmma - 16) * 3 + 80) / 160 : 4 + ((nmma - 16) * 7 + 20) / 40;
+}
+
 __host__ __device__ inline void group_geometry(int phase, int count, int idim, int H, int n_max,
                                                int& mb, int& nb, int& kb) {
   nb = ceil_div(count, n_max);
@@ -73,6 +84,8 @@ __host__ __device__ inline void group_geometry(int phase, int count, int idim, i
 struct GemmParams {
   const GroupEntry* groups;
   const GemmHeader* header;
+  const int64_t* spans;        // [2][grid+1] first k-block iteration of every CTA, per phase
+  const int32_t* span_groups;  // [2][grid+1] work-list group holding that iteration
   const uint16_t* x;           // [T,H] (gate_up token rows)
   const int32_t* sorted_pair;  // [T*K]
   int T, K, TK, H, I_ld;
@@ -119,6 +132,9 @@ struct RouteParams {
   int32_t* pair_pos;
   GroupEntry* groups;          // nullable
   GemmHeader* header;
+  int64_t* spans;              // [2][grid+1] cost-balanced CTA spans for the GEMM
+  int32_t* span_groups;        // [2][grid+1]
+  int grid;                    // CTAs of the GEMM launch
   int I, Is, n_max;
   int32_t* zero_ptr;           // GEMM tile counters cleared by this launch
   int zero_count;

@@ -192,10 +192,14 @@ __device__ void select_token(const float* lrow, const SelCfg& c, int32_t* idx_ou
 // Run by one whole CTA.  Up to kPermStaged ids are first copied to shared
 // memory in one parallel pass, so the serial scatter reads them from there.
 constexpr int kPermStaged = 4096;
+// shared buffer: the staged ids, later the two cost prefixes of the work list
+constexpr int kPermBuf = 2080;  // long longs: >= kPermStaged / 2 and >= 2 * 1040
 
 __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* counts, int32_t* offsets,
                               int32_t* sorted_pair, int32_t* pair_pos, GroupEntry* groups, GemmHeader* header,
-                              int H, int I, int Is, int n_max, int* s_cnt, int* s_cur, int* s_idx) {
+                              int H, int I, int Is, int n_max, int* s_cnt, int* s_cur, long long* s_buf,
+                              int64_t* spans, int32_t* span_groups, int grid) {
+  int* s_idx = reinterpret_cast<int*>(s_buf);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int TK = T * K;
   const bool staged = TK <= kPermStaged;
@@ -250,82 +254,145 @@ __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* 
     if (offsets) offsets[e + 1] = s_cur[e];
   }
   if (tid == 0 && offsets) offsets[0] = 0;
-  if (groups == nullptr || warp != 0) return;
-  int g = 0, gu_t = 0, dn_t = 0;
-  long long gu_i = 0, dn_i = 0;
-  for (int base = 0; base < E; base += 32) {
-    const int e = base + lane;
-    const int c = e < E ? s_cnt[e] : 0;
-    const bool touched = c > 0;
-    const uint32_t m = __ballot_sync(0xffffffffu, touched);
-    int gut = 0, dnt = 0;
-    long long gui = 0, dni = 0;
-    if (touched) {
+  if (groups == nullptr) return;
+  // ---- work list: one group per touched expert (expert order), then the
+  // shared expert; prefix sums of tiles, k-block iterations and k-block costs
+  // per GEMM.  The cost prefix goes to shared memory (the staged ids are no
+  // longer needed) for the span computation below.
+  long long* s_cost0 = s_buf;              // [groups + 1]
+  long long* s_cost1 = s_buf + 1040;       // [groups + 1]
+  __shared__ int s_ngroups;
+  __shared__ long long s_tot[4];           // gate_up iters, down iters, gate_up cost, down cost
+  __syncthreads();
+  if (warp == 0) {
+    int g = 0, gu_t = 0, dn_t = 0;
+    long long gu_i = 0, dn_i = 0, gu_c = 0, dn_c = 0;
+    auto geometry = [&](int c, int idim, int& gut, int& dnt, long long& gui, long long& dni, int& w0, int& w1) {
       int mb, nb, kb;
-      group_geometry(0, c, I, H, n_max, mb, nb, kb);
+      const int nmma = max(16, min(n_max, (c + 15) & ~15));
+      group_geometry(0, c, idim, H, n_max, mb, nb, kb);
       gut = mb * nb;
       gui = static_cast<long long>(gut) * kb;
-      group_geometry(1, c, I, H, n_max, mb, nb, kb);
+      group_geometry(1, c, idim, H, n_max, mb, nb, kb);
       dnt = mb * nb;
       dni = static_cast<long long>(dnt) * kb;
-    }
-    int a = gut, b = dnt;
-    long long ci = gui, di = dni;
+      w0 = kblock_cost(0, nmma);
+      w1 = kblock_cost(1, nmma);
+    };
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int c = e < E ? s_cnt[e] : 0;
+      const bool touched = c > 0;
+      const uint32_t m = __ballot_sync(0xffffffffu, touched);
+      int gut = 0, dnt = 0, w0 = 0, w1 = 0;
+      long long gui = 0, dni = 0;
+      if (touched) geometry(c, I, gut, dnt, gui, dni, w0, w1);
+      const long long guc = gui * w0, dnc = dni * w1;
+      int a = gut, b = dnt;
+      long long ci = gui, di = dni, cc = guc, dc = dnc;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int na = __shfl_up_sync(0xffffffffu, a, off);
-      const int nb2 = __shfl_up_sync(0xffffffffu, b, off);
-      const long long nci = __shfl_up_sync(0xffffffffu, ci, off);
-      const long long ndi = __shfl_up_sync(0xffffffffu, di, off);
-      if (lane >= off) { a += na; b += nb2; ci += nci; di += ndi; }
+      for (int off = 1; off < 32; off <<= 1) {
+        const int na = __shfl_up_sync(0xffffffffu, a, off);
+        const int nb2 = __shfl_up_sync(0xffffffffu, b, off);
+        const long long nci = __shfl_up_sync(0xffffffffu, ci, off);
+        const long long ndi = __shfl_up_sync(0xffffffffu, di, off);
+        const long long ncc = __shfl_up_sync(0xffffffffu, cc, off);
+        const long long ndc = __shfl_up_sync(0xffffffffu, dc, off);
+        if (lane >= off) { a += na; b += nb2; ci += nci; di += ndi; cc += ncc; dc += ndc; }
+      }
+      if (touched) {
+        const int gi = g + __popc(m & ((1u << lane) - 1u));
+        GroupEntry ge;
+        ge.expert = e;
+        ge.row_base = s_cur[e] - c;
+        ge.count = c;
+        ge.idim = I;
+        ge.gu_tile = gu_t + a - gut;
+        ge.dn_tile = dn_t + b - dnt;
+        ge.gu_w = w0;
+        ge.dn_w = w1;
+        ge.gu_iter = gu_i + ci - gui;
+        ge.dn_iter = dn_i + di - dni;
+        groups[gi] = ge;
+        s_cost0[gi] = gu_c + cc - guc;
+        s_cost1[gi] = dn_c + dc - dnc;
+      }
+      g += __popc(m);
+      gu_t += __shfl_sync(0xffffffffu, a, 31);
+      dn_t += __shfl_sync(0xffffffffu, b, 31);
+      gu_i += __shfl_sync(0xffffffffu, ci, 31);
+      dn_i += __shfl_sync(0xffffffffu, di, 31);
+      gu_c += __shfl_sync(0xffffffffu, cc, 31);
+      dn_c += __shfl_sync(0xffffffffu, dc, 31);
     }
-    if (touched) {
-      GroupEntry ge;
-      ge.expert = e;
-      ge.row_base = s_cur[e] - c;
-      ge.count = c;
-      ge.idim = I;
-      ge.gu_tile = gu_t + a - gut;
-      ge.dn_tile = dn_t + b - dnt;
-      ge.gu_iter = gu_i + ci - gui;
-      ge.dn_iter = dn_i + di - dni;
-      groups[g + __popc(m & ((1u << lane) - 1u))] = ge;
+    if (lane == 0) {
+      if (Is > 0) {
+        int gut, dnt, w0, w1;
+        long long gui, dni;
+        geometry(T, Is, gut, dnt, gui, dni, w0, w1);
+        GroupEntry ge;
+        ge.expert = -1;
+        ge.row_base = TK;
+        ge.count = T;
+        ge.idim = Is;
+        ge.gu_tile = gu_t;
+        ge.dn_tile = dn_t;
+        ge.gu_w = w0;
+        ge.dn_w = w1;
+        ge.gu_iter = gu_i;
+        ge.dn_iter = dn_i;
+        groups[g] = ge;
+        s_cost0[g] = gu_c;
+        s_cost1[g] = dn_c;
+        gu_t += gut;
+        dn_t += dnt;
+        gu_i += gui;
+        dn_i += dni;
+        gu_c += gui * w0;
+        dn_c += dni * w1;
+        ++g;
+      }
+      GemmHeader hd;
+      hd.ngroups = g;
+      hd.gu_tiles = gu_t;
+      hd.dn_tiles = dn_t;
+      hd.pad = 0;
+      hd.gu_iters = gu_i;
+      hd.dn_iters = dn_i;
+      *header = hd;
+      s_ngroups = g;
+      s_tot[0] = gu_i;
+      s_tot[1] = dn_i;
+      s_tot[2] = gu_c;
+      s_tot[3] = dn_c;
     }
-    g += __popc(m);
-    gu_t += __shfl_sync(0xffffffffu, a, 31);
-    dn_t += __shfl_sync(0xffffffffu, b, 31);
-    gu_i += __shfl_sync(0xffffffffu, ci, 31);
-    dn_i += __shfl_sync(0xffffffffu, di, 31);
   }
-  if (lane == 0) {
-    if (Is > 0) {
-      GroupEntry ge;
-      int mb, nb, kb;
-      ge.expert = -1;
-      ge.row_base = TK;
-      ge.count = T;
-      ge.idim = Is;
-      ge.gu_tile = gu_t;
-      ge.dn_tile = dn_t;
-      ge.gu_iter = gu_i;
-      ge.dn_iter = dn_i;
-      groups[g] = ge;
-      group_geometry(0, T, Is, H, n_max, mb, nb, kb);
-      gu_t += mb * nb;
-      gu_i += static_cast<long long>(mb * nb) * kb;
-      group_geometry(1, T, Is, H, n_max, mb, nb, kb);
-      dn_t += mb * nb;
-      dn_i += static_cast<long long>(mb * nb) * kb;
-      ++g;
+  __syncthreads();
+  // ---- CTA spans: cut each GEMM's total cost into `grid` equal parts and
+  // round every cut to a whole k-block iteration.
+  const int ng = s_ngroups;
+  for (int q = tid; q < 2 * (grid + 1); q += blockDim.x) {
+    const int ph = q / (grid + 1), c = q % (grid + 1);
+    const long long* cs = ph == 0 ? s_cost0 : s_cost1;
+    const long long total_cost = s_tot[2 + ph], total_it = s_tot[ph];
+    const long long pos = total_cost * c / grid;
+    long long it = total_it;
+    int gsel = ng;
+    if (pos < total_cost && ng > 0) {
+      int lo = 0, hi = ng - 1;  // last group whose cost starts at or before pos
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cs[mid] <= pos) lo = mid; else hi = mid - 1;
+      }
+      const GroupEntry& ge = groups[lo];
+      const long long w = ph == 0 ? ge.gu_w : ge.dn_w;
+      const long long i0 = ph == 0 ? ge.gu_iter : ge.dn_iter;
+      it = i0 + (pos - cs[lo] + w - 1) / w;
+      const long long next = lo + 1 < ng ? (ph == 0 ? groups[lo + 1].gu_iter : groups[lo + 1].dn_iter) : total_it;
+      gsel = it < next ? lo : lo + 1;
     }
-    GemmHeader hd;
-    hd.ngroups = g;
-    hd.gu_tiles = gu_t;
-    hd.dn_tiles = dn_t;
-    hd.pad = 0;
-    hd.gu_iters = gu_i;
-    hd.dn_iters = dn_i;
-    *header = hd;
+    spans[q] = it;
+    span_groups[q] = gsel;
   }
 }
 
@@ -340,7 +407,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
   __shared__ int s_flag;
   __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_cur[kMaxExperts];
-  __shared__ int s_idx[kPermStaged];
+  __shared__ long long s_buf[kPermBuf];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tbi = blockIdx.x, ebi = blockIdx.y;
   const int E_tot = p.E + (p.sh_gate ? 1 : 0);
@@ -472,7 +539,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
   if (!s_flag) return;
   __threadfence();
   permute_block(p.idx, p.T, p.K, p.E, p.counts, p.offsets, p.sorted_pair, p.pair_pos, p.groups, p.header, p.H,
-                p.I, p.Is, p.n_max, s_cnt, s_cur, s_idx);
+                p.I, p.Is, p.n_max, s_cnt, s_cur, s_buf, p.spans, p.span_groups, p.grid);
 }
 
 template <int NJ>
@@ -489,9 +556,9 @@ __global__ void __launch_bounds__(kRouteThreads) permute_kernel(const int32_t* i
                                                                 int32_t* sorted_pair, int32_t* pair_pos) {
   __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_cur[kMaxExperts];
-  __shared__ int s_idx[kPermStaged];
+  __shared__ long long s_buf[kPermBuf];
   permute_block(idx, T, K, E, counts, offsets, sorted_pair, pair_pos, nullptr, nullptr, 0, 0, 0, 1, s_cnt, s_cur,
-                s_idx);
+                s_buf, nullptr, nullptr, 0);
 }
 
 int nj_for(int E) {
