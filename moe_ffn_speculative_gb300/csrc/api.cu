@@ -15,7 +15,6 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr size_t kAlign = 256;
 constexpr int kSmemLimit = 232448;  // 227 KB of dynamic shared memory per CTA
-constexpr int kCtrlBytes = 256 + 256 * 8;
 
 int g_sms[kMaxDevices];
 
@@ -28,7 +27,7 @@ int device_sms() {
   if (g_sms[d] == 0) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return 0;
-    g_sms[d] = n;
+    g_sms[d] = n < kMaxGrid ? n : kMaxGrid;  // one GEMM CTA per SM, up to the span table's size
   }
   return g_sms[d];
 }
@@ -106,7 +105,7 @@ RouterGeom router_geometry(int T, int E_tot, int sms) {
 
 struct Layout {
   RouterGeom rg;
-  int n_max, stages, nbuf, grid, I_ld;
+  int n_max, nbuf, grid, I_ld;
   uint32_t tmem_cols;
   size_t smem;
   int max_gu_tiles, max_dn_tiles, g_max;
@@ -124,12 +123,10 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(L.nbuf * 2 * L.n_max)) cols <<= 1;
   L.tmem_cols = cols;
-  // a stage holds two 16 KB weight halves and two token tiles (the down GEMM
-  // reads h as hi and lo)
-  const int stage_bytes = 2 * kTileBytesA + 2 * L.n_max * 128;
-  L.stages = (kSmemLimit - 1024 - kCtrlBytes) / stage_bytes;
-  if (L.stages > kMaxStages) L.stages = kMaxStages;
-  L.smem = 1024 + static_cast<size_t>(L.stages) * stage_bytes + kCtrlBytes;
+  // all of shared memory: the kernel cuts the stage ring (two 16 KB weight
+  // halves and two token tiles per stage, h as hi and lo) to the widest
+  // token tile of each forward
+  L.smem = kSmemLimit;
   L.grid = sms;
   const int Imax = Is > I ? Is : I;
   L.I_ld = ((Imax + 7) / 8) * 8;
@@ -364,7 +361,8 @@ moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf1
   gp.spans = rp.spans; gp.span_groups = rp.span_groups;
   gp.x = x; gp.h = h;
   gp.T = T; gp.K = K; gp.TK = T * K; gp.H = H; gp.I_ld = L.I_ld;
-  gp.n_max = L.n_max; gp.stages = L.stages; gp.nbuf = L.nbuf; gp.tmem_cols = L.tmem_cols;
+  gp.n_max = L.n_max; gp.stage_space = kSmemLimit - 1024 - kCtrlBytes; gp.nbuf = L.nbuf;
+  gp.tmem_cols = L.tmem_cols;
   gp.swiglu_limit = recipe->swiglu_limit;
   gp.out_ws = out_ws; gp.y = y; gp.direct_y = L.need_out ? 0 : 1;
   gp.topk_w = wts; gp.sh_w = (Is > 0 && sh_gate) ? sh_w : nullptr;

@@ -93,12 +93,13 @@ struct Sched {
   }
 };
 
-// The CTA whose iteration range [span[c], span[c+1]) holds iteration i.
-__device__ __forceinline__ int cta_of(const int64_t* span, int grid, long long i) {
+// The CTA whose iteration range [span[c], span[c+1]) holds iteration i
+// (span: this GEMM's table, staged in shared memory).
+__device__ __forceinline__ int cta_of(const long long* span, int grid, long long i) {
   int lo = 0, hi = grid - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(span + mid) <= i) lo = mid; else hi = mid - 1;
+    if (span[mid] <= i) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
@@ -109,7 +110,7 @@ __device__ __forceinline__ int cta_of(const int64_t* span, int grid, long long i
 // --------------------------------------------------------------------------
 template <int PHASE>
 __device__ __forceinline__ void finish_chunk(const GemmParams& p, const Seg& sg, int r, int j0, const float* a,
-                                             const float* b) {
+                                             const float* b, const float* col_w, const int* col_tok) {
   if (PHASE == 0) {
     // SwiGLU: h = silu(gate) * up, with the clamp when a limit is set
     const int row = sg.m * kHalfRows + r;
@@ -143,16 +144,8 @@ __device__ __forceinline__ void finish_chunk(const GemmParams& p, const Seg& sg,
       const int j = j0 + i;
       if (j < sg.n_cnt) {
         const int sr = sg.row_base + sg.n * p.n_max + j;
-        float wt;
-        int tok;
-        if (sg.expert >= 0) {
-          const int pr = __ldg(p.sorted_pair + sr);
-          wt = __ldg(p.topk_w + pr);
-          tok = pr / p.K;
-        } else {
-          tok = sr - p.TK;
-          wt = p.sh_w ? __ldg(p.sh_w + tok) : 1.f;
-        }
+        const float wt = col_w[j];
+        const int tok = col_tok[j];
         if (p.direct_y) {
           uint16_t* yr = p.y + static_cast<size_t>(tok) * p.H;
           if (row0 < p.H) yr[row0] = f2bf(wt * a[i]);
@@ -199,6 +192,9 @@ struct Smem {
   int* bcast;
   int* s_ok;
   long long* rowoff;
+  long long* span;  // [2][grid+1] CTA spans of both GEMMs
+  float* col_w;     // [n_max] down epilogue: routing weight of each token column
+  int* col_tok;     // [n_max] down epilogue: token of each column
 };
 
 // ---------------------------------------------------------------- TMA producer (weights)
@@ -426,7 +422,7 @@ __device__ bool epilogue(const Smem& sm, const GemmParams& p, int ngroups, long 
                          uint32_t tmem_base, int& seg_i, int32_t* tile_counters, int32_t* status) {
   Sched sc;
   sc.init(p.groups, ngroups, PHASE, p.H, p.n_max, begin, end, g0);
-  const int64_t* span = p.spans + PHASE * (gridDim.x + 1);
+  const long long* span = sm.span + PHASE * (gridDim.x + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
   const int r = quad * 32 + lane;  // accumulator row = TMEM lane
@@ -436,6 +432,23 @@ __device__ bool epilogue(const Smem& sm, const GemmParams& p, int ngroups, long 
   while (sc.next(sg)) {
     const int buf = seg_i % p.nbuf;
     const uint32_t use = static_cast<uint32_t>(seg_i / p.nbuf);
+    if (PHASE == 1) {
+      // each column's routing weight (or shared-expert gate) and token, loaded
+      // in parallel while the MMAs of this segment still run
+      const int epi_t = (warp - 3) * 32 + lane;
+      for (int j = epi_t; j < sg.n_cnt; j += 128) {
+        const int sr = sg.row_base + sg.n * p.n_max + j;
+        if (sg.expert >= 0) {
+          const int pr = __ldg(p.sorted_pair + sr);
+          sm.col_w[j] = __ldg(p.topk_w + pr);
+          sm.col_tok[j] = pr / p.K;
+        } else {
+          const int tok = sr - p.TK;
+          sm.col_w[j] = p.sh_w ? __ldg(p.sh_w + tok) : 1.f;
+          sm.col_tok[j] = tok;
+        }
+      }
+    }
     // one thread waits, the four warps leave or go on together
     if (leader) {
       const bool got = mbar_wait(&sm.accf[buf], use & 1u, sm.abort_flag);
@@ -458,14 +471,16 @@ __device__ bool epilogue(const Smem& sm, const GemmParams& p, int ngroups, long 
         tmem_ld_wait();
         u32_to_f32(ua, fa);
         u32_to_f32(ub, fb);
-        finish_chunk<PHASE>(p, sg, r, j0, fa, fb);
+        finish_chunk<PHASE>(p, sg, r, j0, fa, fb, sm.col_w, sm.col_tok);
       }
       tc_fence_before();
       mbar_arrive(&sm.acce[buf]);
       done = true;
-    } else {
-      const int slot = PHASE * 2 + ((begin >= sg.tile_iter0) ? 0 : 1);
-      float* mine = p.partials + static_cast<size_t>(blockIdx.x * 4 + slot) * 2 * p.n_max * 128;
+    } else if (sg.k0 > 0) {
+      // A later part of a split tile: hand the partial sums to the CTA that
+      // holds the tile's first k-block.  A CTA's span can start inside at
+      // most one tile, so it writes at most one partial per GEMM.
+      float* mine = p.partials + static_cast<size_t>(blockIdx.x * 4 + PHASE * 2) * 2 * p.n_max * 128;
       for (int j0 = 0; j0 < sg.n_cnt; j0 += 16) {
         tmem_ld16(tacc + j0, ua);
         tmem_ld16(tacc + p.n_max + j0, ub);
@@ -482,37 +497,53 @@ __device__ bool epilogue(const Smem& sm, const GemmParams& p, int ngroups, long 
       mbar_arrive(&sm.acce[buf]);
       __threadfence();
       epi_sync();
+      if (leader) atomicAdd(tile_counters + sg.tile, sg.len);
+    } else {
+      // The first part of a split tile: this CTA finishes it.  The later
+      // parts were processed at the start of their CTAs' spans, so their
+      // partials are normally there already; wait (bounded) until all are
+      // counted, then add them to the accumulator in CTA order.
       if (leader) {
-        const int old = atomicAdd(tile_counters + sg.tile, sg.len);
-        const int last = (old + sg.len == sg.kb);
-        if (last) atomicExch(tile_counters + sg.tile, 0);
-        *sm.bcast = last;
+        const int32_t* cnt = tile_counters + sg.tile;
+        const int target = sg.kb - sg.len;
+        bool got = ld_acquire_gpu(cnt) >= target;
+        if (!got) {
+          const long long t0 = clock64();
+          while (!(got = ld_acquire_gpu(cnt) >= target)) {
+            if (*sm.abort_flag || clock64() - t0 > kWaitLimitCycles) break;
+            __nanosleep(32);
+          }
+        }
+        if (got) atomicExch(tile_counters + sg.tile, 0);
+        else record_failure(status, sm.abort_flag, kInfoFixup);
+        *sm.s_ok = got ? 1 : 0;
       }
       epi_sync();
-      if (*reinterpret_cast<volatile int*>(sm.bcast)) {
-        __threadfence();
-        const int c0 = cta_of(span, grid, sg.tile_iter0);
-        const int c1 = cta_of(span, grid, sg.tile_iter0 + sg.kb - 1);
-        for (int j0 = 0; j0 < sg.n_cnt; j0 += 16) {
+      if (!*reinterpret_cast<volatile int*>(sm.s_ok)) return false;
+      __threadfence();
+      const int c1 = cta_of(span, grid, sg.tile_iter0 + sg.kb - 1);
+      for (int j0 = 0; j0 < sg.n_cnt; j0 += 16) {
+        tmem_ld16(tacc + j0, ua);
+        tmem_ld16(tacc + p.n_max + j0, ub);
+        tmem_ld_wait();
+        u32_to_f32(ua, fa);
+        u32_to_f32(ub, fb);
+        for (int c = blockIdx.x + 1; c <= c1; ++c) {
+          if (span[c] == span[c + 1]) continue;  // CTA with an empty range
+          const float* pp = p.partials + static_cast<size_t>(c * 4 + PHASE * 2) * 2 * p.n_max * 128;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) { fa[i] = 0.f; fb[i] = 0.f; }
-          for (int c = c0; c <= c1; ++c) {
-            const long long bc = __ldg(span + c);
-            if (bc == __ldg(span + c + 1)) continue;  // CTA with an empty range
-            const int sl = PHASE * 2 + ((bc >= sg.tile_iter0) ? 0 : 1);
-            const float* pp = p.partials + static_cast<size_t>(c * 4 + sl) * 2 * p.n_max * 128;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              if (j0 + i < sg.n_cnt) {
-                fa[i] += __ldcg(pp + static_cast<size_t>(j0 + i) * 128 + r);
-                fb[i] += __ldcg(pp + static_cast<size_t>(p.n_max + j0 + i) * 128 + r);
-              }
+          for (int i = 0; i < 16; ++i) {
+            if (j0 + i < sg.n_cnt) {
+              fa[i] += __ldcg(pp + static_cast<size_t>(j0 + i) * 128 + r);
+              fb[i] += __ldcg(pp + static_cast<size_t>(p.n_max + j0 + i) * 128 + r);
             }
           }
-          finish_chunk<PHASE>(p, sg, r, j0, fa, fb);
         }
-        done = true;
+        finish_chunk<PHASE>(p, sg, r, j0, fa, fb, sm.col_w, sm.col_tok);
       }
+      tc_fence_before();
+      mbar_arrive(&sm.acce[buf]);
+      done = true;
     }
     if (PHASE == 0 && done) {
       // this gate_up tile's h rows are written: count it towards its
@@ -537,11 +568,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                        const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem sm;
-  sm.base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  sm.S = p.stages;
-  sm.b_bytes = p.n_max * 128;
-  sm.stage_bytes = 2 * kTileBytesA + 2 * sm.b_bytes;
-  uint8_t* ctrl = sm.base + sm.S * sm.stage_bytes;
+  // [control words | stages]: the control block comes first so that the
+  // barriers exist before the stage size is known
+  uint8_t* ctrl = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  sm.base = ctrl + kCtrlBytes;
   sm.full = reinterpret_cast<uint64_t*>(ctrl);
   sm.empty = sm.full + kMaxStages;
   sm.accf = sm.empty + kMaxStages;
@@ -551,11 +581,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   sm.abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   sm.bcast = reinterpret_cast<int*>(tmem_slot + 2);
   sm.s_ok = reinterpret_cast<int*>(tmem_slot + 3);
-  sm.rowoff = reinterpret_cast<long long*>(ctrl + 256);
+  sm.rowoff = reinterpret_cast<long long*>(ctrl + kCtrlRowOff);
+  sm.span = reinterpret_cast<long long*>(ctrl + kCtrlSpans);
+  sm.col_w = reinterpret_cast<float*>(ctrl + kCtrlCols);
+  sm.col_tok = reinterpret_cast<int*>(ctrl + kCtrlCols + 4 * 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < sm.S; ++s) {
+    for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(&sm.full[s], 1 + 32);
       mbar_init(&sm.empty[s], 1);
     }
@@ -579,16 +612,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc(tmem_slot, p.tmem_cols);
     tmem_relinquish();
   }
+  for (int i = threadIdx.x; i < 2 * (static_cast<int>(gridDim.x) + 1); i += blockDim.x) sm.span[i] = p.spans[i];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   const int ng = p.header->ngroups;
+  // Stages are sized for the widest token tile this forward actually has,
+  // so narrow tiles (decode) get more stages in the same shared memory.
+  sm.b_bytes = p.header->n_eff * 128;
+  sm.stage_bytes = 2 * kTileBytesA + 2 * sm.b_bytes;
+  sm.S = min(kMaxStages, p.stage_space / static_cast<int>(sm.stage_bytes));
   // this CTA's cost-balanced spans of the gate_up and down iterations
   const int G1 = gridDim.x + 1;
-  const long long bs[2] = {p.spans[blockIdx.x], p.spans[G1 + blockIdx.x]};
-  const long long es[2] = {p.spans[blockIdx.x + 1], p.spans[G1 + blockIdx.x + 1]};
+  const long long bs[2] = {sm.span[blockIdx.x], sm.span[G1 + blockIdx.x]};
+  const long long es[2] = {sm.span[blockIdx.x + 1], sm.span[G1 + blockIdx.x + 1]};
   const int gs[2] = {p.span_groups[blockIdx.x], p.span_groups[G1 + blockIdx.x]};
 
   if (warp == 0) {

@@ -16,7 +16,7 @@ enum : int32_t { kStatusTimeout = 5 };
 // info values: which wait ran out
 enum : int32_t {
   kInfoEmpty = 1, kInfoFull = 2, kInfoAccFull = 3, kInfoAccEmpty = 4,
-  kInfoGatherEmpty = 5, kInfoDrain = 6, kInfoReady = 7
+  kInfoGatherEmpty = 5, kInfoDrain = 6, kInfoReady = 7, kInfoFixup = 8
 };
 
 // ----------------------------------------------------------------------------
@@ -44,7 +44,7 @@ struct GemmHeader {
   int32_t ngroups;
   int32_t gu_tiles;
   int32_t dn_tiles;
-  int32_t pad;
+  int32_t n_eff;  // widest token tile of this forward (multiple of 16, <= n_max)
   int64_t gu_iters;
   int64_t dn_iters;
 };
@@ -60,6 +60,14 @@ constexpr int kHalfRows = 128;
 constexpr int kTileBytesA = kHalfRows * kBlockK * 2;  // one half, bf16: 16 KB
 constexpr int kGemmThreads = 224;                     // 7 warps
 constexpr int kMaxStages = 8;
+// shared-memory control block: barriers and flags, the gather's row table
+// (<= 256 rows), both GEMMs' CTA span tables (<= kMaxGrid CTAs) and the
+// down epilogue's per-column weight and token (<= 256 columns)
+constexpr int kCtrlBytes = 8192;
+constexpr int kCtrlRowOff = 256;
+constexpr int kCtrlSpans = 256 + 256 * 8;
+constexpr int kCtrlCols = 6144;
+constexpr int kMaxGrid = (kCtrlCols - kCtrlSpans) / 16 - 1;
 constexpr int kGatherLag = 2;                         // cp.async groups in flight (<= stages - 1)
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -90,7 +98,7 @@ struct GemmParams {
   const int32_t* sorted_pair;  // [T*K]
   int T, K, TK, H, I_ld;
   int n_max;                   // token tile width, multiple of 16, <= 256
-  int stages;
+  int stage_space;             // shared-memory bytes for the stage ring
   int nbuf;                    // TMEM accumulator buffers (1 or 2)
   uint32_t tmem_cols;
   float swiglu_limit;

@@ -262,7 +262,14 @@ __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* 
   long long* s_cost0 = s_buf;              // [groups + 1]
   long long* s_cost1 = s_buf + 1040;       // [groups + 1]
   __shared__ int s_ngroups;
+  __shared__ int s_neff;
   __shared__ long long s_tot[4];           // gate_up iters, down iters, gate_up cost, down cost
+  if (tid == 0) s_neff = 16;
+  __syncthreads();
+  // widest token tile: the largest count (capped at n_max), shared expert included
+  for (int e = tid; e < E; e += blockDim.x)
+    if (s_cnt[e] > 0) atomicMax(&s_neff, min(n_max, (s_cnt[e] + 15) & ~15));
+  if (tid == 0 && Is > 0) atomicMax(&s_neff, min(n_max, (T + 15) & ~15));
   __syncthreads();
   if (warp == 0) {
     int g = 0, gu_t = 0, dn_t = 0;
@@ -356,7 +363,7 @@ __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* 
       hd.ngroups = g;
       hd.gu_tiles = gu_t;
       hd.dn_tiles = dn_t;
-      hd.pad = 0;
+      hd.n_eff = s_neff;
       hd.gu_iters = gu_i;
       hd.dn_iters = dn_i;
       *header = hd;
