@@ -36,7 +36,10 @@ from moe_ffn_speculative_gb300 import synthetic as S  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "MoE-FFN layer tokens/s at T=72 on 1 GB300"
 UNIT = "tokens/s"
-KERNEL_SRC = os.path.join(ROOT, "moe_ffn_speculative_gb300", "csrc", "gemm.cu")
+CSRC = os.path.join(ROOT, "moe_ffn_speculative_gb300", "csrc")
+# per expert schedule: the dominant kernel, its ncu summary prefix, its source
+KERNELS = {"stream_k": ("moe_experts_kernel", "experts_kernel", "gemm.cu"),
+           "slice": ("moe_slice_kernel", "slice_kernel", "slice.cu")}
 
 
 def parse():
@@ -48,6 +51,8 @@ def parse():
     ap.add_argument("--config", default="qwen3_8b_dspark", choices=list(S.CONFIGS))
     ap.add_argument("--tokens", type=int, default=None, help="override T of the workload")
     ap.add_argument("--experts", type=int, default=None, help="override E (small profiling cases)")
+    ap.add_argument("--schedule", default="auto", choices=["auto", "stream_k", "slice"],
+                    help="expert schedule (auto: the library's choice for the shape)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -161,10 +166,11 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def ncu_traffic(workload: str):
-    """Per-launch DRAM traffic of the expert-GEMM kernel from the committed ncu
-    summary, or None when the kernel source changed since the capture."""
-    path = os.path.join(ROOT, "profiles", f"experts_kernel_{workload}.md")
+def ncu_traffic(schedule: str, workload: str):
+    """Per-launch DRAM traffic of the schedule's dominant kernel from the
+    committed ncu summary, or None when its source changed since the capture."""
+    _, prefix, src = KERNELS[schedule]
+    path = os.path.join(ROOT, "profiles", f"{prefix}_{workload}.md")
     if not os.path.exists(path):
         return None
     with open(path) as f:
@@ -173,7 +179,7 @@ def ncu_traffic(workload: str):
     h = re.search(r"kernel_source_sha256\s*=\s*([0-9a-f]{64})", text)
     if not m or not h:
         return None
-    with open(KERNEL_SRC, "rb") as f:
+    with open(os.path.join(CSRC, src), "rb") as f:
         cur = hashlib.sha256(f.read()).hexdigest()
     return float(m.group(1)) if cur == h.group(1) else None
 
@@ -268,6 +274,10 @@ def run_gpu(args, cfg, rank, world):
     K = args.steps if args.steps is not None else 20000
     W = max(3, args.warmup if args.warmup is not None else 50)
     rec = ops.Recipe.from_config(cfg)
+    ops.set_schedule({"auto": ops.SCHEDULE_AUTO, "stream_k": ops.SCHEDULE_STREAM_K,
+                      "slice": ops.SCHEDULE_SLICE}[args.schedule])
+    sched = ops.SCHEDULE_NAMES[ops.ffn_schedule(cfg.T, cfg.H, cfg.I, cfg.shared_I, rec,
+                                                gated=cfg.shared_gated and cfg.shared_I > 0)]
     base = S.make_inputs(cfg, device=dev, seed=cfg.seed + 1000 * rank)
     n_copies = max(2, -(-4 * L2_BYTES // (cfg.weight_bytes + 1)))
     layers = [base]
@@ -345,11 +355,14 @@ def run_gpu(args, cfg, rank, world):
             fwd(i)
     ops.set_profile_events(None)
     torch.cuda.synchronize()
-    names = ["router", "experts", "combine"]
-    launched = 3 if (cfg.K > 1 or cfg.shared_I > 0) else 2
-    per_kernel = {}
-    for k in range(launched):
-        per_kernel[names[k]] = float(np.mean([e[2 * k].elapsed_time(e[2 * k + 1]) for e in evs])) * 1e3  # us
+    if sched == "slice":
+        # one fused launch, recorded as the expert-GEMM pair
+        launched, timed = 1, {"fused": 1}
+    else:
+        launched = 3 if (cfg.K > 1 or cfg.shared_I > 0) else 2
+        timed = {n: k for k, n in enumerate(["router", "experts", "combine"][:launched])}
+    per_kernel = {n: float(np.mean([e[2 * k].elapsed_time(e[2 * k + 1]) for e in evs])) * 1e3  # us
+                  for n, k in timed.items()}
 
     # end to end: pinned host x -> device, forward, device y -> pinned host, every step
     x_host = base["x"].cpu().pin_memory()
@@ -378,11 +391,14 @@ def run_gpu(args, cfg, rank, world):
 
     hbm, tflops, peak_src = measured_peaks()
     layer_bytes, ex_bytes, flops = algorithmic(cfg, u)
-    t_ex = per_kernel["experts"] * 1e-6
+    if sched == "slice":
+        # the fused launch is the whole layer: its algorithmic bytes are the layer's
+        ex_bytes = layer_bytes
+    t_ex = per_kernel["fused" if sched == "slice" else "experts"] * 1e-6
     achieved = ex_bytes / t_ex / 1e9
     layer_gbs = layer_bytes / (ms_step * 1e-3) / 1e9
     roof_layer_us = max(layer_bytes / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
-    traffic = ncu_traffic(cfg.name if args.tokens is None and args.experts is None else
+    traffic = ncu_traffic(sched, cfg.name if args.tokens is None and args.experts is None else
                           f"{cfg.name}_T{cfg.T}_E{cfg.E}")
 
     if rank != 0:
@@ -393,10 +409,11 @@ def run_gpu(args, cfg, rank, world):
         "us_per_layer": ms_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "I": cfg.I, "K": cfg.K,
-                   "shared_I": cfg.shared_I, "touched_experts": u, "launch": "cuda_graph_replay",
+                   "shared_I": cfg.shared_I, "touched_experts": u, "schedule": sched,
+                   "launch": "cuda_graph_replay",
                    "l2": f"weights rotate over {n_copies} copies ({n_copies * cfg.weight_bytes / 1e9:.2f} GB) > L2",
                    "parallelism": "replicas" if world > 1 else "single_gpu"},
-        "roofline": {"bound": "hbm", "kernel": "moe_experts_kernel", "achieved": achieved, "peak": hbm,
+        "roofline": {"bound": "hbm", "kernel": KERNELS[sched][0], "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic, "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": ex_bytes},
         "layer_roofline": {"bytes": layer_bytes, "flops": flops, "roofline_us": roof_layer_us,

@@ -196,6 +196,39 @@ MOE_API moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I,
                            moe_bf16* y, int32_t* topk_idx_out, float* topk_w_out,
                            int32_t* counts_out, cudaStream_t stream);
 
+/* Expert schedules of moe_ffn_forward():
+ *   MOE_SCHEDULE_STREAM_K  a router launch (logits, top-k, permutation, work
+ *       list); one persistent launch of both expert GEMMs that streams the
+ *       touched experts' weight k-blocks split evenly over the SMs; the
+ *       weighted combine (skipped for K == 1 without a shared expert).
+ *   MOE_SCHEDULE_SLICE     one persistent launch for layers with few experts
+ *       that every forward touches: one CTA per (expert, 128-row slice of I),
+ *       the gate_up GEMM over all T tokens started before the routing is
+ *       known, the router on spare CTAs, and a deterministic sum of the
+ *       per-slice partial outputs.  An expert no token picked stops streaming
+ *       once the routing is known.  Shape limits: T <= 128, E (+1 with
+ *       sh_gate) <= 16, E*ceil(I/128) + ceil(Is/128) + ceil(T/7) <= SMs.
+ *   MOE_SCHEDULE_AUTO      SLICE where the shape fits and, under uniform
+ *       routing, the expected number of untouched experts E*(1-K/E)^T is at
+ *       most 0.25; STREAM_K otherwise.
+ * Both give the same routing; outputs agree to fp32 summation order. */
+typedef enum {
+  MOE_SCHEDULE_AUTO = 0,
+  MOE_SCHEDULE_STREAM_K = 1,
+  MOE_SCHEDULE_SLICE = 2
+} moe_schedule;
+
+/* Per calling thread: the schedule later moe_ffn_forward() calls use.  A
+ * forced MOE_SCHEDULE_SLICE still runs STREAM_K where the shape does not fit.
+ * Returns MOE_ERR_INVALID_ARG for an unknown value. */
+MOE_API moe_status moe_set_schedule(int schedule);
+
+/* The schedule moe_ffn_forward() would run for this shape on the current
+ * device under the calling thread's setting: MOE_SCHEDULE_STREAM_K or
+ * MOE_SCHEDULE_SLICE, or -1 for invalid arguments.  gated != 0 when sh_gate
+ * will be passed. */
+MOE_API int moe_ffn_schedule(int T, int H, int I, int Is, const moe_recipe* recipe, int gated);
+
 /* Synchronises `stream`, reads the device status word of a workspace used by
  * moe_route() or moe_ffn_forward(), and clears it.  Returns MOE_OK or the
  * first device-side error recorded (MOE_ERR_DEVICE_TIMEOUT); *info_out (if
@@ -207,7 +240,9 @@ MOE_API moe_status moe_get_device_status(void* ws, cudaStream_t stream, int32_t*
  * for i < n_pairs, on its stream.  Per calling thread; NULL turns it off.
  * The launch order is: router, expert GEMMs (gate_up and down in one
  * persistent launch), combine (skipped when K == 1 and there is no shared
- * expert). */
+ * expert).  Under MOE_SCHEDULE_SLICE the one fused launch is recorded as the
+ * expert-GEMM pair; the router pair is recorded empty (both events at the
+ * same point) and the combine pair not at all. */
 MOE_API void moe_set_profile_events(void* const* events, int n_pairs);
 
 #ifdef __cplusplus

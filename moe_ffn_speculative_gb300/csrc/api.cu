@@ -1,6 +1,7 @@
 // C ABI of libmoe_gb300.so: argument validation, workspace layout, TMA
 // descriptors and the launch sequence of the MoE-FFN layer forward.  The
 // contract of every entry point is documented in include/moe.h.
+#include <math.h>
 #include <string.h>
 
 #include <mutex>
@@ -20,6 +21,7 @@ int g_sms[kMaxDevices];
 
 thread_local void* const* t_events = nullptr;
 thread_local int t_nev = 0;
+thread_local int t_schedule = MOE_SCHEDULE_AUTO;
 
 int device_sms() {
   int d = 0;
@@ -64,6 +66,20 @@ bool encode_weights_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// x [T][H] bf16 in boxes of 64 columns x box_rows tokens with the 128-byte
+// swizzle; rows past T read as zero.
+bool encode_x_2d(CUtensorMap* m, const void* base, uint64_t H, uint64_t T, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {H, T};
+  cuuint64_t strides[1] = {H * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -103,15 +119,53 @@ RouterGeom router_geometry(int T, int E_tot, int sms) {
   return g;
 }
 
+// Geometry of the fused small-expert-count kernel (slice.cu).  ok: the
+// layer fits it at this T.  reserve: some T' <= T does, so a workspace sized
+// for T holds its regions (sized for min(T, kSliceMaxTok) tokens).
+struct SlicePlan {
+  bool ok, reserve;
+  int n_tok, s_e, s_sh, s_max, n_units, n_mt, n_rcta, n_tg, stage_space;
+};
+
+SlicePlan slice_plan(int T, int H, int I, int Is, int E, bool gated, int sms) {
+  SlicePlan s;
+  memset(&s, 0, sizeof(s));
+  if (T < 1 || E + (gated ? 1 : 0) > kSliceMaxExperts) return s;
+  const int Tr = T < kSliceMaxTok ? T : kSliceMaxTok;
+  s.n_tok = ((Tr + 15) / 16) * 16;
+  s.s_e = ceil_div(I, kHalfRows);
+  s.s_sh = Is > 0 ? ceil_div(Is, kHalfRows) : 0;
+  s.s_max = s.s_e > s.s_sh ? s.s_e : s.s_sh;
+  s.n_units = E * s.s_e + s.s_sh;
+  s.n_mt = ceil_div(H, kHalfRows);
+  s.n_rcta = ceil_div(Tr, kSliceTokPerTask);
+  s.n_tg = ceil_div(Tr, kSliceTokPerTask);
+  s.stage_space = kSmemLimit - 1024 - kSliceCtrlBytes;
+  // four stages at least: their token-tile parts later hold h (2 k-blocks x hi/lo)
+  const bool smem_ok = s.stage_space / (2 * kTileBytesA + kSliceMaxTok * 128) >= 4;
+  s.reserve = smem_ok && s.n_units + 1 <= sms;
+  s.ok = s.reserve && T <= kSliceMaxTok && s.n_units + s.n_rcta <= sms;
+  return s;
+}
+
+// The fused kernel streams every expert's gate_up weights from the start,
+// before the routing is known, and stops an untouched expert once it is: it
+// pays off when, under uniform routing, untouched experts are rare.
+bool slice_expected(int T, int E, int K) {
+  const double miss = E * pow(1.0 - static_cast<double>(K) / E, static_cast<double>(T));
+  return miss <= 0.25;
+}
+
 struct Layout {
   RouterGeom rg;
+  SlicePlan sp;
   int n_max, nbuf, grid, I_ld;
   uint32_t tmem_cols;
   size_t smem;
   int max_gu_tiles, max_dn_tiles, g_max;
   bool need_out;
   size_t o_status, o_cnt, o_tiles, o_logits, o_shl, o_shw, o_idx, o_w, o_counts, o_offsets, o_sp, o_pp, o_groups,
-      o_header, o_spans, o_span_groups, o_partials, o_h, o_out, total;
+      o_header, o_spans, o_span_groups, o_partials, o_h, o_out, o_sync, o_ready, o_hbuf, o_sout, total;
 };
 
 Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sms) {
@@ -165,11 +219,31 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   L.o_h = o; o = align_up(o + 2 * 2 * rows * L.I_ld);
   L.o_out = o;
   if (L.need_out) o = align_up(o + 4 * rows * H);
+  // fused small-expert-count kernel: counters and the per-slice partial outputs
+  L.sp = slice_plan(T, H, I, Is, E, gated, sms);
+  L.o_sync = L.o_ready = L.o_hbuf = L.o_sout = 0;
+  if (L.sp.reserve) {
+    // counters, slice-ready flags, every expert's h tiles (2 per slice, each
+    // 2*n_tok rows of 128 bytes) and the pair outputs for the combine
+    const int Tr = T < kSliceMaxTok ? T : kSliceMaxTok;
+    const size_t slots = static_cast<size_t>(Tr) * K + Tr;
+    const size_t n_es = static_cast<size_t>(E) + 1;
+    L.o_sync = o; o = align_up(o + 4 * static_cast<size_t>(kSliceSyncWords + L.sp.n_mt));
+    L.o_ready = o; o = align_up(o + 4 * n_es * L.sp.s_max);
+    L.o_hbuf = o; o = align_up(o + n_es * 2 * L.sp.s_max * 2 * static_cast<size_t>(L.sp.n_tok) * 128);
+    L.o_sout = o;
+    if (K > 1 || Is > 0) o = align_up(o + 4 * slots * H);
+  }
   L.total = o;
   return L;
 }
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+bool use_slice(const Layout& L, int T, int E, int K) {
+  if (!L.sp.ok || t_schedule == MOE_SCHEDULE_STREAM_K) return false;
+  return t_schedule == MOE_SCHEDULE_SLICE || slice_expected(T, E, K);
+}
 
 void record_event_on(int i, cudaStream_t s) {
   if (t_events && i < 2 * t_nev && t_events[i]) cudaEventRecord(static_cast<cudaEvent_t>(t_events[i]), s);
@@ -293,7 +367,7 @@ moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf1
   if (T == 0) return MOE_OK;
   if (!x || !gate || !w_gate_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(gate) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(y) ||
-      (sh_gate_up && !aligned16(sh_gate_up)) || (sh_down && !aligned16(sh_down)))
+      (sh_gate_up && !aligned16(sh_gate_up)) || (sh_down && !aligned16(sh_down)) || (sh_gate && !aligned16(sh_gate)))
     return MOE_ERR_INVALID_ARG;
   const size_t xy_bytes = static_cast<size_t>(T) * H * 2;
   if (overlaps(x, xy_bytes, y, xy_bytes)) return MOE_ERR_INVALID_ARG;
@@ -315,6 +389,46 @@ moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf1
   int32_t* tiles = reinterpret_cast<int32_t*>(w + L.o_tiles);
   uint16_t* h = reinterpret_cast<uint16_t*>(w + L.o_h);
   float* out_ws = reinterpret_cast<float*>(w + L.o_out);
+
+  if (use_slice(L, T, E, K)) {
+    // ---- fused small-expert-count schedule: one launch
+    CUtensorMap tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, tm_x;
+    if (!encode_weights_3d(&tm_gu, w_gate_up, H, I, 2ull * E) || !encode_weights_3d(&tm_dn, w_down, I, H, E) ||
+        !encode_x_2d(&tm_x, x, H, T, static_cast<uint32_t>(L.sp.n_tok)))
+      return MOE_ERR_CUDA;
+    if (Is > 0) {
+      if (!encode_weights_3d(&tm_gu_sh, sh_gate_up, H, Is, 2) || !encode_weights_3d(&tm_dn_sh, sh_down, Is, H, 1))
+        return MOE_ERR_CUDA;
+    } else {
+      tm_gu_sh = tm_gu;
+      tm_dn_sh = tm_dn;
+    }
+    SliceParams sp;
+    memset(&sp, 0, sizeof(sp));
+    sp.x = x; sp.gate = gate; sp.router_bias = router_bias; sp.sh_gate = sh_gate;
+    sp.sel = SelCfg{E, K, recipe->score_fn, recipe->n_group, recipe->topk_group, recipe->group_topn,
+                    recipe->norm_topk_prob, recipe->norm_eps, recipe->route_scale, expert_bias};
+    sp.T = T; sp.H = H; sp.E = E; sp.K = K; sp.TK = T * K;
+    sp.n_tok = L.sp.n_tok; sp.s_e = L.sp.s_e; sp.s_sh = L.sp.s_sh; sp.s_max = L.sp.s_max;
+    sp.n_units = L.sp.n_units; sp.n_mt = L.sp.n_mt; sp.n_rcta = L.sp.n_rcta; sp.n_tg = L.sp.n_tg;
+    sp.stage_space = L.sp.stage_space;
+    sp.swiglu_limit = recipe->swiglu_limit;
+    sp.logits = reinterpret_cast<float*>(w + L.o_logits);
+    sp.idx = idx; sp.w = wts; sp.sh_w = sh_w; sp.counts = counts;
+    sp.hbuf = reinterpret_cast<uint8_t*>(w + L.o_hbuf);
+    sp.ready = reinterpret_cast<int32_t*>(w + L.o_ready);
+    sp.out = reinterpret_cast<float*>(w + L.o_sout);
+    sp.direct_y = (K == 1 && Is == 0) ? 1 : 0;
+    sp.y = y;
+    sp.sync = reinterpret_cast<int32_t*>(w + L.o_sync);
+    sp.status = status;
+    record_event_on(0, stream);
+    record_event_on(1, stream);
+    record_event_on(2, stream);
+    const cudaError_t e = launch_slice(tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, tm_x, sp, L.grid, kSmemLimit, stream);
+    record_event_on(3, stream);
+    return cuda_status(e);
+  }
 
   // ---- 1. router + permutation + work list
   RouteParams rp;
@@ -394,6 +508,22 @@ moe_status moe_get_device_status(void* ws, cudaStream_t stream, int32_t* info_ou
   if (info_out) *info_out = words[1];
   if (words[0] != 0 && cudaMemset(ws, 0, sizeof(words)) != cudaSuccess) return MOE_ERR_CUDA;
   return static_cast<moe_status>(words[0]);
+}
+
+moe_status moe_set_schedule(int schedule) {
+  if (schedule != MOE_SCHEDULE_AUTO && schedule != MOE_SCHEDULE_STREAM_K && schedule != MOE_SCHEDULE_SLICE)
+    return MOE_ERR_INVALID_ARG;
+  t_schedule = schedule;
+  return MOE_OK;
+}
+
+int moe_ffn_schedule(int T, int H, int I, int Is, const moe_recipe* recipe, int gated) {
+  if (check_recipe(recipe) != MOE_OK || T < 0 || H < 8 || I < 8 || Is < 0) return -1;
+  const int sms = device_sms();
+  if (sms <= 0) return -1;
+  const int E = recipe->num_experts, K = recipe->top_k;
+  const Layout L = make_layout(T, H, I, Is, E, K, gated != 0 && Is > 0, sms);
+  return use_slice(L, T, E, K) ? MOE_SCHEDULE_SLICE : MOE_SCHEDULE_STREAM_K;
 }
 
 void moe_set_profile_events(void* const* events, int n_pairs) {

@@ -33,14 +33,8 @@
 namespace moe {
 namespace {
 
-__device__ __forceinline__ uint16_t f2bf(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-__device__ __forceinline__ void record_failure(int32_t* status, volatile int* abort_flag, int32_t info) {
-  if (atomicCAS(status, 0, kStatusTimeout) == 0) atomicExch(status + 1, info);
-  *abort_flag = 1;
-}
 
 struct Seg {
   int expert, row_base, count, idim;
@@ -165,20 +159,7 @@ __device__ __forceinline__ void u32_to_f32(const uint32_t (&u)[16], float (&f)[1
   for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(u[i]);
 }
 
-__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 
-// Position in the ring of shared-memory stages (each role keeps its own).
-struct Ring {
-  int stage = 0;
-  uint32_t phase = 0;
-  __device__ void next(int S) {
-    if (++stage == S) { stage = 0; phase ^= 1u; }
-  }
-};
 
 // The CTA's shared memory: S stages of [A gate|A up or two 128-row output
 // halves (16 KB each) | B tile (n_max x 64 bf16) | second B tile (h_lo)],

@@ -6,6 +6,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#ifdef __CUDACC__
+#include <cuda_bf16.h>
+#endif
 
 namespace moe {
 
@@ -16,7 +19,8 @@ enum : int32_t { kStatusTimeout = 5 };
 // info values: which wait ran out
 enum : int32_t {
   kInfoEmpty = 1, kInfoFull = 2, kInfoAccFull = 3, kInfoAccEmpty = 4,
-  kInfoGatherEmpty = 5, kInfoDrain = 6, kInfoReady = 7, kInfoFixup = 8
+  kInfoGatherEmpty = 5, kInfoDrain = 6, kInfoReady = 7, kInfoFixup = 8,
+  kInfoRouter = 9, kInfoTileCount = 10, kInfoHReady = 11
 };
 
 // ----------------------------------------------------------------------------
@@ -115,6 +119,14 @@ struct GemmParams {
   int32_t* status;
 };
 
+// Routing recipe as the selection code reads it (score_fn 0 softmax,
+// 1 sigmoid, 2 sqrt(softplus); renorm = norm_topk_prob).
+struct SelCfg {
+  int E, K, score_fn, n_group, topk_group, group_topn, renorm;
+  float eps, scale;
+  const float* expert_bias;
+};
+
 struct RouteParams {
   const uint16_t* x;
   const uint16_t* gate;
@@ -148,6 +160,43 @@ struct RouteParams {
   int zero_count;
 };
 
+// Fused small-expert-count forward (slice.cu): one CTA per (expert, 128-row
+// slice of its intermediate dimension), the router on spare CTAs.
+struct SliceParams {
+  const uint16_t* x;           // [T,H]
+  const uint16_t* gate;        // [E,H]
+  const float* router_bias;    // [E] (nullable)
+  const uint16_t* sh_gate;     // [H] (nullable)
+  SelCfg sel;
+  int T, H, E, K, TK;
+  int n_tok;                   // gate_up MMA width: T rounded up to 16 (<= kSliceMaxTok)
+  int s_e, s_sh;               // 128-row slices of a routed expert / of the shared expert (0: none)
+  int s_max;                   // max(s_e, s_sh)
+  int n_units;                 // E * s_e + s_sh
+  int n_mt;                    // 128-row output tiles: ceil(H / 128)
+  int n_rcta;                  // router CTAs (after the unit CTAs)
+  int n_tg;                    // token groups of the combine (kSliceTokPerTask tokens each)
+  int stage_space;             // shared-memory bytes for the stage rings
+  int direct_y;                // top-1 without a shared expert: the down epilogue writes y
+  float swiglu_limit;
+  float* logits;               // [T,E]
+  int32_t* idx;                // [T*K]
+  float* w;                    // [T*K]
+  float* sh_w;                 // [T] shared-expert weight (gate, or 1)
+  int32_t* counts;             // [E]
+  uint8_t* hbuf;               // [(E+1) * 2*s_max] h tiles of 2*n_tok rows x 128 B (see slice.cu)
+  int32_t* ready;              // [(E+1) * s_max] slice of h written
+  float* out;                  // [T*K + T, H] fp32 weighted expert outputs (unless direct_y)
+  uint16_t* y;                 // [T,H]
+  int32_t* sync;               // [kSliceSyncWords + n_mt]: router done, task counter, exit counter, -, tile counts
+  int32_t* status;
+};
+constexpr int kSliceMaxTok = 128;
+constexpr int kSliceMaxExperts = 16;  // routed experts + the shared-expert gate row
+constexpr int kSliceTokPerTask = 7;   // one token per warp of a reduction task
+constexpr int kSliceSyncWords = 4;
+constexpr int kSliceCtrlBytes = 4096;  // control block at the start of shared memory
+
 // launchers (route.cu, gemm.cu, combine.cu); return cudaError_t
 cudaError_t launch_route(const RouteParams& p, int tb, cudaStream_t s);
 cudaError_t launch_select_from_logits(const float* logits, int T, int E, int K, const float* expert_bias,
@@ -159,6 +208,9 @@ cudaError_t launch_permute(const int32_t* idx, int T, int K, int E, int32_t* cou
 cudaError_t launch_experts(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, const CUtensorMap& tm_dn,
                            const CUtensorMap& tm_dn_sh, const GemmParams& p, int grid, size_t smem_bytes,
                            cudaStream_t s);
+cudaError_t launch_slice(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, const CUtensorMap& tm_dn,
+                         const CUtensorMap& tm_dn_sh, const CUtensorMap& tm_x, const SliceParams& p, int grid,
+                         size_t smem_bytes, cudaStream_t s);
 cudaError_t launch_combine(const float* out_ws, const int32_t* pair_pos, int T, int K, int H,
                            int has_shared, uint16_t* y, cudaStream_t s);
 
@@ -196,6 +248,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of the phase of `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Waits for the phase of `parity` to complete; returns false if the CTA's
 // abort flag (when given) is raised or the wait runs past kWaitLimitCycles.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
@@ -223,6 +285,20 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       "[%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+      "[%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+// Contiguous bulk copy global -> shared (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -279,6 +355,12 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr)
       : "memory");
 }
+// 32 lanes x one 32-bit column.
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
+  return r;
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor of a K-major tile with 128-byte swizzle:
@@ -292,6 +374,32 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   d |= static_cast<uint64_t>(2) << 61;                  // 128-byte swizzle
   return d;
 }
+
+// ---- small helpers shared by the GEMM kernels
+__device__ __forceinline__ uint16_t f2bf(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void record_failure(int32_t* status, volatile int* abort_flag, int32_t info) {
+  if (atomicCAS(status, 0, kStatusTimeout) == 0) atomicExch(status + 1, info);
+  *abort_flag = 1;
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Position in the ring of shared-memory stages (each role keeps its own).
+struct Ring {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ void next(int S) {
+    if (++stage == S) { stage = 0; phase ^= 1u; }
+  }
+};
+
 #endif  // __CUDACC__
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A

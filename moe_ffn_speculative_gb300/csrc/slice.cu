@@ -1,0 +1,771 @@
+// Fused MoE-FFN forward for layers with few experts that every forward
+// touches (e.g. 8 experts, top-1, a verify batch of 72 tokens): router,
+// grouped SwiGLU experts, shared expert and weighted combine in one
+// persistent launch.
+//
+// Sources (web pages): SpecForge PR #1033 "MoE FFN for DFlash-family drafts:
+// the module", section "Router" (score -> select -> routing_weights);
+// SpecForge PR #1073 "MoE drafts: DeepSeek-V4.1's own DSpark draft" (fused
+// gate_up_proj [E,2I,H] and down_proj [E,H,I]; rows [0,I) of gate_up are the
+// gate); SpecForge PR #941's follow-up comment (clamped SwiGLU); sglang PR
+// #48763 "[Feat] dflash: Serve MoE FFN drafts for DFlash and DSpark", commit
+// note on DraftMoE forward (routing weight times each expert's output, plus
+// the shared expert).
+//
+// Work split.  CTA u < n_units owns unit (expert, s): slice s of 128 rows of
+// the expert's intermediate dimension in the gate_up GEMM, and a share of
+// the expert's 128-row output tiles in the down GEMM, so each unit streams
+// about the same weight bytes and every weight byte is streamed once.
+//   gate_up: 2 x 128 gate/up rows over H for ALL T tokens (x comes from L2
+//     by TMA; the tensor pipe has room to spare).  It needs no routing and
+//     starts at once, while the router runs on the CTAs after the units.  The
+//     routing then picks the expert's tokens: their h = SwiGLU(gate, up) goes
+//     to a global buffer, as the bf16 pair hi + lo already laid out as the
+//     down GEMM's shared-memory operand, and the slice is flagged ready.
+//   down: each output tile accumulates over the expert's whole intermediate
+//     dimension, starting with the unit's own slice, the other slices' h
+//     fetched (bulk copy) once their units flag them.  The epilogue applies
+//     the routing weight and writes y directly (top-1, no shared expert) or
+//     the pair's fp32 output row.
+// An expert that no token picked stops streaming as soon as the routing is
+// known and skips its down GEMM.  With top-k > 1 or a shared expert, combine
+// tasks (output tile, group of tokens), taken in tile order by every CTA
+// without other work, wait until every expert has finished the tile and sum
+// the pair outputs in slot order: the result does not depend on timing.
+//
+// Unit CTA warp roles (224 threads): warp 0 issues the weight TMA loads,
+// warp 1 allocates TMEM and issues the MMAs, warp 2 builds the unit's token
+// list, then fetches the down GEMM's h tiles and publishes finished output
+// tiles; warps 3..6 drain TMEM (SwiGLU into h, then the outputs).
+#include <cuda_bf16.h>
+
+#include "moe_internal.cuh"
+#include "select.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kSliceThreads = 224;  // 7 warps
+constexpr uint32_t kSliceTmemCols = 512;
+
+static_assert(kSliceTokPerTask == kSliceThreads / 32, "one combine token per warp");
+
+struct SliceSmem {
+  uint8_t* base;   // stage rings (gate_up and down use the same memory in turn)
+  uint8_t* bbase;  // gate_up: the token tiles after the S weight parts
+  uint32_t b_bytes;
+  int S;
+  uint64_t *full, *empty, *fullB, *emptyB, *acca, *accf, *acce, *routed, *drain;
+  volatile int* abort_flag;
+  volatile int* kb_stop;  // first gate_up k-block the producer did not issue
+  volatile int* n_e;      // tokens routed to this unit's expert
+  volatile int* task;
+  int* grp_cnt;           // epilogue threads' count of finished down chunks
+  uint32_t* tmem_slot;
+  int* c_tok;    // [kSliceMaxTok] token of each down-GEMM column
+  int* c_slot;   // [kSliceMaxTok] its output slot (pair t*K+k, or T*K+t for the shared expert)
+  float* c_w;    // [kSliceMaxTok] its routing weight (or shared-expert gate)
+  float* s_log;  // router: [7][33] logits of the CTA's tokens
+};
+
+__device__ __forceinline__ void carve(uint8_t* ctrl, SliceSmem& sm) {
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ctrl);
+  sm.full = bars;
+  sm.empty = bars + 8;
+  sm.fullB = bars + 16;
+  sm.emptyB = bars + 24;
+  sm.acca = bars + 32;
+  sm.accf = bars + 33;
+  sm.acce = bars + 34;
+  sm.routed = bars + 35;
+  sm.drain = bars + 36;
+  int* words = reinterpret_cast<int*>(ctrl + 320);
+  sm.tmem_slot = reinterpret_cast<uint32_t*>(words);
+  sm.abort_flag = words + 1;
+  sm.kb_stop = words + 2;
+  sm.n_e = words + 3;
+  sm.task = words + 4;
+  sm.grp_cnt = words + 5;
+  sm.c_tok = reinterpret_cast<int*>(ctrl + 512);
+  sm.c_slot = sm.c_tok + kSliceMaxTok;
+  sm.c_w = reinterpret_cast<float*>(sm.c_slot + kSliceMaxTok);
+  sm.s_log = sm.c_w + kSliceMaxTok;
+  sm.base = ctrl + kSliceCtrlBytes;
+}
+static_assert(512 + 3 * 4 * kSliceMaxTok + 4 * 7 * 33 <= kSliceCtrlBytes, "slice control block");
+
+// Bounded wait until *p >= target.  Gives up (false) after about a second,
+// or at once when another CTA has already recorded a failure.
+__device__ bool wait_count(const int32_t* p, int target, const int32_t* status) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const long long t0 = clock64();
+  while (true) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if (*reinterpret_cast<const volatile int32_t*>(status) != 0) return false;
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+}
+
+// True on every epilogue thread (named barrier 1, 128 threads) when `v` is
+// true on any of them: the four warps take each decision together.
+__device__ __forceinline__ bool epi_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, 1, 128, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void red_release_add(int32_t* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// ---------------------------------------------------------------- router CTA
+// Warp w routes token rc*7 + w: fp32 logits over the gate rows (and the
+// shared-expert gate row), then score -> select -> weights.  The CTA's x rows
+// and the gate rows are bulk-copied to shared memory in chunks of H (two
+// buffers), so every load of a chunk is in flight at once: the router runs
+// beside CTAs that keep HBM saturated, where a chain of dependent loads
+// would wait behind them.
+__device__ void route_tokens(const SliceParams& p, const SliceSmem& sm, int rc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = rc * kSliceTokPerTask;
+  const int nt = min(kSliceTokPerTask, p.T - t0);
+  const int E_tot = p.E + (p.sh_gate ? 1 : 0);
+  const int rows = kSliceTokPerTask + E_tot;  // smem rows per buffer: x rows, then gate rows
+  int hc = (p.stage_space / (2 * rows * 2)) / kBlockK * kBlockK;
+  hc = min(hc, p.H);
+  const int nchunks = ceil_div(p.H, hc);
+  uint16_t* buf[2] = {reinterpret_cast<uint16_t*>(sm.base),
+                      reinterpret_cast<uint16_t*>(sm.base) + static_cast<size_t>(rows) * hc};
+  auto issue = [&](int c) {
+    const int h0 = c * hc, len = min(hc, p.H - h0);
+    uint16_t* dst = buf[c & 1];
+    uint64_t* bar = &sm.full[c & 1];
+    const uint32_t bytes = static_cast<uint32_t>(len) * 2u;
+    mbar_arrive_expect_tx(bar, bytes * static_cast<uint32_t>(nt + E_tot));
+    for (int i = 0; i < nt; ++i)
+      bulk_load(dst + static_cast<size_t>(i) * hc, p.x + static_cast<size_t>(t0 + i) * p.H + h0, bytes, bar);
+    for (int e = 0; e < E_tot; ++e) {
+      const uint16_t* src = e < p.E ? p.gate + static_cast<size_t>(e) * p.H : p.sh_gate;
+      bulk_load(dst + static_cast<size_t>(kSliceTokPerTask + e) * hc, src + h0, bytes, bar);
+    }
+  };
+  if (threadIdx.x == 0) {
+    issue(0);
+    if (nchunks > 1) issue(1);
+  }
+  float acc[kSliceMaxExperts];
+#pragma unroll
+  for (int e = 0; e < kSliceMaxExperts; ++e) acc[e] = 0.f;
+  bool ok = true;
+  for (int c = 0; c < nchunks; ++c) {
+    ok = ok && mbar_wait(&sm.full[c & 1], static_cast<uint32_t>(c >> 1) & 1u, sm.abort_flag);
+    if (ok && warp < nt) {
+      const int len = min(hc, p.H - c * hc);
+      const uint16_t* xs = buf[c & 1] + static_cast<size_t>(warp) * hc;
+      const uint16_t* gs = buf[c & 1] + static_cast<size_t>(kSliceTokPerTask) * hc;
+      for (int i = lane * 8; i < len; i += 256) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(xs + i);
+#pragma unroll
+        for (int e = 0; e < kSliceMaxExperts; ++e)
+          if (e < E_tot) acc[e] = dot8(xv, *reinterpret_cast<const uint4*>(gs + static_cast<size_t>(e) * hc + i), acc[e]);
+      }
+    }
+    ok = __syncthreads_and(ok) != 0;  // buffer c & 1 is free again; every thread takes the same way
+    if (threadIdx.x == 0 && ok && c + 2 < nchunks) issue(c + 2);
+  }
+  if (!ok) {
+    if (threadIdx.x == 0) record_failure(p.status, sm.abort_flag, kInfoRouter);
+    return;
+  }
+  if (warp < nt) {
+    const int t = t0 + warp;
+    float* lrow = sm.s_log + warp * 33;
+#pragma unroll
+    for (int e = 0; e < kSliceMaxExperts; ++e) {
+      if (e < E_tot) {
+        float v = acc[e];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0) {
+          if (e < p.E) {
+            if (p.router_bias) v += __ldg(p.router_bias + e);
+            lrow[e] = v;
+            p.logits[static_cast<size_t>(t) * p.E + e] = v;
+          } else {
+            p.sh_w[t] = 1.f / (1.f + expf(-v));
+          }
+        }
+      }
+    }
+    if (lane == 0 && p.s_sh > 0 && !p.sh_gate) p.sh_w[t] = 1.f;
+    __syncwarp();
+    select_token<1, true>(lrow, p.sel, p.idx + static_cast<size_t>(t) * p.K, p.w + static_cast<size_t>(t) * p.K);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) red_release_add(p.sync + 0, 1);
+}
+
+// ---------------------------------------------------------------- unit CTA roles
+struct Unit {
+  bool shared;
+  int e, s;     // expert (-1: shared) and slice
+  int es;       // expert slot of the h buffer and ready flags: e, or E for the shared expert
+  int nkb;      // gate_up k-blocks: ceil(H / 64)
+  int nkb_d;    // down k-blocks: 2 per slice of the expert
+  int j0, nj;   // the unit's output tiles [j0, j0 + nj)
+};
+
+// h tile (expert slot es, down k-block kb): 2*n_tok rows of 128 bytes, the
+// K-major 128-byte-swizzled image of the MMA operand; rows [0, n16) hold
+// h_hi of the expert's picked tokens, rows [n16, 2*n16) their h_lo, so one
+// MMA of width 2*n16 computes W*h_hi and W*h_lo side by side.
+__device__ __forceinline__ uint8_t* h_tile(const SliceParams& p, int es, int kb) {
+  return p.hbuf + (static_cast<size_t>(es) * 2 * p.s_max + kb) * 2 * p.n_tok * 128;
+}
+
+// Down-GEMM geometry of a chunk of output tiles: how many tiles share one
+// pass over the k-blocks (TMEM columns and stage size), and the stage size.
+struct DownGeom {
+  int cj;            // tiles per chunk
+  uint32_t hbytes;   // h tile bytes: 2*n16 rows
+  uint32_t stage;    // bytes per stage: cj weight boxes + the h tile
+  int S;             // stages
+};
+
+__device__ __forceinline__ DownGeom down_geom(const SliceParams& p, const Unit& u, int n) {
+  DownGeom g;
+  const int n16 = (n + 15) & ~15;
+  g.hbytes = static_cast<uint32_t>(2 * n16 * 128);
+  const int by_tmem = static_cast<int>(kSliceTmemCols) / (2 * n16);
+  const int by_smem = (p.stage_space / 3 - static_cast<int>(g.hbytes)) / kTileBytesA;
+  g.cj = max(1, min(u.nj, min(by_tmem, by_smem)));
+  g.stage = static_cast<uint32_t>(g.cj) * kTileBytesA + g.hbytes;
+  g.S = min(8, p.stage_space / static_cast<int>(g.stage));
+  return g;
+}
+
+// k-block q of a down pass, in the order the unit takes them: its own slice first
+__device__ __forceinline__ int down_kb(const Unit& u, int q) {
+  const int kb = 2 * u.s + q;
+  return kb < u.nkb_d ? kb : kb - u.nkb_d;
+}
+
+__device__ void unit_produce(const SliceParams& p, const SliceSmem& sm, const Unit& u, const CUtensorMap* tm_gu,
+                             const CUtensorMap* tm_gu_sh, const CUtensorMap* tm_dn, const CUtensorMap* tm_dn_sh,
+                             const CUtensorMap* tm_x) {
+  Ring ring;
+  const CUtensorMap* gu = u.shared ? tm_gu_sh : tm_gu;
+  const int zg = u.shared ? 0 : 2 * u.e;
+  const uint32_t tx = 2 * kTileBytesA + sm.b_bytes;
+  int kb = 0;
+  for (; kb < u.nkb; ++kb) {
+    // an expert no token picked stops streaming once the routing is known
+    if (!u.shared && mbar_test_wait(sm.routed, 0) && *sm.n_e == 0) break;
+    if (!mbar_wait(&sm.empty[ring.stage], ring.phase ^ 1u, sm.abort_flag)) {
+      record_failure(p.status, sm.abort_flag, kInfoEmpty);
+      break;
+    }
+    uint8_t* st = sm.base + ring.stage * 2 * kTileBytesA;
+    uint64_t* bar = &sm.full[ring.stage];
+    mbar_arrive_expect_tx(bar, tx);
+    tma_load_3d(st, gu, bar, kb * kBlockK, u.s * kHalfRows, zg);                    // gate rows of the slice
+    tma_load_3d(st + kTileBytesA, gu, bar, kb * kBlockK, u.s * kHalfRows, zg + 1);  // up rows
+    tma_load_2d(sm.bbase + ring.stage * sm.b_bytes, tm_x, bar, kb * kBlockK, 0);    // every token
+    ring.next(sm.S);
+  }
+  if (kb < u.nkb) {
+    *sm.kb_stop = kb;
+    return;
+  }
+  if (!mbar_wait(sm.routed, 0, sm.abort_flag)) return;
+  const int n = *sm.n_e;
+  if (n == 0 || u.nj == 0) return;
+  // The down ring reuses the gate_up ring's memory once the MMAs have read
+  // every gate_up stage.
+  for (int i = 0; i < sm.S; ++i) {
+    if (!mbar_wait(&sm.empty[ring.stage], ring.phase ^ 1u, sm.abort_flag)) {
+      record_failure(p.status, sm.abort_flag, kInfoEmpty);
+      return;
+    }
+    ring.next(sm.S);
+  }
+  const DownGeom g = down_geom(p, u, n);
+  const CUtensorMap* dn = u.shared ? tm_dn_sh : tm_dn;
+  const int zd = u.shared ? 0 : u.e;
+  Ring rb;
+  for (int jc = 0; jc < u.nj; jc += g.cj) {
+    const int cj = min(g.cj, u.nj - jc);
+    for (int q = 0; q < u.nkb_d; ++q) {
+      const int kbd = down_kb(u, q);
+      if (!mbar_wait(&sm.emptyB[rb.stage], rb.phase ^ 1u, sm.abort_flag)) {
+        record_failure(p.status, sm.abort_flag, kInfoEmpty);
+        return;
+      }
+      uint8_t* st = sm.base + rb.stage * g.stage;
+      uint64_t* bar = &sm.fullB[rb.stage];
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(cj) * kTileBytesA);
+      for (int jj = 0; jj < cj; ++jj)
+        tma_load_3d(st + jj * kTileBytesA, dn, bar, kbd * kBlockK, (u.j0 + jc + jj) * kHalfRows, zd);
+      rb.next(g.S);
+    }
+  }
+}
+
+__device__ void unit_mma(const SliceParams& p, const SliceSmem& sm, const Unit& u, uint32_t tmem) {
+  Ring ring;
+  const uint32_t idesc_a = idesc_bf16(kHalfRows, p.n_tok);
+  const uint32_t d_gate = tmem, d_up = tmem + 128;
+  bool ok = true;
+  for (int kb = 0; kb < u.nkb; ++kb) {
+    // the stage, or the news that the producer stopped before it
+    bool got = mbar_try_wait(&sm.full[ring.stage], ring.phase);
+    if (!got) {
+      const long long t0 = clock64();
+      while (true) {
+        if (mbar_try_wait(&sm.full[ring.stage], ring.phase)) { got = true; break; }
+        if (*sm.kb_stop <= kb || *sm.abort_flag) break;
+        if (clock64() - t0 > kWaitLimitCycles) {
+          record_failure(p.status, sm.abort_flag, kInfoFull);
+          break;
+        }
+      }
+    }
+    if (!got) { ok = false; break; }
+    tc_fence_after();
+    const uint32_t a0 = smem_u32(sm.base + ring.stage * 2 * kTileBytesA);
+    const uint32_t a1 = a0 + kTileBytesA, b = smem_u32(sm.bbase + ring.stage * sm.b_bytes);
+#pragma unroll
+    for (int ks = 0; ks < kBlockK / 16; ++ks) {
+      const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
+      const uint64_t bd = sw128_desc(b + ks * 32);
+      mma_bf16(d_gate, sw128_desc(a0 + ks * 32), bd, idesc_a, acc);
+      mma_bf16(d_up, sw128_desc(a1 + ks * 32), bd, idesc_a, acc);
+    }
+    mma_commit(&sm.empty[ring.stage]);
+    ring.next(sm.S);
+  }
+  mma_commit(sm.acca);
+  if (ok && mbar_wait(sm.routed, 0, sm.abort_flag) && *sm.n_e > 0 && u.nj > 0) {
+    const int n = *sm.n_e;
+    const int n16 = (n + 15) & ~15;
+    const DownGeom g = down_geom(p, u, n);
+    const uint32_t idesc_b = idesc_bf16(kHalfRows, 2 * n16);
+    Ring rb;
+    int chunk = 0;
+    for (int jc = 0; jc < u.nj && ok; jc += g.cj, ++chunk) {
+      const int cj = min(g.cj, u.nj - jc);
+      // The TMEM accumulators are free once the epilogue drained the last
+      // chunk.  The first chunk needs no wait: its first stage holds the
+      // unit's own h, fetched only after the epilogue has read the gate_up
+      // accumulators it overwrites.
+      if (chunk > 0) {
+        if (!mbar_wait(sm.acce, static_cast<uint32_t>(chunk - 1) & 1u, sm.abort_flag)) {
+          record_failure(p.status, sm.abort_flag, kInfoAccEmpty);
+          break;
+        }
+        tc_fence_after();
+      }
+      for (int q = 0; q < u.nkb_d; ++q) {
+        if (!mbar_wait(&sm.fullB[rb.stage], rb.phase, sm.abort_flag)) {
+          record_failure(p.status, sm.abort_flag, kInfoFull);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sm.base + rb.stage * g.stage);
+        const uint32_t hb = a0 + static_cast<uint32_t>(cj) * kTileBytesA;
+        for (int jj = 0; jj < cj; ++jj) {
+          const uint32_t d = tmem + static_cast<uint32_t>(jj * 2 * n16);
+#pragma unroll
+          for (int ks = 0; ks < kBlockK / 16; ++ks)
+            mma_bf16(d, sw128_desc(a0 + jj * kTileBytesA + ks * 32), sw128_desc(hb + ks * 32), idesc_b,
+                     (q > 0 || ks > 0) ? 1u : 0u);
+        }
+        mma_commit(&sm.emptyB[rb.stage]);
+        rb.next(g.S);
+      }
+      mma_commit(sm.accf);
+    }
+  }
+  // every MMA issued above has completed once `drain` flips
+  mma_commit(sm.drain);
+  if (!mbar_wait(sm.drain, 0, nullptr)) record_failure(p.status, sm.abort_flag, kInfoDrain);
+}
+
+// Release-publish output tiles [j0, j1) as finished (combine counters).
+__device__ __forceinline__ void publish_tiles(const SliceParams& p, int j0, int j1) {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  for (int j = j0; j < j1; ++j)
+    asm volatile("red.relaxed.gpu.global.add.s32 [%0], 1;" ::"l"(p.sync + kSliceSyncWords + j) : "memory");
+}
+
+// Warp 2: the unit's token list once the router CTAs have finished; then
+// (lane 0) the down GEMM's h tiles, fetched as their slices are flagged, and
+// the release of finished output tiles to the combine.
+__device__ void unit_tokens(const SliceParams& p, const SliceSmem& sm, const Unit& u) {
+  const int lane = threadIdx.x & 31;
+  int ok = 1;
+  if (lane == 0) ok = wait_count(p.sync + 0, p.n_rcta, p.status) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (!ok) {
+    if (lane == 0) {
+      record_failure(p.status, sm.abort_flag, kInfoRouter);
+      *sm.n_e = 0;
+      mbar_arrive(sm.routed);
+    }
+    return;
+  }
+  int n = 0;
+  if (u.shared) {
+    for (int t = lane; t < p.T; t += 32) {
+      sm.c_tok[t] = t;
+      sm.c_slot[t] = p.TK + t;
+      sm.c_w[t] = __ldcg(p.sh_w + t);
+    }
+    n = p.T;
+  } else {
+    // pairs in (token, slot) order; a token picks an expert at most once
+    for (int base = 0; base < p.TK; base += 32) {
+      const int pr = base + lane;
+      const bool hit = pr < p.TK && __ldcg(p.idx + pr) == u.e;
+      const uint32_t mask = __ballot_sync(0xffffffffu, hit);
+      if (hit) {
+        const int c = n + __popc(mask & ((1u << lane) - 1u));
+        if (c < kSliceMaxTok) {
+          sm.c_tok[c] = pr / p.K;
+          sm.c_slot[c] = pr;
+          sm.c_w[c] = __ldcg(p.w + pr);
+        }
+      }
+      n += __popc(mask);
+    }
+    n = min(n, kSliceMaxTok);
+    if (u.s == 0 && lane == 0) p.counts[u.e] = n;
+  }
+  __syncwarp();
+  if (lane == 0) {
+    *sm.n_e = n;
+    mbar_arrive(sm.routed);
+  }
+  if (lane != 0) return;
+  if (n == 0 || u.nj == 0) {
+    // nothing to add to this unit's output tiles
+    if (!p.direct_y && !*sm.abort_flag) publish_tiles(p, u.j0, u.j0 + u.nj);
+    return;
+  }
+  const DownGeom g = down_geom(p, u, n);
+  Ring rb;
+  int chunk = 0;
+  for (int jc = 0; jc < u.nj; jc += g.cj, ++chunk) {
+    const int cj = min(g.cj, u.nj - jc);
+    int seen = -1;  // last slice found ready
+    for (int q = 0; q < u.nkb_d; ++q) {
+      const int kbd = down_kb(u, q);
+      const int sl = kbd >> 1;
+      if (sl != seen) {
+        if (!wait_count(p.ready + u.es * p.s_max + sl, 1, p.status)) {
+          record_failure(p.status, sm.abort_flag, kInfoReady);
+          return;
+        }
+        // the slice's h was written by generic stores: order them before the bulk copy
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        seen = sl;
+      }
+      if (!mbar_wait(&sm.emptyB[rb.stage], rb.phase ^ 1u, sm.abort_flag)) {
+        record_failure(p.status, sm.abort_flag, kInfoGatherEmpty);
+        return;
+      }
+      uint8_t* st = sm.base + rb.stage * g.stage + cj * kTileBytesA;
+      uint64_t* bar = &sm.fullB[rb.stage];
+      mbar_arrive_expect_tx(bar, g.hbytes);
+      bulk_load(st, h_tile(p, u.es, kbd), g.hbytes, bar);
+      rb.next(g.S);
+    }
+    if (!p.direct_y) {
+      // the chunk's outputs are stored once every epilogue thread has counted it
+      const uint32_t target = 128u * static_cast<uint32_t>(chunk + 1);
+      const long long t0 = clock64();
+      while (true) {
+        uint32_t v;
+        asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(sm.grp_cnt)) : "memory");
+        if (v >= target) break;
+        if (*sm.abort_flag) return;
+        if (clock64() - t0 > kWaitLimitCycles) {
+          record_failure(p.status, sm.abort_flag, kInfoAccFull);
+          return;
+        }
+      }
+      publish_tiles(p, u.j0 + jc, u.j0 + jc + cj);
+    }
+  }
+}
+
+// Warps 3..6: SwiGLU of the picked tokens into the h buffer, then the down
+// GEMM's weighted outputs, one chunk of output tiles at a time.
+__device__ void unit_epilogue(const SliceParams& p, const SliceSmem& sm, const Unit& u, uint32_t tmem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = warp & 3;
+  const int r = quad * 32 + lane;  // TMEM lane: slice row (gate_up) / row in the output tile (down)
+  const bool leader = (warp == 3 && lane == 0);
+  const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
+  if (epi_any(!mbar_wait(sm.routed, 0, sm.abort_flag) || *sm.abort_flag)) return;
+  const int n = *sm.n_e;
+  if (n == 0) return;
+  if (epi_any(!mbar_wait(sm.acca, 0, sm.abort_flag))) {
+    if (leader) record_failure(p.status, sm.abort_flag, kInfoAccFull);
+    return;
+  }
+  tc_fence_after();
+  const int n16 = (n + 15) & ~15;
+  {
+    const float lim = p.swiglu_limit;
+    const int k2 = r >> 6, kin = r & 63;
+    uint8_t* th = h_tile(p, u.es, 2 * u.s + k2);
+    uint8_t* tl = th + n16 * 128;
+    for (int c0 = 0; c0 < n; c0 += 8) {
+      uint32_t g[8], v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int tok = sm.c_tok[min(c0 + i, n - 1)];
+        g[i] = tmem_ld1(tmem + lanes + static_cast<uint32_t>(tok));
+        v[i] = tmem_ld1(tmem + lanes + 128u + static_cast<uint32_t>(tok));
+      }
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + i;
+        if (c < n) {
+          float gv = __uint_as_float(g[i]), uv = __uint_as_float(v[i]);
+          if (lim > 0.f) {
+            gv = fminf(gv, lim);
+            uv = fminf(fmaxf(uv, -lim), lim);
+          }
+          const float hv = gv / (1.f + expf(-gv)) * uv;
+          const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
+          const float lo = hv - __bfloat162float(hi);
+          // row c, column kin of a K-major tile with the 128-byte swizzle
+          // (n16 is a multiple of 8: the lo rows keep the same swizzle phase)
+          const uint32_t off = static_cast<uint32_t>(c * 128 + ((((kin >> 3) ^ (c & 7)) << 4) | ((kin & 7) * 2)));
+          *reinterpret_cast<uint16_t*>(th + off) = __bfloat16_as_ushort(hi);
+          *reinterpret_cast<uint16_t*>(tl + off) = f2bf(lo);
+        }
+      }
+    }
+  }
+  // the TMEM accumulators are read: the down GEMM may overwrite them
+  tc_fence_before();
+  // publish the slice's h: every thread's stores precede the leader's release
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  epi_sync();
+  if (leader) red_release_add(p.ready + u.es * p.s_max + u.s, 1);
+  if (u.nj == 0) return;
+  const DownGeom g = down_geom(p, u, n);
+  int chunk = 0;
+  for (int jc = 0; jc < u.nj; jc += g.cj, ++chunk) {
+    const int cj = min(g.cj, u.nj - jc);
+    if (epi_any(!mbar_wait(sm.accf, static_cast<uint32_t>(chunk) & 1u, sm.abort_flag))) {
+      if (leader) record_failure(p.status, sm.abort_flag, kInfoAccFull);
+      return;
+    }
+    tc_fence_after();
+    for (int jj = 0; jj < cj; ++jj) {
+      const int row = (u.j0 + jc + jj) * kHalfRows + r;
+      const uint32_t d = tmem + lanes + static_cast<uint32_t>(jj * 2 * n16);
+      for (int c0 = 0; c0 < n16; c0 += 16) {
+        uint32_t vh[16], vl[16];
+        tmem_ld16(d + static_cast<uint32_t>(c0), vh);        // W * h_hi
+        tmem_ld16(d + static_cast<uint32_t>(n16 + c0), vl);  // W * h_lo
+        tmem_ld_wait();
+        if (row < p.H) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = c0 + i;
+            if (c < n) {
+              const float v = sm.c_w[c] * (__uint_as_float(vh[i]) + __uint_as_float(vl[i]));
+              if (p.direct_y)
+                p.y[static_cast<size_t>(sm.c_tok[c]) * p.H + row] = f2bf(v);
+              else
+                __stcg(p.out + static_cast<size_t>(sm.c_slot[c]) * p.H + row, v);
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(sm.acce);
+    if (!p.direct_y)
+      asm volatile("red.release.cta.shared::cta.add.u32 [%0], 1;" ::"r"(smem_u32(sm.grp_cnt)) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- combine
+// Task (m, g): y[t, m*128 : m*128+128] for the 7 tokens of group g, once
+// every expert (and the shared expert) has finished tile m.  Warp w sums
+// token g*7+w in slot order; lane l four rows.
+__device__ void combine_tasks(const SliceParams& p, const SliceSmem& sm) {
+  if (p.direct_y) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tasks = p.n_mt * p.n_tg;
+  const int target = p.E + (p.s_sh > 0 ? 1 : 0);
+  int32_t* tile_cnt = p.sync + kSliceSyncWords;
+  while (true) {
+    if (threadIdx.x == 0) {
+      int task = atomicAdd(p.sync + 1, 1);
+      if (task < n_tasks && !wait_count(tile_cnt + task / p.n_tg, target, p.status)) {
+        record_failure(p.status, sm.abort_flag, kInfoTileCount);
+        task = n_tasks;
+      }
+      *sm.task = task;
+    }
+    __syncthreads();
+    const int task = *sm.task;
+    __syncthreads();
+    if (task >= n_tasks) break;
+    const int m = task / p.n_tg, tg = task - m * p.n_tg;
+    const int t = tg * kSliceTokPerTask + warp;
+    const int row = m * kHalfRows + lane * 4;
+    if (t < p.T && row < p.H) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int nslot = p.K + (p.s_sh > 0 ? 1 : 0);
+      for (int k = 0; k < nslot; ++k) {
+        const int slot = k < p.K ? t * p.K + k : p.TK + t;
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.out + static_cast<size_t>(slot) * p.H + row));
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      uint2 o;
+      o.x = static_cast<uint32_t>(f2bf(acc.x)) | (static_cast<uint32_t>(f2bf(acc.y)) << 16);
+      o.y = static_cast<uint32_t>(f2bf(acc.z)) | (static_cast<uint32_t>(f2bf(acc.w)) << 16);
+      *reinterpret_cast<uint2*>(p.y + static_cast<size_t>(t) * p.H + row) = o;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kSliceThreads, 1)
+    moe_slice_kernel(const __grid_constant__ CUtensorMap tm_gu, const __grid_constant__ CUtensorMap tm_gu_sh,
+                     const __grid_constant__ CUtensorMap tm_dn, const __grid_constant__ CUtensorMap tm_dn_sh,
+                     const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ SliceParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ctrl = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  SliceSmem sm;
+  carve(ctrl, sm);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bid = static_cast<int>(blockIdx.x);
+  const bool is_unit = bid < p.n_units;
+  Unit u;
+  u.shared = bid >= p.E * p.s_e;
+  u.e = u.shared ? -1 : bid / max(p.s_e, 1);
+  u.s = u.shared ? bid - p.E * p.s_e : bid % max(p.s_e, 1);
+  u.es = u.shared ? p.E : u.e;
+  u.nkb = ceil_div(p.H, kBlockK);
+  const int su = u.shared ? p.s_sh : p.s_e;
+  u.nkb_d = 2 * su;
+  u.j0 = p.n_mt * u.s / max(su, 1);
+  u.nj = p.n_mt * (u.s + 1) / max(su, 1) - u.j0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 8; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.fullB[s], 2);  // weight loads and h fetch arrive separately
+      mbar_init(&sm.emptyB[s], 1);
+    }
+    mbar_init(sm.acca, 1);
+    mbar_init(sm.accf, 1);
+    mbar_init(sm.acce, 128);
+    mbar_init(sm.routed, 1);
+    mbar_init(sm.drain, 1);
+    *sm.abort_flag = 0;
+    *sm.kb_stop = u.nkb;
+    *sm.n_e = 0;
+    *sm.grp_cnt = 0;
+    fence_barrier_init();
+    fence_proxy_async();
+  }
+  if (is_unit && warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_gu);
+    tma_prefetch_desc(&tm_dn);
+    tma_prefetch_desc(&tm_x);
+    if (p.s_sh > 0) {
+      tma_prefetch_desc(&tm_gu_sh);
+      tma_prefetch_desc(&tm_dn_sh);
+    }
+  }
+  if (is_unit && warp == 1) {
+    tmem_alloc(sm.tmem_slot, kSliceTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (is_unit) {
+    const uint32_t tmem = *sm.tmem_slot;
+    sm.b_bytes = static_cast<uint32_t>(p.n_tok) * 128u;
+    sm.S = min(8, p.stage_space / static_cast<int>(2 * kTileBytesA + sm.b_bytes));
+    sm.bbase = sm.base + sm.S * 2 * kTileBytesA;
+    if (warp == 0) {
+      if (lane == 0) unit_produce(p, sm, u, &tm_gu, &tm_gu_sh, &tm_dn, &tm_dn_sh, &tm_x);
+    } else if (warp == 1) {
+      if (lane == 0) unit_mma(p, sm, u, tmem);
+    } else if (warp == 2) {
+      unit_tokens(p, sm, u);
+    } else {
+      unit_epilogue(p, sm, u, tmem);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (*sm.abort_flag) {
+      // let loads already issued land before the shared memory goes away
+      const long long t0 = clock64();
+      while (clock64() - t0 < 4000000ll) {}
+    }
+    if (warp == 1) tmem_dealloc(tmem, kSliceTmemCols);
+  } else if (bid - p.n_units < p.n_rcta) {
+    route_tokens(p, sm, bid - p.n_units);
+  }
+
+  combine_tasks(p, sm);
+
+  // the last CTA out clears the counters and flags for the next forward
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int old = atomicAdd(p.sync + 2, 1);
+    if (old == static_cast<int>(gridDim.x) - 1) {
+      p.sync[0] = 0;
+      p.sync[1] = 0;
+      for (int m = 0; m < p.n_mt; ++m) p.sync[kSliceSyncWords + m] = 0;
+      for (int i = 0; i < (p.E + 1) * p.s_max; ++i) p.ready[i] = 0;
+      __threadfence();
+      p.sync[2] = 0;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_slice(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, const CUtensorMap& tm_dn,
+                         const CUtensorMap& tm_dn_sh, const CUtensorMap& tm_x, const SliceParams& p, int grid,
+                         size_t smem_bytes, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(moe_slice_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem_bytes));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kSliceThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, moe_slice_kernel, tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, tm_x, p);
+}
+
+}  // namespace moe

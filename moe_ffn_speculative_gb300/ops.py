@@ -74,7 +74,12 @@ _SIGS = {
                              _P, _SZ, _P, _P, _P, _P, _P]),
     "moe_get_device_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "moe_set_profile_events": (None, [_P, _I]),
+    "moe_set_schedule": (_I, [_I]),
+    "moe_ffn_schedule": (_I, [_I, _I, _I, _I, ctypes.POINTER(Recipe), _I]),
 }
+
+SCHEDULE_AUTO, SCHEDULE_STREAM_K, SCHEDULE_SLICE = 0, 1, 2
+SCHEDULE_NAMES = {SCHEDULE_STREAM_K: "stream_k", SCHEDULE_SLICE: "slice"}
 
 
 def lib() -> ctypes.CDLL:
@@ -239,6 +244,21 @@ def moe_ffn_forward(x, gate, w_gate_up, w_down, recipe: Recipe, ws: Workspace, r
         ws.nbytes, _ptr(y), _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(counts_out), _stream(stream)),
         "moe_ffn_forward")
     return y
+
+
+def set_schedule(schedule: int) -> None:
+    """Expert schedule of later moe_ffn_forward calls on this thread:
+    SCHEDULE_AUTO, SCHEDULE_STREAM_K or SCHEDULE_SLICE."""
+    _check(lib().moe_set_schedule(int(schedule)), "moe_set_schedule")
+
+
+def ffn_schedule(T: int, H: int, I: int, Is: int, recipe: Recipe, gated: bool = False) -> int:
+    """The schedule moe_ffn_forward would run for this shape (SCHEDULE_STREAM_K
+    or SCHEDULE_SLICE)."""
+    s = lib().moe_ffn_schedule(T, H, I, Is, ctypes.byref(recipe), 1 if gated else 0)
+    if s < 0:
+        raise MoeError(1, "moe_ffn_schedule")
+    return s
 
 
 def set_profile_events(events) -> None:

@@ -16,6 +16,8 @@ Bars (from the routing/equivalence requirements of the MoE-FFN layer):
   |logit| <= ~10), no index mismatch with a margin above 1e-4, weights within
   1e-5.
 """
+import contextlib
+
 import numpy as np
 import pytest
 import torch
@@ -174,6 +176,30 @@ SMALL = {
 }
 
 
+SCHEDULES = {"stream_k": ops.SCHEDULE_STREAM_K, "slice": ops.SCHEDULE_SLICE}
+
+
+@contextlib.contextmanager
+def _schedule(sched):
+    ops.set_schedule(sched)
+    try:
+        yield
+    finally:
+        ops.set_schedule(ops.SCHEDULE_AUTO)
+
+
+def _schedule_of(cfg):
+    rec = ops.Recipe.from_config(cfg)
+    return ops.ffn_schedule(cfg.T, cfg.H, cfg.I, cfg.shared_I, rec, gated=cfg.shared_gated and cfg.shared_I > 0)
+
+
+def _require(cfg, sched):
+    """Force `sched` for the test; skip when the layer's shape does not fit it."""
+    with _schedule(sched):
+        if _schedule_of(cfg) != sched:
+            pytest.skip("layer shape outside this schedule")
+
+
 def _run_layer(cfg, d, stream=None):
     rec = ops.Recipe.from_config(cfg)
     layer = ops.MoELayer(d, rec, cfg.T)
@@ -193,9 +219,16 @@ def _oracle_routing(cfg, d):
     return orec, logits, oidx, ow, O.selection_margin(c, oidx, orec)
 
 
+@pytest.mark.parametrize("sched", list(SCHEDULES))
 @pytest.mark.parametrize("name", list(SMALL))
-def test_layer_small(name):
+def test_layer_small(name, sched):
     cfg = SMALL[name]
+    _require(cfg, SCHEDULES[sched])
+    with _schedule(SCHEDULES[sched]):
+        _check_small(cfg, name, sched)
+
+
+def _check_small(cfg, name, sched):
     d = S.make_inputs(cfg, device="cpu")
     d = {k: (None if v is None else v.cuda()) for k, v in d.items()}
     x_before = d["x"].clone()
@@ -210,21 +243,49 @@ def test_layer_small(name):
     err = rel_rms_error(y, y_ref)
     floor = bf16_floor_error(d, cfg, rows, oidx, ow, y_ref)
     tol = max(Y_REL_RMS_TOL, 1.25 * floor)
-    report(test="layer_small", case=name, rel_rms_err=err, rounding_floor=floor,
+    report(test="layer_small", case=name, schedule=sched, rel_rms_err=err, rounding_floor=floor,
            output_rounding=output_rounding_error(y_ref), tol=tol)
     assert err <= tol, f"rel-RMS error {err} (bf16 rounding floor {floor})"
     st, info = layer.ws.device_status()
     assert st == 0, (st, info)
 
 
-def test_layer_deterministic_and_repeatable():
-    cfg = SMALL["wide_tokens_K8"]
+@pytest.mark.parametrize("name,sched", [("wide_tokens_K8", "stream_k"), ("ragged_gated_shared_router_bias", "slice")])
+def test_layer_deterministic_and_repeatable(name, sched):
+    cfg = SMALL[name]
+    _require(cfg, SCHEDULES[sched])
     d = {k: (None if v is None else v.cuda()) for k, v in S.make_inputs(cfg).items()}
-    layer, y1, *_ = _run_layer(cfg, d)
-    y2 = layer.forward(d["x"])
-    y3 = layer.forward(d["x"])
+    with _schedule(SCHEDULES[sched]):
+        layer, y1, *_ = _run_layer(cfg, d)
+        y2 = layer.forward(d["x"])
+        y3 = layer.forward(d["x"])
     torch.cuda.synchronize()
     assert torch.equal(y1, y2) and torch.equal(y2, y3)
+
+
+def test_slice_untouched_experts_and_schedules_agree():
+    """Most experts get no token (4 tokens, 16 experts, top-1): the fused
+    schedule stops streaming them once the routing is known and skips their
+    down GEMM; both schedules give the same routing and agree on y."""
+    cfg = S.LayerConfig("sparse", T=4, H=256, E=16, I=256, K=1, shared_I=128, shared_gated=True, seed=13)
+    _require(cfg, ops.SCHEDULE_SLICE)
+    d = {k: (None if v is None else v.cuda()) for k, v in S.make_inputs(cfg).items()}
+    outs = {}
+    for sched in SCHEDULES:
+        with _schedule(SCHEDULES[sched]):
+            layer, y, idx, w, counts = _run_layer(cfg, d)
+        assert layer.ws.device_status()[0] == 0
+        outs[sched] = (y, idx, w, counts)
+    assert (outs["slice"][3] == 0).sum().item() >= 12
+    assert torch.equal(outs["slice"][1], outs["stream_k"][1])
+    assert torch.equal(outs["slice"][3], outs["stream_k"][3])
+    assert torch.allclose(outs["slice"][2], outs["stream_k"][2], rtol=0, atol=W_ABS_TOL)
+    orec, _, oidx, ow, margin = _oracle_routing(cfg, d)
+    y_ref = oracle_rows(d, cfg, np.arange(cfg.T), oidx, ow)
+    for sched, (y, *_) in outs.items():
+        err = rel_rms_error(y, y_ref)
+        report(test="slice_untouched", case=sched, rel_rms_err=err)
+        assert err <= Y_REL_RMS_TOL, (sched, err)
 
 
 def test_layer_zero_tokens():
@@ -247,8 +308,15 @@ def test_layer_refuses_in_place_output():
     assert e.value.status == ops.MOE_ERR_INVALID_ARG
 
 
-def test_cuda_graph_replay():
+@pytest.mark.parametrize("sched", list(SCHEDULES))
+def test_cuda_graph_replay(sched):
     cfg = SMALL["ragged_gated_shared_router_bias"]
+    _require(cfg, SCHEDULES[sched])
+    with _schedule(SCHEDULES[sched]):
+        _check_graph_replay(cfg)
+
+
+def _check_graph_replay(cfg):
     d = {k: (None if v is None else v.cuda()) for k, v in S.make_inputs(cfg).items()}
     layer, y_ref, *_ = _run_layer(cfg, d)
     s = torch.cuda.Stream()
@@ -259,21 +327,45 @@ def test_cuda_graph_replay():
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         layer.forward(d["x"], y=y, stream=s)
-    y.zero_()
-    g.replay()
-    torch.cuda.synchronize()
-    assert torch.equal(y, y_ref)
+    # replays reuse the workspace counters: each launch must leave them cleared
+    for _ in range(3):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_ref)
+    assert layer.ws.device_status()[0] == 0
 
 
 # =========================================================================== whole layer, full sizes
 
-FULL = [("qwen3_8b_dspark", 72), ("qwen38_27b_dspark", 72), ("dsv3_style", 72), ("dsv4_style", 9),
-        ("dsv4_style", 72), ("dsv4_style", 576), ("dsv4_style", 4096)]
+# (workload, T, schedule): None = the automatic choice, as bench.py runs it
+FULL = [("qwen3_8b_dspark", 72, None), ("qwen3_8b_dspark", 72, "stream_k"), ("qwen38_27b_dspark", 72, None),
+        ("dsv3_style", 72, None), ("dsv4_style", 9, None), ("dsv4_style", 72, None), ("dsv4_style", 576, None),
+        ("dsv4_style", 4096, None)]
 
 
-@pytest.mark.parametrize("name,T", FULL)
-def test_layer_full_size_sampled(name, T):
+def test_automatic_schedule_choice():
+    """Few experts that every forward touches take the fused schedule; many
+    experts (most untouched at decode sizes) take stream-K."""
+    want = {"qwen3_8b_dspark": ops.SCHEDULE_SLICE, "qwen38_27b_dspark": ops.SCHEDULE_STREAM_K,
+            "dsv3_style": ops.SCHEDULE_STREAM_K, "dsv4_style": ops.SCHEDULE_STREAM_K}
+    for name, sched in want.items():
+        assert _schedule_of(S.CONFIGS[name]) == sched, name
+    assert _schedule_of(S.CONFIGS["qwen3_8b_dspark"].with_(T=129)) == ops.SCHEDULE_STREAM_K
+    assert _schedule_of(S.CONFIGS["qwen3_8b_dspark"].with_(T=9)) == ops.SCHEDULE_STREAM_K  # 8*(7/8)^9 > 0.25
+
+
+@pytest.mark.parametrize("name,T,sched", FULL)
+def test_layer_full_size_sampled(name, T, sched):
     cfg = S.CONFIGS[name].with_(T=T)
+    if sched is not None:
+        _require(cfg, SCHEDULES[sched])
+    with _schedule(SCHEDULES[sched] if sched else ops.SCHEDULE_AUTO):
+        used = ops.SCHEDULE_NAMES[_schedule_of(cfg)]
+        _check_full(cfg, name, T, used)
+
+
+def _check_full(cfg, name, T, used):
     d = S.make_inputs(cfg, device="cuda")
     layer, y, idx, w, counts = _run_layer(cfg, d)
     orec, logits, oidx, ow, margin = _oracle_routing(cfg, d)
@@ -291,7 +383,7 @@ def test_layer_full_size_sampled(name, T):
     y_ref = oracle_rows(d, cfg, rows, oidx[rows], ow[rows])
     err = rel_rms_error(y[torch.as_tensor(rows, device="cuda")], y_ref)
     out_round = output_rounding_error(y_ref)
-    report(test="layer_full", case=f"{name}_T{T}", rel_rms_err=err, output_rounding=out_round,
+    report(test="layer_full", case=f"{name}_T{T}", schedule=used, rel_rms_err=err, output_rounding=out_round,
            logit_err=float(lerr), rows=len(rows))
     assert err <= Y_REL_RMS_TOL, f"rel-RMS error {err} (bf16 output rounding alone: {out_round})"
     y2 = layer.forward(d["x"])
