@@ -148,6 +148,9 @@ SlicePlan slice_plan(int T, int H, int I, int Is, int E, bool gated, int sms) {
   return s;
 }
 
+// Words of one of the slice kernel's two counter sets.
+int slice_set_words(const SlicePlan& s, int E) { return kSliceSyncWords + s.n_mt + (E + 1) * s.s_max; }
+
 // The fused kernel streams every expert's gate_up weights from the start,
 // before the routing is known, and stops an untouched expert once it is: it
 // pays off when, under uniform routing, untouched experts are rare.
@@ -165,7 +168,7 @@ struct Layout {
   int max_gu_tiles, max_dn_tiles, g_max;
   bool need_out;
   size_t o_status, o_cnt, o_tiles, o_logits, o_shl, o_shw, o_idx, o_w, o_counts, o_offsets, o_sp, o_pp, o_groups,
-      o_header, o_spans, o_span_groups, o_partials, o_h, o_out, o_sync, o_ready, o_hbuf, o_sout, total;
+      o_header, o_spans, o_span_groups, o_partials, o_h, o_out, o_sync, o_hbuf, o_sout, total;
 };
 
 Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sms) {
@@ -221,15 +224,14 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   if (L.need_out) o = align_up(o + 4 * rows * H);
   // fused small-expert-count kernel: counters and the per-slice partial outputs
   L.sp = slice_plan(T, H, I, Is, E, gated, sms);
-  L.o_sync = L.o_ready = L.o_hbuf = L.o_sout = 0;
+  L.o_sync = L.o_hbuf = L.o_sout = 0;
   if (L.sp.reserve) {
-    // counters, slice-ready flags, every expert's h tiles (2 per slice, each
+    // two counter sets (with the slice-ready flags), every expert's h tiles (2 per slice, each
     // 2*n_tok rows of 128 bytes) and the pair outputs for the combine
     const int Tr = T < kSliceMaxTok ? T : kSliceMaxTok;
     const size_t slots = static_cast<size_t>(Tr) * K + Tr;
     const size_t n_es = static_cast<size_t>(E) + 1;
-    L.o_sync = o; o = align_up(o + 4 * static_cast<size_t>(kSliceSyncWords + L.sp.n_mt));
-    L.o_ready = o; o = align_up(o + 4 * n_es * L.sp.s_max);
+    L.o_sync = o; o = align_up(o + 4 * (1 + 2 * static_cast<size_t>(slice_set_words(L.sp, E))));
     L.o_hbuf = o; o = align_up(o + n_es * 2 * L.sp.s_max * 2 * static_cast<size_t>(L.sp.n_tok) * 128);
     L.o_sout = o;
     if (K > 1 || Is > 0) o = align_up(o + 4 * slots * H);
@@ -416,11 +418,11 @@ moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf1
     sp.logits = reinterpret_cast<float*>(w + L.o_logits);
     sp.idx = idx; sp.w = wts; sp.sh_w = sh_w; sp.counts = counts;
     sp.hbuf = reinterpret_cast<uint8_t*>(w + L.o_hbuf);
-    sp.ready = reinterpret_cast<int32_t*>(w + L.o_ready);
     sp.out = reinterpret_cast<float*>(w + L.o_sout);
     sp.direct_y = (K == 1 && Is == 0) ? 1 : 0;
     sp.y = y;
     sp.sync = reinterpret_cast<int32_t*>(w + L.o_sync);
+    sp.set_words = slice_set_words(L.sp, E);
     sp.status = status;
     record_event_on(0, stream);
     record_event_on(1, stream);

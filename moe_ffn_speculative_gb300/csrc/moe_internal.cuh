@@ -185,10 +185,13 @@ struct SliceParams {
   float* sh_w;                 // [T] shared-expert weight (gate, or 1)
   int32_t* counts;             // [E]
   uint8_t* hbuf;               // [(E+1) * 2*s_max] h tiles of 2*n_tok rows x 128 B (see slice.cu)
-  int32_t* ready;              // [(E+1) * s_max] slice of h written
   float* out;                  // [T*K + T, H] fp32 weighted expert outputs (unless direct_y)
   uint16_t* y;                 // [T,H]
-  int32_t* sync;               // [kSliceSyncWords + n_mt]: router done, task counter, exit counter, -, tile counts
+  // [1 + 2 * set_words]: a parity word, then two counter sets used by
+  // alternate forwards; a set is kSliceSyncWords words (router done, combine
+  // task, exit count, -), n_mt output-tile counts, (E+1)*s_max slice-ready flags
+  int32_t* sync;
+  int set_words;
   int32_t* status;
 };
 constexpr int kSliceMaxTok = 128;

@@ -61,6 +61,8 @@ struct SliceSmem {
   volatile int* n_e;      // tokens routed to this unit's expert
   volatile int* task;
   int* grp_cnt;           // epilogue threads' count of finished down chunks
+  int32_t* ss;            // this forward's counter set (router done, combine task, exit, -, tile counts)
+  int32_t* ready;         // this forward's slice-ready flags
   uint32_t* tmem_slot;
   int* c_tok;    // [kSliceMaxTok] token of each down-GEMM column
   int* c_slot;   // [kSliceMaxTok] its output slot (pair t*K+k, or T*K+t for the shared expert)
@@ -207,18 +209,54 @@ __device__ void route_tokens(const SliceParams& p, const SliceSmem& sm, int rc) 
     select_token<1, true>(lrow, p.sel, p.idx + static_cast<size_t>(t) * p.K, p.w + static_cast<size_t>(t) * p.K);
   }
   __syncthreads();
-  if (threadIdx.x == 0) red_release_add(p.sync + 0, 1);
+  if (threadIdx.x == 0) red_release_add(sm.ss + 0, 1);
 }
 
 // ---------------------------------------------------------------- unit CTA roles
+// A CTA's share of the experts' work.  A unit (has_a) owns slice s of an
+// expert in the gate_up GEMM; every CTA that is not a unit (the router CTAs
+// once routing is done, and the rest) is a down-only helper of one expert.
+// An expert's output tiles are split evenly over its units and helpers.
 struct Unit {
+  bool has_a;   // runs the gate_up GEMM for slice s
   bool shared;
-  int e, s;     // expert (-1: shared) and slice
+  int e, s;     // expert (-1: shared) and slice (units)
   int es;       // expert slot of the h buffer and ready flags: e, or E for the shared expert
-  int nkb;      // gate_up k-blocks: ceil(H / 64)
+  int nkb;      // gate_up k-blocks: ceil(H / 64), 0 for helpers
   int nkb_d;    // down k-blocks: 2 per slice of the expert
-  int j0, nj;   // the unit's output tiles [j0, j0 + nj)
+  int kstart;   // first down k-block: the unit's own slice, 0 for helpers
+  int j0, nj;   // the CTA's output tiles [j0, j0 + nj)
 };
+
+__device__ __forceinline__ Unit make_unit(const SliceParams& p, int bid) {
+  Unit u;
+  const int n_es = p.E + (p.s_sh > 0 ? 1 : 0);  // experts with units, the shared one last
+  const int n_help = static_cast<int>(gridDim.x) - p.n_units;
+  int w;  // worker index within the expert: units first, then helpers
+  if (bid < p.n_units) {
+    u.has_a = true;
+    u.shared = bid >= p.E * p.s_e;
+    u.es = u.shared ? p.E : bid / max(p.s_e, 1);
+    u.s = u.shared ? bid - p.E * p.s_e : bid % max(p.s_e, 1);
+    w = u.s;
+  } else {
+    const int h = bid - p.n_units;
+    u.has_a = false;
+    u.es = h % n_es;
+    u.shared = u.es == p.E;
+    u.s = -1;
+    w = (u.shared ? p.s_sh : p.s_e) + h / n_es;
+  }
+  u.e = u.shared ? -1 : u.es;
+  const int su = u.shared ? p.s_sh : p.s_e;
+  const int workers = su + (n_help > u.es ? (n_help - 1 - u.es) / n_es + 1 : 0);
+  u.nkb = u.has_a ? ceil_div(p.H, kBlockK) : 0;
+  u.nkb_d = 2 * su;
+  u.kstart = u.has_a ? 2 * u.s : 0;
+  u.j0 = p.n_mt * w / workers;
+  u.nj = p.n_mt * (w + 1) / workers - u.j0;
+  return u;
+}
 
 // h tile (expert slot es, down k-block kb): 2*n_tok rows of 128 bytes, the
 // K-major 128-byte-swizzled image of the MMA operand; rows [0, n16) hold
@@ -251,7 +289,7 @@ __device__ __forceinline__ DownGeom down_geom(const SliceParams& p, const Unit& 
 
 // k-block q of a down pass, in the order the unit takes them: its own slice first
 __device__ __forceinline__ int down_kb(const Unit& u, int q) {
-  const int kb = 2 * u.s + q;
+  const int kb = u.kstart + q;
   return kb < u.nkb_d ? kb : kb - u.nkb_d;
 }
 
@@ -398,10 +436,10 @@ __device__ void unit_mma(const SliceParams& p, const SliceSmem& sm, const Unit& 
 }
 
 // Release-publish output tiles [j0, j1) as finished (combine counters).
-__device__ __forceinline__ void publish_tiles(const SliceParams& p, int j0, int j1) {
+__device__ __forceinline__ void publish_tiles(const SliceSmem& sm, int j0, int j1) {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
   for (int j = j0; j < j1; ++j)
-    asm volatile("red.relaxed.gpu.global.add.s32 [%0], 1;" ::"l"(p.sync + kSliceSyncWords + j) : "memory");
+    asm volatile("red.relaxed.gpu.global.add.s32 [%0], 1;" ::"l"(sm.ss + kSliceSyncWords + j) : "memory");
 }
 
 // Warp 2: the unit's token list once the router CTAs have finished; then
@@ -410,7 +448,7 @@ __device__ __forceinline__ void publish_tiles(const SliceParams& p, int j0, int 
 __device__ void unit_tokens(const SliceParams& p, const SliceSmem& sm, const Unit& u) {
   const int lane = threadIdx.x & 31;
   int ok = 1;
-  if (lane == 0) ok = wait_count(p.sync + 0, p.n_rcta, p.status) ? 1 : 0;
+  if (lane == 0) ok = wait_count(sm.ss + 0, p.n_rcta, p.status) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   if (!ok) {
     if (lane == 0) {
@@ -455,7 +493,7 @@ __device__ void unit_tokens(const SliceParams& p, const SliceSmem& sm, const Uni
   if (lane != 0) return;
   if (n == 0 || u.nj == 0) {
     // nothing to add to this unit's output tiles
-    if (!p.direct_y && !*sm.abort_flag) publish_tiles(p, u.j0, u.j0 + u.nj);
+    if (!p.direct_y && !*sm.abort_flag) publish_tiles(sm, u.j0, u.j0 + u.nj);
     return;
   }
   const DownGeom g = down_geom(p, u, n);
@@ -464,11 +502,18 @@ __device__ void unit_tokens(const SliceParams& p, const SliceSmem& sm, const Uni
   for (int jc = 0; jc < u.nj; jc += g.cj, ++chunk) {
     const int cj = min(g.cj, u.nj - jc);
     int seen = -1;  // last slice found ready
-    for (int q = 0; q < u.nkb_d; ++q) {
+    int q = 0;
+    if (chunk == 0 && u.has_a) {
+      // the epilogue fills the first two stages with the unit's own slice
+      rb.next(g.S);
+      rb.next(g.S);
+      q = 2;
+    }
+    for (; q < u.nkb_d; ++q) {
       const int kbd = down_kb(u, q);
       const int sl = kbd >> 1;
       if (sl != seen) {
-        if (!wait_count(p.ready + u.es * p.s_max + sl, 1, p.status)) {
+        if (!wait_count(sm.ready + u.es * p.s_max + sl, 1, p.status)) {
           record_failure(p.status, sm.abort_flag, kInfoReady);
           return;
         }
@@ -500,7 +545,7 @@ __device__ void unit_tokens(const SliceParams& p, const SliceSmem& sm, const Uni
           return;
         }
       }
-      publish_tiles(p, u.j0 + jc, u.j0 + jc + cj);
+      publish_tiles(sm, u.j0 + jc, u.j0 + jc + cj);
     }
   }
 }
@@ -516,17 +561,25 @@ __device__ void unit_epilogue(const SliceParams& p, const SliceSmem& sm, const U
   if (epi_any(!mbar_wait(sm.routed, 0, sm.abort_flag) || *sm.abort_flag)) return;
   const int n = *sm.n_e;
   if (n == 0) return;
+  const int n16 = (n + 15) & ~15;
+  const DownGeom g = down_geom(p, u, n);
+  if (u.has_a) {
   if (epi_any(!mbar_wait(sm.acca, 0, sm.abort_flag))) {
     if (leader) record_failure(p.status, sm.abort_flag, kInfoAccFull);
     return;
   }
   tc_fence_after();
-  const int n16 = (n + 15) & ~15;
+  // The down GEMM takes the unit's own slice first: its two k-blocks are
+  // the first two stages of the down ring, whose h parts this epilogue
+  // fills directly (the gate_up stages are all read by now), besides the
+  // global copy the expert's other units fetch.
+  const bool local = u.nj > 0;
   {
     const float lim = p.swiglu_limit;
     const int k2 = r >> 6, kin = r & 63;
     uint8_t* th = h_tile(p, u.es, 2 * u.s + k2);
     uint8_t* tl = th + n16 * 128;
+    uint8_t* sh = sm.base + k2 * g.stage + min(g.cj, u.nj) * kTileBytesA;
     for (int c0 = 0; c0 < n; c0 += 8) {
       uint32_t g[8], v[8];
 #pragma unroll
@@ -551,20 +604,33 @@ __device__ void unit_epilogue(const SliceParams& p, const SliceSmem& sm, const U
           // row c, column kin of a K-major tile with the 128-byte swizzle
           // (n16 is a multiple of 8: the lo rows keep the same swizzle phase)
           const uint32_t off = static_cast<uint32_t>(c * 128 + ((((kin >> 3) ^ (c & 7)) << 4) | ((kin & 7) * 2)));
-          *reinterpret_cast<uint16_t*>(th + off) = __bfloat16_as_ushort(hi);
-          *reinterpret_cast<uint16_t*>(tl + off) = f2bf(lo);
+          const uint16_t hb = __bfloat16_as_ushort(hi), lb = f2bf(lo);
+          *reinterpret_cast<uint16_t*>(th + off) = hb;
+          *reinterpret_cast<uint16_t*>(tl + off) = lb;
+          if (local) {
+            *reinterpret_cast<uint16_t*>(sh + off) = hb;
+            *reinterpret_cast<uint16_t*>(sh + n16 * 128 + off) = lb;
+          }
         }
       }
     }
   }
   // the TMEM accumulators are read: the down GEMM may overwrite them
   tc_fence_before();
-  // publish the slice's h: every thread's stores precede the leader's release
+  // publish the slice's h: every thread's stores precede the leader's
+  // release (global copy) and its arrivals on the first two down stages
   asm volatile("fence.proxy.async.global;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   epi_sync();
-  if (leader) red_release_add(p.ready + u.es * p.s_max + u.s, 1);
+  if (leader) {
+    if (local) {
+      mbar_arrive(&sm.fullB[0]);
+      mbar_arrive(&sm.fullB[1]);
+    }
+    red_release_add(sm.ready + u.es * p.s_max + u.s, 1);
+  }
+  }  // has_a
   if (u.nj == 0) return;
-  const DownGeom g = down_geom(p, u, n);
   int chunk = 0;
   for (int jc = 0; jc < u.nj; jc += g.cj, ++chunk) {
     const int cj = min(g.cj, u.nj - jc);
@@ -612,10 +678,10 @@ __device__ void combine_tasks(const SliceParams& p, const SliceSmem& sm) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tasks = p.n_mt * p.n_tg;
   const int target = p.E + (p.s_sh > 0 ? 1 : 0);
-  int32_t* tile_cnt = p.sync + kSliceSyncWords;
+  int32_t* tile_cnt = sm.ss + kSliceSyncWords;
   while (true) {
     if (threadIdx.x == 0) {
-      int task = atomicAdd(p.sync + 1, 1);
+      int task = atomicAdd(sm.ss + 1, 1);
       if (task < n_tasks && !wait_count(tile_cnt + task / p.n_tg, target, p.status)) {
         record_failure(p.status, sm.abort_flag, kInfoTileCount);
         task = n_tasks;
@@ -656,16 +722,17 @@ __global__ void __launch_bounds__(kSliceThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bid = static_cast<int>(blockIdx.x);
   const bool is_unit = bid < p.n_units;
-  Unit u;
-  u.shared = bid >= p.E * p.s_e;
-  u.e = u.shared ? -1 : bid / max(p.s_e, 1);
-  u.s = u.shared ? bid - p.E * p.s_e : bid % max(p.s_e, 1);
-  u.es = u.shared ? p.E : u.e;
-  u.nkb = ceil_div(p.H, kBlockK);
-  const int su = u.shared ? p.s_sh : p.s_e;
-  u.nkb_d = 2 * su;
-  u.j0 = p.n_mt * u.s / max(su, 1);
-  u.nj = p.n_mt * (u.s + 1) / max(su, 1) - u.j0;
+  const Unit u = make_unit(p, bid);
+  // Counter sets alternate between forwards: the previous forward flipped
+  // the parity word as it ended; this one clears the set the previous one
+  // used, which the next one will use.
+  const int par = *reinterpret_cast<const volatile int32_t*>(p.sync) & 1;
+  sm.ss = p.sync + 1 + par * p.set_words;
+  sm.ready = sm.ss + kSliceSyncWords + p.n_mt;
+  if (bid == static_cast<int>(gridDim.x) - 1) {
+    int32_t* other = p.sync + 1 + (par ^ 1) * p.set_words;
+    for (int i = threadIdx.x; i < p.set_words; i += blockDim.x) other[i] = 0;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < 8; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -685,7 +752,8 @@ __global__ void __launch_bounds__(kSliceThreads, 1)
     fence_barrier_init();
     fence_proxy_async();
   }
-  if (is_unit && warp == 0 && lane == 0) {
+  const bool works = is_unit || u.nj > 0;
+  if (works && warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_gu);
     tma_prefetch_desc(&tm_dn);
     tma_prefetch_desc(&tm_x);
@@ -694,7 +762,7 @@ __global__ void __launch_bounds__(kSliceThreads, 1)
       tma_prefetch_desc(&tm_dn_sh);
     }
   }
-  if (is_unit && warp == 1) {
+  if (works && warp == 1) {
     tmem_alloc(sm.tmem_slot, kSliceTmemCols);
     tmem_relinquish();
   }
@@ -702,7 +770,9 @@ __global__ void __launch_bounds__(kSliceThreads, 1)
   __syncthreads();
   tc_fence_after();
 
-  if (is_unit) {
+  // router CTAs route first, then help with the down GEMM
+  if (!is_unit && bid - p.n_units < p.n_rcta) route_tokens(p, sm, bid - p.n_units);
+  if (works) {
     const uint32_t tmem = *sm.tmem_slot;
     sm.b_bytes = static_cast<uint32_t>(p.n_tok) * 128u;
     sm.S = min(8, p.stage_space / static_cast<int>(2 * kTileBytesA + sm.b_bytes));
@@ -725,25 +795,16 @@ __global__ void __launch_bounds__(kSliceThreads, 1)
       while (clock64() - t0 < 4000000ll) {}
     }
     if (warp == 1) tmem_dealloc(tmem, kSliceTmemCols);
-  } else if (bid - p.n_units < p.n_rcta) {
-    route_tokens(p, sm, bid - p.n_units);
   }
 
   combine_tasks(p, sm);
 
-  // the last CTA out clears the counters and flags for the next forward
+  // the last CTA out (every CTA has read the parity word) flips it
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const int old = atomicAdd(p.sync + 2, 1);
-    if (old == static_cast<int>(gridDim.x) - 1) {
-      p.sync[0] = 0;
-      p.sync[1] = 0;
-      for (int m = 0; m < p.n_mt; ++m) p.sync[kSliceSyncWords + m] = 0;
-      for (int i = 0; i < (p.E + 1) * p.s_max; ++i) p.ready[i] = 0;
-      __threadfence();
-      p.sync[2] = 0;
-    }
+    const int old = atomicAdd(sm.ss + 2, 1);
+    if (old == static_cast<int>(gridDim.x) - 1) *reinterpret_cast<volatile int32_t*>(p.sync) = par ^ 1;
   }
 }
 
