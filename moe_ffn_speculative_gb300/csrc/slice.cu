@@ -450,6 +450,7 @@ __device__ void unit_tokens(const SliceParams& p, const SliceSmem& sm, const Uni
   int ok = 1;
   if (lane == 0) ok = wait_count(sm.ss + 0, p.n_rcta, p.status) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();  // orders every lane's reads of the routing after lane 0's acquire
   if (!ok) {
     if (lane == 0) {
       record_failure(p.status, sm.abort_flag, kInfoRouter);
@@ -494,6 +495,13 @@ __device__ void unit_tokens(const SliceParams& p, const SliceSmem& sm, const Uni
   if (n == 0 || u.nj == 0) {
     // nothing to add to this unit's output tiles
     if (!p.direct_y && !*sm.abort_flag) publish_tiles(sm, u.j0, u.j0 + u.nj);
+    return;
+  }
+  // The down ring aliases the gate_up ring: a unit's h fetches must wait
+  // until its MMAs have read every gate_up stage (and so every gate_up load
+  // has landed), however early the other slices are flagged ready.
+  if (u.has_a && !mbar_wait(sm.acca, 0, sm.abort_flag)) {
+    record_failure(p.status, sm.abort_flag, kInfoAccFull);
     return;
   }
   const DownGeom g = down_geom(p, u, n);

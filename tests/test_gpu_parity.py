@@ -391,3 +391,25 @@ def _check_full(cfg, name, T, used):
     assert torch.equal(y, y2), "not deterministic"
     st, info = layer.ws.device_status()
     assert st == 0, (st, info)
+
+
+@pytest.mark.parametrize("sched", list(SCHEDULES))
+def test_repeated_forwards_bit_identical(sched):
+    """Many forwards of the headline layer, with fresh (zeroed) workspaces
+    now and then, give bit-identical outputs: the kernels' cross-CTA
+    hand-offs (readiness flags, counters, aliased shared-memory rings) are
+    race-free under the timing spread of real runs."""
+    cfg = S.CONFIGS["qwen3_8b_dspark"]
+    _require(cfg, SCHEDULES[sched])
+    d = S.make_inputs(cfg, device="cuda")
+    rec = ops.Recipe.from_config(cfg)
+    with _schedule(SCHEDULES[sched]):
+        layer = ops.MoELayer(d, rec, cfg.T)
+        y_ref = layer.forward(d["x"]).clone()
+        for it in range(120):
+            if it % 20 == 0:
+                layer = ops.MoELayer(d, rec, cfg.T)
+            y = layer.forward(d["x"])
+            torch.cuda.synchronize()
+            assert torch.equal(y, y_ref), f"forward {it} differs"
+        assert layer.ws.device_status()[0] == 0
