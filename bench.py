@@ -395,7 +395,12 @@ def run_gpu(args, cfg, rank, world):
     if sched == "slice":
         # the fused launch is the whole layer: its algorithmic bytes are the layer's
         ex_bytes = layer_bytes
-    t_ex = per_kernel["fused" if sched == "slice" else "experts"] * 1e-6
+    if sched == "slice":
+        # the step is this one launch: its average duration over the timed
+        # graph region (inter-kernel gaps included) is the step time
+        t_ex = ms_step * 1e-3
+    else:
+        t_ex = per_kernel["experts"] * 1e-6
     achieved = ex_bytes / t_ex / 1e9
     layer_gbs = layer_bytes / (ms_step * 1e-3) / 1e9
     roof_layer_us = max(layer_bytes / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
@@ -411,7 +416,7 @@ def run_gpu(args, cfg, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "I": cfg.I, "K": cfg.K,
                    "shared_I": cfg.shared_I, "touched_experts": u, "schedule": sched,
-                   "launch": f"cuda_graph_replay, {G} layers per graph",
+                   "launch": f"cuda_graph_replay, {G} layer{'s' if G > 1 else ''} per graph",
                    "l2": f"weights rotate over {n_copies} copies ({n_copies * cfg.weight_bytes / 1e9:.2f} GB) > L2",
                    "parallelism": "replicas" if world > 1 else "single_gpu"},
         "roofline": {"bound": "hbm", "kernel": KERNELS[sched][0], "achieved": achieved, "peak": hbm,
