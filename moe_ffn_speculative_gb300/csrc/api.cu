@@ -104,17 +104,25 @@ moe_status check_recipe(const moe_recipe* r) {
 
 struct RouterGeom {
   int tb, quads, hsplit, n_eb, n_tb;
+  bool fold_sh;
 };
 
-RouterGeom router_geometry(int T, int E_tot, int sms) {
+// gated: a shared-expert gate row joins the E gate rows, unless it would
+// need an expert block of its own (then it is folded: fold_sh).
+RouterGeom router_geometry(int T, int E, bool gated, int sms) {
   RouterGeom g;
+  g.fold_sh = gated && E > 32 && ceil_div(E + 1, 32) > ceil_div(E, 32);
+  const int E_tot = E + ((gated && !g.fold_sh) ? 1 : 0);
   const int qn = ceil_div(E_tot, 4);
   g.quads = 1;
   while (g.quads < qn && g.quads < 8) g.quads <<= 1;
   g.hsplit = 8 / g.quads;
   g.n_eb = ceil_div(qn, g.quads);
+  // 4-token blocks when the grid would not fill the GPU with 8, and still
+  // fits in one wave (a router CTA holds a whole SM's registers)
   g.tb = 8;
-  if (static_cast<long long>(ceil_div(T, 8)) * g.n_eb < sms) g.tb = 4;
+  if (static_cast<long long>(ceil_div(T, 8)) * g.n_eb < sms && static_cast<long long>(ceil_div(T, 4)) * g.n_eb <= sms)
+    g.tb = 4;
   g.n_tb = ceil_div(T, g.tb);
   return g;
 }
@@ -173,7 +181,7 @@ struct Layout {
 
 Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sms) {
   Layout L;
-  L.rg = router_geometry(T, E + (gated ? 1 : 0), sms);
+  L.rg = router_geometry(T, E, gated, sms);
   int nm = ((T + 15) / 16) * 16;
   L.n_max = nm < 16 ? 16 : (nm > 256 ? 256 : nm);
   L.nbuf = (4 * L.n_max <= 512) ? 2 : 1;
@@ -206,7 +214,7 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   // stream-K arrival counters (gate_up, down) and gate_up readiness counters
   L.o_tiles = o; o = align_up(o + 4 * static_cast<size_t>(2 * L.max_gu_tiles + L.max_dn_tiles));
   L.o_logits = o; o = align_up(o + 4 * static_cast<size_t>(T) * E);
-  L.o_shl = o; o = align_up(o + 4 * static_cast<size_t>(T));
+  L.o_shl = o; o = align_up(o + 4 * static_cast<size_t>(T) * (L.rg.fold_sh ? L.rg.n_eb * L.rg.hsplit : 1));
   L.o_shw = o; o = align_up(o + 4 * static_cast<size_t>(T));
   L.o_idx = o; o = align_up(o + 4 * static_cast<size_t>(TK));
   L.o_w = o; o = align_up(o + 4 * static_cast<size_t>(TK));
@@ -293,7 +301,7 @@ moe_status moe_route(const moe_bf16* x, int T, int H, const moe_bf16* gate, cons
     return MOE_ERR_WORKSPACE;
   const int sms = device_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
-  const RouterGeom rg = router_geometry(T, E, sms);
+  const RouterGeom rg = router_geometry(T, E, false, sms);
   char* w = static_cast<char*>(ws);
   const size_t o_cnt = kAlign;
   const size_t o_logits = o_cnt + align_up(4 * static_cast<size_t>(ceil_div(T, 4) + 1));
@@ -441,6 +449,7 @@ moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf1
   rp.group_topn = recipe->group_topn; rp.renorm = recipe->norm_topk_prob; rp.eps = recipe->norm_eps;
   rp.scale = recipe->route_scale;
   rp.quads = L.rg.quads; rp.hsplit = L.rg.hsplit; rp.n_eb = L.rg.n_eb; rp.n_tb = L.rg.n_tb;
+  rp.fold_sh = L.rg.fold_sh ? 1 : 0;
   rp.logits = reinterpret_cast<float*>(w + L.o_logits);
   rp.sh_logit = reinterpret_cast<float*>(w + L.o_shl);
   rp.idx = idx; rp.w = wts; rp.sh_w = Is > 0 ? sh_w : nullptr;

@@ -231,6 +231,9 @@ __device__ bool produce(const Smem& sm, const GemmParams& p, int ngroups, const 
                         const long long (&e)[2], const int (&g)[2], const CUtensorMap* tm_gu,
                         const CUtensorMap* tm_gu_sh, const CUtensorMap* tm_dn, const CUtensorMap* tm_dn_sh,
                         Ring& ring, int32_t* status) {
+  // Weights are streamed once: evict them first, so that L2 keeps what the
+  // layer reuses (x, h, partials, the next kernels' code and metadata).
+  const uint64_t pol = l2_evict_first_policy();
   WeightCursor ld;
   ld.init(p, ngroups, b, e, g);
   while (ld.valid) {
@@ -244,7 +247,7 @@ __device__ bool produce(const Smem& sm, const GemmParams& p, int ngroups, const 
     int c0, c1, c2;
     for (int h = 0; h < 2; ++h) {
       const CUtensorMap* tm = ld.box(tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, h, c0, c1, c2);
-      tma_load_3d(a0 + h * kTileBytesA, tm, bar, c0, c1, c2);
+      tma_load_3d_hint(a0 + h * kTileBytesA, tm, bar, c0, c1, c2, pol);
     }
     ld.step();
     ring.next(sm.S);

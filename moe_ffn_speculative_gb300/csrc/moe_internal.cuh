@@ -138,7 +138,8 @@ struct RouteParams {
   float eps, scale;
   int quads, hsplit, n_eb, n_tb;
   float* logits;               // [T, E]
-  float* sh_logit;             // [T] (when sh_gate)
+  float* sh_logit;             // [T] (when sh_gate), or [T][n_eb*hsplit] partial sums (fold_sh)
+  int fold_sh;                 // the shared-gate row is folded into per-block partials
   int32_t* idx;                // [T*K]
   float* w;                    // [T*K]
   float* sh_w;                 // [T] (nullable)
@@ -295,6 +296,21 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "[%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
+}
+// The same with an L2 cache policy (createpolicy), e.g. evict-first for
+// weights that are streamed once.
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                                 int c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+      "{%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 // Contiguous bulk copy global -> shared (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

@@ -24,190 +24,289 @@ constexpr int kRouteThreads = 256;
 constexpr int kMaxExperts = 1024;
 // Counting-sort permutation of the (token, slot) pairs by expert, stable in
 // the pair index p = t*K + k, and (optionally) the grouped-GEMM work list.
-// Run by one whole CTA.  Up to kPermStaged ids are first copied to shared
-// memory in one parallel pass, so the serial scatter reads them from there.
+// Run by one whole CTA of kRouteThreads threads.  Up to kPermStaged ids are
+// first copied to shared memory; then each warp counts and scatters its own
+// contiguous chunk of pairs (per-warp cursors), so the stable order needs no
+// serial pass.  Larger inputs take one warp through all pairs.
 constexpr int kPermStaged = 4096;
+constexpr int kPermWarps = kRouteThreads / 32;
 // shared buffer: the staged ids, later the two cost prefixes of the work list
 constexpr int kPermBuf = 2080;  // long longs: >= kPermStaged / 2 and >= 2 * 1040
+
+// Exclusive prefix sum of in[0, n) into out (n <= 4 * blockDim.x); every
+// thread of the CTA calls it.  Thread t owns elements [per*t, per*t + per).
+__device__ void block_scan_excl(const int* in, int* out, int n, int* s_warp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (n + blockDim.x - 1) / blockDim.x;
+  const int i0 = tid * per;
+  int loc[4], sum = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = i0 + j;
+    loc[j] = (j < per && i < n) ? in[i] : 0;
+    sum += loc[j];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  int run = incl - sum;
+  for (int w = 0; w < warp; ++w) run += s_warp[w];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = i0 + j;
+    if (j < per && i < n) {
+      out[i] = run;
+      run += loc[j];
+    }
+  }
+  __syncthreads();
+}
 
 __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* counts, int32_t* offsets,
                               int32_t* sorted_pair, int32_t* pair_pos, GroupEntry* groups, GemmHeader* header,
                               int H, int I, int Is, int n_max, int* s_cnt, int* s_cur, long long* s_buf,
-                              int64_t* spans, int32_t* span_groups, int grid) {
+                              uint16_t* s_wc, int64_t* spans, int32_t* span_groups, int grid) {
+  __shared__ int s_warp[kPermWarps];
   int* s_idx = reinterpret_cast<int*>(s_buf);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int TK = T * K;
   const bool staged = TK <= kPermStaged;
   for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
-  if (staged)
-    for (int p = tid; p < TK; p += blockDim.x) s_idx[p] = __ldcg(idx + p);
+  if (staged) {
+    for (int q = tid; q < TK; q += blockDim.x) s_idx[q] = __ldcg(idx + q);
+    for (int q = tid; q < kPermWarps * E; q += blockDim.x) s_wc[q] = 0;
+  }
   __syncthreads();
   // ids outside [0, E) are not counted and get no row
-  for (int p = tid; p < TK; p += blockDim.x) {
-    const int e = staged ? s_idx[p] : __ldcg(idx + p);
-    if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicAdd(&s_cnt[e], 1);
+  const int chunk = (TK + kPermWarps - 1) / kPermWarps;
+  const int p0 = warp * chunk, p1 = min(TK, p0 + chunk);
+  uint16_t* wc = s_wc + warp * E;  // this warp's per-expert counts, then cursors
+  if (staged) {
+    // count the warp's chunk: one leader per expert and batch adds the batch's count
+    for (int base = p0; base < p1; base += 32) {
+      const int q = base + lane;
+      const int ev = q < p1 ? s_idx[q] : -1;
+      const bool act = static_cast<unsigned>(ev) < static_cast<unsigned>(E);
+      const uint32_t peers = __match_any_sync(0xffffffffu, act ? ev : -1 - lane);
+      if (act && lane == __ffs(peers) - 1) wc[ev] = static_cast<uint16_t>(wc[ev] + __popc(peers));
+      __syncwarp();
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+      int c = 0;
+      for (int w = 0; w < kPermWarps; ++w) c += s_wc[w * E + e];
+      s_cnt[e] = c;
+    }
+  } else {
+    for (int q = tid; q < TK; q += blockDim.x) {
+      const int e = __ldcg(idx + q);
+      if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicAdd(&s_cnt[e], 1);
+    }
   }
   __syncthreads();
-  if (warp == 0) {
-    int carry = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      const int v = e < E ? s_cnt[e] : 0;
-      int incl = v;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += n;
+  block_scan_excl(s_cnt, s_cur, E, s_warp);  // s_cur[e]: first row of expert e
+  if (staged) {
+    // each warp's rows of expert e follow those of the warps before it
+    for (int e = tid; e < E; e += blockDim.x) {
+      int run = s_cur[e];
+      for (int w = 0; w < kPermWarps; ++w) {
+        const int c = s_wc[w * E + e];
+        s_wc[w * E + e] = static_cast<uint16_t>(run);
+        run += c;
       }
-      if (e < E) s_cur[e] = carry + incl - v;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    __syncwarp();
-    for (int base = 0; base < TK; base += 32) {
-      const int p = base + lane;
-      const int ev = p < TK ? (staged ? s_idx[p] : __ldcg(idx + p)) : -1;
+    __syncthreads();
+    for (int base = p0; base < p1; base += 32) {
+      const int q = base + lane;
+      const int ev = q < p1 ? s_idx[q] : -1;
       const bool act = static_cast<unsigned>(ev) < static_cast<unsigned>(E);
-      const int e = act ? ev : -1 - lane;
-      const uint32_t peers = __match_any_sync(0xffffffffu, e);
+      const uint32_t peers = __match_any_sync(0xffffffffu, act ? ev : -1 - lane);
       const int rank = __popc(peers & ((1u << lane) - 1u));
       const int leader = __ffs(peers) - 1;
-      int bpos = (act && lane == leader) ? s_cur[e] : 0;
+      int bpos = (act && lane == leader) ? static_cast<int>(wc[ev]) : 0;
       bpos = __shfl_sync(0xffffffffu, bpos, leader);
       if (act) {
-        sorted_pair[bpos + rank] = p;
-        pair_pos[p] = bpos + rank;
+        sorted_pair[bpos + rank] = q;
+        pair_pos[q] = bpos + rank;
       }
       __syncwarp();
-      if (act && lane == leader) s_cur[e] = bpos + __popc(peers);
+      if (act && lane == leader) wc[ev] = static_cast<uint16_t>(bpos + __popc(peers));
+      __syncwarp();
+    }
+  } else if (warp == 0) {
+    // inputs too large to stage: one warp scatters every pair in order,
+    // with cursors in s_wc's place (s_cnt + s_cur give the starts)
+    for (int base = 0; base < TK; base += 32) {
+      const int q = base + lane;
+      const int ev = q < TK ? __ldcg(idx + q) : -1;
+      const bool act = static_cast<unsigned>(ev) < static_cast<unsigned>(E);
+      const uint32_t peers = __match_any_sync(0xffffffffu, act ? ev : -1 - lane);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int leader = __ffs(peers) - 1;
+      int bpos = (act && lane == leader) ? s_cur[ev] : 0;
+      bpos = __shfl_sync(0xffffffffu, bpos, leader);
+      if (act) {
+        sorted_pair[bpos + rank] = q;
+        pair_pos[q] = bpos + rank;
+      }
+      __syncwarp();
+      if (act && lane == leader) s_cur[ev] = bpos + __popc(peers);
       __syncwarp();
     }
   }
   __syncthreads();
-  // s_cur[e] now holds the end of expert e's rows
+  if (!staged) {  // the serial scatter advanced s_cur to the ends: back to the starts
+    for (int e = tid; e < E; e += blockDim.x) s_cur[e] -= s_cnt[e];
+    __syncthreads();
+  }
   for (int e = tid; e < E; e += blockDim.x) {
     if (counts) counts[e] = s_cnt[e];
-    if (offsets) offsets[e + 1] = s_cur[e];
+    if (offsets) offsets[e + 1] = s_cur[e] + s_cnt[e];
   }
   if (tid == 0 && offsets) offsets[0] = 0;
   if (groups == nullptr) return;
   // ---- work list: one group per touched expert (expert order), then the
   // shared expert; prefix sums of tiles, k-block iterations and k-block costs
-  // per GEMM.  The cost prefix goes to shared memory (the staged ids are no
-  // longer needed) for the span computation below.
+  // per GEMM.  Thread t owns experts [per*t, per*t + per); one block-wide
+  // scan gives every prefix.  The cost prefixes go to shared memory (the
+  // staged ids are no longer needed) for the span computation below.
   long long* s_cost0 = s_buf;              // [groups + 1]
   long long* s_cost1 = s_buf + 1040;       // [groups + 1]
   __shared__ int s_ngroups;
   __shared__ int s_neff;
   __shared__ long long s_tot[4];           // gate_up iters, down iters, gate_up cost, down cost
+  __shared__ long long s_wtot[kPermWarps][4];
   if (tid == 0) s_neff = 16;
   __syncthreads();
-  // widest token tile: the largest count (capped at n_max), shared expert included
-  for (int e = tid; e < E; e += blockDim.x)
-    if (s_cnt[e] > 0) atomicMax(&s_neff, min(n_max, (s_cnt[e] + 15) & ~15));
-  if (tid == 0 && Is > 0) atomicMax(&s_neff, min(n_max, (T + 15) & ~15));
-  __syncthreads();
-  if (warp == 0) {
-    int g = 0, gu_t = 0, dn_t = 0;
-    long long gu_i = 0, dn_i = 0, gu_c = 0, dn_c = 0;
-    auto geometry = [&](int c, int idim, int& gut, int& dnt, long long& gui, long long& dni, int& w0, int& w1) {
-      int mb, nb, kb;
+  // widest token tile: the largest count (capped at n_max), shared expert
+  // included; reduced within each warp first, so one shared atomic per warp
+  {
+    int wmax = (tid == 0 && Is > 0) ? min(n_max, (T + 15) & ~15) : 16;
+    for (int e = tid; e < E; e += blockDim.x)
+      if (s_cnt[e] > 0) wmax = max(wmax, min(n_max, (s_cnt[e] + 15) & ~15));
+    wmax = __reduce_max_sync(0xffffffffu, wmax);
+    if (lane == 0) atomicMax(&s_neff, wmax);
+  }
+  // geometry of a routed expert's tiles (every routed expert has the same I)
+  const int mb0 = ceil_div(I, kHalfRows), kb0 = ceil_div(H, kBlockK);
+  const int mb1 = ceil_div(H, 2 * kHalfRows), kb1 = ceil_div(I, kBlockK);
+  const int per = (E + blockDim.x - 1) / blockDim.x;
+  const int e0 = tid * per;
+  // this thread's sums: touched experts, token blocks, gate_up cost, down cost
+  long long v[4] = {0, 0, 0, 0};
+  for (int j = 0; j < per; ++j) {
+    const int e = e0 + j;
+    const int c = e < E ? s_cnt[e] : 0;
+    if (c > 0) {
+      const int nb = ceil_div(c, n_max);
       const int nmma = max(16, min(n_max, (c + 15) & ~15));
-      group_geometry(0, c, idim, H, n_max, mb, nb, kb);
-      gut = mb * nb;
-      gui = static_cast<long long>(gut) * kb;
-      group_geometry(1, c, idim, H, n_max, mb, nb, kb);
-      dnt = mb * nb;
-      dni = static_cast<long long>(dnt) * kb;
-      w0 = kblock_cost(0, nmma);
-      w1 = kblock_cost(1, nmma);
-    };
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      const int c = e < E ? s_cnt[e] : 0;
-      const bool touched = c > 0;
-      const uint32_t m = __ballot_sync(0xffffffffu, touched);
-      int gut = 0, dnt = 0, w0 = 0, w1 = 0;
-      long long gui = 0, dni = 0;
-      if (touched) geometry(c, I, gut, dnt, gui, dni, w0, w1);
-      const long long guc = gui * w0, dnc = dni * w1;
-      int a = gut, b = dnt;
-      long long ci = gui, di = dni, cc = guc, dc = dnc;
+      v[0] += 1;
+      v[1] += nb;
+      v[2] += static_cast<long long>(nb) * mb0 * kb0 * kblock_cost(0, nmma);
+      v[3] += static_cast<long long>(nb) * mb1 * kb1 * kblock_cost(1, nmma);
+    }
+  }
+  long long incl[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int na = __shfl_up_sync(0xffffffffu, a, off);
-        const int nb2 = __shfl_up_sync(0xffffffffu, b, off);
-        const long long nci = __shfl_up_sync(0xffffffffu, ci, off);
-        const long long ndi = __shfl_up_sync(0xffffffffu, di, off);
-        const long long ncc = __shfl_up_sync(0xffffffffu, cc, off);
-        const long long ndc = __shfl_up_sync(0xffffffffu, dc, off);
-        if (lane >= off) { a += na; b += nb2; ci += nci; di += ndi; cc += ncc; dc += ndc; }
-      }
-      if (touched) {
-        const int gi = g + __popc(m & ((1u << lane) - 1u));
-        GroupEntry ge;
-        ge.expert = e;
-        ge.row_base = s_cur[e] - c;
-        ge.count = c;
-        ge.idim = I;
-        ge.gu_tile = gu_t + a - gut;
-        ge.dn_tile = dn_t + b - dnt;
-        ge.gu_w = w0;
-        ge.dn_w = w1;
-        ge.gu_iter = gu_i + ci - gui;
-        ge.dn_iter = dn_i + di - dni;
-        groups[gi] = ge;
-        s_cost0[gi] = gu_c + cc - guc;
-        s_cost1[gi] = dn_c + dc - dnc;
-      }
-      g += __popc(m);
-      gu_t += __shfl_sync(0xffffffffu, a, 31);
-      dn_t += __shfl_sync(0xffffffffu, b, 31);
-      gu_i += __shfl_sync(0xffffffffu, ci, 31);
-      dn_i += __shfl_sync(0xffffffffu, di, 31);
-      gu_c += __shfl_sync(0xffffffffu, cc, 31);
-      dn_c += __shfl_sync(0xffffffffu, dc, 31);
+  for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const long long o = __shfl_up_sync(0xffffffffu, incl[q], off);
+      if (lane >= off) incl[q] += o;
     }
-    if (lane == 0) {
-      if (Is > 0) {
-        int gut, dnt, w0, w1;
-        long long gui, dni;
-        geometry(T, Is, gut, dnt, gui, dni, w0, w1);
-        GroupEntry ge;
-        ge.expert = -1;
-        ge.row_base = TK;
-        ge.count = T;
-        ge.idim = Is;
-        ge.gu_tile = gu_t;
-        ge.dn_tile = dn_t;
-        ge.gu_w = w0;
-        ge.dn_w = w1;
-        ge.gu_iter = gu_i;
-        ge.dn_iter = dn_i;
-        groups[g] = ge;
-        s_cost0[g] = gu_c;
-        s_cost1[g] = dn_c;
-        gu_t += gut;
-        dn_t += dnt;
-        gu_i += gui;
-        dn_i += dni;
-        gu_c += gui * w0;
-        dn_c += dni * w1;
-        ++g;
-      }
-      GemmHeader hd;
-      hd.ngroups = g;
-      hd.gu_tiles = gu_t;
-      hd.dn_tiles = dn_t;
-      hd.n_eff = s_neff;
-      hd.gu_iters = gu_i;
-      hd.dn_iters = dn_i;
-      *header = hd;
-      s_ngroups = g;
-      s_tot[0] = gu_i;
-      s_tot[1] = dn_i;
-      s_tot[2] = gu_c;
-      s_tot[3] = dn_c;
+  }
+  if (lane == 31)
+    for (int q = 0; q < 4; ++q) s_wtot[warp][q] = incl[q];
+  __syncthreads();
+  long long run[4], tot[4];
+  for (int q = 0; q < 4; ++q) {
+    run[q] = incl[q] - v[q];
+    tot[q] = 0;
+  }
+  for (int w = 0; w < kPermWarps; ++w)
+    for (int q = 0; q < 4; ++q) {
+      if (w < warp) run[q] += s_wtot[w][q];
+      tot[q] += s_wtot[w][q];
     }
+  for (int j = 0; j < per; ++j) {
+    const int e = e0 + j;
+    const int c = e < E ? s_cnt[e] : 0;
+    if (c > 0) {
+      const int nb = ceil_div(c, n_max);
+      const int nmma = max(16, min(n_max, (c + 15) & ~15));
+      const int gi = static_cast<int>(run[0]);
+      const int w0 = kblock_cost(0, nmma), w1 = kblock_cost(1, nmma);
+      GroupEntry ge;
+      ge.expert = e;
+      ge.row_base = s_cur[e];
+      ge.count = c;
+      ge.idim = I;
+      ge.gu_tile = static_cast<int>(run[1]) * mb0;
+      ge.dn_tile = static_cast<int>(run[1]) * mb1;
+      ge.gu_w = w0;
+      ge.dn_w = w1;
+      ge.gu_iter = run[1] * mb0 * kb0;
+      ge.dn_iter = run[1] * mb1 * kb1;
+      groups[gi] = ge;
+      s_cost0[gi] = run[2];
+      s_cost1[gi] = run[3];
+      run[0] += 1;
+      run[1] += nb;
+      run[2] += static_cast<long long>(nb) * mb0 * kb0 * w0;
+      run[3] += static_cast<long long>(nb) * mb1 * kb1 * w1;
+    }
+  }
+  __syncthreads();  // s_neff is final
+  if (tid == 0) {
+    int g = static_cast<int>(tot[0]);
+    int gu_t = static_cast<int>(tot[1]) * mb0, dn_t = static_cast<int>(tot[1]) * mb1;
+    long long gu_i = tot[1] * mb0 * kb0, dn_i = tot[1] * mb1 * kb1, gu_c = tot[2], dn_c = tot[3];
+    if (Is > 0) {
+      int mb, nb, kb;
+      const int nmma = max(16, min(n_max, (T + 15) & ~15));
+      const int w0 = kblock_cost(0, nmma), w1 = kblock_cost(1, nmma);
+      GroupEntry ge;
+      ge.expert = -1;
+      ge.row_base = TK;
+      ge.count = T;
+      ge.idim = Is;
+      ge.gu_tile = gu_t;
+      ge.dn_tile = dn_t;
+      ge.gu_w = w0;
+      ge.dn_w = w1;
+      ge.gu_iter = gu_i;
+      ge.dn_iter = dn_i;
+      groups[g] = ge;
+      s_cost0[g] = gu_c;
+      s_cost1[g] = dn_c;
+      group_geometry(0, T, Is, H, n_max, mb, nb, kb);
+      gu_t += mb * nb;
+      gu_i += static_cast<long long>(mb) * nb * kb;
+      gu_c += static_cast<long long>(mb) * nb * kb * w0;
+      group_geometry(1, T, Is, H, n_max, mb, nb, kb);
+      dn_t += mb * nb;
+      dn_i += static_cast<long long>(mb) * nb * kb;
+      dn_c += static_cast<long long>(mb) * nb * kb * w1;
+      ++g;
+    }
+    GemmHeader hd;
+    hd.ngroups = g;
+    hd.gu_tiles = gu_t;
+    hd.dn_tiles = dn_t;
+    hd.n_eff = s_neff;
+    hd.gu_iters = gu_i;
+    hd.dn_iters = dn_i;
+    *header = hd;
+    s_ngroups = g;
+    s_tot[0] = gu_i;
+    s_tot[1] = dn_i;
+    s_tot[2] = gu_c;
+    s_tot[3] = dn_c;
   }
   __syncthreads();
   // ---- CTA spans: cut each GEMM's total cost into `grid` equal parts and
@@ -250,9 +349,15 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
   __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_cur[kMaxExperts];
   __shared__ long long s_buf[kPermBuf];
+  __shared__ uint16_t s_wc[kPermWarps * kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tbi = blockIdx.x, ebi = blockIdx.y;
-  const int E_tot = p.E + (p.sh_gate ? 1 : 0);
+  // The shared-expert gate is one more row of the GEMV, unless that row
+  // would add an expert block (fold_sh): then the quad-0 warps of every
+  // block add x.sh_gate over a disjoint subset of H steps and leave partial
+  // sums that the selecting warp adds in block order.
+  const bool fold = p.fold_sh != 0;
+  const int E_tot = p.E + ((p.sh_gate && !fold) ? 1 : 0);
   {  // clear the GEMM tile counters for this forward
     const int nthr = gridDim.x * gridDim.y * kRouteThreads;
     const int gid = (blockIdx.y * gridDim.x + blockIdx.x) * kRouteThreads + threadIdx.x;
@@ -273,37 +378,58 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
   const int hs_len = ceil_div(ceil_div(p.H, p.hsplit), 8) * 8;
   const int h_lo = hs * hs_len;
   const int h_hi = min(p.H, h_lo + hs_len);
-  float acc[TB][4];
+  float acc[TB][4], acc_sh[TB];
 #pragma unroll
-  for (int t = 0; t < TB; ++t)
+  for (int t = 0; t < TB; ++t) {
+    acc_sh[t] = 0.f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[t][q] = 0.f;
+  }
+  const bool do_sh = fold && quad == 0;
   // one step of loads stays in flight while the previous step is multiplied
-  uint4 gv[4], xv[TB];
-  auto load_step = [&](int c, uint4 (&g)[4], uint4 (&xx)[TB]) {
+  uint4 gv[4], xv[TB], sv;
+  auto load_step = [&](int c, int step, uint4 (&g)[4], uint4 (&xx)[TB], uint4& sg) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) g[q] = ev[q] ? ldg128(rows[q] + c) : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int t = 0; t < TB; ++t)
       xx[t] = (t0 + t < p.T) ? ldg128(p.x + static_cast<size_t>(t0 + t) * p.H + c) : make_uint4(0, 0, 0, 0);
+    sg = (do_sh && step % p.n_eb == ebi) ? ldg128(p.sh_gate + c) : make_uint4(0, 0, 0, 0);
   };
-  int c = h_lo + lane * 8;
-  if (c < h_hi) load_step(c, gv, xv);
+  int c = h_lo + lane * 8, step = 0;
+  if (c < h_hi) load_step(c, 0, gv, xv, sv);
   while (c < h_hi) {
     const int cn = c + 256;
-    uint4 gn[4], xn[TB];
-    if (cn < h_hi) load_step(cn, gn, xn);
+    uint4 gn[4], xn[TB], sn;
+    if (cn < h_hi) load_step(cn, step + 1, gn, xn, sn);
 #pragma unroll
     for (int t = 0; t < TB; ++t)
 #pragma unroll
       for (int q = 0; q < 4; ++q) acc[t][q] = dot8(xv[t], gv[q], acc[t][q]);
+    if (do_sh && step % p.n_eb == ebi) {
+#pragma unroll
+      for (int t = 0; t < TB; ++t) acc_sh[t] = dot8(xv[t], sv, acc_sh[t]);
+    }
     if (cn < h_hi) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) gv[q] = gn[q];
 #pragma unroll
       for (int t = 0; t < TB; ++t) xv[t] = xn[t];
+      sv = sn;
     }
     c = cn;
+    ++step;
+  }
+  if (do_sh) {
+    // this block's partial of x.sh_gate for each token: slot ebi*hsplit + hs
+#pragma unroll
+    for (int t = 0; t < TB; ++t) {
+      float v = acc_sh[t];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (lane == 0 && t0 + t < p.T)
+        p.sh_logit[static_cast<size_t>(t0 + t) * p.n_eb * p.hsplit + ebi * p.hsplit + hs] = v;
+    }
   }
 #pragma unroll
   for (int t = 0; t < TB; ++t)
@@ -365,7 +491,16 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
       const int tok = t0 + warp;
       select_token<NJ, false>(p.logits + static_cast<size_t>(tok) * p.E, sel,
                               p.idx + static_cast<size_t>(tok) * p.K, p.w + static_cast<size_t>(tok) * p.K);
-      if (lane == 0 && p.sh_w) p.sh_w[tok] = p.sh_gate ? 1.f / (1.f + expf(-__ldcg(p.sh_logit + tok))) : 1.f;
+      if (lane == 0 && p.sh_w) {
+        float v = 0.f;
+        if (fold) {  // the blocks' partials of x.sh_gate, in block order
+          const int np = p.n_eb * p.hsplit;
+          for (int i = 0; i < np; ++i) v += __ldcg(p.sh_logit + static_cast<size_t>(tok) * np + i);
+        } else if (p.sh_gate) {
+          v = __ldcg(p.sh_logit + tok);
+        }
+        p.sh_w[tok] = p.sh_gate ? 1.f / (1.f + expf(-v)) : 1.f;
+      }
     }
   }
   if (!p.do_permute) return;
@@ -381,7 +516,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
   if (!s_flag) return;
   __threadfence();
   permute_block(p.idx, p.T, p.K, p.E, p.counts, p.offsets, p.sorted_pair, p.pair_pos, p.groups, p.header, p.H,
-                p.I, p.Is, p.n_max, s_cnt, s_cur, s_buf, p.spans, p.span_groups, p.grid);
+                p.I, p.Is, p.n_max, s_cnt, s_cur, s_buf, s_wc, p.spans, p.span_groups, p.grid);
 }
 
 template <int NJ>
@@ -399,8 +534,9 @@ __global__ void __launch_bounds__(kRouteThreads) permute_kernel(const int32_t* i
   __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_cur[kMaxExperts];
   __shared__ long long s_buf[kPermBuf];
+  __shared__ uint16_t s_wc[kPermWarps * kMaxExperts];
   permute_block(idx, T, K, E, counts, offsets, sorted_pair, pair_pos, nullptr, nullptr, 0, 0, 0, 1, s_cnt, s_cur,
-                s_buf, nullptr, nullptr, 0);
+                s_buf, s_wc, nullptr, nullptr, 0);
 }
 
 int nj_for(int E) {
