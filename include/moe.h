@@ -208,9 +208,10 @@ MOE_API moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I,
  *       per-slice partial outputs.  An expert no token picked stops streaming
  *       once the routing is known.  Shape limits: T <= 128, E (+1 with
  *       sh_gate) <= 16, E*ceil(I/128) + ceil(Is/128) + ceil(T/7) <= SMs.
- *   MOE_SCHEDULE_AUTO      SLICE where the shape fits and, under uniform
- *       routing, the expected number of untouched experts E*(1-K/E)^T is at
- *       most 0.25; STREAM_K otherwise.
+ *   MOE_SCHEDULE_AUTO      SLICE where the shape fits, the expected number
+ *       of untouched experts under uniform routing, E*(1-K/E)^T, is at most
+ *       0.25, and there is at least one 128-row down output tile per SM
+ *       (E*ceil(H/128) >= SMs); STREAM_K otherwise.
  * Both give the same routing; outputs agree to fp32 summation order. */
 typedef enum {
   MOE_SCHEDULE_AUTO = 0,

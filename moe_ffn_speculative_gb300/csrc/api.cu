@@ -252,7 +252,10 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 
 bool use_slice(const Layout& L, int T, int E, int K) {
   if (!L.sp.ok || t_schedule == MOE_SCHEDULE_STREAM_K) return false;
-  return t_schedule == MOE_SCHEDULE_SLICE || slice_expected(T, E, K);
+  if (t_schedule == MOE_SCHEDULE_SLICE) return true;
+  // automatic: untouched experts rare, and at least one down output tile per
+  // CTA (a dense or nearly dense layer spreads its down GEMM better as stream-K)
+  return slice_expected(T, E, K) && E * L.sp.n_mt >= L.grid;
 }
 
 void record_event_on(int i, cudaStream_t s) {

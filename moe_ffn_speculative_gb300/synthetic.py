@@ -83,6 +83,26 @@ CONFIGS: Dict[str, LayerConfig] = {
                               score_fn=SQRTSOFTPLUS, expert_bias_std=0.05, route_scale=1.5,
                               swiglu_limit=7.0, shared_I=1024, seed=4),
 }
+
+# Further MoE-FFN shapes the pages name, for parity and measurement (the
+# pages give the expert shape and recipe; hidden sizes and shared-expert
+# widths they leave open are the plainest readings, see the design notes):
+# * DeepSeek-V4-Flash drafter: 64 experts x 2048, top-6, ungated shared expert,
+#   sqrt(softplus), selection bias, scale 1.5, SwiGLU clamp 10;
+# * DeepSeek-V4.1's own DSpark draft: 128 experts x 2304, top-3, one shared
+#   expert, sqrt(softplus) x 1.5, clamped SwiGLU, expert bias;
+# * a dense draft layer (no expert fields: E = 1, top-1) of Qwen3-8B's MLP
+#   width, through the same engine.
+VARIANTS: Dict[str, LayerConfig] = {
+    "dsv4_flash_drafter": LayerConfig("dsv4_flash_drafter", T=72, H=4096, E=64, I=2048, K=6,
+                                      score_fn=SQRTSOFTPLUS, expert_bias_std=0.05, route_scale=1.5,
+                                      swiglu_limit=10.0, shared_I=2048, seed=21),
+    "dsv41_dspark_draft": LayerConfig("dsv41_dspark_draft", T=72, H=4096, E=128, I=2304, K=3,
+                                      score_fn=SQRTSOFTPLUS, expert_bias_std=0.05, route_scale=1.5,
+                                      swiglu_limit=10.0, shared_I=2304, seed=22),
+    "dense_draft": LayerConfig("dense_draft", T=72, H=4096, E=1, I=12288, K=1, seed=23),
+}
+CONFIGS.update(VARIANTS)
 DSV4_TOKEN_SWEEP = (9, 72, 576, 4096)
 
 
