@@ -210,8 +210,10 @@ MOE_API moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I,
  *       sh_gate) <= 16, E*ceil(I/128) + ceil(Is/128) + ceil(T/7) <= SMs.
  *   MOE_SCHEDULE_AUTO      SLICE where the shape fits, the expected number
  *       of untouched experts under uniform routing, E*(1-K/E)^T, is at most
- *       0.25, and there is at least one 128-row down output tile per SM
- *       (E*ceil(H/128) >= SMs); STREAM_K otherwise.
+ *       0.25, and the down GEMM's work items (128-row output tiles, each cut
+ *       into up to 2*ceil(I/128) k-block ranges so that the items do not
+ *       outnumber the SMs) occupy at least three quarters of the SMs;
+ *       STREAM_K otherwise.
  * Both give the same routing; outputs agree to fp32 summation order. */
 typedef enum {
   MOE_SCHEDULE_AUTO = 0,

@@ -133,6 +133,7 @@ RouterGeom router_geometry(int T, int E, bool gated, int sms) {
 struct SlicePlan {
   bool ok, reserve;
   int n_tok, s_e, s_sh, s_max, n_units, n_mt, n_rcta, n_tg, stage_space;
+  int parts;  // k-block ranges per down output tile, so that the down items occupy the SMs
 };
 
 SlicePlan slice_plan(int T, int H, int I, int Is, int E, bool gated, int sms) {
@@ -149,6 +150,12 @@ SlicePlan slice_plan(int T, int H, int I, int Is, int E, bool gated, int sms) {
   s.n_rcta = ceil_div(Tr, kSliceTokPerTask);
   s.n_tg = ceil_div(Tr, kSliceTokPerTask);
   s.stage_space = kSmemLimit - 1024 - kSliceCtrlBytes;
+  {
+    const int n_es = E + (s.s_sh > 0 ? 1 : 0);
+    const int s_min = s.s_sh > 0 && s.s_sh < s.s_e ? s.s_sh : s.s_e;
+    const int by_sm = sms / (n_es * s.n_mt);
+    s.parts = by_sm < 1 ? 1 : (by_sm < 2 * s_min ? by_sm : 2 * s_min);
+  }
   // four stages at least: their token-tile parts later hold h (2 k-blocks x hi/lo)
   const bool smem_ok = s.stage_space / (2 * kTileBytesA + kSliceMaxTok * 128) >= 4;
   s.reserve = smem_ok && s.n_units + 1 <= sms;
@@ -242,7 +249,7 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
     L.o_sync = o; o = align_up(o + 4 * (1 + 2 * static_cast<size_t>(slice_set_words(L.sp, E))));
     L.o_hbuf = o; o = align_up(o + n_es * 2 * L.sp.s_max * 2 * static_cast<size_t>(L.sp.n_tok) * 128);
     L.o_sout = o;
-    if (K > 1 || Is > 0) o = align_up(o + 4 * slots * H);
+    if (K > 1 || Is > 0 || L.sp.parts > 1) o = align_up(o + 4 * slots * H * static_cast<size_t>(L.sp.parts));
   }
   L.total = o;
   return L;
@@ -253,9 +260,10 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 bool use_slice(const Layout& L, int T, int E, int K) {
   if (!L.sp.ok || t_schedule == MOE_SCHEDULE_STREAM_K) return false;
   if (t_schedule == MOE_SCHEDULE_SLICE) return true;
-  // automatic: untouched experts rare, and at least one down output tile per
-  // CTA (a dense or nearly dense layer spreads its down GEMM better as stream-K)
-  return slice_expected(T, E, K) && E * L.sp.n_mt >= L.grid;
+  // automatic: untouched experts rare, and enough down items (output tiles
+  // x k-block parts) to occupy three quarters of the CTAs
+  const int n_es = E + (L.sp.s_sh > 0 ? 1 : 0);
+  return slice_expected(T, E, K) && 4 * n_es * L.sp.n_mt * L.sp.parts >= 3 * L.grid;
 }
 
 void record_event_on(int i, cudaStream_t s) {
@@ -430,7 +438,8 @@ moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf1
     sp.idx = idx; sp.w = wts; sp.sh_w = sh_w; sp.counts = counts;
     sp.hbuf = reinterpret_cast<uint8_t*>(w + L.o_hbuf);
     sp.out = reinterpret_cast<float*>(w + L.o_sout);
-    sp.direct_y = (K == 1 && Is == 0) ? 1 : 0;
+    sp.parts = L.sp.parts;
+    sp.direct_y = (K == 1 && Is == 0 && L.sp.parts == 1) ? 1 : 0;
     sp.y = y;
     sp.sync = reinterpret_cast<int32_t*>(w + L.o_sync);
     sp.set_words = slice_set_words(L.sp, E);

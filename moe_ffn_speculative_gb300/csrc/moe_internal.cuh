@@ -178,7 +178,8 @@ struct SliceParams {
   int n_rcta;                  // router CTAs (after the unit CTAs)
   int n_tg;                    // token groups of the combine (kSliceTokPerTask tokens each)
   int stage_space;             // shared-memory bytes for the stage rings
-  int direct_y;                // top-1 without a shared expert: the down epilogue writes y
+  int parts;                   // k-block ranges per down output tile (fp32 partials when > 1)
+  int direct_y;                // top-1, no shared expert, one part: the down epilogue writes y
   float swiglu_limit;
   float* logits;               // [T,E]
   int32_t* idx;                // [T*K]
@@ -186,7 +187,7 @@ struct SliceParams {
   float* sh_w;                 // [T] shared-expert weight (gate, or 1)
   int32_t* counts;             // [E]
   uint8_t* hbuf;               // [(E+1) * 2*s_max] h tiles of 2*n_tok rows x 128 B (see slice.cu)
-  float* out;                  // [T*K + T, H] fp32 weighted expert outputs (unless direct_y)
+  float* out;                  // [parts][T*K + T, H] fp32 weighted expert outputs (unless direct_y)
   uint16_t* y;                 // [T,H]
   // [1 + 2 * set_words]: a parity word, then two counter sets used by
   // alternate forwards; a set is kSliceSyncWords words (router done, combine

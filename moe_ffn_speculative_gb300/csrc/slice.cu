@@ -55,7 +55,7 @@ struct SliceSmem {
   uint8_t* bbase;  // gate_up: the token tiles after the S weight parts
   uint32_t b_bytes;
   int S;
-  uint64_t *full, *empty, *fullB, *emptyB, *acca, *accf, *acce, *routed, *drain;
+  uint64_t *full, *empty, *fullB, *emptyB, *acca, *accf, *acce, *routed, *drain, *hread;
   volatile int* abort_flag;
   volatile int* kb_stop;  // first gate_up k-block the producer did not issue
   volatile int* n_e;      // tokens routed to this unit's expert
@@ -81,6 +81,7 @@ __device__ __forceinline__ void carve(uint8_t* ctrl, SliceSmem& sm) {
   sm.acce = bars + 34;
   sm.routed = bars + 35;
   sm.drain = bars + 36;
+  sm.hread = bars + 37;  // the epilogue has read the gate_up accumulators
   int* words = reinterpret_cast<int*>(ctrl + 320);
   sm.tmem_slot = reinterpret_cast<uint32_t*>(words);
   sm.abort_flag = words + 1;
@@ -216,7 +217,9 @@ __device__ void route_tokens(const SliceParams& p, const SliceSmem& sm, int rc) 
 // A CTA's share of the experts' work.  A unit (has_a) owns slice s of an
 // expert in the gate_up GEMM; every CTA that is not a unit (the router CTAs
 // once routing is done, and the rest) is a down-only helper of one expert.
-// An expert's output tiles are split evenly over its units and helpers.
+// An expert's down work is n_mt 128-row output tiles, each cut into
+// p.parts ranges of its k-blocks (items, tile-major); the items are split
+// evenly over the expert's units and helpers.
 struct Unit {
   bool has_a;   // runs the gate_up GEMM for slice s
   bool shared;
@@ -225,7 +228,7 @@ struct Unit {
   int nkb;      // gate_up k-blocks: ceil(H / 64), 0 for helpers
   int nkb_d;    // down k-blocks: 2 per slice of the expert
   int kstart;   // first down k-block: the unit's own slice, 0 for helpers
-  int j0, nj;   // the CTA's output tiles [j0, j0 + nj)
+  int i0, ni;   // the CTA's down items [i0, i0 + ni)
 };
 
 __device__ __forceinline__ Unit make_unit(const SliceParams& p, int bid) {
@@ -253,8 +256,9 @@ __device__ __forceinline__ Unit make_unit(const SliceParams& p, int bid) {
   u.nkb = u.has_a ? ceil_div(p.H, kBlockK) : 0;
   u.nkb_d = 2 * su;
   u.kstart = u.has_a ? 2 * u.s : 0;
-  u.j0 = p.n_mt * w / workers;
-  u.nj = p.n_mt * (w + 1) / workers - u.j0;
+  const int items = p.n_mt * p.parts;
+  u.i0 = items * w / workers;
+  u.ni = items * (w + 1) / workers - u.i0;
   return u;
 }
 
@@ -281,16 +285,52 @@ __device__ __forceinline__ DownGeom down_geom(const SliceParams& p, const Unit& 
   g.hbytes = static_cast<uint32_t>(2 * n16 * 128);
   const int by_tmem = static_cast<int>(kSliceTmemCols) / (2 * n16);
   const int by_smem = (p.stage_space / 3 - static_cast<int>(g.hbytes)) / kTileBytesA;
-  g.cj = max(1, min(u.nj, min(by_tmem, by_smem)));
+  g.cj = p.parts == 1 ? max(1, min(u.ni, min(by_tmem, by_smem))) : 1;
   g.stage = static_cast<uint32_t>(g.cj) * kTileBytesA + g.hbytes;
   g.S = min(8, p.stage_space / static_cast<int>(g.stage));
   return g;
 }
 
-// k-block q of a down pass, in the order the unit takes them: its own slice first
-__device__ __forceinline__ int down_kb(const Unit& u, int q) {
-  const int kb = u.kstart + q;
-  return kb < u.nkb_d ? kb : kb - u.nkb_d;
+// One pass of the down GEMM over a range of k-blocks for cj output tiles
+// together (one TMEM accumulator each).  With one part per tile a pass is a
+// chunk of whole tiles over every k-block, a unit's own slice first; with
+// several parts a pass is one item: a tile over its part's k-blocks.
+struct Pass {
+  int j0, cj;    // output tiles [j0, j0 + cj)
+  int ka, kn;    // k-blocks [ka, ka + kn)
+  int rot;       // taken from ka + rot on, wrapping
+  int part;
+};
+
+__device__ __forceinline__ int n_passes(const SliceParams& p, const Unit& u, const DownGeom& g) {
+  return p.parts == 1 ? ceil_div(u.ni, g.cj) : u.ni;
+}
+
+__device__ __forceinline__ Pass down_pass(const SliceParams& p, const Unit& u, const DownGeom& g, int pi) {
+  Pass ps;
+  if (p.parts == 1) {
+    ps.j0 = u.i0 + pi * g.cj;
+    ps.cj = min(g.cj, u.ni - pi * g.cj);
+    ps.ka = 0;
+    ps.kn = u.nkb_d;
+    ps.rot = u.kstart;
+    ps.part = 0;
+  } else {
+    const int it = u.i0 + pi;
+    ps.j0 = it / p.parts;
+    ps.cj = 1;
+    ps.part = it - ps.j0 * p.parts;
+    ps.ka = u.nkb_d * ps.part / p.parts;
+    ps.kn = u.nkb_d * (ps.part + 1) / p.parts - ps.ka;
+    ps.rot = 0;
+  }
+  return ps;
+}
+
+// k-block q of a pass
+__device__ __forceinline__ int pass_kb(const Pass& ps, int q) {
+  const int k = q + ps.rot;
+  return ps.ka + (k < ps.kn ? k : k - ps.kn);
 }
 
 __device__ void unit_produce(const SliceParams& p, const SliceSmem& sm, const Unit& u, const CUtensorMap* tm_gu,
@@ -322,7 +362,7 @@ __device__ void unit_produce(const SliceParams& p, const SliceSmem& sm, const Un
   }
   if (!mbar_wait(sm.routed, 0, sm.abort_flag)) return;
   const int n = *sm.n_e;
-  if (n == 0 || u.nj == 0) return;
+  if (n == 0 || u.ni == 0) return;
   // The down ring reuses the gate_up ring's memory once the MMAs have read
   // every gate_up stage.
   for (int i = 0; i < sm.S; ++i) {
@@ -336,19 +376,20 @@ __device__ void unit_produce(const SliceParams& p, const SliceSmem& sm, const Un
   const CUtensorMap* dn = u.shared ? tm_dn_sh : tm_dn;
   const int zd = u.shared ? 0 : u.e;
   Ring rb;
-  for (int jc = 0; jc < u.nj; jc += g.cj) {
-    const int cj = min(g.cj, u.nj - jc);
-    for (int q = 0; q < u.nkb_d; ++q) {
-      const int kbd = down_kb(u, q);
+  const int np = n_passes(p, u, g);
+  for (int pi = 0; pi < np; ++pi) {
+    const Pass ps = down_pass(p, u, g, pi);
+    for (int q = 0; q < ps.kn; ++q) {
+      const int kbd = pass_kb(ps, q);
       if (!mbar_wait(&sm.emptyB[rb.stage], rb.phase ^ 1u, sm.abort_flag)) {
         record_failure(p.status, sm.abort_flag, kInfoEmpty);
         return;
       }
       uint8_t* st = sm.base + rb.stage * g.stage;
       uint64_t* bar = &sm.fullB[rb.stage];
-      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(cj) * kTileBytesA);
-      for (int jj = 0; jj < cj; ++jj)
-        tma_load_3d(st + jj * kTileBytesA, dn, bar, kbd * kBlockK, (u.j0 + jc + jj) * kHalfRows, zd);
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(ps.cj) * kTileBytesA);
+      for (int jj = 0; jj < ps.cj; ++jj)
+        tma_load_3d(st + jj * kTileBytesA, dn, bar, kbd * kBlockK, (ps.j0 + jj) * kHalfRows, zd);
       rb.next(g.S);
     }
   }
@@ -388,27 +429,34 @@ __device__ void unit_mma(const SliceParams& p, const SliceSmem& sm, const Unit& 
     ring.next(sm.S);
   }
   mma_commit(sm.acca);
-  if (ok && mbar_wait(sm.routed, 0, sm.abort_flag) && *sm.n_e > 0 && u.nj > 0) {
+  if (ok && mbar_wait(sm.routed, 0, sm.abort_flag) && *sm.n_e > 0 && u.ni > 0) {
     const int n = *sm.n_e;
     const int n16 = (n + 15) & ~15;
     const DownGeom g = down_geom(p, u, n);
     const uint32_t idesc_b = idesc_bf16(kHalfRows, 2 * n16);
     Ring rb;
-    int chunk = 0;
-    for (int jc = 0; jc < u.nj && ok; jc += g.cj, ++chunk) {
-      const int cj = min(g.cj, u.nj - jc);
+    const int np = n_passes(p, u, g);
+    for (int pi = 0; pi < np && ok; ++pi) {
+      const Pass ps = down_pass(p, u, g, pi);
+      const int cj = ps.cj;
       // The TMEM accumulators are free once the epilogue drained the last
-      // chunk.  The first chunk needs no wait: its first stage holds the
-      // unit's own h, fetched only after the epilogue has read the gate_up
-      // accumulators it overwrites.
-      if (chunk > 0) {
-        if (!mbar_wait(sm.acce, static_cast<uint32_t>(chunk - 1) & 1u, sm.abort_flag)) {
+      // pass; a unit's first pass waits until its epilogue has read the
+      // gate_up accumulators (helpers have none).
+      if (pi > 0) {
+        if (!mbar_wait(sm.acce, static_cast<uint32_t>(pi - 1) & 1u, sm.abort_flag)) {
           record_failure(p.status, sm.abort_flag, kInfoAccEmpty);
           break;
         }
         tc_fence_after();
+      } else if (u.has_a) {
+        // the down accumulators overwrite the gate_up ones: after the epilogue read them
+        if (!mbar_wait(sm.hread, 0, sm.abort_flag)) {
+          record_failure(p.status, sm.abort_flag, kInfoHReady);
+          break;
+        }
+        tc_fence_after();
       }
-      for (int q = 0; q < u.nkb_d; ++q) {
+      for (int q = 0; q < ps.kn; ++q) {
         if (!mbar_wait(&sm.fullB[rb.stage], rb.phase, sm.abort_flag)) {
           record_failure(p.status, sm.abort_flag, kInfoFull);
           ok = false;
@@ -440,6 +488,13 @@ __device__ __forceinline__ void publish_tiles(const SliceSmem& sm, int j0, int j
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
   for (int j = j0; j < j1; ++j)
     asm volatile("red.relaxed.gpu.global.add.s32 [%0], 1;" ::"l"(sm.ss + kSliceSyncWords + j) : "memory");
+}
+
+// Each of the CTA's down items counts once for its tile.
+__device__ __forceinline__ void publish_items(const SliceParams& p, const SliceSmem& sm, const Unit& u) {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  for (int i = u.i0; i < u.i0 + u.ni; ++i)
+    asm volatile("red.relaxed.gpu.global.add.s32 [%0], 1;" ::"l"(sm.ss + kSliceSyncWords + i / p.parts) : "memory");
 }
 
 // Warp 2: the unit's token list once the router CTAs have finished; then
@@ -492,9 +547,9 @@ __device__ void unit_tokens(const SliceParams& p, const SliceSmem& sm, const Uni
     mbar_arrive(sm.routed);
   }
   if (lane != 0) return;
-  if (n == 0 || u.nj == 0) {
+  if (n == 0 || u.ni == 0) {
     // nothing to add to this unit's output tiles
-    if (!p.direct_y && !*sm.abort_flag) publish_tiles(sm, u.j0, u.j0 + u.nj);
+    if (!p.direct_y && !*sm.abort_flag) publish_items(p, sm, u);
     return;
   }
   // The down ring aliases the gate_up ring: a unit's h fetches must wait
@@ -506,19 +561,20 @@ __device__ void unit_tokens(const SliceParams& p, const SliceSmem& sm, const Uni
   }
   const DownGeom g = down_geom(p, u, n);
   Ring rb;
-  int chunk = 0;
-  for (int jc = 0; jc < u.nj; jc += g.cj, ++chunk) {
-    const int cj = min(g.cj, u.nj - jc);
+  const int np = n_passes(p, u, g);
+  for (int pi = 0; pi < np; ++pi) {
+    const Pass ps = down_pass(p, u, g, pi);
+    const int cj = ps.cj;
     int seen = -1;  // last slice found ready
     int q = 0;
-    if (chunk == 0 && u.has_a) {
+    if (pi == 0 && u.has_a && p.parts == 1) {
       // the epilogue fills the first two stages with the unit's own slice
       rb.next(g.S);
       rb.next(g.S);
       q = 2;
     }
-    for (; q < u.nkb_d; ++q) {
-      const int kbd = down_kb(u, q);
+    for (; q < ps.kn; ++q) {
+      const int kbd = pass_kb(ps, q);
       const int sl = kbd >> 1;
       if (sl != seen) {
         if (!wait_count(sm.ready + u.es * p.s_max + sl, 1, p.status)) {
@@ -540,8 +596,8 @@ __device__ void unit_tokens(const SliceParams& p, const SliceSmem& sm, const Uni
       rb.next(g.S);
     }
     if (!p.direct_y) {
-      // the chunk's outputs are stored once every epilogue thread has counted it
-      const uint32_t target = 128u * static_cast<uint32_t>(chunk + 1);
+      // the pass's outputs are stored once every epilogue thread has counted it
+      const uint32_t target = 128u * static_cast<uint32_t>(pi + 1);
       const long long t0 = clock64();
       while (true) {
         uint32_t v;
@@ -553,7 +609,7 @@ __device__ void unit_tokens(const SliceParams& p, const SliceSmem& sm, const Uni
           return;
         }
       }
-      publish_tiles(sm, u.j0 + jc, u.j0 + jc + cj);
+      publish_tiles(sm, ps.j0, ps.j0 + cj);
     }
   }
 }
@@ -581,13 +637,13 @@ __device__ void unit_epilogue(const SliceParams& p, const SliceSmem& sm, const U
   // the first two stages of the down ring, whose h parts this epilogue
   // fills directly (the gate_up stages are all read by now), besides the
   // global copy the expert's other units fetch.
-  const bool local = u.nj > 0;
+  const bool local = u.ni > 0 && p.parts == 1;
   {
     const float lim = p.swiglu_limit;
     const int k2 = r >> 6, kin = r & 63;
     uint8_t* th = h_tile(p, u.es, 2 * u.s + k2);
     uint8_t* tl = th + n16 * 128;
-    uint8_t* sh = sm.base + k2 * g.stage + min(g.cj, u.nj) * kTileBytesA;
+    uint8_t* sh = sm.base + k2 * g.stage + min(g.cj, u.ni) * kTileBytesA;
     for (int c0 = 0; c0 < n; c0 += 8) {
       uint32_t g[8], v[8];
 #pragma unroll
@@ -631,6 +687,7 @@ __device__ void unit_epilogue(const SliceParams& p, const SliceSmem& sm, const U
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   epi_sync();
   if (leader) {
+    mbar_arrive(sm.hread);
     if (local) {
       mbar_arrive(&sm.fullB[0]);
       mbar_arrive(&sm.fullB[1]);
@@ -638,17 +695,21 @@ __device__ void unit_epilogue(const SliceParams& p, const SliceSmem& sm, const U
     red_release_add(sm.ready + u.es * p.s_max + u.s, 1);
   }
   }  // has_a
-  if (u.nj == 0) return;
-  int chunk = 0;
-  for (int jc = 0; jc < u.nj; jc += g.cj, ++chunk) {
-    const int cj = min(g.cj, u.nj - jc);
-    if (epi_any(!mbar_wait(sm.accf, static_cast<uint32_t>(chunk) & 1u, sm.abort_flag))) {
+  if (u.ni == 0) return;
+  // a part's fp32 partials go to its own plane of the pair outputs
+  float* out = p.out;
+  const int np = n_passes(p, u, g);
+  for (int pi = 0; pi < np; ++pi) {
+    const Pass ps = down_pass(p, u, g, pi);
+    const int cj = ps.cj;
+    if (p.parts > 1) out = p.out + static_cast<size_t>(ps.part) * (p.TK + p.T) * p.H;
+    if (epi_any(!mbar_wait(sm.accf, static_cast<uint32_t>(pi) & 1u, sm.abort_flag))) {
       if (leader) record_failure(p.status, sm.abort_flag, kInfoAccFull);
       return;
     }
     tc_fence_after();
     for (int jj = 0; jj < cj; ++jj) {
-      const int row = (u.j0 + jc + jj) * kHalfRows + r;
+      const int row = (ps.j0 + jj) * kHalfRows + r;
       const uint32_t d = tmem + lanes + static_cast<uint32_t>(jj * 2 * n16);
       for (int c0 = 0; c0 < n16; c0 += 16) {
         uint32_t vh[16], vl[16];
@@ -664,7 +725,7 @@ __device__ void unit_epilogue(const SliceParams& p, const SliceSmem& sm, const U
               if (p.direct_y)
                 p.y[static_cast<size_t>(sm.c_tok[c]) * p.H + row] = f2bf(v);
               else
-                __stcg(p.out + static_cast<size_t>(sm.c_slot[c]) * p.H + row, v);
+                __stcg(out + static_cast<size_t>(sm.c_slot[c]) * p.H + row, v);
             }
           }
         }
@@ -679,13 +740,13 @@ __device__ void unit_epilogue(const SliceParams& p, const SliceSmem& sm, const U
 
 // ---------------------------------------------------------------- combine
 // Task (m, g): y[t, m*128 : m*128+128] for the 7 tokens of group g, once
-// every expert (and the shared expert) has finished tile m.  Warp w sums
-// token g*7+w in slot order; lane l four rows.
+// every expert (and the shared expert) has finished every part of tile m.
+// Warp w sums token g*7+w in (slot, part) order; lane l four rows.
 __device__ void combine_tasks(const SliceParams& p, const SliceSmem& sm) {
   if (p.direct_y) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tasks = p.n_mt * p.n_tg;
-  const int target = p.E + (p.s_sh > 0 ? 1 : 0);
+  const int target = (p.E + (p.s_sh > 0 ? 1 : 0)) * p.parts;
   int32_t* tile_cnt = sm.ss + kSliceSyncWords;
   while (true) {
     if (threadIdx.x == 0) {
@@ -708,8 +769,11 @@ __device__ void combine_tasks(const SliceParams& p, const SliceSmem& sm) {
       const int nslot = p.K + (p.s_sh > 0 ? 1 : 0);
       for (int k = 0; k < nslot; ++k) {
         const int slot = k < p.K ? t * p.K + k : p.TK + t;
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.out + static_cast<size_t>(slot) * p.H + row));
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        for (int part = 0; part < p.parts; ++part) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(
+              p.out + (static_cast<size_t>(part) * (p.TK + p.T) + slot) * p.H + row));
+          acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
       }
       uint2 o;
       o.x = static_cast<uint32_t>(f2bf(acc.x)) | (static_cast<uint32_t>(f2bf(acc.y)) << 16);
@@ -753,6 +817,7 @@ __global__ void __launch_bounds__(kSliceThreads, 1)
     mbar_init(sm.acce, 128);
     mbar_init(sm.routed, 1);
     mbar_init(sm.drain, 1);
+    mbar_init(sm.hread, 1);
     *sm.abort_flag = 0;
     *sm.kb_stop = u.nkb;
     *sm.n_e = 0;
@@ -760,7 +825,7 @@ __global__ void __launch_bounds__(kSliceThreads, 1)
     fence_barrier_init();
     fence_proxy_async();
   }
-  const bool works = is_unit || u.nj > 0;
+  const bool works = is_unit || u.ni > 0;
   if (works && warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_gu);
     tma_prefetch_desc(&tm_dn);

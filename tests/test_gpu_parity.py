@@ -342,7 +342,7 @@ def _check_graph_replay(cfg):
 FULL = [("qwen3_8b_dspark", 72, None), ("qwen3_8b_dspark", 72, "stream_k"), ("qwen38_27b_dspark", 72, None),
         ("dsv3_style", 72, None), ("dsv4_style", 9, None), ("dsv4_style", 72, None), ("dsv4_style", 576, None),
         ("dsv4_style", 4096, None), ("dsv4_flash_drafter", 72, None), ("dsv41_dspark_draft", 72, None),
-        ("dense_draft", 72, None), ("dense_draft", 72, "slice")]
+        ("dense_draft", 72, None), ("dense_draft", 72, "stream_k")]
 
 
 def test_automatic_schedule_choice():
@@ -354,8 +354,10 @@ def test_automatic_schedule_choice():
         assert _schedule_of(S.CONFIGS[name]) == sched, name
     assert _schedule_of(S.CONFIGS["qwen3_8b_dspark"].with_(T=129)) == ops.SCHEDULE_STREAM_K
     assert _schedule_of(S.CONFIGS["qwen3_8b_dspark"].with_(T=9)) == ops.SCHEDULE_STREAM_K  # 8*(7/8)^9 > 0.25
-    # one expert: 32 down tiles cannot occupy every SM in the fused schedule
-    assert _schedule_of(S.CONFIGS["dense_draft"]) == ops.SCHEDULE_STREAM_K
+    # one expert: its 32 down tiles are cut into k-block ranges to occupy the SMs
+    assert _schedule_of(S.CONFIGS["dense_draft"]) == ops.SCHEDULE_SLICE
+    # tiny: 8 one-tile experts cannot occupy the SMs
+    assert _schedule_of(S.CONFIGS["tiny"]) == ops.SCHEDULE_STREAM_K
 
 
 @pytest.mark.parametrize("name,T,sched", FULL)
