@@ -24,11 +24,15 @@ drafters, which these shapes and distributions stand in for):
 x ~ N(0, 1); every weight ~ N(0, 0.02); all bf16.  Router bias ~ N(0, 0.1) and
 expert bias ~ N(0, 0.05) in fp32.  Tensors are drawn in the fixed order x,
 gate, router_bias, expert_bias, w_gate_up, w_down, sh_gate_up, sh_down,
-sh_gate from one torch.Generator seeded with the workload's seed.
+sh_gate from one torch.Generator seeded with the workload's seed.  Layers
+with FP4 routed experts draw uniform code bytes and e8m0 scale bytes uniform
+on three values around the one that gives the weights an RMS near w_std,
+in place of the bf16 expert weights.
 """
 from __future__ import annotations
 
 import dataclasses
+import math
 from dataclasses import dataclass
 from typing import Dict, Optional
 
@@ -61,12 +65,16 @@ class LayerConfig:
     seed: int = 0
     x_std: float = 1.0
     w_std: float = 0.02
+    expert_format: str = "bf16"  # routed experts: "bf16" or "fp4" (e2m1 codes + e8m0 scales)
 
     def with_(self, **kw) -> "LayerConfig":
         return dataclasses.replace(self, **kw)
 
     @property
     def weight_bytes(self) -> int:
+        """Bytes of all routed experts' weights."""
+        if self.expert_format == "fp4":
+            return 3 * self.E * self.H * self.I // 2 + 3 * self.E * self.H * self.I // 32
         return 3 * self.E * self.H * self.I * 2
 
 
@@ -119,10 +127,25 @@ def _normal_rows(gen, n_outer: int, inner_shape, std: float, device) -> torch.Te
     return out
 
 
+def _bytes(gen, shape, lo: int, hi: int, device) -> torch.Tensor:
+    """uint8 tensor uniform on [lo, hi)."""
+    return torch.randint(lo, hi, shape, generator=gen, device=device, dtype=torch.uint8)
+
+
+def _fp4_scale_center(w_std: float) -> int:
+    """e8m0 byte around which FP4 block scales are drawn so that weights of
+    uniformly drawn codes have about the RMS w_std (the sixteen e2m1 values
+    have an RMS of about 2.93)."""
+    return 127 + int(round(math.log2(w_std / 2.93)))
+
+
 def make_inputs(cfg: LayerConfig, device="cpu", seed: Optional[int] = None) -> Dict[str, torch.Tensor]:
     """Draw one layer's inputs and weights.  Keys: x, gate, router_bias,
     expert_bias, w_gate_up [E,2I,H], w_down [E,H,I], sh_gate_up [2Is,H],
-    sh_down [H,Is], sh_gate [H] (absent entries are None)."""
+    sh_down [H,Is], sh_gate [H] (absent entries are None).  With FP4 routed
+    experts, w_gate_up / w_down are None and w_gate_up_q [E,2I,H/2],
+    w_gate_up_s [E,2I,H/32], w_down_q [E,H,I/2], w_down_s [E,H,I/32] (uint8
+    codes and e8m0 scales) take their place in the draw order."""
     device = torch.device(device)
     gen = torch.Generator(device=device)
     gen.manual_seed(cfg.seed if seed is None else seed)
@@ -134,8 +157,16 @@ def make_inputs(cfg: LayerConfig, device="cpu", seed: Optional[int] = None) -> D
                         if cfg.router_bias_std > 0 else None)
     d["expert_bias"] = (_normal(gen, (cfg.E,), cfg.expert_bias_std, torch.float32, device)
                         if cfg.expert_bias_std > 0 else None)
-    d["w_gate_up"] = _normal_rows(gen, cfg.E, (2 * cfg.I, cfg.H), cfg.w_std, device)
-    d["w_down"] = _normal_rows(gen, cfg.E, (cfg.H, cfg.I), cfg.w_std, device)
+    if cfg.expert_format == "fp4":
+        c = _fp4_scale_center(cfg.w_std)
+        d["w_gate_up_q"] = _bytes(gen, (cfg.E, 2 * cfg.I, cfg.H // 2), 0, 256, device)
+        d["w_gate_up_s"] = _bytes(gen, (cfg.E, 2 * cfg.I, cfg.H // 32), c - 1, c + 2, device)
+        d["w_down_q"] = _bytes(gen, (cfg.E, cfg.H, cfg.I // 2), 0, 256, device)
+        d["w_down_s"] = _bytes(gen, (cfg.E, cfg.H, cfg.I // 32), c - 1, c + 2, device)
+        d["w_gate_up"] = d["w_down"] = None
+    else:
+        d["w_gate_up"] = _normal_rows(gen, cfg.E, (2 * cfg.I, cfg.H), cfg.w_std, device)
+        d["w_down"] = _normal_rows(gen, cfg.E, (cfg.H, cfg.I), cfg.w_std, device)
     if cfg.shared_I > 0:
         d["sh_gate_up"] = _normal(gen, (2 * cfg.shared_I, cfg.H), cfg.w_std, bf, device)
         d["sh_down"] = _normal(gen, (cfg.H, cfg.shared_I), cfg.w_std, bf, device)

@@ -29,7 +29,11 @@ Sources (web pages, cited by title and section):
   commit notes on the expert bias (shifts the picks, never the weights), on
   select receiving the shifted scores, on the DeepSeek-V4 family (sqrt(softplus)
   scores, always renormalised, route_scale, clamped SwiGLU, one ungated shared
-  expert) and on the fused gate_up_proj / down_proj expert layout.
+  expert), on the fused gate_up_proj / down_proj expert layout and on the
+  export formats of the official checkpoint (FP4 routed experts).
+* [P5] MoE-Infinity PR #143 "converge DFlash spec-decode stack" -- commit note
+  on the resident GPT-OSS loader (MXFP4 codes and scales, uint8,
+  output-major).
 
 Readings of points the pages leave open (each also listed in the design doc):
 
@@ -341,3 +345,54 @@ def moe_layer(x, gate, w_gate_up, w_down, recipe: Recipe, router_bias=None,
     return dict(logits=logits, scores=s, choice=c, idx=idx, weights=w,
                 counts=counts, offsets=offsets, sorted_pair=sorted_pair,
                 pair_pos=pair_pos, y=y)
+
+
+# --------------------------------------------------------------------------
+# FP4 routed experts ([P4] commit note on the DeepSeek-V4.1 export formats:
+# two e2m1 codes per byte along the input dimension, the low nibble first,
+# one e8m0 scale per 32 inputs; [P5] MXFP4 commit note: uint8 codes
+# [E, N, K//2] and scales [E, N, K//32], output-major).  The layer computes
+# with the exactly dequantized weights ([P4]: import dequantizes to bf16).
+# --------------------------------------------------------------------------
+
+def e2m1_value(code: int) -> float:
+    """Value of one 4-bit e2m1 code: bit 3 the sign, bits 2..1 a 2-bit
+    exponent with bias 1, bit 0 a 1-bit mantissa; exponent 0 is the subnormal
+    range (0 or 0.5).  The element format of the OCP microscaling formats."""
+    sign = -1.0 if (code >> 3) & 1 else 1.0
+    e = (code >> 1) & 3
+    m = code & 1
+    if e == 0:
+        return sign * 0.5 * m
+    return sign * 2.0 ** (e - 1) * (1.0 + 0.5 * m)
+
+
+def e8m0_value(s: int) -> float:
+    """Value of one e8m0 scale byte: 2^(s - 127); 255 encodes NaN."""
+    return float("nan") if s == 255 else 2.0 ** (int(s) - 127)
+
+
+E2M1_TABLE = np.array([e2m1_value(c) for c in range(16)])
+E8M0_TABLE = np.array([e8m0_value(s) for s in range(256)])
+
+
+def dequant_fp4(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Exact float64 weights [..., N, K] from codes [..., N, K/2] (uint8, two
+    codes per byte along K, the low nibble holding the even index) and scales
+    [..., N, K/32] (uint8 e8m0, one per 32 consecutive inputs)."""
+    codes = np.asarray(codes, np.uint8)
+    scales = np.asarray(scales, np.uint8)
+    k = codes.shape[-1] * 2
+    assert scales.shape[-1] * 32 == k and scales.shape[:-1] == codes.shape[:-1]
+    vals = np.empty(codes.shape[:-1] + (k,))
+    vals[..., 0::2] = E2M1_TABLE[codes & 0xF]
+    vals[..., 1::2] = E2M1_TABLE[codes >> 4]
+    return vals * np.repeat(E8M0_TABLE[scales], 32, axis=-1)
+
+
+def moe_layer_fp4(x, gate, gu_codes, gu_scales, dn_codes, dn_scales, recipe: Recipe, **kw):
+    """The layer with FP4 routed experts: gate_up [E,2I,H/2] codes with
+    [E,2I,H/32] scales, down [E,H,I/2] codes with [E,H,I/32] scales; every
+    other tensor as in moe_layer()."""
+    return moe_layer(x, gate, dequant_fp4(gu_codes, gu_scales), dequant_fp4(dn_codes, dn_scales),
+                     recipe, **kw)

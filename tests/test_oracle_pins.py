@@ -356,3 +356,90 @@ def test_empty_input_routes_empty():
                       O.Recipe(4, 2))
     assert out["idx"].shape == (0, 2) and out["y"].shape == (0, 8)
     assert out["counts"].tolist() == [0, 0, 0, 0]
+
+
+# ---------------------------------------------------------------- FP4 routed experts
+# Format of the DeepSeek-V4.1 export (SpecForge PR #1073, commit note on the
+# official checkpoint's formats) and the MXFP4 layout of MoE-Infinity PR #143
+# (codes [E,N,K//2], scales [E,N,K//32], output-major).
+
+# The sixteen e2m1 values as the OCP microscaling specification lists them
+# (codes 0..7 positive, 8..15 their negatives), typed here, not computed.
+E2M1_LISTED = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+               -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def test_e2m1_code_table():
+    assert list(O.E2M1_TABLE) == E2M1_LISTED
+    assert math.copysign(1.0, O.E2M1_TABLE[8]) == -1.0  # negative zero
+
+
+def test_e8m0_matches_library_decoder():
+    torch = pytest.importorskip("torch")
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.E8M0_TABLE[:255], lib[:255])
+    assert math.isnan(O.E8M0_TABLE[255]) and math.isnan(lib[255])
+    assert O.E8M0_TABLE[127] == 1.0 and O.E8M0_TABLE[0] == 2.0 ** -127
+
+
+def test_fp4_nibble_order_and_scale_blocks():
+    # one row of K = 64: byte j holds inputs 2j (low nibble) and 2j+1 (high)
+    codes = np.zeros((1, 32), np.uint8)
+    codes[0, 0] = 0x21          # input 0 -> code 1 (0.5), input 1 -> code 2 (1.0)
+    codes[0, 16] = 0xF7         # input 32 -> code 7 (6.0), input 33 -> code 15 (-6.0)
+    scales = np.array([[127, 129]], np.uint8)  # inputs [0,32) x 1, [32,64) x 4
+    w = O.dequant_fp4(codes, scales)
+    assert w.shape == (1, 64)
+    expect = np.zeros(64)
+    expect[0], expect[1] = 0.5, 1.0
+    expect[32], expect[33] = 24.0, -24.0
+    np.testing.assert_array_equal(w[0], expect)
+
+
+def test_fp4_round_trip_brute_force():
+    # an independent encoder: every weight of the form v * 2^k with v in the
+    # listed table is encoded by searching the table; dequantizing gives it back
+    rng = np.random.default_rng(5)
+    n, k = 3, 96
+    vals = rng.choice(np.array(E2M1_LISTED[:8] + E2M1_LISTED[9:]), size=(n, k))
+    sc = rng.integers(100, 150, size=(n, k // 32)).astype(np.uint8)
+    w = vals * np.repeat(2.0 ** (sc.astype(np.int64) - 127), 32, axis=1)
+    codes = np.zeros((n, k // 2), np.uint8)
+    for r in range(n):
+        for j in range(k):
+            c = E2M1_LISTED.index(vals[r, j]) if vals[r, j] != 0 else 0
+            codes[r, j // 2] |= np.uint8(c << (4 * (j % 2)))
+    np.testing.assert_array_equal(O.dequant_fp4(codes, sc), w)
+
+
+def test_fp4_layer_equals_layer_on_decoded_weights():
+    # the FP4 layer is the bf16-formula layer on the decoded weights; the
+    # decoding here goes byte by byte through the listed table
+    rng = np.random.default_rng(6)
+    T, H, E, I, K = 5, 64, 4, 64, 2
+    x = rng.standard_normal((T, H))
+    gate = rng.standard_normal((E, H)) * 0.1
+    gq = rng.integers(0, 256, size=(E, 2 * I, H // 2)).astype(np.uint8)
+    gs = rng.integers(118, 122, size=(E, 2 * I, H // 32)).astype(np.uint8)
+    dq = rng.integers(0, 256, size=(E, H, I // 2)).astype(np.uint8)
+    ds = rng.integers(118, 122, size=(E, H, I // 32)).astype(np.uint8)
+
+    def decode(q, s):
+        out = np.zeros(q.shape[:-1] + (q.shape[-1] * 2,))
+        for ix in np.ndindex(q.shape):
+            b = int(q[ix])
+            j = ix[-1]
+            sc = 2.0 ** (int(s[ix[:-1] + (2 * j // 32,)]) - 127)
+            out[ix[:-1] + (2 * j,)] = E2M1_LISTED[b & 15] * sc
+            out[ix[:-1] + (2 * j + 1,)] = E2M1_LISTED[b >> 4] * sc
+        return out
+
+    rec = O.Recipe(num_experts=E, top_k=K, score_fn=O.SCORE_SQRTSOFTPLUS, route_scale=1.5, swiglu_limit=10.0)
+    a = O.moe_layer_fp4(x, gate, gq, gs, dq, ds, rec)
+    b = O.moe_layer(x, gate, decode(gq, gs), decode(dq, ds), rec)
+    np.testing.assert_array_equal(a["idx"], b["idx"])
+    np.testing.assert_array_equal(a["y"], b["y"])
+    # and a swapped nibble order would change the result
+    swapped = ((gq & 15) << 4) | (gq >> 4)
+    c = O.moe_layer_fp4(x, gate, swapped.astype(np.uint8), gs, dq, ds, rec)
+    assert np.abs(c["y"] - a["y"]).max() > 1e-3
