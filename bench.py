@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--experts", type=int, default=None, help="override E (small profiling cases)")
     ap.add_argument("--schedule", default="auto", choices=["auto", "stream_k", "slice"],
                     help="expert schedule (auto: the library's choice for the shape)")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "fp4"],
+                    help="routed experts' format: bf16, or FP4 (e2m1 codes + e8m0 scale per 32 inputs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -142,8 +144,10 @@ def algorithmic(cfg, counts_u: int):
     """Bytes and FLOPs of one layer forward and of its expert-GEMM launch,
     counting only the touched experts' weights (each read once)."""
     T, H, I, E, K, Is = cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.shared_I
-    gu_w = counts_u * 2 * I * H * 2 + 2 * Is * H * 2
-    dn_w = counts_u * H * I * 2 + H * Is * 2
+    # routed weights: bf16, or FP4 codes (half a byte) plus one scale byte per 32
+    wb = (0.5 + 1 / 32) if cfg.expert_format == "fp4" else 2
+    gu_w = int(counts_u * 2 * I * H * wb) + 2 * Is * H * 2
+    dn_w = int(counts_u * H * I * wb) + H * Is * 2
     act = T * H * 2 * 2  # x read, y written
     gate = E * H * 2 + (H * 2 if cfg.shared_gated else 0)
     biases = E * 4 * ((cfg.router_bias_std > 0) + (cfg.expert_bias_std > 0))
@@ -201,10 +205,15 @@ def cpu_oracle_pass(cfg, host, w64, tokens):
 
 
 def cpu_prepare(cfg):
+    import oracle as O
     host = S.make_inputs(cfg, device="cpu")
     w64 = {}
     for e in range(cfg.E):
-        w64[e] = (host["w_gate_up"][e].double().numpy(), host["w_down"][e].double().numpy())
+        if cfg.expert_format == "fp4":
+            w64[e] = (O.dequant_fp4(host["w_gate_up_q"][e].numpy(), host["w_gate_up_s"][e].numpy()),
+                      O.dequant_fp4(host["w_down_q"][e].numpy(), host["w_down_s"][e].numpy()))
+        else:
+            w64[e] = (host["w_gate_up"][e].double().numpy(), host["w_down"][e].double().numpy())
     if host["sh_gate_up"] is not None:
         w64["sh_gate_up"] = host["sh_gate_up"].double().numpy()
         w64["sh_down"] = host["sh_down"].double().numpy()
@@ -274,33 +283,43 @@ def run_gpu(args, cfg, rank, world):
     K = args.steps if args.steps is not None else 20000
     W = max(3, args.warmup if args.warmup is not None else 50)
     rec = ops.Recipe.from_config(cfg)
+    fp4 = cfg.expert_format == "fp4"
+    if fp4:
+        raise SystemExit("the FP4 expert kernel is disabled in this build (moe_ffn_forward_fp4 refuses)")
     ops.set_schedule({"auto": ops.SCHEDULE_AUTO, "stream_k": ops.SCHEDULE_STREAM_K,
                       "slice": ops.SCHEDULE_SLICE}[args.schedule])
-    sched = ops.SCHEDULE_NAMES[ops.ffn_schedule(cfg.T, cfg.H, cfg.I, cfg.shared_I, rec,
-                                                gated=cfg.shared_gated and cfg.shared_I > 0)]
+    # FP4 routed experts always run the stream-K schedule
+    sched = "stream_k" if fp4 else ops.SCHEDULE_NAMES[ops.ffn_schedule(
+        cfg.T, cfg.H, cfg.I, cfg.shared_I, rec, gated=cfg.shared_gated and cfg.shared_I > 0)]
     base = S.make_inputs(cfg, device=dev, seed=cfg.seed + 1000 * rank)
     n_copies = max(2, -(-4 * L2_BYTES // (cfg.weight_bytes + 1)))
+    wkeys = ["w_gate_up_q", "w_down_q"] if fp4 else ["w_gate_up", "w_down"]
     layers = [base]
     for c in range(1, n_copies):
         dd = dict(base)
-        dd["w_gate_up"] = base["w_gate_up"].clone()
-        dd["w_down"] = base["w_down"].clone()
-        if base["sh_gate_up"] is not None:
-            dd["sh_gate_up"] = base["sh_gate_up"].clone()
-            dd["sh_down"] = base["sh_down"].clone()
+        for k in wkeys + (["sh_gate_up", "sh_down"] if base["sh_gate_up"] is not None else []):
+            dd[k] = base[k].clone()
         layers.append(dd)
+    if fp4:
+        sc = ops.fp4_prepare_scales(base["w_gate_up_s"], base["w_down_s"])
+        for dd in layers:
+            dd["scales"] = sc.clone()
     ws = ops.Workspace(ops.ffn_workspace_bytes(cfg.T, cfg.H, cfg.I, cfg.shared_I, rec), dev)
     x = base["x"]
     y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
     counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
+    def call(dd, xx, yy, cnt=None):
+        kw = dict(router_bias=dd["router_bias"], expert_bias=dd["expert_bias"], sh_gate_up=dd["sh_gate_up"],
+                  sh_down=dd["sh_down"], sh_gate=dd["sh_gate"], y=yy, counts_out=cnt, stream=stream)
+        if fp4:
+            ops.moe_ffn_forward_fp4(xx, dd["gate"], dd["w_gate_up_q"], dd["w_down_q"], dd["scales"], rec, ws, **kw)
+        else:
+            ops.moe_ffn_forward(xx, dd["gate"], dd["w_gate_up"], dd["w_down"], rec, ws, **kw)
+
     def fwd(i, yy=y, cnt=None):
-        dd = layers[i % n_copies]
-        ops.moe_ffn_forward(x, dd["gate"], dd["w_gate_up"], dd["w_down"], rec, ws,
-                            router_bias=dd["router_bias"], expert_bias=dd["expert_bias"],
-                            sh_gate_up=dd["sh_gate_up"], sh_down=dd["sh_down"], sh_gate=dd["sh_gate"], y=yy,
-                            counts_out=cnt, stream=stream)
+        call(layers[i % n_copies], x, yy, cnt)
 
     with torch.cuda.stream(stream):
         fwd(0, cnt=counts)
@@ -376,11 +395,7 @@ def run_gpu(args, cfg, rank, world):
         e0.record(stream)
         for i in range(n_e2e):
             x_dev.copy_(x_host, non_blocking=True)
-            dd = layers[i % n_copies]
-            ops.moe_ffn_forward(x_dev, dd["gate"], dd["w_gate_up"], dd["w_down"], rec, ws,
-                                router_bias=dd["router_bias"], expert_bias=dd["expert_bias"],
-                                sh_gate_up=dd["sh_gate_up"], sh_down=dd["sh_down"], sh_gate=dd["sh_gate"], y=y,
-                                stream=stream)
+            call(layers[i % n_copies], x_dev, y)
             y_host.copy_(y, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize()
@@ -404,18 +419,22 @@ def run_gpu(args, cfg, rank, world):
     achieved = ex_bytes / t_ex / 1e9
     layer_gbs = layer_bytes / (ms_step * 1e-3) / 1e9
     roof_layer_us = max(layer_bytes / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
-    traffic = ncu_traffic(sched, cfg.name if args.tokens is None and args.experts is None else
-                          f"{cfg.name}_T{cfg.T}_E{cfg.E}")
+    wl = cfg.name if args.tokens is None and args.experts is None else f"{cfg.name}_T{cfg.T}_E{cfg.E}"
+    traffic = ncu_traffic(sched, wl + ("_fp4" if fp4 else ""))
 
     if rank != 0:
         return
     line = {
-        "metric": METRIC if cfg.name == "qwen3_8b_dspark" and cfg.T == 72 else f"MoE-FFN layer tokens/s ({cfg.name}, T={cfg.T})",
+        "metric": (METRIC if cfg.name == "qwen3_8b_dspark" and cfg.T == 72 and not fp4 else
+                   f"MoE-FFN layer tokens/s ({cfg.name}{', FP4 experts' if fp4 else ''}, T={cfg.T})"),
         "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms_step,
         "us_per_layer": ms_step * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        # the MMA operand type: FP4 experts are expanded to f16 on chip
+        "dtype": "f16" if fp4 else "bf16", "data": "synthetic",
         "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "I": cfg.I, "K": cfg.K,
                    "shared_I": cfg.shared_I, "touched_experts": u, "schedule": sched,
+                   "routed_experts": "fp4 (e2m1 + e8m0/32)" if fp4 else "bf16",
                    "launch": f"cuda_graph_replay, {G} layer{'s' if G > 1 else ''} per graph",
                    "l2": f"weights rotate over {n_copies} copies ({n_copies * cfg.weight_bytes / 1e9:.2f} GB) > L2",
                    "parallelism": "replicas" if world > 1 else "single_gpu"},
@@ -438,6 +457,8 @@ def run_gpu(args, cfg, rank, world):
 def main():
     args = parse()
     cfg = S.CONFIGS[args.config]
+    if args.weights == "fp4":
+        cfg = cfg.with_(expert_format="fp4")
     if args.tokens is not None:
         cfg = cfg.with_(T=args.tokens)
     if args.experts is not None:

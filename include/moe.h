@@ -67,7 +67,11 @@ typedef enum {
   MOE_ERR_UNSUPPORTED = 2,    /* well-formed but outside the kernels' limits */
   MOE_ERR_WORKSPACE = 3,      /* workspace missing, too small or misaligned  */
   MOE_ERR_CUDA = 4,           /* a CUDA runtime call failed                  */
-  MOE_ERR_DEVICE_TIMEOUT = 5  /* a bounded device-side wait ran out          */
+  MOE_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait ran out          */
+  MOE_ERR_DEVICE_RANGE = 6    /* an input outside the exact range of the FP4
+                                 path (a block scale, or x / h beyond f16);
+                                 recorded on the device, the output is not
+                                 exact                                       */
 } moe_status;
 
 typedef enum {
@@ -232,10 +236,62 @@ MOE_API moe_status moe_set_schedule(int schedule);
  * will be passed. */
 MOE_API int moe_ffn_schedule(int T, int H, int I, int Is, const moe_recipe* recipe, int gated);
 
+/* ---- FP4 routed experts.  The format of DeepSeek-V4.1's official checkpoint
+ * (SpecForge PR #1073, commit note on its export formats): every routed
+ * expert weight is stored as e2m1 codes, two per byte along the input
+ * dimension with the even input in the low nibble, and one e8m0 scale byte
+ * (value 2^(s-127)) per 32 consecutive inputs; the MXFP4 tensors of
+ * MoE-Infinity PR #143 have the same output-major layout:
+ *   w_gate_up_q [E,2I,H/2] uint8   w_gate_up_s [E,2I,H/32] uint8
+ *   w_down_q    [E,H,I/2]  uint8   w_down_s    [E,H,I/32]  uint8
+ * The layer computes with the exactly dequantized weights (code value x
+ * scale), as the bf16 draft those weights import into does.
+ * Limits: H and I multiples of 64 (whole 64-input k-blocks), H <= 65536,
+ * I <= 16384. */
+
+/* Bytes of the prepared block scales of one layer (0 for unsupported
+ * shapes). */
+MOE_API size_t moe_fp4_scales_bytes(int E, int H, int I);
+
+/* Re-lays the two scale tensors into the blocks the expert kernel copies
+ * whole (for every expert, 256-row tile and 64-input k-block, the 128-row
+ * halves' scale pairs: 512 bytes).  Once per set of weights, e.g. at load
+ * time; asynchronous on `stream`.
+ *   scales   device buffer of >= moe_fp4_scales_bytes(E,H,I) bytes, 16-byte
+ *            aligned, owned by the caller and passed to every
+ *            moe_ffn_forward_fp4() with these weights.
+ * Returns MOE_ERR_WORKSPACE when scales_bytes is too small. */
+MOE_API moe_status moe_fp4_prepare_scales(const uint8_t* w_gate_up_s, const uint8_t* w_down_s, int E, int H,
+                                          int I, void* scales, size_t scales_bytes, cudaStream_t stream);
+
+/* moe_ffn_forward() with FP4 routed experts: w_gate_up_q, w_down_q as above
+ * (16-byte aligned), `scales` from moe_fp4_prepare_scales().  Router, shared
+ * expert (bf16), workspace (moe_ffn_workspace_bytes), outputs and errors as in
+ * moe_ffn_forward().  Always the STREAM_K schedule.
+ * Arithmetic: the routed experts' products are exact f16 x f16 -> fp32 on the
+ * tensor cores, so they need every e8m0 scale in [104, 140] (2^-23 .. 2^13,
+ * where code x scale is exact in f16), |x| < 65520 and |h| < 65520 (the SwiGLU
+ * output, carried as an f16 hi + lo pair); anything outside is recorded as
+ * MOE_ERR_DEVICE_RANGE in the workspace status (moe_get_device_status).  x
+ * values below 2^-17 in magnitude round to the f16 grid (error < 2^-25).
+ * STATUS: the FP4 expert kernel is built but not launched: it faulted the GPU
+ * on the full-size DeepSeek-V4.1 draft layer (E=128, H=4096, I=2304, T=72)
+ * while matching the oracle on small layers, and stays disabled until that
+ * cause is found.  Every call with T > 0 returns MOE_ERR_UNSUPPORTED after
+ * the argument checks. */
+MOE_API moe_status moe_ffn_forward_fp4(const moe_bf16* x, int T, int H, int I, const moe_bf16* gate,
+                                       const float* router_bias, const float* expert_bias,
+                                       const uint8_t* w_gate_up_q, const uint8_t* w_down_q, const void* scales,
+                                       size_t scales_bytes, const moe_bf16* sh_gate_up, const moe_bf16* sh_down,
+                                       int Is, const moe_bf16* sh_gate, const moe_recipe* recipe, void* ws,
+                                       size_t ws_bytes, moe_bf16* y, int32_t* topk_idx_out, float* topk_w_out,
+                                       int32_t* counts_out, cudaStream_t stream);
+
 /* Synchronises `stream`, reads the device status word of a workspace used by
  * moe_route() or moe_ffn_forward(), and clears it.  Returns MOE_OK or the
- * first device-side error recorded (MOE_ERR_DEVICE_TIMEOUT); *info_out (if
- * not NULL) receives the kernel-specific detail word. */
+ * first device-side error recorded (MOE_ERR_DEVICE_TIMEOUT, or
+ * MOE_ERR_DEVICE_RANGE from the FP4 path); *info_out (if not NULL) receives
+ * the kernel-specific detail word. */
 MOE_API moe_status moe_get_device_status(void* ws, cudaStream_t stream, int32_t* info_out);
 
 /* Profiling hook: when `events` is not NULL, moe_ffn_forward() records

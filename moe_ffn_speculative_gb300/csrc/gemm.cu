@@ -26,7 +26,18 @@
 // allocates TMEM and issues the MMAs, warp 2 gathers the token rows with
 // cp.async into the 128-byte-swizzled B tile, warps 3..6 drain TMEM in the
 // epilogue (SwiGLU for gate_up; routing weight and store for down).
+//
+// FP4 routed experts (SpecForge PR #1073, commit note on the official
+// checkpoint's formats: two e2m1 codes per byte along the input, low nibble
+// first, one e8m0 scale per 32 inputs): warp 0 streams the packed codes (8 KB
+// per k-block) and the k-block's 512 bytes of block scales into a deeper ring
+// of their own; four more warps (352 threads) expand them with the hardware
+// e2m1 -> f16 conversion, multiply by the scale (exact in f16 for scales in
+// [2^-23, 2^13]) and write the 128-byte-swizzled f16 A tile the MMA reads.
+// Those groups multiply in f16 (x as its f16 copy, h as an f16 hi + lo pair);
+// the bf16 shared expert goes through unchanged.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "moe_internal.cuh"
 
@@ -102,7 +113,7 @@ __device__ __forceinline__ int cta_of(const long long* span, int grid, long long
 // epilogues of one 16-column chunk; a[i], b[i] = half-0 / half-1 accumulator
 // of row r (TMEM lane) and token column j0 + i
 // --------------------------------------------------------------------------
-template <int PHASE>
+template <int PHASE, bool kFp4>
 __device__ __forceinline__ void finish_chunk(const GemmParams& p, const Seg& sg, int r, int j0, const float* a,
                                              const float* b, const float* col_w, const int* col_tok) {
   if (PHASE == 0) {
@@ -113,6 +124,8 @@ __device__ __forceinline__ void finish_chunk(const GemmParams& p, const Seg& sg,
     // bits): row r holds hi in [0, I_ld) and lo in [I_ld, 2*I_ld)
     uint16_t* hp = p.h + static_cast<size_t>(sg.row_base + sg.n * p.n_max) * (2 * p.I_ld) + row;
     const float lim = p.swiglu_limit;
+    const bool half16 = kFp4 && sg.expert >= 0;  // the pair in f16 for the FP4 down GEMM
+    bool over = false;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int j = j0 + i;
@@ -123,12 +136,22 @@ __device__ __forceinline__ void finish_chunk(const GemmParams& p, const Seg& sg,
           u = fminf(fmaxf(u, -lim), lim);
         }
         const float hv = g / (1.f + expf(-g)) * u;
-        const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
-        const float lo = hv - __bfloat162float(hi);
-        hp[static_cast<size_t>(j) * (2 * p.I_ld)] = __bfloat16_as_ushort(hi);
-        hp[static_cast<size_t>(j) * (2 * p.I_ld) + p.I_ld] = f2bf(lo);
+        uint16_t whi, wlo;
+        if (half16) {
+          const __half hi = __float2half_rn(hv);
+          whi = __half_as_ushort(hi);
+          wlo = __half_as_ushort(__float2half_rn(hv - __half2float(hi)));
+          over |= !(fabsf(hv) < 65520.f);
+        } else {
+          const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
+          whi = __bfloat16_as_ushort(hi);
+          wlo = f2bf(hv - __bfloat162float(hi));
+        }
+        hp[static_cast<size_t>(j) * (2 * p.I_ld)] = whi;
+        hp[static_cast<size_t>(j) * (2 * p.I_ld) + p.I_ld] = wlo;
       }
     }
+    if (over) record_range(p.status, kInfoHRange);
   } else {
     // routing weight (or shared-expert gate) times the expert output
     const int row0 = sg.m * 2 * kHalfRows + r;
@@ -176,6 +199,11 @@ struct Smem {
   long long* span;  // [2][grid+1] CTA spans of both GEMMs
   float* col_w;     // [n_max] down epilogue: routing weight of each token column
   int* col_tok;     // [n_max] down epilogue: token of each column
+  // FP4: SP stages of packed codes (8 KB) and of block scales (512 B)
+  uint8_t* pbase;
+  uint8_t* sbase;
+  uint64_t *pfull, *pempty;
+  int SP;
 };
 
 // ---------------------------------------------------------------- TMA producer (weights)
@@ -210,11 +238,13 @@ struct WeightCursor {
   __device__ void step() {
     if (++kk >= sg.len) next_segment();
   }
-  // tensor map and box coordinates of half h of the current k-block
+  // tensor map and box coordinates of half h of the current k-block (FP4
+  // codes: the routed maps are byte tensors, 32 bytes per k-block)
+  template <bool kFp4>
   __device__ const CUtensorMap* box(const CUtensorMap* tm_gu, const CUtensorMap* tm_gu_sh, const CUtensorMap* tm_dn,
                                     const CUtensorMap* tm_dn_sh, int h, int& c0, int& c1, int& c2) const {
     const int plane = sg.expert >= 0 ? sg.expert : 0;
-    c0 = (sg.k0 + kk) * kBlockK;
+    c0 = (sg.k0 + kk) * ((kFp4 && sg.expert >= 0) ? kBlockK / 2 : kBlockK);
     if (ph == 0) {
       c1 = sg.m * kHalfRows;
       c2 = 2 * plane + h;
@@ -227,6 +257,16 @@ struct WeightCursor {
   }
 };
 
+// Byte offset of the prepared block scales of (expert, tile m, k-block kb):
+// 512 bytes each, gate_up blocks of all experts first, then down blocks.
+__device__ __forceinline__ size_t fp4_scale_offset(const GemmParams& p, int phase, int e, int m, int kb) {
+  const int mb0 = ceil_div(p.I, kHalfRows), kb0 = p.H / kBlockK;
+  if (phase == 0) return ((static_cast<size_t>(e) * mb0 + m) * kb0 + kb) * 512;
+  const int mb1 = ceil_div(p.H, 2 * kHalfRows), kb1 = p.I / kBlockK;
+  return static_cast<size_t>(p.E) * mb0 * kb0 * 512 + ((static_cast<size_t>(e) * mb1 + m) * kb1 + kb) * 512;
+}
+
+template <bool kFp4>
 __device__ bool produce(const Smem& sm, const GemmParams& p, int ngroups, const long long (&b)[2],
                         const long long (&e)[2], const int (&g)[2], const CUtensorMap* tm_gu,
                         const CUtensorMap* tm_gu_sh, const CUtensorMap* tm_dn, const CUtensorMap* tm_dn_sh,
@@ -236,7 +276,30 @@ __device__ bool produce(const Smem& sm, const GemmParams& p, int ngroups, const 
   const uint64_t pol = l2_evict_first_policy();
   WeightCursor ld;
   ld.init(p, ngroups, b, e, g);
+  Ring pring;  // FP4 code stages
   while (ld.valid) {
+    if (kFp4 && ld.sg.expert >= 0) {
+      // packed codes and block scales of a routed k-block; the converter
+      // warps turn them into the A stage
+      if (!mbar_wait(&sm.pempty[pring.stage], pring.phase ^ 1u, sm.abort_flag)) {
+        record_failure(status, sm.abort_flag, kInfoEmpty);
+        return false;
+      }
+      uint64_t* bar = &sm.pfull[pring.stage];
+      mbar_arrive_expect_tx(bar, kPackedBytes + 512);
+      int c0, c1, c2;
+      for (int h = 0; h < 2; ++h) {
+        const CUtensorMap* tm = ld.box<kFp4>(tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, h, c0, c1, c2);
+        tma_load_3d_hint(sm.pbase + pring.stage * kPackedBytes + h * (kPackedBytes / 2), tm, bar, c0, c1, c2, pol);
+      }
+      const uint8_t* sc = ld.ph == 0 ? p.gu_scale : p.dn_scale;
+      bulk_load(sm.sbase + pring.stage * 512, sc + fp4_scale_offset(p, ld.ph, ld.sg.expert, ld.sg.m, ld.sg.k0 + ld.kk),
+                512, bar);
+      pring.next(sm.SP);
+      ld.step();
+      ring.next(sm.S);  // the A ring advances for every k-block
+      continue;
+    }
     if (!mbar_wait(&sm.empty[ring.stage], ring.phase ^ 1u, sm.abort_flag)) {
       record_failure(status, sm.abort_flag, kInfoEmpty);
       return false;
@@ -246,7 +309,7 @@ __device__ bool produce(const Smem& sm, const GemmParams& p, int ngroups, const 
     mbar_arrive_expect_tx(bar, 2 * kTileBytesA);
     int c0, c1, c2;
     for (int h = 0; h < 2; ++h) {
-      const CUtensorMap* tm = ld.box(tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, h, c0, c1, c2);
+      const CUtensorMap* tm = ld.box<kFp4>(tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, h, c0, c1, c2);
       tma_load_3d_hint(a0 + h * kTileBytesA, tm, bar, c0, c1, c2, pol);
     }
     ld.step();
@@ -256,7 +319,7 @@ __device__ bool produce(const Smem& sm, const GemmParams& p, int ngroups, const 
 }
 
 // ---------------------------------------------------------------- MMA issuer (one thread)
-template <int PHASE>
+template <int PHASE, bool kFp4>
 __device__ bool issue_mma(const Smem& sm, const GemmParams& p, int ngroups, long long begin, long long end, int g0,
                           uint32_t tmem_base, Ring& ring, int& seg_i, int32_t* status) {
   Sched sc;
@@ -273,7 +336,8 @@ __device__ bool issue_mma(const Smem& sm, const GemmParams& p, int ngroups, long
     const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * 2 * p.n_max);
     const uint32_t d1 = d0 + static_cast<uint32_t>(p.n_max);
     const int nmma = max(16, (sg.n_cnt + 15) & ~15);
-    const uint32_t idesc = idesc_bf16(kHalfRows, nmma);
+    // FP4 routed groups: f16 weights (expanded) and f16 token rows
+    const uint32_t idesc = (kFp4 && sg.expert >= 0) ? idesc_f16(kHalfRows, nmma) : idesc_bf16(kHalfRows, nmma);
     for (int kk = 0; kk < sg.len; ++kk) {
       if (!mbar_wait(&sm.full[ring.stage], ring.phase, sm.abort_flag)) {
         record_failure(status, sm.abort_flag, kInfoFull);
@@ -308,16 +372,16 @@ __device__ bool issue_mma(const Smem& sm, const GemmParams& p, int ngroups, long
 // ---------------------------------------------------------------- token-row gather (B), one warp
 // gate_up: rows of x for the expert's tokens; down: the expert's h rows (hi and
 // lo), after the gate_up tiles that write them have signalled.
-template <int PHASE>
+template <int PHASE, bool kFp4>
 __device__ bool gather(const Smem& sm, const GemmParams& p, int ngroups, long long begin, long long end, int g0,
                        Ring& ring, int& pending, int& arr_stage, int lag, int32_t* status) {
   const int lane = threadIdx.x & 31;
   Sched sc;
   sc.init(p.groups, ngroups, PHASE, p.H, p.n_max, begin, end, g0);
   constexpr int kBTiles = PHASE == 0 ? 1 : 2;
-  const uint16_t* bsrc = PHASE == 0 ? p.x : p.h;
   Seg sg;
   while (sc.next(sg)) {
+    const uint16_t* bsrc = PHASE == 0 ? ((kFp4 && sg.expert >= 0) ? p.xh : p.x) : p.h;
     const int nrows = max(16, (sg.n_cnt + 15) & ~15);
     const int kdim = PHASE == 0 ? p.H : sg.idim;
     __syncwarp();
@@ -400,8 +464,108 @@ __device__ bool gather(const Smem& sm, const GemmParams& p, int ngroups, long lo
   return true;
 }
 
+// ---------------------------------------------------------------- FP4 expansion (4 warps)
+// All 128 converter threads vote; every one of them must call it.
+__device__ __forceinline__ bool conv_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+// 2^(s - 127) as an f16 pair, for s in [kFp4ScaleMin, kFp4ScaleMax] (normal
+// f16 down to 2^-14, subnormal below).
+__device__ __forceinline__ uint32_t e8m0_to_h2(uint32_t s) {
+  const int e = static_cast<int>(s) - 127;
+  const uint32_t b = e >= -14 ? static_cast<uint32_t>(e + 15) << 10 : 1u << (e + 24);
+  return b | (b << 16);
+}
+
+// Eight e2m1 codes (byte j: inputs 2j in the low nibble, 2j+1 in the high
+// one) -> eight f16 times the scale pair sc, in input order.
+__device__ __forceinline__ uint4 expand8(uint32_t w, uint32_t sc) {
+  uint4 o;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t"
+      "mul.rn.f16x2 %0, %0, %5;\n\t"
+      "mul.rn.f16x2 %1, %1, %5;\n\t"
+      "mul.rn.f16x2 %2, %2, %5;\n\t"
+      "mul.rn.f16x2 %3, %3, %5;\n\t"
+      "}"
+      : "=&r"(o.x), "=&r"(o.y), "=&r"(o.z), "=&r"(o.w)
+      : "r"(w), "r"(sc));
+  return o;
+}
+
+// Walks the CTA's k-blocks in the producer's order; for every routed one,
+// waits for its codes and a free A stage, and writes row r of both halves of
+// the A stage: the 64 inputs of the k-block as f16, 128-byte swizzled.
+__device__ bool convert(const Smem& sm, const GemmParams& p, int ngroups, const long long (&b)[2],
+                        const long long (&e)[2], const int (&g)[2], int32_t* status) {
+  const int r = threadIdx.x - 7 * 32;
+  WeightCursor ld;
+  ld.init(p, ngroups, b, e, g);
+  Ring ring, pring;
+  bool range_ok = true;
+  while (ld.valid) {
+    if (ld.sg.expert < 0) {  // a bf16 k-block the producer loads itself
+      ld.step();
+      ring.next(sm.S);
+      continue;
+    }
+    bool ok = mbar_wait(&sm.empty[ring.stage], ring.phase ^ 1u, sm.abort_flag) &&
+              mbar_wait(&sm.pfull[pring.stage], pring.phase, sm.abort_flag);
+    if (ok) {
+      const uint8_t* cs = sm.pbase + pring.stage * kPackedBytes + r * 32;
+      const uint16_t* ss = reinterpret_cast<const uint16_t*>(sm.sbase + pring.stage * 512);
+      uint8_t* a = sm.base + ring.stage * sm.stage_bytes + r * 128;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t s2 = ss[h * kHalfRows + r];  // scales of inputs [0,32) and [32,64)
+        const uint32_t s0 = s2 & 0xffu, s1 = s2 >> 8;
+        range_ok &= s0 >= kFp4ScaleMin && s0 <= kFp4ScaleMax && s1 >= kFp4ScaleMin && s1 <= kFp4ScaleMax;
+        const uint32_t sc0 = e8m0_to_h2(min(max(s0, static_cast<uint32_t>(kFp4ScaleMin)), static_cast<uint32_t>(kFp4ScaleMax)));
+        const uint32_t sc1 = e8m0_to_h2(min(max(s1, static_cast<uint32_t>(kFp4ScaleMin)), static_cast<uint32_t>(kFp4ScaleMax)));
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+          const int q = qq ^ ((r >> 2) & 1);  // spreads the rows' 16-byte reads over the banks
+          const uint4 w = *reinterpret_cast<const uint4*>(cs + h * (kPackedBytes / 2) + q * 16);
+          const uint32_t sc = q ? sc1 : sc0;
+          const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = q * 4 + j;  // 16-byte chunk of the 128-byte row
+            *reinterpret_cast<uint4*>(a + h * kTileBytesA + ((c ^ (r & 7)) << 4)) = expand8(wv[j], sc);
+          }
+        }
+      }
+      fence_proxy_async();
+    }
+    if (!conv_all(ok)) {
+      if (r == 0) record_failure(status, sm.abort_flag, kInfoFull);
+      return false;
+    }
+    if (r == 0) {
+      mbar_arrive(&sm.pempty[pring.stage]);
+      mbar_arrive(&sm.full[ring.stage]);
+    }
+    pring.next(sm.SP);
+    ld.step();
+    ring.next(sm.S);
+  }
+  if (!range_ok) record_range(status, kInfoScaleRange);
+  return true;
+}
+
 // ---------------------------------------------------------------- epilogue (4 warps)
-template <int PHASE>
+template <int PHASE, bool kFp4>
 __device__ bool epilogue(const Smem& sm, const GemmParams& p, int ngroups, long long begin, long long end, int g0,
                          uint32_t tmem_base, int& seg_i, int32_t* tile_counters, int32_t* status) {
   Sched sc;
@@ -455,7 +619,7 @@ __device__ bool epilogue(const Smem& sm, const GemmParams& p, int ngroups, long 
         tmem_ld_wait();
         u32_to_f32(ua, fa);
         u32_to_f32(ub, fb);
-        finish_chunk<PHASE>(p, sg, r, j0, fa, fb, sm.col_w, sm.col_tok);
+        finish_chunk<PHASE, kFp4>(p, sg, r, j0, fa, fb, sm.col_w, sm.col_tok);
       }
       tc_fence_before();
       mbar_arrive(&sm.acce[buf]);
@@ -523,7 +687,7 @@ __device__ bool epilogue(const Smem& sm, const GemmParams& p, int ngroups, long 
             }
           }
         }
-        finish_chunk<PHASE>(p, sg, r, j0, fa, fb, sm.col_w, sm.col_tok);
+        finish_chunk<PHASE, kFp4>(p, sg, r, j0, fa, fb, sm.col_w, sm.col_tok);
       }
       tc_fence_before();
       mbar_arrive(&sm.acce[buf]);
@@ -546,7 +710,8 @@ __device__ bool epilogue(const Smem& sm, const GemmParams& p, int ngroups, long 
 // gate_up k-block iterations, then the down GEMM over its share of the down
 // iterations.  The launch is cooperative (every CTA resident), so the down
 // phase's bounded waits on the gate_up tiles of other CTAs always resolve.
-__global__ void __launch_bounds__(kGemmThreads, 1)
+template <bool kFp4>
+__global__ void __launch_bounds__(kFp4 ? kGemmThreadsFp4 : kGemmThreads, 1)
     moe_experts_kernel(const __grid_constant__ CUtensorMap tm_gu, const __grid_constant__ CUtensorMap tm_gu_sh,
                        const __grid_constant__ CUtensorMap tm_dn, const __grid_constant__ CUtensorMap tm_dn_sh,
                        const __grid_constant__ GemmParams p) {
@@ -581,6 +746,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&sm.acce[b], 128);
     }
     mbar_init(sm.drain, 1);
+    if (kFp4) {
+      // the FP4 rings' barriers open the stage region
+      uint64_t* pb = reinterpret_cast<uint64_t*>(ctrl + kCtrlBytes);
+      for (int s = 0; s < kMaxPStages; ++s) {
+        mbar_init(pb + s, 1);
+        mbar_init(pb + kMaxPStages + s, 1);
+      }
+    }
     *sm.abort_flag = 0;
     *sm.bcast = 0;
     fence_barrier_init();
@@ -608,6 +781,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   sm.b_bytes = p.header->n_eff * 128;
   sm.stage_bytes = 2 * kTileBytesA + 2 * sm.b_bytes;
   sm.S = min(kMaxStages, p.stage_space / static_cast<int>(sm.stage_bytes));
+  if (kFp4) {
+    // [barriers 1 KB | SP x 8 KB codes | SP x 512 B scales (1 KB aligned) |
+    //  S A stages]: three A stages where the codes keep four stages or more
+    const int st = static_cast<int>(sm.stage_bytes), ps = kPackedBytes + 512;
+    const int space = p.stage_space - 2048;
+    sm.S = (3 * st + 4 * ps <= space) ? 3 : 2;
+    sm.SP = min(kMaxPStages, (space - sm.S * st) / ps);
+    sm.pfull = reinterpret_cast<uint64_t*>(ctrl + kCtrlBytes);
+    sm.pempty = sm.pfull + kMaxPStages;
+    sm.pbase = ctrl + kCtrlBytes + 1024;
+    sm.sbase = sm.pbase + sm.SP * kPackedBytes;
+    sm.base = sm.sbase + ((sm.SP * 512 + 1023) & ~1023);
+  }
   // this CTA's cost-balanced spans of the gate_up and down iterations
   const int G1 = gridDim.x + 1;
   const long long bs[2] = {sm.span[blockIdx.x], sm.span[G1 + blockIdx.x]};
@@ -617,7 +803,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       Ring ring;
-      const bool ok = produce(sm, p, ng, bs, es, gs, &tm_gu, &tm_gu_sh, &tm_dn, &tm_dn_sh, ring, p.status);
+      const bool ok = produce<kFp4>(sm, p, ng, bs, es, gs, &tm_gu, &tm_gu_sh, &tm_dn, &tm_dn_sh, ring, p.status);
       if (!ok) {
         // let the loads already issued land before the CTA can exit
         const long long t0 = clock64();
@@ -628,8 +814,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       Ring ring;
       int seg_i = 0;
-      if (issue_mma<0>(sm, p, ng, bs[0], es[0], gs[0], tmem_base, ring, seg_i, p.status))
-        issue_mma<1>(sm, p, ng, bs[1], es[1], gs[1], tmem_base, ring, seg_i, p.status);
+      if (issue_mma<0, kFp4>(sm, p, ng, bs[0], es[0], gs[0], tmem_base, ring, seg_i, p.status))
+        issue_mma<1, kFp4>(sm, p, ng, bs[1], es[1], gs[1], tmem_base, ring, seg_i, p.status);
       // every MMA issued above has completed once `drain` flips
       mma_commit(sm.drain);
       if (!mbar_wait(sm.drain, 0, nullptr)) record_failure(p.status, sm.abort_flag, kInfoDrain);
@@ -640,8 +826,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // copies kept in flight before arriving; below the stage count, so the
     // stage this warp waits to refill never depends on an arrival it holds
     const int lag = kGatherLag < sm.S - 1 ? kGatherLag : sm.S - 1;
-    if (gather<0>(sm, p, ng, bs[0], es[0], gs[0], ring, pending, arr_stage, lag, p.status))
-      gather<1>(sm, p, ng, bs[1], es[1], gs[1], ring, pending, arr_stage, lag, p.status);
+    if (gather<0, kFp4>(sm, p, ng, bs[0], es[0], gs[0], ring, pending, arr_stage, lag, p.status))
+      gather<1, kFp4>(sm, p, ng, bs[1], es[1], gs[1], ring, pending, arr_stage, lag, p.status);
     cp_async_wait<0>();
     fence_proxy_async();
     while (pending > 0) {
@@ -649,10 +835,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (++arr_stage == sm.S) arr_stage = 0;
       --pending;
     }
-  } else {
+  } else if (warp < 7) {
     int seg_i = 0;
-    if (epilogue<0>(sm, p, ng, bs[0], es[0], gs[0], tmem_base, seg_i, p.tile_counters_gu, p.status))
-      epilogue<1>(sm, p, ng, bs[1], es[1], gs[1], tmem_base, seg_i, p.tile_counters_dn, p.status);
+    if (epilogue<0, kFp4>(sm, p, ng, bs[0], es[0], gs[0], tmem_base, seg_i, p.tile_counters_gu, p.status))
+      epilogue<1, kFp4>(sm, p, ng, bs[1], es[1], gs[1], tmem_base, seg_i, p.tile_counters_dn, p.status);
+  } else if (kFp4) {
+    convert(sm, p, ng, bs, es, gs, p.status);
   }
 
   tc_fence_before();
@@ -686,17 +874,60 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   *reinterpret_cast<uint2*>(y + static_cast<size_t>(t) * H + c) = o;
 }
 
+// Re-lays e8m0 block scales [E,2I,H/32] and [E,H,I/32] into the blocks the
+// FP4 expert kernel copies whole: for every (expert, tile, k-block) the two
+// 128-row halves' scale pairs, 512 bytes (rows past the matrix: scale 1).
+__global__ void __launch_bounds__(256) fp4_scales_kernel(const uint8_t* __restrict__ gu_s,
+                                                         const uint8_t* __restrict__ dn_s, int E, int H, int I,
+                                                         uint8_t* __restrict__ out) {
+  const int mb0 = ceil_div(I, kHalfRows), kb0 = H / kBlockK;
+  const int mb1 = ceil_div(H, 2 * kHalfRows), kb1 = I / kBlockK;
+  const long long n0 = static_cast<long long>(E) * mb0 * kb0 * 256;  // scale pairs
+  const long long n = n0 + static_cast<long long>(E) * mb1 * kb1 * 256;
+  for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n; i += static_cast<long long>(gridDim.x) * 256) {
+    const bool dn = i >= n0;
+    const long long j = dn ? i - n0 : i;
+    const int r = static_cast<int>(j % kHalfRows), h = static_cast<int>((j / kHalfRows) % 2);
+    const long long blk = j / 256;  // (e, m, kb)
+    const int kbs = dn ? kb1 : kb0, mbs = dn ? mb1 : mb0;
+    const int kb = static_cast<int>(blk % kbs), m = static_cast<int>((blk / kbs) % mbs);
+    const int e = static_cast<int>(blk / (static_cast<long long>(kbs) * mbs));
+    uint16_t v = 0x7f7f;
+    if (!dn) {
+      const int row = m * kHalfRows + r;
+      if (row < I) {
+        const uint8_t* src = gu_s + (static_cast<size_t>(e) * 2 * I + h * I + row) * (H / 32) + kb * 2;
+        v = static_cast<uint16_t>(src[0] | (src[1] << 8));
+      }
+    } else {
+      const int row = m * 2 * kHalfRows + h * kHalfRows + r;
+      if (row < H) {
+        const uint8_t* src = dn_s + (static_cast<size_t>(e) * H + row) * (I / 32) + kb * 2;
+        v = static_cast<uint16_t>(src[0] | (src[1] << 8));
+      }
+    }
+    reinterpret_cast<uint16_t*>(out)[i] = v;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_fp4_scales(const uint8_t* gu_s, const uint8_t* dn_s, int E, int H, int I, uint8_t* out,
+                              cudaStream_t s) {
+  fp4_scales_kernel<<<4 * 152, 256, 0, s>>>(gu_s, dn_s, E, H, I, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_experts(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, const CUtensorMap& tm_dn,
                            const CUtensorMap& tm_dn_sh, const GemmParams& p, int grid, size_t smem_bytes,
-                           cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(moe_experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           cudaStream_t s, bool fp4) {
+  auto kern = fp4 ? moe_experts_kernel<true> : moe_experts_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem_bytes));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kGemmThreads);
+  cfg.blockDim = dim3(fp4 ? kGemmThreadsFp4 : kGemmThreads);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -704,7 +935,7 @@ cudaError_t launch_experts(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, moe_experts_kernel, tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, p);
+  return cudaLaunchKernelEx(&cfg, kern, tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, p);
 }
 
 cudaError_t launch_combine(const float* out_ws, const int32_t* pair_pos, int T, int K, int H, int has_shared,

@@ -15,12 +15,15 @@ namespace moe {
 // ----------------------------------------------------------------------------
 // status word (first 8 bytes of every workspace): {code, info}
 // ----------------------------------------------------------------------------
-enum : int32_t { kStatusTimeout = 5 };
+enum : int32_t { kStatusTimeout = 5, kStatusRange = 6 };
 // info values: which wait ran out
 enum : int32_t {
   kInfoEmpty = 1, kInfoFull = 2, kInfoAccFull = 3, kInfoAccEmpty = 4,
   kInfoGatherEmpty = 5, kInfoDrain = 6, kInfoReady = 7, kInfoFixup = 8,
-  kInfoRouter = 9, kInfoTileCount = 10, kInfoHReady = 11
+  kInfoRouter = 9, kInfoTileCount = 10, kInfoHReady = 11,
+  // range errors (kStatusRange): an FP4 block scale outside [104, 140], or a
+  // value of x or h outside the f16 range of the FP4 experts' MMAs
+  kInfoScaleRange = 12, kInfoXRange = 13, kInfoHRange = 14
 };
 
 // ----------------------------------------------------------------------------
@@ -63,6 +66,11 @@ constexpr int kBlockK = 64;
 constexpr int kHalfRows = 128;
 constexpr int kTileBytesA = kHalfRows * kBlockK * 2;  // one half, bf16: 16 KB
 constexpr int kGemmThreads = 224;                     // 7 warps
+constexpr int kGemmThreadsFp4 = 352;                  // + 4 warps that expand FP4 weights
+constexpr int kPackedBytes = 2 * kHalfRows * kBlockK / 2;  // FP4 codes of one k-block, both halves: 8 KB
+constexpr int kMaxPStages = 16;                       // stages of FP4 codes
+// e8m0 block scales whose products with every e2m1 value are exact in f16
+constexpr int kFp4ScaleMin = 104, kFp4ScaleMax = 140;
 constexpr int kMaxStages = 8;
 // shared-memory control block: barriers and flags, the gather's row table
 // (<= 256 rows), both GEMMs' CTA span tables (<= kMaxGrid CTAs) and the
@@ -82,8 +90,10 @@ __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; 
 // (the shared expert, large token counts) add MMA, gather and epilogue
 // work, more in the down GEMM (h as hi and lo doubles its MMAs and gathers).
 // The slopes are fitted to per-CTA timings of 16- and 80-column tiles.
-__host__ __device__ inline int kblock_cost(int phase, int nmma) {
-  return phase == 0 ? 4 + ((nmma - 16) * 3 + 80) / 160 : 4 + ((nmma - 16) * 7 + 20) / 40;
+// An FP4 k-block streams about a quarter of the bytes (8.5 KB).
+__host__ __device__ inline int kblock_cost(int phase, int nmma, bool fp4 = false) {
+  const int base = fp4 ? 1 : 4;
+  return phase == 0 ? base + ((nmma - 16) * 3 + 80) / 160 : base + ((nmma - 16) * 7 + 20) / 40;
 }
 
 __host__ __device__ inline void group_geometry(int phase, int count, int idim, int H, int n_max,
@@ -117,6 +127,12 @@ struct GemmParams {
   int32_t* tile_counters_dn;   // [down tiles]
   int32_t* ready;              // [gate_up tiles] finished gate_up tiles per (group, token block)
   int32_t* status;
+  // FP4 routed experts (moe_ffn_forward_fp4): codes come through the tensor
+  // maps, the e8m0 scales are read here; routed groups multiply in f16
+  const uint16_t* xh;          // [T,H] f16 copy of x
+  const uint8_t* gu_scale;     // [E,2I,H/32]
+  const uint8_t* dn_scale;     // [E,H,I/32]
+  int I, E;                    // routed experts' I, expert count
 };
 
 // Routing recipe as the selection code reads it (score_fn 0 softmax,
@@ -159,6 +175,9 @@ struct RouteParams {
   int I, Is, n_max;
   int32_t* zero_ptr;           // GEMM tile counters cleared by this launch
   int zero_count;
+  int fp4;                     // routed experts are FP4: their k-blocks cost less
+  uint16_t* xh;                // [T,H] f16 copy of x written for FP4 experts (nullable)
+  int32_t* status;             // range errors of that copy
 };
 
 // Fused small-expert-count forward (slice.cu): one CTA per (expert, 128-row
@@ -212,7 +231,10 @@ cudaError_t launch_permute(const int32_t* idx, int T, int K, int E, int32_t* cou
                            int32_t* sorted_pair, int32_t* pair_pos, cudaStream_t s);
 cudaError_t launch_experts(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, const CUtensorMap& tm_dn,
                            const CUtensorMap& tm_dn_sh, const GemmParams& p, int grid, size_t smem_bytes,
-                           cudaStream_t s);
+                           cudaStream_t s, bool fp4);
+// FP4 block scales re-laid into 512-byte (expert, tile, k-block) blocks.
+cudaError_t launch_fp4_scales(const uint8_t* gu_s, const uint8_t* dn_s, int E, int H, int I, uint8_t* out,
+                              cudaStream_t s);
 cudaError_t launch_slice(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, const CUtensorMap& tm_dn,
                          const CUtensorMap& tm_dn_sh, const CUtensorMap& tm_x, const SliceParams& p, int grid,
                          size_t smem_bytes, cudaStream_t s);
@@ -405,6 +427,12 @@ __device__ __forceinline__ void record_failure(int32_t* status, volatile int* ab
   *abort_flag = 1;
 }
 
+// A value outside the exact range of the computation: recorded, the forward
+// runs on (its output is not exact).
+__device__ __forceinline__ void record_range(int32_t* status, int32_t info) {
+  if (atomicCAS(status, 0, kStatusRange) == 0) atomicExch(status + 1, info);
+}
+
 __device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -427,6 +455,10 @@ struct Ring {
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+// The same with f16 A and B (type fields 0).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 }  // namespace moe

@@ -14,6 +14,8 @@
 #include <float.h>
 #include <math.h>
 
+#include <cuda_fp16.h>
+
 #include "moe_internal.cuh"
 #include "select.cuh"
 
@@ -70,7 +72,7 @@ __device__ void block_scan_excl(const int* in, int* out, int n, int* s_warp) {
 __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* counts, int32_t* offsets,
                               int32_t* sorted_pair, int32_t* pair_pos, GroupEntry* groups, GemmHeader* header,
                               int H, int I, int Is, int n_max, int* s_cnt, int* s_cur, long long* s_buf,
-                              uint16_t* s_wc, int64_t* spans, int32_t* span_groups, int grid) {
+                              uint16_t* s_wc, int64_t* spans, int32_t* span_groups, int grid, bool fp4) {
   __shared__ int s_warp[kPermWarps];
   int* s_idx = reinterpret_cast<int*>(s_buf);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -207,8 +209,8 @@ __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* 
       const int nmma = max(16, min(n_max, (c + 15) & ~15));
       v[0] += 1;
       v[1] += nb;
-      v[2] += static_cast<long long>(nb) * mb0 * kb0 * kblock_cost(0, nmma);
-      v[3] += static_cast<long long>(nb) * mb1 * kb1 * kblock_cost(1, nmma);
+      v[2] += static_cast<long long>(nb) * mb0 * kb0 * kblock_cost(0, nmma, fp4);
+      v[3] += static_cast<long long>(nb) * mb1 * kb1 * kblock_cost(1, nmma, fp4);
     }
   }
   long long incl[4] = {v[0], v[1], v[2], v[3]};
@@ -240,7 +242,7 @@ __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* 
       const int nb = ceil_div(c, n_max);
       const int nmma = max(16, min(n_max, (c + 15) & ~15));
       const int gi = static_cast<int>(run[0]);
-      const int w0 = kblock_cost(0, nmma), w1 = kblock_cost(1, nmma);
+      const int w0 = kblock_cost(0, nmma, fp4), w1 = kblock_cost(1, nmma, fp4);
       GroupEntry ge;
       ge.expert = e;
       ge.row_base = s_cur[e];
@@ -341,6 +343,15 @@ __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* 
 // logits (row E is the shared-expert gate when present); the last CTA of a
 // token block selects its tokens; the last token block builds the
 // permutation and the work list.
+// Two bf16 values -> two f16 values (round to nearest even); `over` is set
+// when one leaves the f16 range.
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w, bool& over) {
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+  over |= !(fabsf(lo) < 65520.f) || !(fabsf(hi) < 65520.f);
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 template <int TB, int NJ>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams p) {
   __shared__ float red[8][TB][4];
@@ -386,6 +397,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
     for (int q = 0; q < 4; ++q) acc[t][q] = 0.f;
   }
   const bool do_sh = fold && quad == 0;
+  // FP4 experts multiply in f16: the quad-0 warps of expert block 0 (which
+  // cover H once) also write the f16 copy of their x columns
+  const bool xh_w = p.xh != nullptr && ebi == 0 && quad == 0;
   // one step of loads stays in flight while the previous step is multiplied
   uint4 gv[4], xv[TB], sv;
   auto load_step = [&](int c, int step, uint4 (&g)[4], uint4 (&xx)[TB], uint4& sg) {
@@ -409,6 +423,21 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
     if (do_sh && step % p.n_eb == ebi) {
 #pragma unroll
       for (int t = 0; t < TB; ++t) acc_sh[t] = dot8(xv[t], sv, acc_sh[t]);
+    }
+    if (xh_w) {
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        if (t0 + t < p.T) {
+          bool over = false;
+          uint4 o;
+          o.x = bf2_to_h2(xv[t].x, over);
+          o.y = bf2_to_h2(xv[t].y, over);
+          o.z = bf2_to_h2(xv[t].z, over);
+          o.w = bf2_to_h2(xv[t].w, over);
+          *reinterpret_cast<uint4*>(p.xh + static_cast<size_t>(t0 + t) * p.H + c) = o;
+          if (over) record_range(p.status, kInfoXRange);
+        }
+      }
     }
     if (cn < h_hi) {
 #pragma unroll
@@ -516,7 +545,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
   if (!s_flag) return;
   __threadfence();
   permute_block(p.idx, p.T, p.K, p.E, p.counts, p.offsets, p.sorted_pair, p.pair_pos, p.groups, p.header, p.H,
-                p.I, p.Is, p.n_max, s_cnt, s_cur, s_buf, s_wc, p.spans, p.span_groups, p.grid);
+                p.I, p.Is, p.n_max, s_cnt, s_cur, s_buf, s_wc, p.spans, p.span_groups, p.grid, p.fp4 != 0);
 }
 
 template <int NJ>
@@ -536,7 +565,7 @@ __global__ void __launch_bounds__(kRouteThreads) permute_kernel(const int32_t* i
   __shared__ long long s_buf[kPermBuf];
   __shared__ uint16_t s_wc[kPermWarps * kMaxExperts];
   permute_block(idx, T, K, E, counts, offsets, sorted_pair, pair_pos, nullptr, nullptr, 0, 0, 0, 1, s_cnt, s_cur,
-                s_buf, s_wc, nullptr, nullptr, 0);
+                s_buf, s_wc, nullptr, nullptr, 0, false);
 }
 
 int nj_for(int E) {

@@ -17,7 +17,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
 HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "moe.h")
 
-MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT = range(6)
+(MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT,
+ MOE_ERR_DEVICE_RANGE) = range(7)
 SCORE_SOFTMAX, SCORE_SIGMOID, SCORE_SQRTSOFTPLUS = 0, 1, 2
 
 
@@ -76,6 +77,10 @@ _SIGS = {
     "moe_set_profile_events": (None, [_P, _I]),
     "moe_set_schedule": (_I, [_I]),
     "moe_ffn_schedule": (_I, [_I, _I, _I, _I, ctypes.POINTER(Recipe), _I]),
+    "moe_fp4_scales_bytes": (_SZ, [_I, _I, _I]),
+    "moe_fp4_prepare_scales": (_I, [_P, _P, _I, _I, _I, _P, _SZ, _P]),
+    "moe_ffn_forward_fp4": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P, _I, _P,
+                                 ctypes.POINTER(Recipe), _P, _SZ, _P, _P, _P, _P, _P]),
 }
 
 SCHEDULE_AUTO, SCHEDULE_STREAM_K, SCHEDULE_SLICE = 0, 1, 2
@@ -246,6 +251,47 @@ def moe_ffn_forward(x, gate, w_gate_up, w_down, recipe: Recipe, ws: Workspace, r
     return y
 
 
+def _u8(t: torch.Tensor) -> torch.Tensor:
+    if t.dtype != torch.uint8:
+        raise TypeError("expected a uint8 tensor")
+    return t
+
+
+def fp4_prepare_scales(w_gate_up_s, w_down_s, stream=None) -> torch.Tensor:
+    """The e8m0 scales [E,2I,H/32] and [E,H,I/32] re-laid for
+    moe_ffn_forward_fp4 (once per set of weights); returns the uint8 buffer."""
+    _need_cuda(w_gate_up_s, w_down_s)
+    E, H = w_down_s.shape[0], w_down_s.shape[1]
+    I = w_gate_up_s.shape[1] // 2
+    n = lib().moe_fp4_scales_bytes(E, H, I)
+    if n == 0:
+        raise MoeError(MOE_ERR_UNSUPPORTED, "moe_fp4_scales_bytes")
+    out = torch.empty(n, dtype=torch.uint8, device=w_down_s.device)
+    _check(lib().moe_fp4_prepare_scales(_ptr(_u8(w_gate_up_s)), _ptr(_u8(w_down_s)), E, H, I, _ptr(out), n,
+                                        _stream(stream)), "moe_fp4_prepare_scales")
+    return out
+
+
+def moe_ffn_forward_fp4(x, gate, w_gate_up_q, w_down_q, scales, recipe: Recipe, ws: Workspace, router_bias=None,
+                        expert_bias=None, sh_gate_up=None, sh_down=None, sh_gate=None, y=None,
+                        topk_idx_out=None, topk_w_out=None, counts_out=None, stream=None):
+    """The whole layer with FP4 routed experts (codes [E,2I,H/2], [E,H,I/2];
+    ``scales`` from fp4_prepare_scales); returns y [T,H] bf16."""
+    _need_cuda(x, gate, w_gate_up_q, w_down_q, scales, router_bias, expert_bias, sh_gate_up, sh_down, sh_gate, y,
+               topk_idx_out, topk_w_out, counts_out)
+    T, H = x.shape
+    I = w_down_q.shape[2] * 2
+    Is = 0 if sh_gate_up is None else sh_down.shape[1]
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _check(lib().moe_ffn_forward_fp4(
+        _ptr(_u16(x)), T, H, I, _ptr(_u16(gate)), _ptr(router_bias), _ptr(expert_bias), _ptr(_u8(w_gate_up_q)),
+        _ptr(_u8(w_down_q)), _ptr(_u8(scales)), scales.numel(), _ptr(sh_gate_up), _ptr(sh_down), Is, _ptr(sh_gate),
+        ctypes.byref(recipe), ws.ptr(), ws.nbytes, _ptr(y), _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(counts_out),
+        _stream(stream)), "moe_ffn_forward_fp4")
+    return y
+
+
 def set_schedule(schedule: int) -> None:
     """Expert schedule of later moe_ffn_forward calls on this thread:
     SCHEDULE_AUTO, SCHEDULE_STREAM_K or SCHEDULE_SLICE."""
@@ -282,17 +328,31 @@ class MoELayer:
     def __init__(self, tensors: dict, recipe: Recipe, max_tokens: int):
         self.t = tensors
         self.recipe = recipe
-        self.H = tensors["w_down"].shape[1]
-        self.I = tensors["w_down"].shape[2]
+        # FP4 routed experts when the codes are given (w_gate_up_q, w_down_q,
+        # and their scales w_gate_up_s, w_down_s, re-laid once here)
+        self.fp4 = tensors.get("w_down_q") is not None
+        if self.fp4:
+            self.H = tensors["w_down_q"].shape[1]
+            self.I = tensors["w_down_q"].shape[2] * 2
+            self.scales = fp4_prepare_scales(tensors["w_gate_up_s"], tensors["w_down_s"])
+        else:
+            self.H = tensors["w_down"].shape[1]
+            self.I = tensors["w_down"].shape[2]
         self.Is = 0 if tensors.get("sh_gate_up") is None else tensors["sh_down"].shape[1]
         self.max_tokens = max_tokens
         self.ws = Workspace(ffn_workspace_bytes(max_tokens, self.H, self.I, self.Is, recipe),
-                            tensors["w_down"].device)
+                            tensors["gate"].device)
 
     def forward(self, x, y=None, topk_idx_out=None, topk_w_out=None, counts_out=None, stream=None):
         if x.shape[0] > self.max_tokens:
             raise ValueError("more tokens than the workspace was sized for")
         t = self.t
+        if self.fp4:
+            return moe_ffn_forward_fp4(x, t["gate"], t["w_gate_up_q"], t["w_down_q"], self.scales, self.recipe,
+                                       self.ws, router_bias=t.get("router_bias"), expert_bias=t.get("expert_bias"),
+                                       sh_gate_up=t.get("sh_gate_up"), sh_down=t.get("sh_down"),
+                                       sh_gate=t.get("sh_gate"), y=y, topk_idx_out=topk_idx_out,
+                                       topk_w_out=topk_w_out, counts_out=counts_out, stream=stream)
         return moe_ffn_forward(x, t["gate"], t["w_gate_up"], t["w_down"], self.recipe, self.ws,
                                router_bias=t.get("router_bias"), expert_bias=t.get("expert_bias"),
                                sh_gate_up=t.get("sh_gate_up"), sh_down=t.get("sh_down"), sh_gate=t.get("sh_gate"),
