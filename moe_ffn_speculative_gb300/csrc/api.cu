@@ -204,7 +204,17 @@ struct Layout {
 Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sms) {
   Layout L;
   L.rg = router_geometry(T, E, gated, sms);
+  // Token tile width: every token of a decode-sized forward in one tile;
+  // above 128 tokens about four times an expert's mean load (at least 64),
+  // so that routed experts rarely need a second tile while the shared
+  // expert's T tokens (several narrower tiles) no longer size every stage
+  // of the ring for 256 columns.
   int nm = ((T + 15) / 16) * 16;
+  if (T > 128) {
+    const long long load4 = (4ll * T * K + E - 1) / E;
+    const int cap = static_cast<int>(load4 < 64 ? 64 : ((load4 + 15) / 16) * 16);
+    if (cap < nm) nm = cap;
+  }
   L.n_max = nm < 16 ? 16 : (nm > 256 ? 256 : nm);
   L.nbuf = (4 * L.n_max <= 512) ? 2 : 1;
   uint32_t cols = 32;
