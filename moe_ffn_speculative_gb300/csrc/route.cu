@@ -400,8 +400,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
   // FP4 experts multiply in f16: the quad-0 warps of expert block 0 (which
   // cover H once) also write the f16 copy of their x columns
   const bool xh_w = p.xh != nullptr && ebi == 0 && quad == 0;
-  // one step of loads stays in flight while the previous step is multiplied
-  uint4 gv[4], xv[TB], sv;
+  // D - 1 steps of loads stay in flight while a step is multiplied (two
+  // for 4-token blocks; one for 8-token blocks, whose registers are full)
+  constexpr int D = TB <= 4 ? 3 : 2;
+  uint4 gb[D][4], xb[D][TB], sb[D];
   auto load_step = [&](int c, int step, uint4 (&g)[4], uint4 (&xx)[TB], uint4& sg) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) g[q] = ev[q] ? ldg128(rows[q] + c) : make_uint4(0, 0, 0, 0);
@@ -410,44 +412,43 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
       xx[t] = (t0 + t < p.T) ? ldg128(p.x + static_cast<size_t>(t0 + t) * p.H + c) : make_uint4(0, 0, 0, 0);
     sg = (do_sh && step % p.n_eb == ebi) ? ldg128(p.sh_gate + c) : make_uint4(0, 0, 0, 0);
   };
-  int c = h_lo + lane * 8, step = 0;
-  if (c < h_hi) load_step(c, 0, gv, xv, sv);
-  while (c < h_hi) {
-    const int cn = c + 256;
-    uint4 gn[4], xn[TB], sn;
-    if (cn < h_hi) load_step(cn, step + 1, gn, xn, sn);
+  const int c0 = h_lo + lane * 8;
 #pragma unroll
-    for (int t = 0; t < TB; ++t)
+  for (int d = 0; d + 1 < D; ++d)
+    if (c0 + d * 256 < h_hi) load_step(c0 + d * 256, d, gb[d], xb[d], sb[d]);
+  for (int base = 0; c0 + base * 256 < h_hi; base += D) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) acc[t][q] = dot8(xv[t], gv[q], acc[t][q]);
-    if (do_sh && step % p.n_eb == ebi) {
+    for (int d = 0; d < D; ++d) {
+      const int step = base + d;
+      const int c = c0 + step * 256;
+      if (c < h_hi) {
+        const int dn = (d + D - 1) % D;  // the slot freed one step ago
+        if (c + (D - 1) * 256 < h_hi) load_step(c + (D - 1) * 256, step + D - 1, gb[dn], xb[dn], sb[dn]);
 #pragma unroll
-      for (int t = 0; t < TB; ++t) acc_sh[t] = dot8(xv[t], sv, acc_sh[t]);
-    }
-    if (xh_w) {
+        for (int t = 0; t < TB; ++t)
 #pragma unroll
-      for (int t = 0; t < TB; ++t) {
-        if (t0 + t < p.T) {
-          bool over = false;
-          uint4 o;
-          o.x = bf2_to_h2(xv[t].x, over);
-          o.y = bf2_to_h2(xv[t].y, over);
-          o.z = bf2_to_h2(xv[t].z, over);
-          o.w = bf2_to_h2(xv[t].w, over);
-          *reinterpret_cast<uint4*>(p.xh + static_cast<size_t>(t0 + t) * p.H + c) = o;
-          if (over) record_range(p.status, kInfoXRange);
+          for (int q = 0; q < 4; ++q) acc[t][q] = dot8(xb[d][t], gb[d][q], acc[t][q]);
+        if (do_sh && step % p.n_eb == ebi) {
+#pragma unroll
+          for (int t = 0; t < TB; ++t) acc_sh[t] = dot8(xb[d][t], sb[d], acc_sh[t]);
+        }
+        if (xh_w) {
+#pragma unroll
+          for (int t = 0; t < TB; ++t) {
+            if (t0 + t < p.T) {
+              bool over = false;
+              uint4 o;
+              o.x = bf2_to_h2(xb[d][t].x, over);
+              o.y = bf2_to_h2(xb[d][t].y, over);
+              o.z = bf2_to_h2(xb[d][t].z, over);
+              o.w = bf2_to_h2(xb[d][t].w, over);
+              *reinterpret_cast<uint4*>(p.xh + static_cast<size_t>(t0 + t) * p.H + c) = o;
+              if (over) record_range(p.status, kInfoXRange);
+            }
+          }
         }
       }
     }
-    if (cn < h_hi) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) gv[q] = gn[q];
-#pragma unroll
-      for (int t = 0; t < TB; ++t) xv[t] = xn[t];
-      sv = sn;
-    }
-    c = cn;
-    ++step;
   }
   if (do_sh) {
     // this block's partial of x.sh_gate for each token: slot ebi*hsplit + hs

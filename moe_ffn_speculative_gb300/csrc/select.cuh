@@ -42,16 +42,27 @@ __device__ __forceinline__ uint4 ldg128(const uint16_t* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
+// Order-preserving image of a float in the unsigned integers (larger float,
+// larger image; -inf maps below every finite value; -0 and +0 map alike, as
+// they compare equal).  NaN never reaches it.
+__device__ __forceinline__ uint32_t ord_key(float v) {
+  const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // (value, index) maximum over the warp; ties go to the lower index.  The
-// order is total, so every lane ends with the same winner.
+// order is total, so every lane ends with the same winner.  Two warp-wide
+// reductions (the largest value, then the smallest index holding it) and one
+// shuffle of the winner's carried value; an index is lane + 32*j, so the
+// winner's lane is its index mod 32.
 __device__ __forceinline__ void warp_argmax(float& v, int& ix, float& carry) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, off);
-    const int oi = __shfl_xor_sync(0xffffffffu, ix, off);
-    const float oc = __shfl_xor_sync(0xffffffffu, carry, off);
-    if (ov > v || (ov == v && oi < ix)) { v = ov; ix = oi; carry = oc; }
-  }
+  const uint32_t k = ord_key(v);
+  const uint32_t best = __reduce_max_sync(0xffffffffu, k);
+  const uint32_t cand = (k == best) ? static_cast<uint32_t>(ix) : 0xffffffffu;
+  const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+  carry = __shfl_sync(0xffffffffu, carry, static_cast<int>(win & 31u));
+  v = __shfl_sync(0xffffffffu, v, static_cast<int>(win & 31u));
+  ix = static_cast<int>(win);
 }
 
 
