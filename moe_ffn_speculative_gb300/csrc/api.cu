@@ -95,6 +95,21 @@ bool encode_codes_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// h [rows][2*I_ld] (16-bit: hi columns then lo columns), loaded in boxes of
+// 64 columns x 16 rows with the 128-byte swizzle; rows past the end read as
+// zero.
+bool encode_h_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), 16};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -205,14 +220,15 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   Layout L;
   L.rg = router_geometry(T, E, gated, sms);
   // Token tile width: every token of a decode-sized forward in one tile;
-  // above 128 tokens about four times an expert's mean load (at least 64),
-  // so that routed experts rarely need a second tile while the shared
-  // expert's T tokens (several narrower tiles) no longer size every stage
-  // of the ring for 256 columns.
+  // above 128 tokens about four times an expert's mean load, between 64 and
+  // 128, so that routed experts rarely need a second tile while the shared
+  // expert's T tokens (several narrower tiles) neither size every stage of
+  // the ring for 256 columns nor take the second TMEM accumulator buffer
+  // (two buffers of 2 x 128 columns fill the 512).
   int nm = ((T + 15) / 16) * 16;
   if (T > 128) {
     const long long load4 = (4ll * T * K + E - 1) / E;
-    const int cap = static_cast<int>(load4 < 64 ? 64 : ((load4 + 15) / 16) * 16);
+    const int cap = static_cast<int>(load4 < 64 ? 64 : (load4 > 128 ? 128 : ((load4 + 15) / 16) * 16));
     if (cap < nm) nm = cap;
   }
   L.n_max = nm < 16 ? 16 : (nm > 256 ? 256 : nm);
@@ -564,8 +580,14 @@ moe_status ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf16* g
     gp.gu_scale = fp4->scales;
     gp.dn_scale = fp4->scales;  // one buffer: the down blocks follow the gate_up blocks
   }
+  // the down GEMM's token rows by TMA when every k-block is whole
+  CUtensorMap tm_h = tm_dn;
+  if (I % kBlockK == 0 && Is % kBlockK == 0) {
+    if (!encode_h_2d(&tm_h, h, 2ull * L.I_ld, static_cast<uint64_t>(T) * K + T)) return MOE_ERR_CUDA;
+    gp.h_tma = 1;
+  }
   record_event_on(2, stream);
-  e = launch_experts(tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, gp, L.grid, L.smem, stream, fp4 != nullptr);
+  e = launch_experts(tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, tm_h, gp, L.grid, L.smem, stream, fp4 != nullptr);
   record_event_on(3, stream);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 

@@ -374,8 +374,23 @@ __device__ bool issue_mma(const Smem& sm, const GemmParams& p, int ngroups, long
 // lo), after the gate_up tiles that write them have signalled.
 template <int PHASE, bool kFp4>
 __device__ bool gather(const Smem& sm, const GemmParams& p, int ngroups, long long begin, long long end, int g0,
-                       Ring& ring, int& pending, int& arr_stage, int lag, int32_t* status) {
+                       Ring& ring, int& pending, int& arr_stage, int lag, const CUtensorMap* tm_h,
+                       int32_t* status) {
   const int lane = threadIdx.x & 31;
+  // The down GEMM's token rows (h hi and lo) of one (expert, token block)
+  // are consecutive rows of h: loaded by TMA in boxes of 16 rows x 64
+  // columns, lane 0 counting their bytes on the stage's barrier.
+  const bool h_tma = PHASE == 1 && p.h_tma != 0;
+  if (h_tma) {
+    // copies of the gate_up phase still in flight land and count first
+    cp_async_wait<0>();
+    fence_proxy_async();
+    while (pending > 0) {
+      mbar_arrive(&sm.full[arr_stage]);
+      if (++arr_stage == sm.S) arr_stage = 0;
+      --pending;
+    }
+  }
   Sched sc;
   sc.init(p.groups, ngroups, PHASE, p.H, p.n_max, begin, end, g0);
   constexpr int kBTiles = PHASE == 0 ? 1 : 2;
@@ -429,6 +444,8 @@ __device__ bool gather(const Smem& sm, const GemmParams& p, int ngroups, long lo
           return false;
         }
       }
+      // rows written by other CTAs' generic stores, read by TMA below
+      if (h_tma) asm volatile("fence.proxy.async.global;" ::: "memory");
     }
     __syncwarp();
     for (int kk = 0; kk < sg.len; ++kk) {
@@ -439,6 +456,22 @@ __device__ bool gather(const Smem& sm, const GemmParams& p, int ngroups, long lo
         return false;
       }
       const uint32_t bbase = smem_u32(sm.base + ring.stage * sm.stage_bytes) + 2 * kTileBytesA;
+      if (h_tma) {
+        uint64_t* bar = &sm.full[ring.stage];
+        if (lane == 0) {
+          const int nb = nrows / 16;
+          const int row0 = sg.row_base + sg.n * p.n_max;
+          mbar_arrive_expect_tx(bar, static_cast<uint32_t>(2 * nb * 2048));
+          uint8_t* b0 = sm.base + ring.stage * sm.stage_bytes + 2 * kTileBytesA;
+          for (int t = 0; t < 2; ++t)
+            for (int i = 0; i < nb; ++i)
+              tma_load_2d(b0 + t * sm.b_bytes + i * 2048, tm_h, bar, t * p.I_ld + kx, row0 + 16 * i);
+        } else {
+          mbar_arrive(bar);
+        }
+        ring.next(sm.S);
+        continue;
+      }
       for (int q = lane; q < nrows * 8 * kBTiles; q += 32) {
         const int t = (kBTiles == 2 && q >= nrows * 8) ? 1 : 0;  // 0: x or h_hi, 1: h_lo
         const int qq = q - t * nrows * 8;
@@ -695,7 +728,8 @@ __device__ bool epilogue(const Smem& sm, const GemmParams& p, int ngroups, long 
     }
     if (PHASE == 0 && done) {
       // this gate_up tile's h rows are written: count it towards its
-      // (expert, token block)
+      // (expert, token block); the down GEMM may read them by TMA
+      asm volatile("fence.proxy.async.global;" ::: "memory");
       __threadfence();
       epi_sync();
       if (leader) atomicAdd(p.ready + sg.ready_idx, 1);
@@ -714,7 +748,7 @@ template <bool kFp4>
 __global__ void __launch_bounds__(kFp4 ? kGemmThreadsFp4 : kGemmThreads, 1)
     moe_experts_kernel(const __grid_constant__ CUtensorMap tm_gu, const __grid_constant__ CUtensorMap tm_gu_sh,
                        const __grid_constant__ CUtensorMap tm_dn, const __grid_constant__ CUtensorMap tm_dn_sh,
-                       const __grid_constant__ GemmParams p) {
+                       const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem sm;
   // [control words | stages]: the control block comes first so that the
@@ -764,6 +798,7 @@ __global__ void __launch_bounds__(kFp4 ? kGemmThreadsFp4 : kGemmThreads, 1)
     tma_prefetch_desc(&tm_gu_sh);
     tma_prefetch_desc(&tm_dn);
     tma_prefetch_desc(&tm_dn_sh);
+    if (p.h_tma) tma_prefetch_desc(&tm_h);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, p.tmem_cols);
@@ -826,8 +861,8 @@ __global__ void __launch_bounds__(kFp4 ? kGemmThreadsFp4 : kGemmThreads, 1)
     // copies kept in flight before arriving; below the stage count, so the
     // stage this warp waits to refill never depends on an arrival it holds
     const int lag = kGatherLag < sm.S - 1 ? kGatherLag : sm.S - 1;
-    if (gather<0, kFp4>(sm, p, ng, bs[0], es[0], gs[0], ring, pending, arr_stage, lag, p.status))
-      gather<1, kFp4>(sm, p, ng, bs[1], es[1], gs[1], ring, pending, arr_stage, lag, p.status);
+    if (gather<0, kFp4>(sm, p, ng, bs[0], es[0], gs[0], ring, pending, arr_stage, lag, &tm_h, p.status))
+      gather<1, kFp4>(sm, p, ng, bs[1], es[1], gs[1], ring, pending, arr_stage, lag, &tm_h, p.status);
     cp_async_wait<0>();
     fence_proxy_async();
     while (pending > 0) {
@@ -919,8 +954,8 @@ cudaError_t launch_fp4_scales(const uint8_t* gu_s, const uint8_t* dn_s, int E, i
 }
 
 cudaError_t launch_experts(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, const CUtensorMap& tm_dn,
-                           const CUtensorMap& tm_dn_sh, const GemmParams& p, int grid, size_t smem_bytes,
-                           cudaStream_t s, bool fp4) {
+                           const CUtensorMap& tm_dn_sh, const CUtensorMap& tm_h, const GemmParams& p, int grid,
+                           size_t smem_bytes, cudaStream_t s, bool fp4) {
   auto kern = fp4 ? moe_experts_kernel<true> : moe_experts_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem_bytes));
@@ -935,7 +970,7 @@ cudaError_t launch_experts(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, p);
+  return cudaLaunchKernelEx(&cfg, kern, tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, tm_h, p);
 }
 
 cudaError_t launch_combine(const float* out_ws, const int32_t* pair_pos, int T, int K, int H, int has_shared,

@@ -133,6 +133,7 @@ struct GemmParams {
   const uint8_t* gu_scale;     // [E,2I,H/32]
   const uint8_t* dn_scale;     // [E,H,I/32]
   int I, E;                    // routed experts' I, expert count
+  int h_tma;                   // the down GEMM loads h rows by TMA (I, Is multiples of 64)
 };
 
 // Routing recipe as the selection code reads it (score_fn 0 softmax,
@@ -230,8 +231,8 @@ cudaError_t launch_select_from_logits(const float* logits, int T, int E, int K, 
 cudaError_t launch_permute(const int32_t* idx, int T, int K, int E, int32_t* counts, int32_t* offsets,
                            int32_t* sorted_pair, int32_t* pair_pos, cudaStream_t s);
 cudaError_t launch_experts(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, const CUtensorMap& tm_dn,
-                           const CUtensorMap& tm_dn_sh, const GemmParams& p, int grid, size_t smem_bytes,
-                           cudaStream_t s, bool fp4);
+                           const CUtensorMap& tm_dn_sh, const CUtensorMap& tm_h, const GemmParams& p, int grid,
+                           size_t smem_bytes, cudaStream_t s, bool fp4);
 // FP4 block scales re-laid into 512-byte (expert, tile, k-block) blocks.
 cudaError_t launch_fp4_scales(const uint8_t* gu_s, const uint8_t* dn_s, int E, int H, int I, uint8_t* out,
                               cudaStream_t s);
