@@ -380,6 +380,8 @@ def run_gpu(args, cfg, rank, world):
         launched, timed = 1, {"fused": 1}
     else:
         launched = 3 if (cfg.K > 1 or cfg.shared_I > 0) else 2
+        if cfg.T > 1024:  # the router's logits by a separate GEMM launch
+            launched += 1
         timed = {n: k for k, n in enumerate(["router", "experts", "combine"][:launched])}
     per_kernel = {n: float(np.mean([e[2 * k].elapsed_time(e[2 * k + 1]) for e in evs])) * 1e3  # us
                   for n, k in timed.items()}

@@ -538,7 +538,22 @@ moe_status ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf16* g
     rp.status = status;
   }
   record_event_on(0, stream);
-  cudaError_t e = launch_route(rp, L.rg.tb, stream);
+  cudaError_t e = cudaSuccess;
+  int tb = L.rg.tb;
+  if (T > 1024 && !fp4) {
+    // many tokens: the logits by a tiled CUDA-core GEMM (enough 64 x 64
+    // tiles to fill the SMs only from about a thousand tokens on), then the
+    // router launch only selects, permutes and builds the work list (one
+    // CTA per 8 tokens)
+    e = launch_logits_gemm(x, gate, sh_gate, router_bias, T, H, E, rp.logits, rp.sh_logit, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    rp.logits_given = 1;
+    rp.fold_sh = 0;
+    rp.n_eb = 1;
+    tb = 8;
+    rp.n_tb = ceil_div(T, tb);
+  }
+  e = launch_route(rp, tb, stream);
   record_event_on(1, stream);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 

@@ -177,6 +177,7 @@ struct RouteParams {
   int32_t* zero_ptr;           // GEMM tile counters cleared by this launch
   int zero_count;
   int fp4;                     // routed experts are FP4: their k-blocks cost less
+  int logits_given;            // logits (and sh_logit) were computed by logits_gemm_kernel: route only
   uint16_t* xh;                // [T,H] f16 copy of x written for FP4 experts (nullable)
   int32_t* status;             // range errors of that copy
 };
@@ -224,6 +225,10 @@ constexpr int kSliceCtrlBytes = 4096;  // control block at the start of shared m
 
 // launchers (route.cu, gemm.cu, combine.cu); return cudaError_t
 cudaError_t launch_route(const RouteParams& p, int tb, cudaStream_t s);
+// Tiled CUDA-core logits GEMM for many tokens (the router's first step).
+cudaError_t launch_logits_gemm(const uint16_t* x, const uint16_t* gate, const uint16_t* sh_gate,
+                               const float* router_bias, int T, int H, int E, float* logits, float* sh_logit,
+                               cudaStream_t s);
 cudaError_t launch_select_from_logits(const float* logits, int T, int E, int K, const float* expert_bias,
                                       int score_fn, int n_group, int topk_group, int group_topn,
                                       int renorm, float eps, float scale, int32_t* idx, float* w,

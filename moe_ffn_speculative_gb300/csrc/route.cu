@@ -374,6 +374,19 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
     const int gid = (blockIdx.y * gridDim.x + blockIdx.x) * kRouteThreads + threadIdx.x;
     for (int i = gid; i < p.zero_count; i += nthr) p.zero_ptr[i] = 0;
   }
+  const int t0 = tbi * TB;
+  const SelCfg sel{p.E, p.K, p.score_fn, p.n_group, p.topk_group, p.group_topn, p.renorm, p.eps, p.scale,
+                   p.expert_bias};
+  if (p.logits_given) {
+    // the logits (and the shared-gate logit) come from logits_gemm_kernel:
+    // warp w routes token t0 + w
+    if (warp < TB && t0 + warp < p.T) {
+      const int tok = t0 + warp;
+      select_token<NJ, false>(p.logits + static_cast<size_t>(tok) * p.E, sel,
+                              p.idx + static_cast<size_t>(tok) * p.K, p.w + static_cast<size_t>(tok) * p.K);
+      if (lane == 0 && p.sh_w) p.sh_w[tok] = p.sh_gate ? 1.f / (1.f + expf(-__ldcg(p.sh_logit + tok))) : 1.f;
+    }
+  } else {
   // ---- logits block
   const int quad = warp / p.hsplit, hs = warp % p.hsplit;
   const int e0 = (ebi * p.quads + quad) * 4;
@@ -385,7 +398,6 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
     ev[q] = quad < p.quads && e < E_tot;
     rows[q] = e < p.E ? p.gate + static_cast<size_t>(e) * p.H : p.sh_gate;
   }
-  const int t0 = tbi * TB;
   const int hs_len = ceil_div(ceil_div(p.H, p.hsplit), 8) * 8;
   const int h_lo = hs * hs_len;
   const int h_hi = min(p.H, h_lo + hs_len);
@@ -492,8 +504,6 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
       if (p.n_eb == 1) s_log[t][e] = v;
     }
   }
-  const SelCfg sel{p.E, p.K, p.score_fn, p.n_group, p.topk_group, p.group_topn, p.renorm, p.eps, p.scale,
-                   p.expert_bias};
   if (p.n_eb == 1) {
     // this block holds every expert's logit of its tokens: select from shared memory
     __syncthreads();
@@ -533,6 +543,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
       }
     }
   }
+  }  // logits computed here
   if (!p.do_permute) return;
   __threadfence();
   __syncthreads();
@@ -547,6 +558,74 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
   __threadfence();
   permute_block(p.idx, p.T, p.K, p.E, p.counts, p.offsets, p.sorted_pair, p.pair_pos, p.groups, p.header, p.H,
                 p.I, p.Is, p.n_max, s_cnt, s_cur, s_buf, s_wc, p.spans, p.span_groups, p.grid, p.fp4 != 0);
+}
+
+// logits = x . gate^T (+ router_bias) for many tokens: a CTA computes a
+// 64-token x 64-expert tile with x and gate staged through shared memory as
+// fp32, each thread a 4 x 4 block accumulated over H in increasing order
+// (fp32 fused multiply-adds of the exact bf16 products).  Column E is the
+// shared-expert gate when sh_gate is given (-> sh_logit).
+constexpr int kLgBM = 64, kLgBN = 64, kLgBK = 32;
+
+__global__ void __launch_bounds__(256) logits_gemm_kernel(const uint16_t* __restrict__ x,
+                                                          const uint16_t* __restrict__ gate,
+                                                          const uint16_t* __restrict__ sh_gate,
+                                                          const float* __restrict__ router_bias, int T, int H, int E,
+                                                          float* __restrict__ logits, float* __restrict__ sh_logit) {
+  __shared__ __align__(16) float As[kLgBK][kLgBM + 4];
+  __shared__ __align__(16) float Bs[kLgBK][kLgBN + 4];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int t0 = blockIdx.x * kLgBM, e0 = blockIdx.y * kLgBN;
+  const int E_tot = E + (sh_gate ? 1 : 0);
+  // loader: row lr of both tiles, 8 consecutive h at lc
+  const int lr = tid >> 2, lc = (tid & 3) * 8;
+  const int tok = t0 + lr, ex = e0 + lr;
+  const uint16_t* xrow = tok < T ? x + static_cast<size_t>(tok) * H : nullptr;
+  const uint16_t* grow = ex < E ? gate + static_cast<size_t>(ex) * H : (ex < E_tot ? sh_gate : nullptr);
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  uint4 xv = (xrow && lc < H) ? ldg128(xrow + lc) : zero;
+  uint4 gv = (grow && lc < H) ? ldg128(grow + lc) : zero;
+  for (int h0 = 0; h0 < H; h0 += kLgBK) {
+    __syncthreads();  // the previous chunk is read
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      As[lc + 2 * i][lr] = bf_lo(xw[i]);
+      As[lc + 2 * i + 1][lr] = bf_hi(xw[i]);
+      Bs[lc + 2 * i][lr] = bf_lo(gw[i]);
+      Bs[lc + 2 * i + 1][lr] = bf_hi(gw[i]);
+    }
+    __syncthreads();
+    const int hn = h0 + kLgBK + lc;  // the next chunk's loads overlap this chunk's products
+    xv = (xrow && hn < H) ? ldg128(xrow + hn) : zero;
+    gv = (grow && hn < H) ? ldg128(grow + hn) : zero;
+#pragma unroll
+    for (int k = 0; k < kLgBK; ++k) {
+      const float4 a = *reinterpret_cast<const float4*>(&As[k][ty * 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&Bs[k][tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) logits[static_cast<size_t>(t) * E + e] = acc[i][j] + (router_bias ? __ldg(router_bias + e) : 0.f);
+      else if (e < E_tot) sh_logit[t] = acc[i][j];
+    }
+  }
 }
 
 template <int NJ>
@@ -568,6 +647,19 @@ __global__ void __launch_bounds__(kRouteThreads) permute_kernel(const int32_t* i
   permute_block(idx, T, K, E, counts, offsets, sorted_pair, pair_pos, nullptr, nullptr, 0, 0, 0, 1, s_cnt, s_cur,
                 s_buf, s_wc, nullptr, nullptr, 0, false);
 }
+
+}  // namespace
+
+cudaError_t launch_logits_gemm(const uint16_t* x, const uint16_t* gate, const uint16_t* sh_gate,
+                               const float* router_bias, int T, int H, int E, float* logits, float* sh_logit,
+                               cudaStream_t s) {
+  const int E_tot = E + (sh_gate ? 1 : 0);
+  dim3 grid(ceil_div(T, kLgBM), ceil_div(E_tot, kLgBN));
+  logits_gemm_kernel<<<grid, 256, 0, s>>>(x, gate, sh_gate, router_bias, T, H, E, logits, sh_logit);
+  return cudaGetLastError();
+}
+
+namespace {
 
 int nj_for(int E) {
   const int nj = ceil_div(E, 32);

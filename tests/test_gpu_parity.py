@@ -171,6 +171,11 @@ SMALL = {
                                                shared_I=128, seed=9),
     "single_expert_dense": S.LayerConfig("r6", T=20, H=128, E=1, I=64, K=1, route_scale=2.0, seed=10),
     "one_token": S.LayerConfig("r7", T=1, H=64, E=8, I=32, K=2, shared_I=32, seed=11),
+    # > 1024 tokens (the tiled logits GEMM) with H not a multiple of its
+    # 32-wide chunks, router bias and the shared-expert gate as one more
+    # GEMM column
+    "many_tokens_gated_ragged_h": S.LayerConfig("r9", T=1100, H=136, E=12, I=64, K=2, shared_I=64,
+                                                shared_gated=True, router_bias_std=0.1, seed=14),
     "wide_tokens_K8": S.LayerConfig("r8", T=300, H=320, E=64, I=160, K=8, score_fn=1, n_group=8, topk_group=4,
                                     expert_bias_std=0.05, shared_I=96, seed=12),
 }
