@@ -23,9 +23,10 @@
 // token rows are gathered once the gate_up tiles that write them signal.
 //
 // Warp roles (224 threads): warp 0 issues the weight TMA loads, warp 1
-// allocates TMEM and issues the MMAs, warp 2 gathers the token rows with
-// cp.async into the 128-byte-swizzled B tile, warps 3..6 drain TMEM in the
-// epilogue (SwiGLU for gate_up; routing weight and store for down).
+// allocates TMEM and issues the MMAs, warp 2 fills the 128-byte-swizzled B
+// tile (gate_up: the expert's token rows of x by cp.async; down: its rows of
+// h, consecutive, by TMA), warps 3..6 drain TMEM in the epilogue (SwiGLU for
+// gate_up; routing weight and store for down).
 //
 // FP4 routed experts (SpecForge PR #1073, commit note on the official
 // checkpoint's formats: two e2m1 codes per byte along the input, low nibble
