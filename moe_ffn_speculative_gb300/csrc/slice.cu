@@ -333,14 +333,28 @@ __device__ __forceinline__ int pass_kb(const Pass& ps, int q) {
   return ps.ka + (k < ps.kn ? k : k - ps.kn);
 }
 
-__device__ void unit_produce(const SliceParams& p, const SliceSmem& sm, const Unit& u, const CUtensorMap* tm_gu,
-                             const CUtensorMap* tm_gu_sh, const CUtensorMap* tm_dn, const CUtensorMap* tm_dn_sh,
-                             const CUtensorMap* tm_x) {
-  Ring ring;
+// The loads of gate_up k-block kb into its (free) stage: the slice's gate and
+// up rows and every token's x.
+__device__ __forceinline__ void unit_load_gu(const SliceParams& p, const SliceSmem& sm, const Unit& u,
+                                             const CUtensorMap* tm_gu, const CUtensorMap* tm_gu_sh,
+                                             const CUtensorMap* tm_x, int kb, int stage) {
   const CUtensorMap* gu = u.shared ? tm_gu_sh : tm_gu;
   const int zg = u.shared ? 0 : 2 * u.e;
-  const uint32_t tx = 2 * kTileBytesA + sm.b_bytes;
-  int kb = 0;
+  uint8_t* st = sm.base + stage * 2 * kTileBytesA;
+  uint64_t* bar = &sm.full[stage];
+  mbar_arrive_expect_tx(bar, 2 * kTileBytesA + sm.b_bytes);
+  tma_load_3d(st, gu, bar, kb * kBlockK, u.s * kHalfRows, zg);                    // gate rows of the slice
+  tma_load_3d(st + kTileBytesA, gu, bar, kb * kBlockK, u.s * kHalfRows, zg + 1);  // up rows
+  tma_load_2d(sm.bbase + stage * sm.b_bytes, tm_x, bar, kb * kBlockK, 0);         // every token
+}
+
+// k-blocks [0, kb_first) were issued into the fresh ring by the prologue.
+__device__ void unit_produce(const SliceParams& p, const SliceSmem& sm, const Unit& u, const CUtensorMap* tm_gu,
+                             const CUtensorMap* tm_gu_sh, const CUtensorMap* tm_dn, const CUtensorMap* tm_dn_sh,
+                             const CUtensorMap* tm_x, int kb_first) {
+  Ring ring;
+  for (int i = 0; i < kb_first; ++i) ring.next(sm.S);
+  int kb = kb_first;
   for (; kb < u.nkb; ++kb) {
     // an expert no token picked stops streaming once the routing is known
     if (!u.shared && mbar_test_wait(sm.routed, 0) && *sm.n_e == 0) break;
@@ -348,12 +362,7 @@ __device__ void unit_produce(const SliceParams& p, const SliceSmem& sm, const Un
       record_failure(p.status, sm.abort_flag, kInfoEmpty);
       break;
     }
-    uint8_t* st = sm.base + ring.stage * 2 * kTileBytesA;
-    uint64_t* bar = &sm.full[ring.stage];
-    mbar_arrive_expect_tx(bar, tx);
-    tma_load_3d(st, gu, bar, kb * kBlockK, u.s * kHalfRows, zg);                    // gate rows of the slice
-    tma_load_3d(st + kTileBytesA, gu, bar, kb * kBlockK, u.s * kHalfRows, zg + 1);  // up rows
-    tma_load_2d(sm.bbase + ring.stage * sm.b_bytes, tm_x, bar, kb * kBlockK, 0);    // every token
+    unit_load_gu(p, sm, u, tm_gu, tm_gu_sh, tm_x, kb, ring.stage);
     ring.next(sm.S);
   }
   if (kb < u.nkb) {
@@ -795,16 +804,10 @@ __global__ void __launch_bounds__(kSliceThreads, 1)
   const int bid = static_cast<int>(blockIdx.x);
   const bool is_unit = bid < p.n_units;
   const Unit u = make_unit(p, bid);
-  // Counter sets alternate between forwards: the previous forward flipped
-  // the parity word as it ended; this one clears the set the previous one
-  // used, which the next one will use.
-  const int par = *reinterpret_cast<const volatile int32_t*>(p.sync) & 1;
-  sm.ss = p.sync + 1 + par * p.set_words;
-  sm.ready = sm.ss + kSliceSyncWords + p.n_mt;
-  if (bid == static_cast<int>(gridDim.x) - 1) {
-    int32_t* other = p.sync + 1 + (par ^ 1) * p.set_words;
-    for (int i = threadIdx.x; i < p.set_words; i += blockDim.x) other[i] = 0;
-  }
+  sm.b_bytes = static_cast<uint32_t>(p.n_tok) * 128u;
+  sm.S = min(8, p.stage_space / static_cast<int>(2 * kTileBytesA + sm.b_bytes));
+  sm.bbase = sm.base + sm.S * 2 * kTileBytesA;
+  int kb_first = 0;  // gate_up k-blocks issued by the prologue (thread 0 is the producer)
   if (threadIdx.x == 0) {
     for (int s = 0; s < 8; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -824,6 +827,22 @@ __global__ void __launch_bounds__(kSliceThreads, 1)
     *sm.grp_cnt = 0;
     fence_barrier_init();
     fence_proxy_async();
+    if (is_unit) {
+      // the first ring-full of weight loads goes out before the rest of the
+      // prologue (the counter-set read, TMEM allocation, the block barrier)
+      kb_first = min(sm.S, u.nkb);
+      for (int kb = 0; kb < kb_first; ++kb) unit_load_gu(p, sm, u, &tm_gu, &tm_gu_sh, &tm_x, kb, kb);
+    }
+  }
+  // Counter sets alternate between forwards: the previous forward flipped
+  // the parity word as it ended; this one clears the set the previous one
+  // used, which the next one will use.
+  const int par = *reinterpret_cast<const volatile int32_t*>(p.sync) & 1;
+  sm.ss = p.sync + 1 + par * p.set_words;
+  sm.ready = sm.ss + kSliceSyncWords + p.n_mt;
+  if (bid == static_cast<int>(gridDim.x) - 1) {
+    int32_t* other = p.sync + 1 + (par ^ 1) * p.set_words;
+    for (int i = threadIdx.x; i < p.set_words; i += blockDim.x) other[i] = 0;
   }
   const bool works = is_unit || u.ni > 0;
   if (works && warp == 0 && lane == 0) {
@@ -847,11 +866,8 @@ __global__ void __launch_bounds__(kSliceThreads, 1)
   if (!is_unit && bid - p.n_units < p.n_rcta) route_tokens(p, sm, bid - p.n_units);
   if (works) {
     const uint32_t tmem = *sm.tmem_slot;
-    sm.b_bytes = static_cast<uint32_t>(p.n_tok) * 128u;
-    sm.S = min(8, p.stage_space / static_cast<int>(2 * kTileBytesA + sm.b_bytes));
-    sm.bbase = sm.base + sm.S * 2 * kTileBytesA;
     if (warp == 0) {
-      if (lane == 0) unit_produce(p, sm, u, &tm_gu, &tm_gu_sh, &tm_dn, &tm_dn_sh, &tm_x);
+      if (lane == 0) unit_produce(p, sm, u, &tm_gu, &tm_gu_sh, &tm_dn, &tm_dn_sh, &tm_x, kb_first);
     } else if (warp == 1) {
       if (lane == 0) unit_mma(p, sm, u, tmem);
     } else if (warp == 2) {
