@@ -140,29 +140,63 @@ __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* 
       if (act && lane == leader) wc[ev] = static_cast<uint16_t>(bpos + __popc(peers));
       __syncwarp();
     }
-  } else if (warp == 0) {
-    // inputs too large to stage: one warp scatters every pair in order,
-    // with cursors in s_wc's place (s_cnt + s_cur give the starts)
-    for (int base = 0; base < TK; base += 32) {
-      const int q = base + lane;
-      const int ev = q < TK ? __ldcg(idx + q) : -1;
-      const bool act = static_cast<unsigned>(ev) < static_cast<unsigned>(E);
-      const uint32_t peers = __match_any_sync(0xffffffffu, act ? ev : -1 - lane);
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      const int leader = __ffs(peers) - 1;
-      int bpos = (act && lane == leader) ? s_cur[ev] : 0;
-      bpos = __shfl_sync(0xffffffffu, bpos, leader);
-      if (act) {
-        sorted_pair[bpos + rank] = q;
-        pair_pos[q] = bpos + rank;
+  } else {
+    // inputs too large to stage at once: chunks of kPermStaged ids in order,
+    // each scattered like the staged case by all warps (a warp's rows of an
+    // expert follow those of the warps before it and of the chunks before);
+    // the warps' cursors count from the expert's rows so far (16 bits hold a
+    // chunk), s_cur advances by each chunk's counts
+    for (int c0 = 0; c0 < TK; c0 += kPermStaged) {
+      const int cn = min(kPermStaged, TK - c0);
+      __syncthreads();  // the previous chunk is scattered and counted in s_cur
+      for (int q = tid; q < cn; q += blockDim.x) s_idx[q] = __ldcg(idx + c0 + q);
+      for (int q = tid; q < kPermWarps * E; q += blockDim.x) s_wc[q] = 0;
+      __syncthreads();
+      const int ch = (cn + kPermWarps - 1) / kPermWarps;
+      const int q0 = warp * ch, q1 = min(cn, q0 + ch);
+      for (int base = q0; base < q1; base += 32) {
+        const int q = base + lane;
+        const int ev = q < q1 ? s_idx[q] : -1;
+        const bool act = static_cast<unsigned>(ev) < static_cast<unsigned>(E);
+        const uint32_t peers = __match_any_sync(0xffffffffu, act ? ev : -1 - lane);
+        if (act && lane == __ffs(peers) - 1) wc[ev] = static_cast<uint16_t>(wc[ev] + __popc(peers));
+        __syncwarp();
       }
-      __syncwarp();
-      if (act && lane == leader) s_cur[ev] = bpos + __popc(peers);
-      __syncwarp();
+      __syncthreads();
+      for (int e = tid; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < kPermWarps; ++w) {
+          const int c = s_wc[w * E + e];
+          s_wc[w * E + e] = static_cast<uint16_t>(run);
+          run += c;
+        }
+      }
+      __syncthreads();
+      for (int base = q0; base < q1; base += 32) {
+        const int q = base + lane;
+        const int ev = q < q1 ? s_idx[q] : -1;
+        const bool act = static_cast<unsigned>(ev) < static_cast<unsigned>(E);
+        const uint32_t peers = __match_any_sync(0xffffffffu, act ? ev : -1 - lane);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        const int leader = __ffs(peers) - 1;
+        int rel = (act && lane == leader) ? static_cast<int>(wc[ev]) : 0;
+        rel = __shfl_sync(0xffffffffu, rel, leader);
+        if (act) {
+          const int pos = s_cur[ev] + rel + rank;
+          sorted_pair[pos] = c0 + q;
+          pair_pos[c0 + q] = pos;
+        }
+        __syncwarp();
+        if (act && lane == leader) wc[ev] = static_cast<uint16_t>(rel + __popc(peers));
+        __syncwarp();
+      }
+      __syncthreads();
+      // the last warp's cursor ends at the chunk's count of the expert
+      for (int e = tid; e < E; e += blockDim.x) s_cur[e] += s_wc[(kPermWarps - 1) * E + e];
     }
   }
   __syncthreads();
-  if (!staged) {  // the serial scatter advanced s_cur to the ends: back to the starts
+  if (!staged) {  // the chunks advanced s_cur to the ends: back to the starts
     for (int e = tid; e < E; e += blockDim.x) s_cur[e] -= s_cnt[e];
     __syncthreads();
   }
@@ -561,11 +595,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
 }
 
 // logits = x . gate^T (+ router_bias) for many tokens: a CTA computes a
-// 64-token x 64-expert tile with x and gate staged through shared memory as
-// fp32, each thread a 4 x 4 block accumulated over H in increasing order
+// 128-token x 64-expert tile with x and gate staged through shared memory as
+// fp32, each thread an 8 x 4 block accumulated over H in increasing order
 // (fp32 fused multiply-adds of the exact bf16 products).  Column E is the
 // shared-expert gate when sh_gate is given (-> sh_logit).
-constexpr int kLgBM = 64, kLgBN = 64, kLgBK = 32;
+constexpr int kLgBM = 128, kLgBN = 64, kLgBK = 32;
 
 __global__ void __launch_bounds__(256) logits_gemm_kernel(const uint16_t* __restrict__ x,
                                                           const uint16_t* __restrict__ gate,
@@ -577,47 +611,54 @@ __global__ void __launch_bounds__(256) logits_gemm_kernel(const uint16_t* __rest
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int t0 = blockIdx.x * kLgBM, e0 = blockIdx.y * kLgBN;
   const int E_tot = E + (sh_gate ? 1 : 0);
-  // loader: row lr of both tiles, 8 consecutive h at lc
+  // loader: x rows lr and lr + 64, gate row lr; 8 consecutive h at lc
   const int lr = tid >> 2, lc = (tid & 3) * 8;
-  const int tok = t0 + lr, ex = e0 + lr;
-  const uint16_t* xrow = tok < T ? x + static_cast<size_t>(tok) * H : nullptr;
+  const uint16_t* xrow0 = t0 + lr < T ? x + static_cast<size_t>(t0 + lr) * H : nullptr;
+  const uint16_t* xrow1 = t0 + lr + 64 < T ? x + static_cast<size_t>(t0 + lr + 64) * H : nullptr;
+  const int ex = e0 + lr;
   const uint16_t* grow = ex < E ? gate + static_cast<size_t>(ex) * H : (ex < E_tot ? sh_gate : nullptr);
-  float acc[4][4];
+  float acc[8][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
   const uint4 zero = make_uint4(0, 0, 0, 0);
-  uint4 xv = (xrow && lc < H) ? ldg128(xrow + lc) : zero;
+  uint4 xv0 = (xrow0 && lc < H) ? ldg128(xrow0 + lc) : zero;
+  uint4 xv1 = (xrow1 && lc < H) ? ldg128(xrow1 + lc) : zero;
   uint4 gv = (grow && lc < H) ? ldg128(grow + lc) : zero;
   for (int h0 = 0; h0 < H; h0 += kLgBK) {
     __syncthreads();  // the previous chunk is read
-    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    const uint32_t x0w[4] = {xv0.x, xv0.y, xv0.z, xv0.w}, x1w[4] = {xv1.x, xv1.y, xv1.z, xv1.w};
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      As[lc + 2 * i][lr] = bf_lo(xw[i]);
-      As[lc + 2 * i + 1][lr] = bf_hi(xw[i]);
+      As[lc + 2 * i][lr] = bf_lo(x0w[i]);
+      As[lc + 2 * i + 1][lr] = bf_hi(x0w[i]);
+      As[lc + 2 * i][lr + 64] = bf_lo(x1w[i]);
+      As[lc + 2 * i + 1][lr + 64] = bf_hi(x1w[i]);
       Bs[lc + 2 * i][lr] = bf_lo(gw[i]);
       Bs[lc + 2 * i + 1][lr] = bf_hi(gw[i]);
     }
     __syncthreads();
     const int hn = h0 + kLgBK + lc;  // the next chunk's loads overlap this chunk's products
-    xv = (xrow && hn < H) ? ldg128(xrow + hn) : zero;
+    xv0 = (xrow0 && hn < H) ? ldg128(xrow0 + hn) : zero;
+    xv1 = (xrow1 && hn < H) ? ldg128(xrow1 + hn) : zero;
     gv = (grow && hn < H) ? ldg128(grow + hn) : zero;
 #pragma unroll
     for (int k = 0; k < kLgBK; ++k) {
-      const float4 a = *reinterpret_cast<const float4*>(&As[k][ty * 4]);
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[k][ty * 8]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[k][ty * 8 + 4]);
       const float4 b = *reinterpret_cast<const float4*>(&Bs[k][tx * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty * 4 + i;
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + ty * 8 + i;
     if (t >= T) continue;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
