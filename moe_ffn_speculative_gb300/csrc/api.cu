@@ -372,6 +372,15 @@ moe_status moe_route(const moe_bf16* x, int T, int H, const moe_bf16* gate, cons
   p.tb_counter = reinterpret_cast<int32_t*>(w + o_cnt);
   p.glob_counter = p.tb_counter + ceil_div(T, 4);
   p.do_permute = 0;
+  if (T > 1024) {
+    // many tokens: the logits by the tiled CUDA-core GEMM, then selection only
+    const cudaError_t e = launch_logits_gemm(x, gate, nullptr, router_bias, T, H, E, p.logits, nullptr, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    p.logits_given = 1;
+    p.n_eb = 1;
+    p.n_tb = ceil_div(T, 8);
+    return cuda_status(launch_route(p, 8, stream));
+  }
   return cuda_status(launch_route(p, rg.tb, stream));
 }
 
