@@ -219,15 +219,18 @@ struct Layout {
 Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sms) {
   Layout L;
   L.rg = router_geometry(T, E, gated, sms);
-  // Token tile width: every token of a decode-sized forward in one tile;
-  // above 128 tokens about four times an expert's mean load, between 64 and
-  // 128, so that routed experts rarely need a second tile while the shared
-  // expert's T tokens (several narrower tiles) neither size every stage of
-  // the ring for 256 columns nor take the second TMEM accumulator buffer
-  // (two buffers of 2 x 128 columns fill the 512).
+  // Token tile width: every token of a decode-sized forward in one tile.
+  // Above 128 tokens, when an expert's mean load leaves room in 128 columns,
+  // about four times that load (between 64 and 128), so that routed experts
+  // rarely need a second tile while the shared expert's T tokens (several
+  // narrower tiles) neither size every stage of the ring for 256 columns nor
+  // take the second TMEM accumulator buffer (two buffers of 2 x 128 columns
+  // fill the 512).  Heavily loaded experts (a dense layer) keep one tile of
+  // up to 256 columns: a second tile would stream their weights twice.
   int nm = ((T + 15) / 16) * 16;
-  if (T > 128) {
-    const long long load4 = (4ll * T * K + E - 1) / E;
+  const long long mean = (static_cast<long long>(T) * K + E - 1) / E;
+  if (T > 128 && mean + 32 <= 128) {
+    const long long load4 = 4 * mean;
     const int cap = static_cast<int>(load4 < 64 ? 64 : (load4 > 128 ? 128 : ((load4 + 15) / 16) * 16));
     if (cap < nm) nm = cap;
   }
