@@ -284,8 +284,6 @@ def run_gpu(args, cfg, rank, world):
     W = max(3, args.warmup if args.warmup is not None else 50)
     rec = ops.Recipe.from_config(cfg)
     fp4 = cfg.expert_format == "fp4"
-    if fp4:
-        raise SystemExit("the FP4 expert kernel is disabled in this build (moe_ffn_forward_fp4 refuses)")
     ops.set_schedule({"auto": ops.SCHEDULE_AUTO, "stream_k": ops.SCHEDULE_STREAM_K,
                       "slice": ops.SCHEDULE_SLICE}[args.schedule])
     # FP4 routed experts always run the stream-K schedule

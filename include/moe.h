@@ -274,11 +274,7 @@ MOE_API moe_status moe_fp4_prepare_scales(const uint8_t* w_gate_up_s, const uint
  * output, carried as an f16 hi + lo pair); anything outside is recorded as
  * MOE_ERR_DEVICE_RANGE in the workspace status (moe_get_device_status).  x
  * values below 2^-17 in magnitude round to the f16 grid (error < 2^-25).
- * STATUS: the FP4 expert kernel is built but not launched: it faulted the GPU
- * on the full-size DeepSeek-V4.1 draft layer (E=128, H=4096, I=2304, T=72)
- * while matching the oracle on small layers, and stays disabled until that
- * cause is found.  Every call with T > 0 returns MOE_ERR_UNSUPPORTED after
- * the argument checks. */
+ * H and I must be multiples of 64 (else MOE_ERR_UNSUPPORTED). */
 MOE_API moe_status moe_ffn_forward_fp4(const moe_bf16* x, int T, int H, int I, const moe_bf16* gate,
                                        const float* router_bias, const float* expert_bias,
                                        const uint8_t* w_gate_up_q, const uint8_t* w_down_q, const void* scales,

@@ -673,10 +673,6 @@ moe_status moe_ffn_forward_fp4(const moe_bf16* x, int T, int H, int I, const moe
   if (!fp4_shape_ok(recipe->num_experts, H, I)) return MOE_ERR_UNSUPPORTED;
   if (T > 0 && (!w_gate_up_q || !w_down_q || !scales)) return MOE_ERR_INVALID_ARG;
   if (T > 0 && scales_bytes < fp4_scales_bytes(recipe->num_experts, H, I)) return MOE_ERR_INVALID_ARG;
-  // The FP4 expert kernel faulted the GPU on the full-size DeepSeek-V4.1
-  // draft layer (E = 128, H = 4096, I = 2304, T = 72) while passing on small
-  // layers; until that cause is found it is not launched.
-  if (T > 0) return MOE_ERR_UNSUPPORTED;
   const Fp4Experts f{w_gate_up_q, w_down_q, static_cast<const uint8_t*>(scales)};
   return ffn_forward(x, T, H, I, gate, router_bias, expert_bias, reinterpret_cast<const moe_bf16*>(w_gate_up_q),
                      reinterpret_cast<const moe_bf16*>(w_down_q), sh_gate_up, sh_down, Is, sh_gate, recipe, ws,

@@ -278,7 +278,22 @@ __device__ bool produce(const Smem& sm, const GemmParams& p, int ngroups, const 
   WeightCursor ld;
   ld.init(p, ngroups, b, e, g);
   Ring pring;  // FP4 code stages
+  // FP4: routed k-blocks advance this warp's A-ring cursor without waiting
+  // on the A ring (only on the deeper code ring), so the cursor can run more
+  // than one phase of an `empty` barrier ahead of the MMAs, where a parity
+  // wait no longer tells the phases apart.  Before the next bf16 k-block the
+  // converter must have taken the last routed one (it waited on that A stage
+  // in order), which brings the cursor back within one phase.
+  int last_ps = -1;
+  uint32_t last_pphase = 0;
   while (ld.valid) {
+    if (kFp4 && ld.sg.expert < 0 && last_ps >= 0) {
+      if (!mbar_wait(&sm.pempty[last_ps], last_pphase, sm.abort_flag)) {
+        record_failure(status, sm.abort_flag, kInfoEmpty);
+        return false;
+      }
+      last_ps = -1;
+    }
     if (kFp4 && ld.sg.expert >= 0) {
       // packed codes and block scales of a routed k-block; the converter
       // warps turn them into the A stage
@@ -296,6 +311,8 @@ __device__ bool produce(const Smem& sm, const GemmParams& p, int ngroups, const 
       const uint8_t* sc = ld.ph == 0 ? p.gu_scale : p.dn_scale;
       bulk_load(sm.sbase + pring.stage * 512, sc + fp4_scale_offset(p, ld.ph, ld.sg.expert, ld.sg.m, ld.sg.k0 + ld.kk),
                 512, bar);
+      last_ps = pring.stage;
+      last_pphase = pring.phase;
       pring.next(sm.SP);
       ld.step();
       ring.next(sm.S);  // the A ring advances for every k-block
@@ -554,8 +571,13 @@ __device__ bool convert(const Smem& sm, const GemmParams& p, int ngroups, const 
       ring.next(sm.S);
       continue;
     }
-    bool ok = mbar_wait(&sm.empty[ring.stage], ring.phase ^ 1u, sm.abort_flag) &&
-              mbar_wait(&sm.pfull[pring.stage], pring.phase, sm.abort_flag);
+    // Codes first: the producer issues them only after its own wait on the
+    // A stage before this one (or, after routed k-blocks, after this warp's
+    // last release), so the MMAs are then at most one phase of this stage's
+    // `empty` barrier behind, which the parity wait needs; bf16 k-blocks
+    // skipped above would otherwise leave this warp several phases ahead.
+    bool ok = mbar_wait(&sm.pfull[pring.stage], pring.phase, sm.abort_flag) &&
+              mbar_wait(&sm.empty[ring.stage], ring.phase ^ 1u, sm.abort_flag);
     if (ok) {
       const uint8_t* cs = sm.pbase + pring.stage * kPackedBytes + r * 32;
       const uint16_t* ss = reinterpret_cast<const uint16_t*>(sm.sbase + pring.stage * 512);
