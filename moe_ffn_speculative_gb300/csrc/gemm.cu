@@ -882,8 +882,11 @@ __global__ void __launch_bounds__(kFp4 ? kGemmThreadsFp4 : kGemmThreads, 1)
     Ring ring;
     int pending = 0, arr_stage = 0;
     // copies kept in flight before arriving; below the stage count, so the
-    // stage this warp waits to refill never depends on an arrival it holds
-    const int lag = kGatherLag < sm.S - 1 ? kGatherLag : sm.S - 1;
+    // stage this warp waits to refill never depends on an arrival it holds.
+    // FP4 k-blocks stream in a quarter of a bf16 one's time: one group in
+    // flight, so that a stage's arrival waits for the MMAs two k-blocks
+    // back rather than the previous one's and two k-blocks' MMAs overlap.
+    const int lag = kFp4 ? 1 : (kGatherLag < sm.S - 1 ? kGatherLag : sm.S - 1);
     if (gather<0, kFp4>(sm, p, ng, bs[0], es[0], gs[0], ring, pending, arr_stage, lag, &tm_h, p.status))
       gather<1, kFp4>(sm, p, ng, bs[1], es[1], gs[1], ring, pending, arr_stage, lag, &tm_h, p.status);
     cp_async_wait<0>();
