@@ -46,8 +46,6 @@ namespace moe {
 namespace {
 
 
-
-
 struct Seg {
   int expert, row_base, count, idim;
   int m, n, k0, len, kb, tile, n_cnt;
@@ -182,7 +180,6 @@ __device__ __forceinline__ void u32_to_f32(const uint32_t (&u)[16], float (&f)[1
 #pragma unroll
   for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(u[i]);
 }
-
 
 
 // The CTA's shared memory: S stages of [A gate|A up or two 128-row output

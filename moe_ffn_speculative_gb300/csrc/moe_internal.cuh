@@ -130,8 +130,8 @@ struct GemmParams {
   // FP4 routed experts (moe_ffn_forward_fp4): codes come through the tensor
   // maps, the e8m0 scales are read here; routed groups multiply in f16
   const uint16_t* xh;          // [T,H] f16 copy of x
-  const uint8_t* gu_scale;     // [E,2I,H/32]
-  const uint8_t* dn_scale;     // [E,H,I/32]
+  const uint8_t* gu_scale;     // prepared scale blocks (moe_fp4_prepare_scales): 512 bytes per
+  const uint8_t* dn_scale;     // (expert, tile, k-block), gate_up blocks first, then down
   int I, E;                    // routed experts' I, expert count
   int h_tma;                   // the down GEMM loads h rows by TMA (I, Is multiples of 64)
 };
