@@ -36,6 +36,15 @@ from moe_ffn_speculative_gb300 import synthetic as S  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "MoE-FFN layer tokens/s at T=72 on 1 GB300"
 UNIT = "tokens/s"
+
+
+def metric_for(cfg) -> str:
+    """The headline metric for the headline layer, else one naming the
+    workload (both arms print the same name for the same workload)."""
+    fp4 = cfg.expert_format == "fp4"
+    if cfg.name == "qwen3_8b_dspark" and cfg.T == 72 and not fp4:
+        return METRIC
+    return f"MoE-FFN layer tokens/s ({cfg.name}{', FP4 experts' if fp4 else ''}, T={cfg.T})"
 CSRC = os.path.join(ROOT, "moe_ffn_speculative_gb300", "csrc")
 # per expert schedule: the dominant kernel, its ncu summary prefix, its source
 KERNELS = {"stream_k": ("moe_experts_kernel", "experts_kernel", "gemm.cu"),
@@ -259,11 +268,13 @@ def run_reference(args, cfg, rank, world):
         cpu_oracle_pass(cfg, host, w64, samples[W + i])
     dt = time.perf_counter() - t0
     value = K * tok_per_step / dt
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": K, "warmup": W,
+    line = {"metric": metric_for(cfg), "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": K, "warmup": W,
             "ms_per_step": dt / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "I": cfg.I, "K": cfg.K,
-                       "shared_I": cfg.shared_I, "tokens_per_step_sample": tok_per_step},
+                       "shared_I": cfg.shared_I,
+                       "routed_experts": "fp4 (e2m1 + e8m0/32)" if cfg.expert_format == "fp4" else "bf16",
+                       "tokens_per_step_sample": tok_per_step},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                              "sample": f"{tok_per_step} of the {cfg.T} tokens per step, fp64 numpy oracle"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -425,8 +436,7 @@ def run_gpu(args, cfg, rank, world):
     if rank != 0:
         return
     line = {
-        "metric": (METRIC if cfg.name == "qwen3_8b_dspark" and cfg.T == 72 and not fp4 else
-                   f"MoE-FFN layer tokens/s ({cfg.name}{', FP4 experts' if fp4 else ''}, T={cfg.T})"),
+        "metric": metric_for(cfg),
         "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms_step,
         "us_per_layer": ms_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
