@@ -1,0 +1,71 @@
+"""bench.py on the host: the algorithmic bytes and FLOPs it divides by, the
+metric names of both arms, and the JSON line of the reference arm (the fp64
+oracle on the host cores), which runs without a GPU."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from moe_ffn_speculative_gb300 import synthetic as S  # noqa: E402
+
+
+# Per-layer bytes and FLOPs of the four decode workloads at their expected
+# touched-expert counts U = E·(1 − (1 − K/E)^T) (fractional there, rounded
+# here), tabulated independently of bench.py; bytes to three or four
+# significant digits, FLOPs to two or three.
+TABLE = [
+    ("qwen3_8b_dspark", 8, 303e6, 2.7e9),
+    ("qwen38_27b_dspark", 388, 6.18e9, 16.2e9),
+    ("dsv3_style", 230, 20.35e9, 57.3e9),
+    ("dsv4_style", 210, 5.30e9, 12.8e9),
+]
+
+
+@pytest.mark.parametrize("name,U,bytes_,flops", TABLE)
+def test_algorithmic_bytes_and_flops_match_the_table(name, U, bytes_, flops):
+    layer_bytes, ex_bytes, fl = bench.algorithmic(S.CONFIGS[name], U)
+    assert abs(layer_bytes / bytes_ - 1) < 5e-3
+    assert abs(fl / flops - 1) < 2e-2
+    # the expert launch reads every touched weight once (and more: x, h, outputs)
+    cfg = S.CONFIGS[name]
+    weights = U * 3 * cfg.I * cfg.H * 2 + 3 * cfg.shared_I * cfg.H * 2
+    assert ex_bytes > weights
+
+
+def test_fp4_weights_count_half_a_byte_and_a_scale_per_32():
+    cfg = S.CONFIGS["dsv41_dspark_draft"]
+    b16, _, _ = bench.algorithmic(cfg, 100)
+    b4, _, _ = bench.algorithmic(cfg.with_(expert_format="fp4"), 100)
+    routed16 = 100 * 3 * cfg.I * cfg.H * 2
+    assert b16 - b4 == pytest.approx(routed16 * (1 - (0.5 + 1 / 32) / 2), rel=1e-6)
+
+
+def test_metric_names():
+    assert bench.metric_for(S.CONFIGS["qwen3_8b_dspark"]) == bench.METRIC
+    assert bench.metric_for(S.CONFIGS["dsv4_style"].with_(T=576)) == "MoE-FFN layer tokens/s (dsv4_style, T=576)"
+    assert "FP4 experts" in bench.metric_for(S.CONFIGS["qwen3_8b_dspark"].with_(expert_format="fp4"))
+
+
+def test_reference_arm_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["higher_is_better"] is True and line["steps"] == 1 and line["warmup"] == 1
+    assert line["value"] > 0 and line["config"]["workload"] == "qwen3_8b_dspark"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
