@@ -6,8 +6,8 @@
  *   1. Router, the score -> select -> routing_weights template of SpecForge
  *      PR #1033 "MoE FFN for DFlash-family drafts: the module", section
  *      "Router": fp32 logits of a linear gate (sglang PR #48763 "[Feat]
- *      dflash: Serve MoE FFN drafts for DFlash and DSpark", commit note
- *      "Router logits go to TopK in fp32"), optionally with a folded router
+ *      dflash: Serve MoE FFN drafts for DFlash and DSpark", commit note on
+ *      the router's fp32 logits), optionally with a folded router
  *      bias added to the logits (SpecForge PR #941 "SGLang draft classes for
  *      the Qwen3.8-27B DSpark MoE drafter", section "What"); softmax, sigmoid
  *      or sqrt(softplus) scores; a selection-only expert bias (SpecForge PR
@@ -24,20 +24,20 @@
  * Conventions (every entry point):
  *   - Every tensor pointer is a DEVICE pointer owned by the caller; tensors are
  *     contiguous, row-major.  bf16 tensors are passed as raw 16-bit words.
- *     Indices are int32 (PR #48763: "int32 ids, as the fused routers emit").
+ *     Indices are int32 (PR #48763: the fused routers' id type).
  *   - Calls are asynchronous on `stream` and never synchronise the host, so a
  *     sequence of them can be captured in a CUDA graph.  The library performs
  *     no device allocation; scratch space is the caller's workspace.
  *   - Argument errors are returned synchronously, before any launch.  Errors
  *     found on the device (a bounded wait that ran out) are recorded in the
  *     workspace's status word and read with moe_get_device_status().
- *   - T == 0 returns MOE_OK and launches nothing (PR #48763: a rank with no
- *     tokens routes an empty top-k output).
+ *   - T == 0 returns MOE_OK and launches nothing (PR #48763: an empty batch gives
+ *     an empty routing).
  *   - x is only read; y must not alias x (PR #48763 fix: the shared expert
  *     must read x before in-place experts overwrite it).
- *   - Requested features are never silently dropped (PR #48763: dropped expert
- *     bias, unapplied routed_scaling_factor): what the kernels cannot do is
- *     refused with MOE_ERR_UNSUPPORTED.
+ *   - Requested features are never silently dropped (PR #48763 fixed an
+ *     ignored expert bias and a routed_scaling_factor that was never applied):
+ *     what the kernels cannot do is refused with MOE_ERR_UNSUPPORTED.
  *   - Limits: 1 <= E <= 1024, 1 <= K <= min(E, 32), H and I multiples of 8,
  *     8 <= H <= 65536, 8 <= I <= 16384, T <= 65536, n_group <= 32 and
  *     divides E, K <= topk_group * (E / n_group).

@@ -29,8 +29,8 @@
 // gate_up; routing weight and store for down).
 //
 // FP4 routed experts (SpecForge PR #1073, commit note on the official
-// checkpoint's formats: two e2m1 codes per byte along the input, low nibble
-// first, one e8m0 scale per 32 inputs): warp 0 streams the packed codes (8 KB
+// checkpoint's formats: each byte packs the e2m1 codes of two consecutive
+// inputs, the even one in its low four bits; 32 inputs share an e8m0 scale): warp 0 streams the packed codes (8 KB
 // per k-block) and the k-block's 512 bytes of block scales into a deeper ring
 // of their own; four more warps (352 threads) expand them with the hardware
 // e2m1 -> f16 conversion, multiply by the scale (exact in f16 for scales in

@@ -26,7 +26,8 @@ Sources (web pages, cited by title and section):
   (sqrtsoftplus, selection-only bias, groups, scaling, clamped SwiGLU, ungated
   shared expert with the same clamp).
 * [P4] SpecForge PR #1073 "MoE drafts: DeepSeek-V4.1's own DSpark draft" --
-  commit notes on the expert bias (shifts the picks, never the weights), on
+  commit notes on the expert bias (it moves which experts are picked, not
+  their weights), on
   select receiving the shifted scores, on the DeepSeek-V4 family (sqrt(softplus)
   scores, always renormalised, route_scale, clamped SwiGLU, one ungated shared
   expert), on the fused gate_up_proj / down_proj expert layout and on the
@@ -124,7 +125,7 @@ def score(logits: np.ndarray, score_fn: int) -> np.ndarray:
 
 def shift(scores: np.ndarray, expert_bias: Optional[np.ndarray]) -> np.ndarray:
     """choice = scores + expert_bias: the bias steers only the selection
-    ([P4] "shifts the top-k picks, never the weights")."""
+    ([P4]: it changes which experts are picked, not their weights)."""
     if expert_bias is None:
         return np.asarray(scores, np.float64).copy()
     return np.asarray(scores, np.float64) + np.asarray(expert_bias, np.float64)[None, :]
@@ -151,8 +152,8 @@ def select_topk(choice: np.ndarray, k: int) -> np.ndarray:
 def group_scores(choice: np.ndarray, n_group: int, group_topn: int) -> np.ndarray:
     """Score of each contiguous expert group: the sum of its ``group_topn``
     largest shifted scores (DeepSeek-V3 group-limited routing, [P2] Router
-    table "select" override; [P3] follow-up "use_grouped_topk /
-    num_expert_group / topk_group")."""
+    table "select" override; [P3] follow-up: the keys use_grouped_topk,
+    num_expert_group and topk_group)."""
     t, e = choice.shape
     g = choice.reshape(t, n_group, e // n_group)
     top = -np.sort(-g, axis=2)[:, :, :group_topn]
@@ -325,8 +326,8 @@ def moe_layer(x, gate, w_gate_up, w_down, recipe: Recipe, router_bias=None,
               expert_bias=None, sh_gate_up=None, sh_down=None, sh_gate=None):
     """The whole layer on small inputs: returns dict(logits, scores, choice,
     idx, weights, counts, offsets, sorted_pair, pair_pos, y).  A token count of
-    0 routes an empty top-k and returns an empty output ([P1] DraftMoE forward:
-    "a rank with no tokens routes an empty top-k output")."""
+    0 routes an empty top-k and returns an empty output ([P1] DraftMoE forward: an empty
+    batch gives an empty routing)."""
     x = np.asarray(x, np.float64)
     t, h = x.shape
     e = recipe.num_experts
@@ -349,10 +350,10 @@ def moe_layer(x, gate, w_gate_up, w_down, recipe: Recipe, router_bias=None,
 
 # --------------------------------------------------------------------------
 # FP4 routed experts ([P4] commit note on the DeepSeek-V4.1 export formats:
-# two e2m1 codes per byte along the input dimension, the low nibble first,
-# one e8m0 scale per 32 inputs; [P5] MXFP4 commit note: uint8 codes
+# each byte packs the e2m1 codes of two consecutive inputs, the even one in
+# its low four bits, and 32 inputs share one e8m0 scale; [P5] MXFP4 commit note: uint8 codes
 # [E, N, K//2] and scales [E, N, K//32], output-major).  The layer computes
-# with the exactly dequantized weights ([P4]: import dequantizes to bf16).
+# with the exactly dequantized weights ([P4]: the import turns them into bf16).
 # --------------------------------------------------------------------------
 
 def e2m1_value(code: int) -> float:
