@@ -36,7 +36,7 @@ Sources (web pages, cited by title and section):
   on the resident GPT-OSS loader (MXFP4 codes and scales, uint8,
   output-major).
 
-Readings of points the pages leave open (each also listed in the design doc):
+Readings of points the pages leave open:
 
 * gate/up order inside ``gate_up_proj``: rows [0, I) are the gate (w1), rows
   [I, 2I) the up projection (w3).
