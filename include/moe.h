@@ -112,8 +112,9 @@ MOE_API size_t moe_route_workspace_bytes(int T, int E);
  *   topk_idx    [T,K] int32           descending shifted score, ties -> lower e
  *   topk_w      [T,K] fp32            routing weights
  *   ws          workspace of >= moe_route_workspace_bytes(T, E) bytes,
- *               256-byte aligned, zero-filled before its first use (the
- *               library leaves its counters at zero after every call).
+ *               256-byte aligned, zero-filled before its first use and again
+ *               before a call with another T (the library leaves its counters
+ *               at zero after every call, but where they sit depends on T).
  */
 MOE_API moe_status moe_route(const moe_bf16* x, int T, int H, const moe_bf16* gate,
                      const float* router_bias, const float* expert_bias,
@@ -167,9 +168,12 @@ MOE_API moe_status moe_permute(const int32_t* topk_idx, int T, int K, int E,
                        int32_t* sorted_pair, int32_t* pair_pos,
                        void* ws, size_t ws_bytes, cudaStream_t stream);
 
-/* Workspace bytes for moe_ffn_forward() on the CURRENT device (the size
- * depends on its SM count).  Is = 0 means no shared expert.  Returns 0 for an
- * invalid recipe. */
+/* Workspace bytes for moe_ffn_forward() of exactly T tokens on the CURRENT
+ * device (the size depends on its SM count).  Is = 0 means no shared expert.
+ * Returns 0 for an invalid recipe.  The size is not monotone in T (above 128
+ * tokens the token tile narrows to about four times an expert's mean load):
+ * a workspace meant for every T up to a maximum takes the largest value over
+ * that range. */
 MOE_API size_t moe_ffn_workspace_bytes(int T, int H, int I, int Is, const moe_recipe* recipe);
 
 /* Zero-fill a workspace (required once before its first use). */
@@ -184,8 +188,10 @@ MOE_API moe_status moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t st
  *   sh_down    [H,Is] bf16
  *   sh_gate    [H] bf16 or NULL: g_t = sigmoid(x_t . sh_gate), else g_t = 1
  *   ws         >= moe_ffn_workspace_bytes(T,H,I,Is,recipe) bytes, 256-byte
- *              aligned, zero-filled before its first use; one workspace must
- *              not be used by two calls that may overlap on the GPU.
+ *              aligned, zero-filled before its first use and again before a
+ *              call with another T, H, I, Is or recipe (its self-resetting
+ *              counters sit at offsets that depend on them); one workspace
+ *              must not be used by two calls that may overlap on the GPU.
  *   y          [T,H] bf16 output (round to nearest even from fp32)
  *   topk_idx_out [T,K] int32, topk_w_out [T,K] fp32, counts_out [E] int32:
  *              optional copies of the routing (each may be NULL).

@@ -156,6 +156,10 @@ class Workspace:
     def ptr(self) -> int:
         return self.buf.data_ptr()
 
+    def reset(self, stream=None) -> None:
+        """Zero-fill again (moe_workspace_init), as a call with another shape needs."""
+        _check(lib().moe_workspace_init(self.ptr(), self.nbytes, _stream(stream)), "moe_workspace_init")
+
     def device_status(self, stream=None) -> Tuple[int, int]:
         info = ctypes.c_int32(0)
         st = lib().moe_get_device_status(self.ptr(), _stream(stream), ctypes.byref(info))
@@ -166,6 +170,17 @@ def ffn_workspace_bytes(T: int, H: int, I: int, Is: int, recipe: Recipe) -> int:
     n = lib().moe_ffn_workspace_bytes(T, H, I, Is, ctypes.byref(recipe))
     if n == 0:
         raise MoeError(MOE_ERR_INVALID_ARG, "moe_ffn_workspace_bytes")
+    return n
+
+
+def ffn_workspace_bytes_upto(max_tokens: int, H: int, I: int, Is: int, recipe: Recipe) -> int:
+    """Bytes of a workspace that serves every token count 1..max_tokens: the
+    size for exactly T is not monotone in T (above 128 tokens the token tile
+    narrows to about four times an expert's mean load, shrinking its
+    partial-accumulator region)."""
+    n = 0
+    for T in range(1, max_tokens + 1):
+        n = max(n, ffn_workspace_bytes(T, H, I, Is, recipe))
     return n
 
 
@@ -340,12 +355,20 @@ class MoELayer:
             self.I = tensors["w_down"].shape[2]
         self.Is = 0 if tensors.get("sh_gate_up") is None else tensors["sh_down"].shape[1]
         self.max_tokens = max_tokens
-        self.ws = Workspace(ffn_workspace_bytes(max_tokens, self.H, self.I, self.Is, recipe),
+        self.ws = Workspace(ffn_workspace_bytes_upto(max_tokens, self.H, self.I, self.Is, recipe),
                             tensors["gate"].device)
+        self._last_tokens = None
 
     def forward(self, x, y=None, topk_idx_out=None, topk_w_out=None, counts_out=None, stream=None):
-        if x.shape[0] > self.max_tokens:
+        T = x.shape[0]
+        if T > self.max_tokens:
             raise ValueError("more tokens than the workspace was sized for")
+        if T > 0:
+            # the workspace's self-resetting counters sit at offsets that
+            # depend on the token count: another count starts from zeros
+            if self._last_tokens is not None and T != self._last_tokens:
+                self.ws.reset(stream)
+            self._last_tokens = T
         t = self.t
         if self.fp4:
             return moe_ffn_forward_fp4(x, t["gate"], t["w_gate_up_q"], t["w_down_q"], self.scales, self.recipe,

@@ -4,6 +4,8 @@ hold a known pattern; after each forward (both expert schedules, the
 many-token router path, FP4 routed experts) and after moe_route, the margins
 must be unchanged.  The library is only ever given pointers inside the
 views, so a stray write lands in a margin, never outside this test's memory.
+Last, one layer object reused across token counts (its workspace sized for
+all of them and zero-filled again when the count changes).
 """
 import pytest
 import torch
@@ -123,3 +125,25 @@ def test_route_writes_stay_inside_its_workspace():
         torch.cuda.synchronize()
     assert ws.device_status() == (0, 0)
     assert ws.margins_intact(), "a write outside the router's workspace"
+
+
+def test_layer_reused_across_token_counts():
+    """One MoELayer serves token counts that change its schedule and token
+    tile: 128 tokens take the fused kernel (12 experts and the gated shared
+    expert, untouched experts rare), 9 tokens stream-K with one 16-column
+    tile, 200 tokens stream-K with 80-column tiles (a smaller workspace need
+    than at 128).  Every forward equals that of a layer built for exactly
+    its count."""
+    cfg = S.LayerConfig("reuse", T=200, H=2048, E=12, I=128, K=1, shared_I=128, shared_gated=True,
+                        router_bias_std=0.1, seed=43)
+    d = {k: (None if v is None else v.cuda()) for k, v in S.make_inputs(cfg).items()}
+    rec = ops.Recipe.from_config(cfg)
+    layer = ops.MoELayer(d, rec, max_tokens=cfg.T)
+    for T in (128, 200, 9, 200, 128):
+        x = d["x"][:T].contiguous()
+        y = layer.forward(x)
+        torch.cuda.synchronize()
+        assert layer.ws.device_status() == (0, 0)
+        y_ref = ops.MoELayer(d, rec, max_tokens=T).forward(x)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_ref), f"T={T}"
