@@ -4,6 +4,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "moe.h"
@@ -17,7 +18,7 @@ constexpr int kMaxDevices = 64;
 constexpr size_t kAlign = 256;
 constexpr int kSmemLimit = 232448;  // 227 KB of dynamic shared memory per CTA
 
-int g_sms[kMaxDevices];
+std::atomic<int> g_sms[kMaxDevices];  // SM count per device, filled on first use (0: not yet)
 
 thread_local void* const* t_events = nullptr;
 thread_local int t_nev = 0;
@@ -26,12 +27,14 @@ thread_local int t_schedule = MOE_SCHEDULE_AUTO;
 int device_sms() {
   int d = 0;
   if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return 0;
-  if (g_sms[d] == 0) {
+  int v = g_sms[d].load(std::memory_order_relaxed);
+  if (v == 0) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return 0;
-    g_sms[d] = n < kMaxGrid ? n : kMaxGrid;  // one GEMM CTA per SM, up to the span table's size
+    v = n < kMaxGrid ? n : kMaxGrid;  // one GEMM CTA per SM, up to the span table's size
+    g_sms[d].store(v, std::memory_order_relaxed);
   }
-  return g_sms[d];
+  return v;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
