@@ -46,6 +46,8 @@ def metric_for(cfg) -> str:
     if cfg.name == "qwen3_8b_dspark" and cfg.T == 72 and not fp4:
         return METRIC
     return f"MoE-FFN layer tokens/s ({cfg.name}{', FP4 experts' if fp4 else ''}, T={cfg.T})"
+
+
 CSRC = os.path.join(ROOT, "moe_ffn_speculative_gb300", "csrc")
 # per expert schedule: the dominant kernel, its ncu summary prefix, its source
 KERNELS = {"stream_k": ("moe_experts_kernel", "experts_kernel", "gemm.cu"),

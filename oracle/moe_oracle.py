@@ -27,8 +27,7 @@ Sources (web pages, cited by title and section):
   shared expert with the same clamp).
 * [P4] SpecForge PR #1073 "MoE drafts: DeepSeek-V4.1's own DSpark draft" --
   commit notes on the expert bias (it moves which experts are picked, not
-  their weights), on
-  select receiving the shifted scores, on the DeepSeek-V4 family (sqrt(softplus)
+  their weights), on select receiving the shifted scores, on the DeepSeek-V4 family (sqrt(softplus)
   scores, always renormalised, route_scale, clamped SwiGLU, one ungated shared
   expert), on the fused gate_up_proj / down_proj expert layout and on the
   export formats of the official checkpoint (FP4 routed experts).
@@ -326,8 +325,8 @@ def moe_layer(x, gate, w_gate_up, w_down, recipe: Recipe, router_bias=None,
               expert_bias=None, sh_gate_up=None, sh_down=None, sh_gate=None):
     """The whole layer on small inputs: returns dict(logits, scores, choice,
     idx, weights, counts, offsets, sorted_pair, pair_pos, y).  A token count of
-    0 routes an empty top-k and returns an empty output ([P1] DraftMoE forward: an empty
-    batch gives an empty routing)."""
+    0 routes an empty top-k and returns an empty output ([P1] DraftMoE
+    forward: an empty batch gives an empty routing)."""
     x = np.asarray(x, np.float64)
     t, h = x.shape
     e = recipe.num_experts
@@ -351,8 +350,8 @@ def moe_layer(x, gate, w_gate_up, w_down, recipe: Recipe, router_bias=None,
 # --------------------------------------------------------------------------
 # FP4 routed experts ([P4] commit note on the DeepSeek-V4.1 export formats:
 # each byte packs the e2m1 codes of two consecutive inputs, the even one in
-# its low four bits, and 32 inputs share one e8m0 scale; [P5] MXFP4 commit note: uint8 codes
-# [E, N, K//2] and scales [E, N, K//32], output-major).  The layer computes
+# its low four bits, and 32 inputs share one e8m0 scale; [P5] MXFP4 commit
+# note: uint8 codes [E, N, K//2] and scales [E, N, K//32], output-major).  The layer computes
 # with the exactly dequantized weights ([P4]: the import turns them into bf16).
 # --------------------------------------------------------------------------
 
