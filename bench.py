@@ -67,8 +67,14 @@ def parse():
                     help="expert schedule (auto: the library's choice for the shape)")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "fp4"],
                     help="routed experts' format: bf16, or FP4 (e2m1 codes + e8m0 scale per 32 inputs)")
+    ap.add_argument("--workloads", default="targets", choices=["none", "targets", "all"],
+                    help="also measure the other T=72 decode workloads (targets), plus the DeepSeek-V4-style "
+                         "token sweep (all)")
+    ap.add_argument("--sustain", type=float, default=1.0, help="seconds of the sustained replay (headline)")
+    ap.add_argument("--sustain-extra", type=float, default=0.5, help="seconds of the sustained replay (others)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-child", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -232,21 +238,49 @@ def cpu_prepare(cfg):
     return host, w64
 
 
-def cpu_baseline(cfg, seconds: float):
+def cpu_child(spec: dict) -> dict:
+    """Runs in a child process whose BLAS thread count the parent fixed:
+    full-layer oracle passes over the workload's T tokens for `seconds`."""
+    torch.set_num_threads(int(spec["threads"]))
+    cfg = S.CONFIGS[spec["name"]].with_(T=int(spec["T"]), expert_format=spec["format"])
     host, w64 = cpu_prepare(cfg)
     t0 = time.perf_counter()
-    n_tok = 0
-    passes = 0
+    n_tok = passes = 0
     while True:
         cpu_oracle_pass(cfg, host, w64, np.arange(cfg.T))
         n_tok += cfg.T
         passes += 1
-        if time.perf_counter() - t0 >= seconds:
+        if time.perf_counter() - t0 >= float(spec["seconds"]):
             break
-    dt = time.perf_counter() - t0
-    return {"value": n_tok / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{passes} full layer passes of T={cfg.T} tokens ({dt:.1f} s), fp64 numpy oracle, "
-                      f"expert weights pre-converted to fp64"}
+    return {"tokens": n_tok, "passes": passes, "seconds": time.perf_counter() - t0}
+
+
+def _cpu_run(cfg, seconds: float, threads: int) -> dict:
+    env = dict(os.environ)
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = str(threads)
+    env["CUDA_VISIBLE_DEVICES"] = ""  # the oracle runs on the host cores only
+    spec = json.dumps({"name": cfg.name, "T": cfg.T, "format": cfg.expert_format, "seconds": seconds,
+                       "threads": threads})
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", spec], capture_output=True,
+                       text=True, env=env, cwd=ROOT, timeout=600)
+    if r.returncode != 0:
+        raise SystemExit(f"CPU oracle child failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(cfg, seconds: float):
+    """The fp64 oracle on the host cores, in child processes with the BLAS
+    thread count fixed: every core, then one core."""
+    ncpu = os.cpu_count() or 1
+    allc = _cpu_run(cfg, seconds * 2 / 3, ncpu)
+    one = _cpu_run(cfg, seconds / 3, 1)
+    return {"value": allc["tokens"] / allc["seconds"], "unit": UNIT, "cores": ncpu, "kind": "oracle",
+            "threads": {"blas": ncpu, "env": "OPENBLAS/OMP/MKL_NUM_THREADS"},
+            "sample": f"{allc['passes']} full layer passes of T={cfg.T} tokens ({allc['seconds']:.1f} s, "
+                      f"{ncpu} BLAS threads), fp64 numpy oracle, expert weights pre-converted to fp64",
+            "single_core": {"value": one["tokens"] / one["seconds"], "unit": UNIT, "cores": 1,
+                            "sample": f"{one['passes']} full layer passes ({one['seconds']:.1f} s, 1 BLAS thread)"}}
 
 
 def run_reference(args, cfg, rank, world):
@@ -279,12 +313,228 @@ def run_reference(args, cfg, rank, world):
                        "routed_experts": "fp4 (e2m1 + e8m0/32)" if cfg.expert_format == "fp4" else "bf16",
                        "tokens_per_step_sample": tok_per_step},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "threads": {"blas": "library default (every core)"},
                              "sample": f"{tok_per_step} of the {cfg.T} tokens per step, fp64 numpy oracle"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # ----------------------------------------------------------------------------- GPU arm
+
+# The other decode workloads with a >= 70% roofline target, measured in the
+# same process and under the same clock record as the headline; with
+# --workloads all also the rest of the DeepSeek-V4-style token sweep.
+TARGET_WORKLOADS = [("qwen38_27b_dspark", 72), ("dsv3_style", 72), ("dsv4_style", 72)]
+SWEEP_WORKLOADS = [("dsv4_style", 9), ("dsv4_style", 576), ("dsv4_style", 4096)]
+NOMINAL_HBM_GBS = 8000.0
+
+
+class Workload:
+    """One layer's weights (rotating over copies larger than L2), workspace
+    and launch closure on one stream."""
+
+    def __init__(self, cfg, dev, rank, schedule: str):
+        from moe_ffn_speculative_gb300 import ops
+        self.ops = ops
+        self.cfg = cfg
+        self.rec = ops.Recipe.from_config(cfg)
+        self.fp4 = cfg.expert_format == "fp4"
+        ops.set_schedule({"auto": ops.SCHEDULE_AUTO, "stream_k": ops.SCHEDULE_STREAM_K,
+                          "slice": ops.SCHEDULE_SLICE}[schedule])
+        # FP4 routed experts always run the stream-K schedule
+        self.sched = "stream_k" if self.fp4 else ops.SCHEDULE_NAMES[ops.ffn_schedule(
+            cfg.T, cfg.H, cfg.I, cfg.shared_I, self.rec, gated=cfg.shared_gated and cfg.shared_I > 0)]
+        base = S.make_inputs(cfg, device=dev, seed=cfg.seed + 1000 * rank)
+        self.base = base
+        self.n_copies = max(2, -(-4 * L2_BYTES // (cfg.weight_bytes + 1)))
+        wkeys = ["w_gate_up_q", "w_down_q"] if self.fp4 else ["w_gate_up", "w_down"]
+        self.layers = [base]
+        for _ in range(1, self.n_copies):
+            dd = dict(base)
+            for k in wkeys + (["sh_gate_up", "sh_down"] if base["sh_gate_up"] is not None else []):
+                dd[k] = base[k].clone()
+            self.layers.append(dd)
+        if self.fp4:
+            sc = ops.fp4_prepare_scales(base["w_gate_up_s"], base["w_down_s"])
+            for dd in self.layers:
+                dd["scales"] = sc.clone()
+        self.ws = ops.Workspace(ops.ffn_workspace_bytes(cfg.T, cfg.H, cfg.I, cfg.shared_I, self.rec), dev)
+        self.x = base["x"]
+        self.y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+        self.stream = torch.cuda.Stream(device=dev)
+        # launches of the library per layer: router (+ logits GEMM above 1024
+        # tokens), expert GEMMs, combine -- or the one fused launch
+        if self.sched == "slice":
+            self.launched, self.timed = 1, {"fused": 1}
+        else:
+            self.launched = 3 if (cfg.K > 1 or cfg.shared_I > 0) else 2
+            self.timed = {n: k for k, n in enumerate(["router", "experts", "combine"][:self.launched])}
+            if cfg.T > 1024 and not self.fp4:
+                self.launched += 1
+
+    def call(self, dd, xx, yy, cnt=None):
+        ops, kw = self.ops, dict(router_bias=dd["router_bias"], expert_bias=dd["expert_bias"],
+                                 sh_gate_up=dd["sh_gate_up"], sh_down=dd["sh_down"], sh_gate=dd["sh_gate"], y=yy,
+                                 counts_out=cnt, stream=self.stream)
+        if self.fp4:
+            ops.moe_ffn_forward_fp4(xx, dd["gate"], dd["w_gate_up_q"], dd["w_down_q"], dd["scales"], self.rec,
+                                    self.ws, **kw)
+        else:
+            ops.moe_ffn_forward(xx, dd["gate"], dd["w_gate_up"], dd["w_down"], self.rec, self.ws, **kw)
+
+    def fwd(self, i, cnt=None):
+        self.call(self.layers[i % self.n_copies], self.x, self.y, cnt)
+
+    def first_forward(self):
+        counts = torch.empty(self.cfg.E, dtype=torch.int32, device=self.x.device)
+        with torch.cuda.stream(self.stream):
+            self.fwd(0, cnt=counts)
+        torch.cuda.synchronize()
+        st, info = self.ws.device_status(self.stream)
+        if st != 0:
+            raise SystemExit(f"{self.cfg.name}: device status {st} ({info}) after the first forward")
+        return int((counts > 0).sum().item())
+
+    def graph(self, G, events=None):
+        """One CUDA graph of G consecutive layers (weight copies in turn), as a
+        decode step's graph holds a model's layers back to back; with
+        `events` (a list of G event lists) every launch is bracketed by
+        event-record nodes."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            for i in range(G):
+                if events is not None:
+                    self.ops.set_profile_events(events[i])
+                self.fwd(i)
+        if events is not None:
+            self.ops.set_profile_events(None)
+        torch.cuda.synchronize()
+        return g
+
+    def replay_ms(self, graph, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            for _ in range(n):
+                graph.replay()
+            e1.record(self.stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    def kernel_us(self, G, replays):
+        """Average device time of each library launch of a layer, from event
+        nodes around the launches inside graph replays (the launch
+        configuration of the timed region)."""
+        n_ev = 2 * 3
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(G)]
+        for row in evs:  # torch creates the CUDA event on its first record
+            for e in row:
+                e.record(self.stream)
+        torch.cuda.synchronize()
+        g = self.graph(G, evs)
+        acc = {n: [] for n in self.timed}
+        for _ in range(replays):
+            g.replay()
+            torch.cuda.synchronize()
+            for row in evs:
+                for n, k in self.timed.items():
+                    acc[n].append(row[2 * k].elapsed_time(row[2 * k + 1]) * 1e3)
+        del g
+        return {n: float(np.mean(v)) for n, v in acc.items()}
+
+    def e2e(self, n):
+        """Through the C ABI with host buffers: pinned x -> device, forward,
+        device y -> pinned host, every step (eager launches)."""
+        x_host = self.x.cpu().pin_memory()
+        y_host = torch.empty((self.cfg.T, self.cfg.H), dtype=torch.bfloat16).pin_memory()
+        x_dev = torch.empty_like(self.x)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            for i in range(n):
+                x_dev.copy_(x_host, non_blocking=True)
+                self.call(self.layers[i % self.n_copies], x_dev, self.y)
+                y_host.copy_(self.y, non_blocking=True)
+            e1.record(self.stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    def check_status(self, where):
+        st, info = self.ws.device_status(self.stream)
+        if st != 0:
+            raise SystemExit(f"{self.cfg.name}: device status {st} ({info}) {where}")
+
+    def close(self):
+        self.ops.set_schedule(self.ops.SCHEDULE_AUTO)
+        del self.layers, self.base, self.ws, self.x, self.y
+        torch.cuda.empty_cache()
+
+
+def pick_G(K, n_copies):
+    """Layers per graph: divides K and is a multiple of the weight copies."""
+    return next((g for g in (8, 6, 4, 2) if K % g == 0 and g % n_copies == 0), 1)
+
+
+def roofline_record(wl, u, per_kernel, ms_step, hbm, tflops, peak_src, traffic_key):
+    """The dominant kernel's roofline (algorithmic bytes over its event-timed
+    duration) and the layer's (roofline time over the step time)."""
+    cfg = wl.cfg
+    layer_bytes, ex_bytes, flops = algorithmic(cfg, u)
+    kname = "fused" if wl.sched == "slice" else "experts"
+    if wl.sched == "slice":
+        ex_bytes = layer_bytes  # the fused launch is the whole layer
+    achieved = ex_bytes / (per_kernel[kname] * 1e-6) / 1e9
+    roof_layer_us = max(layer_bytes / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
+    traffic = ncu_traffic(wl.sched, traffic_key)
+    roof = {"bound": "hbm", "kernel": KERNELS[wl.sched][0], "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "frac_vs_nominal": achieved / NOMINAL_HBM_GBS, "traffic": traffic,
+            "peak_source": peak_src, "algorithmic_bytes_per_launch": ex_bytes,
+            "kernel_us": per_kernel[kname], "timing": "event nodes around the launch in graph replay"}
+    layer = {"bytes": layer_bytes, "flops": flops, "roofline_us": roof_layer_us,
+             "achieved_gbs": layer_bytes / (ms_step * 1e-3) / 1e9, "frac": roof_layer_us / (ms_step * 1e3),
+             "frac_vs_nominal": layer_bytes / (NOMINAL_HBM_GBS * 1e9) * 1e6 / (ms_step * 1e3)}
+    return roof, layer
+
+
+def workload_key(cfg, args_override: bool):
+    wl = cfg.name if not args_override else f"{cfg.name}_T{cfg.T}_E{cfg.E}"
+    return wl + ("_fp4" if cfg.expert_format == "fp4" else "")
+
+
+def measure_extra(cfg, dev, rank, K, W, hbm, tflops, peak_src, sustain_s):
+    """One more workload in the same process: graph replay of K layers after
+    W warm-up layers, per-kernel event times, and a sustained replay."""
+    wl = Workload(cfg, dev, rank, "auto")
+    try:
+        u = wl.first_forward()
+        G = pick_G(K, wl.n_copies)
+        g = wl.graph(G)
+        for _ in range(-(-W // G)):
+            g.replay()
+        torch.cuda.synchronize()
+        ms_step = wl.replay_ms(g, K // G) / K
+        n_sus = max(1, int(sustain_s / (ms_step * 1e-3) / G))
+        ms_sus = wl.replay_ms(g, n_sus) / (n_sus * G)
+        del g
+        per_kernel = wl.kernel_us(G, max(2, min(25, 200 // G)))
+        wl.check_status("after the timed region")
+        roof, layer = roofline_record(wl, u, per_kernel, ms_step, hbm, tflops, peak_src,
+                                      workload_key(cfg, False))
+        return {"workload": cfg.name, "T": cfg.T, "metric": metric_for(cfg), "schedule": wl.sched,
+                "touched_experts": u, "us_per_layer": ms_step * 1e3, "tokens_per_s": cfg.T / (ms_step * 1e-3),
+                "steps": K, "layer_frac": layer["frac"], "kernel_frac": roof["frac"],
+                "kernel_frac_vs_nominal": roof["frac_vs_nominal"], "kernel_us": per_kernel,
+                "traffic": roof["traffic"], "algorithmic_bytes_per_launch": roof["algorithmic_bytes_per_launch"],
+                "layer_bytes": layer["bytes"],
+                "sustained": {"layers": n_sus * G, "seconds": ms_sus * n_sus * G * 1e-3,
+                              "us_per_layer": ms_sus * 1e3,
+                              "layer_frac": layer["roofline_us"] / (ms_sus * 1e3)},
+                "l2": f"weights rotate over {wl.n_copies} copies "
+                      f"({wl.n_copies * cfg.weight_bytes / 1e9:.2f} GB) > L2"}
+    finally:
+        wl.close()
+
 
 def run_gpu(args, cfg, rank, world):
     from moe_ffn_speculative_gb300 import ops
@@ -293,151 +543,68 @@ def run_gpu(args, cfg, rank, world):
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
     build()
+    ops.lib()
     dev = torch.device("cuda", torch.cuda.current_device())
     K = args.steps if args.steps is not None else 20000
     W = max(3, args.warmup if args.warmup is not None else 50)
-    rec = ops.Recipe.from_config(cfg)
-    fp4 = cfg.expert_format == "fp4"
-    ops.set_schedule({"auto": ops.SCHEDULE_AUTO, "stream_k": ops.SCHEDULE_STREAM_K,
-                      "slice": ops.SCHEDULE_SLICE}[args.schedule])
-    # FP4 routed experts always run the stream-K schedule
-    sched = "stream_k" if fp4 else ops.SCHEDULE_NAMES[ops.ffn_schedule(
-        cfg.T, cfg.H, cfg.I, cfg.shared_I, rec, gated=cfg.shared_gated and cfg.shared_I > 0)]
-    base = S.make_inputs(cfg, device=dev, seed=cfg.seed + 1000 * rank)
-    n_copies = max(2, -(-4 * L2_BYTES // (cfg.weight_bytes + 1)))
-    wkeys = ["w_gate_up_q", "w_down_q"] if fp4 else ["w_gate_up", "w_down"]
-    layers = [base]
-    for c in range(1, n_copies):
-        dd = dict(base)
-        for k in wkeys + (["sh_gate_up", "sh_down"] if base["sh_gate_up"] is not None else []):
-            dd[k] = base[k].clone()
-        layers.append(dd)
-    if fp4:
-        sc = ops.fp4_prepare_scales(base["w_gate_up_s"], base["w_down_s"])
-        for dd in layers:
-            dd["scales"] = sc.clone()
-    ws = ops.Workspace(ops.ffn_workspace_bytes(cfg.T, cfg.H, cfg.I, cfg.shared_I, rec), dev)
-    x = base["x"]
-    y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
-    counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
-    stream = torch.cuda.Stream(device=dev)
-
-    def call(dd, xx, yy, cnt=None):
-        kw = dict(router_bias=dd["router_bias"], expert_bias=dd["expert_bias"], sh_gate_up=dd["sh_gate_up"],
-                  sh_down=dd["sh_down"], sh_gate=dd["sh_gate"], y=yy, counts_out=cnt, stream=stream)
-        if fp4:
-            ops.moe_ffn_forward_fp4(xx, dd["gate"], dd["w_gate_up_q"], dd["w_down_q"], dd["scales"], rec, ws, **kw)
-        else:
-            ops.moe_ffn_forward(xx, dd["gate"], dd["w_gate_up"], dd["w_down"], rec, ws, **kw)
-
-    def fwd(i, yy=y, cnt=None):
-        call(layers[i % n_copies], x, yy, cnt)
-
-    with torch.cuda.stream(stream):
-        fwd(0, cnt=counts)
-    torch.cuda.synchronize()
-    u = int((counts > 0).sum().item())
-    st, info = ws.device_status(stream)
-    if st != 0:
-        raise SystemExit(f"device status {st} ({info}) after the first forward")
-
-    # One CUDA graph of G consecutive layers (weight copies in turn), as a
-    # decode step's graph holds a model's layers back to back; G divides K,
-    # so exactly K layers are timed.
-    G = next((g for g in (8, 6, 4, 2) if K % g == 0 and g % n_copies == 0), 1)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(G):
-            fwd(i)
-    torch.cuda.synchronize()
-    for i in range(-(-W // G)):
+    hbm, tflops, peak_src = measured_peaks()
+    wl = Workload(cfg, dev, rank, args.schedule)
+    u = wl.first_forward()
+    G = pick_G(K, wl.n_copies)
+    graph = wl.graph(G)
+    for _ in range(-(-W // G)):
         graph.replay()
     torch.cuda.synchronize()
 
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     time.sleep(0.3)
+    # ---- the timed region: exactly K layers (K // G graph replays)
     barrier(world)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for i in range(K // G):
+    with torch.cuda.stream(wl.stream):
+        ev0.record(wl.stream)
+        for _ in range(K // G):
             graph.replay()
-        ev1.record(stream)
+        ev1.record(wl.stream)
     torch.cuda.synchronize()
     barrier(world)
-    ms_total = ev0.elapsed_time(ev1)
-    clk = clocks.stop()
-    ms_total = max_over_ranks(ms_total, world)
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world)
     ms_step = ms_total / K
     value = cfg.T * K * world / (ms_total / 1e3)
-
-    # per-kernel durations (eager launches, events around every kernel)
-    n_prof = min(K, 400)
-    n_k = 3
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * n_k)] for _ in range(n_prof)]
-    for row in evs:  # torch creates the CUDA event on its first record
-        for e in row:
-            e.record(stream)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        for i in range(n_prof):
-            ops.set_profile_events(evs[i])
-            fwd(i)
-    ops.set_profile_events(None)
-    torch.cuda.synchronize()
-    if sched == "slice":
-        # one fused launch, recorded as the expert-GEMM pair
-        launched, timed = 1, {"fused": 1}
-    else:
-        launched = 3 if (cfg.K > 1 or cfg.shared_I > 0) else 2
-        if cfg.T > 1024:  # the router's logits by a separate GEMM launch
-            launched += 1
-        timed = {n: k for k, n in enumerate(["router", "experts", "combine"][:launched])}
-    per_kernel = {n: float(np.mean([e[2 * k].elapsed_time(e[2 * k + 1]) for e in evs])) * 1e3  # us
-                  for n, k in timed.items()}
-
-    # end to end: pinned host x -> device, forward, device y -> pinned host, every step
-    x_host = base["x"].cpu().pin_memory()
-    y_host = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
-    x_dev = torch.empty_like(x)
+    # ---- the same graph replayed for at least `sustain` seconds
+    n_sus = max(1, int(args.sustain / (ms_step * 1e-3) / G))
+    ms_sus = max_over_ranks(wl.replay_ms(graph, n_sus), world) / (n_sus * G)
+    del graph
+    per_kernel = wl.kernel_us(G, max(2, min(25, 200 // G)))
+    # ---- end to end through the C ABI with host buffers
     n_e2e = min(K, 2000)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(n_e2e):
-            x_dev.copy_(x_host, non_blocking=True)
-            call(layers[i % n_copies], x_dev, y)
-            y_host.copy_(y, non_blocking=True)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = max_over_ranks(e0.elapsed_time(e1), world)
+    ms_e2e = max_over_ranks(wl.e2e(n_e2e), world)
     e2e_value = cfg.T * n_e2e * world / (ms_e2e / 1e3)
-    st, info = ws.device_status(stream)
-    if st != 0:
-        raise SystemExit(f"device status {st} ({info}) after the timed region")
+    wl.check_status("after the timed region")
+    override = args.tokens is not None or args.experts is not None
+    roof, layer = roofline_record(wl, u, per_kernel, ms_step, hbm, tflops, peak_src, workload_key(cfg, override))
+    layer["sustained"] = {"layers": n_sus * G, "seconds": ms_sus * n_sus * G * 1e-3, "us_per_layer": ms_sus * 1e3,
+                          "frac": layer["roofline_us"] / (ms_sus * 1e3)}
+    sched, n_copies, launched = wl.sched, wl.n_copies, wl.launched
+    wl.close()
 
-    hbm, tflops, peak_src = measured_peaks()
-    layer_bytes, ex_bytes, flops = algorithmic(cfg, u)
-    if sched == "slice":
-        # the fused launch is the whole layer: its algorithmic bytes are the layer's
-        ex_bytes = layer_bytes
-    if sched == "slice":
-        # the step is this one launch: its average duration over the timed
-        # graph region (inter-kernel gaps included) is the step time
-        t_ex = ms_step * 1e-3
-    else:
-        t_ex = per_kernel["experts"] * 1e-6
-    achieved = ex_bytes / t_ex / 1e9
-    layer_gbs = layer_bytes / (ms_step * 1e-3) / 1e9
-    roof_layer_us = max(layer_bytes / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
-    wl = cfg.name if args.tokens is None and args.experts is None else f"{cfg.name}_T{cfg.T}_E{cfg.E}"
-    traffic = ncu_traffic(sched, wl + ("_fp4" if fp4 else ""))
+    # ---- the other decode workloads, same process, same clock record
+    extra = []
+    if args.workloads != "none" and args.tokens is None and args.experts is None and args.weights == "bf16" \
+            and args.schedule == "auto":
+        todo = TARGET_WORKLOADS + (SWEEP_WORKLOADS if args.workloads == "all" else [])
+        for name, T in todo:
+            c = S.CONFIGS[name].with_(T=T)
+            if c.name == cfg.name and c.T == cfg.T:
+                continue
+            extra.append(measure_extra(c, dev, rank, K, W, hbm, tflops, peak_src, args.sustain_extra))
+    clk = clocks.stop()
 
     if rank != 0:
         return
+    fp4 = cfg.expert_format == "fp4"
     line = {
         "metric": metric_for(cfg),
         "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms_step,
@@ -451,17 +618,16 @@ def run_gpu(args, cfg, rank, world):
                    "launch": f"cuda_graph_replay, {G} layer{'s' if G > 1 else ''} per graph",
                    "l2": f"weights rotate over {n_copies} copies ({n_copies * cfg.weight_bytes / 1e9:.2f} GB) > L2",
                    "parallelism": "replicas" if world > 1 else "single_gpu"},
-        "roofline": {"bound": "hbm", "kernel": KERNELS[sched][0], "achieved": achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic, "peak_source": peak_src,
-                     "algorithmic_bytes_per_launch": ex_bytes},
-        "layer_roofline": {"bytes": layer_bytes, "flops": flops, "roofline_us": roof_layer_us,
-                           "achieved_gbs": layer_gbs, "frac": roof_layer_us / (ms_step * 1e3)},
+        "roofline": roof,
+        "layer_roofline": layer,
         "kernel_us": per_kernel,
         "gpu_launches": launched * K,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cfg.T * cfg.H * 2,
                 "d2h_bytes_per_step": cfg.T * cfg.H * 2, "steps": n_e2e, "launch": "eager"},
         "clocks": clk,
     }
+    if extra:
+        line["workloads"] = extra
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -469,6 +635,9 @@ def run_gpu(args, cfg, rank, world):
 
 def main():
     args = parse()
+    if args.cpu_child:
+        print(json.dumps(cpu_child(json.loads(args.cpu_child))), flush=True)
+        return
     cfg = S.CONFIGS[args.config]
     if args.weights == "fp4":
         cfg = cfg.with_(expert_format="fp4")

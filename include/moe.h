@@ -99,8 +99,9 @@ typedef struct {
 /* Human-readable name of a status code (static storage). */
 MOE_API const char* moe_status_string(moe_status s);
 
-/* Bytes of workspace moe_route() needs for T tokens and E experts (token-block
- * completion counters and, when logits_out is NULL, the [T,E] fp32 logits). */
+/* Bytes of workspace moe_route() needs for T tokens and E experts: the fixed
+ * header (status block, token-block completion counters sized for any T) and
+ * the [T,E] fp32 logits (used when logits_out is NULL). */
 MOE_API size_t moe_route_workspace_bytes(int T, int E);
 
 /* Router: logits = x . gate^T (+ router_bias), fp32 accumulation of the exact
@@ -112,9 +113,11 @@ MOE_API size_t moe_route_workspace_bytes(int T, int E);
  *   topk_idx    [T,K] int32           descending shifted score, ties -> lower e
  *   topk_w      [T,K] fp32            routing weights
  *   ws          workspace of >= moe_route_workspace_bytes(T, E) bytes,
- *               256-byte aligned, zero-filled before its first use and again
- *               before a call with another T (the library leaves its counters
- *               at zero after every call, but where they sit depends on T).
+ *               256-byte aligned, zero-filled once before its first use
+ *               (moe_workspace_init).  Its counters sit at fixed offsets and
+ *               every call leaves them at zero, so the workspace then serves
+ *               any later call it is large enough for, whatever its T; after
+ *               a device-side error (moe_get_device_status) zero-fill it again.
  */
 MOE_API moe_status moe_route(const moe_bf16* x, int T, int H, const moe_bf16* gate,
                      const float* router_bias, const float* expert_bias,
@@ -129,9 +132,13 @@ MOE_API moe_status moe_route(const moe_bf16* x, int T, int H, const moe_bf16* ga
  * packaging variant of moe_route().
  *   Same arguments and results as moe_route() minus ws / ws_bytes.
  *   Scratch: one file-scope device array of about 1.1 MB inside the library
- *     (token-block counters and the [T,E] fp32 logits), held on every GPU that
- *     loads the library until the process exits.  No cudaMalloc / cudaFree or
- *     other allocating call is made.
+ *     (moe_route's workspace for the largest call it takes: the token-block
+ *     counters and the [T,E] fp32 logits, which hold the logits when
+ *     logits_out is NULL), held on every GPU that loads the library until the
+ *     process exits.  No cudaMalloc / cudaFree or other allocating call is
+ *     made.
+ *   Arguments are checked as moe_route() checks them before the array is
+ *     touched: a refused call leaves it as it was.
  *   Limits: T <= MOE_NOALLOC_MAX_TOKENS and T*E <= MOE_NOALLOC_MAX_LOGITS,
  *     else MOE_ERR_UNSUPPORTED before anything runs.
  *   The first call on each device looks the array's device address up
@@ -176,7 +183,8 @@ MOE_API moe_status moe_permute(const int32_t* topk_idx, int T, int K, int E,
  * that range. */
 MOE_API size_t moe_ffn_workspace_bytes(int T, int H, int I, int Is, const moe_recipe* recipe);
 
-/* Zero-fill a workspace (required once before its first use). */
+/* Zero-fill a workspace (required once before its first use, and again after
+ * a device-side error). */
 MOE_API moe_status moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* The whole layer: y = sum_k w_tk * Expert_{idx_tk}(x_t) + g_t * Shared(x_t).
@@ -188,10 +196,15 @@ MOE_API moe_status moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t st
  *   sh_down    [H,Is] bf16
  *   sh_gate    [H] bf16 or NULL: g_t = sigmoid(x_t . sh_gate), else g_t = 1
  *   ws         >= moe_ffn_workspace_bytes(T,H,I,Is,recipe) bytes, 256-byte
- *              aligned, zero-filled before its first use and again before a
- *              call with another T, H, I, Is or recipe (its self-resetting
- *              counters sit at offsets that depend on them); one workspace
- *              must not be used by two calls that may overlap on the GPU.
+ *              aligned, zero-filled once before its first use
+ *              (moe_workspace_init).  Every counter the kernels keep sits in
+ *              a fixed header whose offsets depend on neither T nor the shape,
+ *              and every call leaves it at zero, so the workspace then serves
+ *              any later call (another T, shape or recipe) it is large enough
+ *              for; after a device-side error (moe_get_device_status)
+ *              zero-fill it again.  One workspace must not be used by two
+ *              calls that may overlap on the GPU.  A workspace smaller than
+ *              the call needs is refused with MOE_ERR_WORKSPACE.
  *   y          [T,H] bf16 output (round to nearest even from fp32)
  *   topk_idx_out [T,K] int32, topk_w_out [T,K] fp32, counts_out [E] int32:
  *              optional copies of the routing (each may be NULL).
@@ -293,7 +306,22 @@ MOE_API moe_status moe_ffn_forward_fp4(const moe_bf16* x, int T, int H, int I, c
  * moe_route() or moe_ffn_forward(), and clears it.  Returns MOE_OK or the
  * first device-side error recorded (MOE_ERR_DEVICE_TIMEOUT, or
  * MOE_ERR_DEVICE_RANGE from the FP4 path); *info_out (if not NULL) receives
- * the kernel-specific detail word. */
+ * the kernel-specific detail word (for MOE_ERR_DEVICE_TIMEOUT: which wait
+ * ran out; MOE_INFO_HOLD for the start gate below).
+ *
+ * Start gate: the int32 at byte offset MOE_WS_HOLD_OFFSET of a workspace.
+ * While it is non-zero, the expert kernels of moe_ffn_forward() and
+ * moe_ffn_forward_fp4() wait at their start; once it is zero they go on.  A
+ * wait that lasts past a quarter of the device wait limit (about a quarter
+ * second of SM clocks; every other device wait gives up after about one
+ * second) ends the forward with MOE_ERR_DEVICE_TIMEOUT / MOE_INFO_HOLD: every CTA
+ * lets its issued copies land, releases its tensor memory and returns, so
+ * the context stays usable and the next forward on the same workspace is
+ * correct.  The gate lets a host hold a queued forward from outside (and
+ * exercises that failure path); it is zero in a zero-filled workspace and
+ * the library never writes it. */
+#define MOE_WS_HOLD_OFFSET 8
+#define MOE_INFO_HOLD 15
 MOE_API moe_status moe_get_device_status(void* ws, cudaStream_t stream, int32_t* info_out);
 
 /* Profiling hook: when `events` is not NULL, moe_ffn_forward() records
@@ -303,7 +331,9 @@ MOE_API moe_status moe_get_device_status(void* ws, cudaStream_t stream, int32_t*
  * persistent launch), combine (skipped when K == 1 and there is no shared
  * expert).  Under MOE_SCHEDULE_SLICE the one fused launch is recorded as the
  * expert-GEMM pair; the router pair is recorded empty (both events at the
- * same point) and the combine pair not at all. */
+ * same point) and the combine pair not at all.  During a stream capture the
+ * events are recorded as external event-record nodes of the graph, so every
+ * replay records them. */
 MOE_API void moe_set_profile_events(void* const* events, int n_pairs);
 
 #ifdef __cplusplus

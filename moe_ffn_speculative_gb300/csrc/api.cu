@@ -191,13 +191,11 @@ SlicePlan slice_plan(int T, int H, int I, int Is, int E, bool gated, int sms) {
   }
   // four stages at least: their token-tile parts later hold h (2 k-blocks x hi/lo)
   const bool smem_ok = s.stage_space / (2 * kTileBytesA + kSliceMaxTok * 128) >= 4;
-  s.reserve = smem_ok && s.n_units + 1 <= sms;
+  s.reserve = smem_ok && s.n_units + 1 <= sms &&
+              kSliceSyncWords + s.n_mt + (E + 1) * s.s_max <= kSliceMaxSetWords;
   s.ok = s.reserve && T <= kSliceMaxTok && s.n_units + s.n_rcta <= sms;
   return s;
 }
-
-// Words of one of the slice kernel's two counter sets.
-int slice_set_words(const SlicePlan& s, int E) { return kSliceSyncWords + s.n_mt + (E + 1) * s.s_max; }
 
 // The fused kernel streams every expert's gate_up weights from the start,
 // before the routing is known, and stops an untouched expert once it is: it
@@ -262,9 +260,11 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   L.g_max = static_cast<int>(u_max) + (Is > 0 ? 1 : 0);
   L.need_out = (K > 1 || Is > 0);
   const size_t rows = static_cast<size_t>(TK) + T;
-  size_t o = 0;
-  L.o_status = o; o += kAlign;
-  L.o_cnt = o; o = align_up(o + 4 * (L.rg.n_tb + 1));
+  // the fixed header: status block and every self-resetting counter
+  L.o_status = 0;
+  L.o_cnt = kRouteCntOffset;
+  L.o_sync = kSliceSyncOffset;
+  size_t o = kWsHeaderBytes;
   // stream-K arrival counters (gate_up, down) and gate_up readiness counters
   L.o_tiles = o; o = align_up(o + 4 * static_cast<size_t>(2 * L.max_gu_tiles + L.max_dn_tiles));
   L.o_logits = o; o = align_up(o + 4 * static_cast<size_t>(T) * E);
@@ -287,14 +287,13 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   if (L.need_out) o = align_up(o + 4 * rows * H);
   // fused small-expert-count kernel: counters and the per-slice partial outputs
   L.sp = slice_plan(T, H, I, Is, E, gated, sms);
-  L.o_sync = L.o_hbuf = L.o_sout = 0;
+  L.o_hbuf = L.o_sout = 0;
   if (L.sp.reserve) {
-    // two counter sets (with the slice-ready flags), every expert's h tiles (2 per slice, each
-    // 2*n_tok rows of 128 bytes) and the pair outputs for the combine
+    // every expert's h tiles (2 per slice, each 2*n_tok rows of 128 bytes)
+    // and the pair outputs for the combine; the counter sets are in the header
     const int Tr = T < kSliceMaxTok ? T : kSliceMaxTok;
     const size_t slots = static_cast<size_t>(Tr) * K + Tr;
     const size_t n_es = static_cast<size_t>(E) + 1;
-    L.o_sync = o; o = align_up(o + 4 * (1 + 2 * static_cast<size_t>(slice_set_words(L.sp, E))));
     L.o_hbuf = o; o = align_up(o + n_es * 2 * L.sp.s_max * 2 * static_cast<size_t>(L.sp.n_tok) * 128);
     L.o_sout = o;
     if (K > 1 || Is > 0 || L.sp.parts > 1) o = align_up(o + 4 * slots * H * static_cast<size_t>(L.sp.parts));
@@ -314,8 +313,16 @@ bool use_slice(const Layout& L, int T, int E, int K) {
   return slice_expected(T, E, K) && 4 * n_es * L.sp.n_mt * L.sp.parts >= 3 * L.grid;
 }
 
+// Inside a stream capture the event becomes an event-record node of the
+// graph (recorded on every replay), so kernels can be timed in graph replay.
 void record_event_on(int i, cudaStream_t s) {
-  if (t_events && i < 2 * t_nev && t_events[i]) cudaEventRecord(static_cast<cudaEvent_t>(t_events[i]), s);
+  if (!t_events || i >= 2 * t_nev || !t_events[i]) return;
+  cudaEvent_t ev = static_cast<cudaEvent_t>(t_events[i]);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, s);
 }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -324,6 +331,22 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 }  // namespace
+
+namespace moe {
+
+moe_status route_check_args(const moe_bf16* x, int T, int H, const moe_bf16* gate, const moe_recipe* recipe,
+                            const int32_t* topk_idx, const float* topk_w) {
+  const moe_status st = check_recipe(recipe);
+  if (st != MOE_OK) return st;
+  if (T < 0 || H < 8 || H % 8 != 0) return H % 8 != 0 && H >= 8 ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
+  if (H > 65536 || T > 65536) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x || !gate || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(gate)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+}  // namespace moe
 
 extern "C" {
 
@@ -342,20 +365,15 @@ const char* moe_status_string(moe_status s) {
 
 size_t moe_route_workspace_bytes(int T, int E) {
   if (T < 0 || E < 1) return 0;
-  const int n_tb = ceil_div(T, 4);  // the smallest token block the router uses
-  return kAlign + align_up(4 * static_cast<size_t>(n_tb + 1)) + align_up(4 * static_cast<size_t>(T) * E);
+  // [status block][token-block counters for any T][logits T x E]
+  return kRouteCntOffset + kRouteCntBytes + align_up(4 * static_cast<size_t>(T) * E);
 }
 
 moe_status moe_route(const moe_bf16* x, int T, int H, const moe_bf16* gate, const float* router_bias,
                      const float* expert_bias, const moe_recipe* recipe, float* logits_out, int32_t* topk_idx,
                      float* topk_w, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  moe_status st = check_recipe(recipe);
-  if (st != MOE_OK) return st;
-  if (T < 0 || H < 8 || H % 8 != 0) return H % 8 != 0 && H >= 8 ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
-  if (H > 65536 || T > 65536) return MOE_ERR_UNSUPPORTED;
-  if (T == 0) return MOE_OK;
-  if (!x || !gate || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(gate)) return MOE_ERR_INVALID_ARG;
+  const moe_status st = moe::route_check_args(x, T, H, gate, recipe, topk_idx, topk_w);
+  if (st != MOE_OK || T == 0) return st;
   const int E = recipe->num_experts;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0 || ws_bytes < moe_route_workspace_bytes(T, E))
     return MOE_ERR_WORKSPACE;
@@ -363,8 +381,8 @@ moe_status moe_route(const moe_bf16* x, int T, int H, const moe_bf16* gate, cons
   if (sms <= 0) return MOE_ERR_CUDA;
   const RouterGeom rg = router_geometry(T, E, false, sms);
   char* w = static_cast<char*>(ws);
-  const size_t o_cnt = kAlign;
-  const size_t o_logits = o_cnt + align_up(4 * static_cast<size_t>(ceil_div(T, 4) + 1));
+  const size_t o_cnt = kRouteCntOffset;
+  const size_t o_logits = kRouteCntOffset + kRouteCntBytes;
   RouteParams p;
   memset(&p, 0, sizeof(p));
   p.x = x; p.gate = gate; p.router_bias = router_bias; p.expert_bias = expert_bias; p.sh_gate = nullptr;
@@ -462,6 +480,8 @@ moe_status ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf16* g
     return MOE_ERR_INVALID_ARG;
   const size_t xy_bytes = static_cast<size_t>(T) * H * 2;
   if (overlaps(x, xy_bytes, y, xy_bytes)) return MOE_ERR_INVALID_ARG;
+  // a workspace that cannot even hold the fixed header is refused before any device query
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0 || ws_bytes < kWsHeaderBytes) return MOE_ERR_WORKSPACE;
   const int E = recipe->num_experts, K = recipe->top_k;
   const int sms = device_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
@@ -512,7 +532,7 @@ moe_status ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf16* g
     sp.direct_y = (K == 1 && Is == 0 && L.sp.parts == 1) ? 1 : 0;
     sp.y = y;
     sp.sync = reinterpret_cast<int32_t*>(w + L.o_sync);
-    sp.set_words = slice_set_words(L.sp, E);
+    sp.set_words = kSliceMaxSetWords;
     sp.status = status;
     record_event_on(0, stream);
     record_event_on(1, stream);

@@ -272,6 +272,10 @@ __device__ bool produce(const Smem& sm, const GemmParams& p, int ngroups, const 
   // Weights are streamed once: evict them first, so that L2 keeps what the
   // layer reuses (x, h, partials, the next kernels' code and metadata).
   const uint64_t pol = l2_evict_first_policy();
+  if (!wait_start_gate(status)) {
+    record_failure(status, sm.abort_flag, kInfoHold);
+    return false;
+  }
   WeightCursor ld;
   ld.init(p, ngroups, b, e, g);
   Ring pring;  // FP4 code stages

@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include "moe.h"
 #ifdef __CUDACC__
 #include <cuda_bf16.h>
 #endif
@@ -23,7 +25,9 @@ enum : int32_t {
   kInfoRouter = 9, kInfoTileCount = 10, kInfoHReady = 11,
   // range errors (kStatusRange): an FP4 block scale outside [104, 140], or a
   // value of x or h outside the f16 range of the FP4 experts' MMAs
-  kInfoScaleRange = 12, kInfoXRange = 13, kInfoHRange = 14
+  kInfoScaleRange = 12, kInfoXRange = 13, kInfoHRange = 14,
+  // the start gate (status word 2) stayed closed for the whole wait
+  kInfoHold = 15
 };
 
 // ----------------------------------------------------------------------------
@@ -214,7 +218,7 @@ struct SliceParams {
   // alternate forwards; a set is kSliceSyncWords words (router done, combine
   // task, exit count, -), n_mt output-tile counts, (E+1)*s_max slice-ready flags
   int32_t* sync;
-  int set_words;
+  int set_words;               // stride of the two sets (kSliceMaxSetWords); a set is cleared whole
   int32_t* status;
 };
 constexpr int kSliceMaxTok = 128;
@@ -222,6 +226,41 @@ constexpr int kSliceMaxExperts = 16;  // routed experts + the shared-expert gate
 constexpr int kSliceTokPerTask = 7;   // one token per warp of a reduction task
 constexpr int kSliceSyncWords = 4;
 constexpr int kSliceCtrlBytes = 4096;  // control block at the start of shared memory
+// Words of one slice counter set for the largest shape the entry points
+// accept (H <= 65536: 512 output tiles; E + 1 <= 17 expert slots; I, Is <=
+// 16384: 128 slices): every shape's set fits, so the sets sit at fixed
+// offsets whatever the shape.
+constexpr int kSliceMaxSetWords = kSliceSyncWords + 512 + (kSliceMaxExperts + 1) * 128;
+
+// ---------------------------------------------------------------------------
+// Fixed workspace header (every workspace of moe_route / moe_ffn_forward):
+// the status block, then every counter that returns to zero by itself after
+// a call, at offsets that depend on neither the token count nor the shape,
+// so one zero-filled workspace serves calls of any size it is large enough
+// for.  Everything after the header is data a call writes before it reads.
+//   [0, 256)                   status block: {code, info, hold, -}
+//   [256, 256 + kRouteCntBytes)  router token-block counters + completion
+//                              counter (4-token blocks of up to 65536 tokens)
+//   [.., + kSliceSyncBytes)    fused kernel: parity word + two counter sets
+// ---------------------------------------------------------------------------
+constexpr size_t kWsAlign = 256;
+constexpr size_t ws_align_up(size_t v) { return (v + kWsAlign - 1) / kWsAlign * kWsAlign; }
+constexpr int kMaxTokens = 65536;
+constexpr size_t kRouteCntOffset = kWsAlign;
+constexpr size_t kRouteCntBytes = ws_align_up(4 * (kMaxTokens / 4 + 1));
+constexpr size_t kSliceSyncOffset = kRouteCntOffset + kRouteCntBytes;
+constexpr size_t kSliceSyncBytes = ws_align_up(4 * (1 + 2 * static_cast<size_t>(kSliceMaxSetWords)));
+constexpr size_t kWsHeaderBytes = kSliceSyncOffset + kSliceSyncBytes;
+// Word 2 of the status block: the start gate.  While it is non-zero the
+// expert kernels wait at their start (bounded), then record
+// MOE_ERR_DEVICE_TIMEOUT with info kInfoHold and abort the forward.
+constexpr int kStatusHoldWord = 2;
+
+// Host-side argument checks of the router entry points (api.cu): MOE_OK
+// when the call may proceed (T == 0 included), else the status to return.
+// Nothing touches a device before they pass.
+moe_status route_check_args(const uint16_t* x, int T, int H, const uint16_t* gate, const moe_recipe* recipe,
+                            const int32_t* topk_idx, const float* topk_w);
 
 // launchers (route.cu, gemm.cu, combine.cu); return cudaError_t
 cudaError_t launch_route(const RouteParams& p, int tb, cudaStream_t s);
@@ -443,6 +482,22 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+// The start gate (status word kStatusHoldWord): true once it is zero; false
+// when it stays non-zero past kGateLimitCycles or another CTA has already
+// recorded a failure.  The limit is a quarter of every other wait's, so a
+// closed gate is always the first failure a forward records.
+constexpr long long kGateLimitCycles = kWaitLimitCycles / 4;
+__device__ __forceinline__ bool wait_start_gate(const int32_t* status) {
+  if (ld_acquire_gpu(status + kStatusHoldWord) == 0) return true;
+  const long long t0 = clock64();
+  while (true) {
+    __nanosleep(256);
+    if (ld_acquire_gpu(status + kStatusHoldWord) == 0) return true;
+    if (*reinterpret_cast<const volatile int32_t*>(status) != 0) return false;
+    if (clock64() - t0 > kGateLimitCycles) return false;
+  }
 }
 
 // Position in the ring of shared-memory stages (each role keeps its own).

@@ -14,13 +14,10 @@
 
 namespace {
 
-constexpr size_t kAlign = 256;
-constexpr size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
-
-// Layout of the array, identical to moe_route's workspace for T tokens:
+// Layout of the array: moe_route's workspace for the largest call it takes,
 // [status 256 B][token-block counters][logits T*E fp32].
-constexpr size_t kCounterBytes = align_up(4 * (MOE_NOALLOC_MAX_TOKENS / 4 + 1));
-constexpr size_t kScratchBytes = kAlign + kCounterBytes + align_up(4 * static_cast<size_t>(MOE_NOALLOC_MAX_LOGITS));
+constexpr size_t kScratchBytes =
+    moe::kRouteCntOffset + moe::kRouteCntBytes + moe::ws_align_up(4 * static_cast<size_t>(MOE_NOALLOC_MAX_LOGITS));
 
 // Every GPU that loads the library holds this array until the process exits.
 static __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
@@ -56,19 +53,17 @@ extern "C" moe_status moe_route_noalloc(const moe_bf16* x, int T, int H, const m
                                         const float* router_bias, const float* expert_bias,
                                         const moe_recipe* recipe, float* logits_out, int32_t* topk_idx,
                                         float* topk_w, cudaStream_t stream) {
-  if (!recipe) return MOE_ERR_INVALID_ARG;
-  if (T < 0) return MOE_ERR_INVALID_ARG;
-  if (T == 0) return moe_route(x, T, H, gate, router_bias, expert_bias, recipe, logits_out, topk_idx, topk_w,
-                               nullptr, 0, stream);
+  // the checks moe_route makes, before anything touches the shared array
+  moe_status st = moe::route_check_args(x, T, H, gate, recipe, topk_idx, topk_w);
+  if (st != MOE_OK || T == 0) return st;
   // sizes beyond the fixed array are refused before anything runs
-  if (T > MOE_NOALLOC_MAX_TOKENS || recipe->num_experts < 1 ||
-      static_cast<long long>(T) * recipe->num_experts > MOE_NOALLOC_MAX_LOGITS)
+  if (T > MOE_NOALLOC_MAX_TOKENS || static_cast<long long>(T) * recipe->num_experts > MOE_NOALLOC_MAX_LOGITS)
     return MOE_ERR_UNSUPPORTED;
-  moe_status st;
   void* scratch = scratch_on_current_device(&st);
   if (st != MOE_OK) return st;
   // the counters must start at zero; the array keeps the previous call's contents
-  if (cudaMemsetAsync(scratch, 0, kAlign + kCounterBytes, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  const size_t used = moe::kRouteCntOffset + moe::ws_align_up(4 * static_cast<size_t>(moe::ceil_div(T, 4) + 1));
+  if (cudaMemsetAsync(scratch, 0, used, stream) != cudaSuccess) return MOE_ERR_CUDA;
   return moe_route(x, T, H, gate, router_bias, expert_bias, recipe, logits_out, topk_idx, topk_w, scratch,
                    kScratchBytes, stream);
 }

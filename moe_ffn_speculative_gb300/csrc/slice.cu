@@ -352,6 +352,12 @@ __device__ __forceinline__ void unit_load_gu(const SliceParams& p, const SliceSm
 __device__ void unit_produce(const SliceParams& p, const SliceSmem& sm, const Unit& u, const CUtensorMap* tm_gu,
                              const CUtensorMap* tm_gu_sh, const CUtensorMap* tm_dn, const CUtensorMap* tm_dn_sh,
                              const CUtensorMap* tm_x, int kb_first) {
+  if (u.has_a && !wait_start_gate(p.status)) {
+    // the start gate stayed closed: the MMAs stop after the prologue's loads
+    record_failure(p.status, sm.abort_flag, kInfoHold);
+    *sm.kb_stop = kb_first;
+    return;
+  }
   Ring ring;
   for (int i = 0; i < kb_first; ++i) ring.next(sm.S);
   int kb = kb_first;

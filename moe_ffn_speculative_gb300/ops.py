@@ -20,6 +20,9 @@ HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "moe.h")
 (MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT,
  MOE_ERR_DEVICE_RANGE) = range(7)
 SCORE_SOFTMAX, SCORE_SIGMOID, SCORE_SQRTSOFTPLUS = 0, 1, 2
+# the workspace's start gate (include/moe.h) and the info word of its timeout
+WS_HOLD_OFFSET = 8
+INFO_HOLD = 15
 
 
 class MoeError(RuntimeError):
@@ -157,8 +160,14 @@ class Workspace:
         return self.buf.data_ptr()
 
     def reset(self, stream=None) -> None:
-        """Zero-fill again (moe_workspace_init), as a call with another shape needs."""
+        """Zero-fill again (moe_workspace_init), as after a device-side error."""
         _check(lib().moe_workspace_init(self.ptr(), self.nbytes, _stream(stream)), "moe_workspace_init")
+
+    def set_start_gate(self, closed: bool, stream=None) -> None:
+        """Close (non-zero) or open (zero) the workspace's start gate."""
+        v = torch.tensor([1 if closed else 0], dtype=torch.int32, device=self.buf.device)
+        with torch.cuda.stream(stream or torch.cuda.current_stream()):
+            self.buf[WS_HOLD_OFFSET:WS_HOLD_OFFSET + 4].copy_(v.view(torch.uint8))
 
     def device_status(self, stream=None) -> Tuple[int, int]:
         info = ctypes.c_int32(0)
@@ -355,20 +364,15 @@ class MoELayer:
             self.I = tensors["w_down"].shape[2]
         self.Is = 0 if tensors.get("sh_gate_up") is None else tensors["sh_down"].shape[1]
         self.max_tokens = max_tokens
+        # one workspace for every token count up to max_tokens: its counters
+        # sit in a fixed header and return to zero after every call
         self.ws = Workspace(ffn_workspace_bytes_upto(max_tokens, self.H, self.I, self.Is, recipe),
                             tensors["gate"].device)
-        self._last_tokens = None
 
     def forward(self, x, y=None, topk_idx_out=None, topk_w_out=None, counts_out=None, stream=None):
         T = x.shape[0]
         if T > self.max_tokens:
             raise ValueError("more tokens than the workspace was sized for")
-        if T > 0:
-            # the workspace's self-resetting counters sit at offsets that
-            # depend on the token count: another count starts from zeros
-            if self._last_tokens is not None and T != self._last_tokens:
-                self.ws.reset(stream)
-            self._last_tokens = T
         t = self.t
         if self.fp4:
             return moe_ffn_forward_fp4(x, t["gate"], t["w_gate_up_q"], t["w_down_q"], self.scales, self.recipe,

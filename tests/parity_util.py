@@ -93,6 +93,15 @@ def output_rounding_error(y_ref):
     return float(np.abs(bf(y_ref) - y_ref).max() / np.sqrt(np.mean(y_ref ** 2)))
 
 
+def expert_coverage(idx_rows, counts) -> tuple:
+    """(touched experts that the compared rows reach, touched experts in the
+    forward): the compared rows meet every expert tile the GPU streamed only
+    when the two are equal."""
+    touched = set(np.nonzero(np.asarray(counts) > 0)[0].tolist())
+    reached = set(np.unique(np.asarray(idx_rows)).tolist()) & touched
+    return len(reached), len(touched)
+
+
 def report(**kw):
     """Append one parity record to $MOE_PARITY_REPORT (a JSON-lines file)."""
     import json

@@ -75,3 +75,49 @@ def test_zero_tokens_launch_nothing(lib):
     rec = ops.Recipe.make(8, 2)
     assert _forward(lib, rec, T=0) == ops.MOE_OK
     assert lib.moe_route_from_logits(None, 0, None, ctypes.byref(rec), None, None, None) == ops.MOE_OK
+
+
+def test_workspace_refusals_before_any_device_call(lib):
+    """A workspace missing, misaligned or smaller than the fixed header is
+    refused on the host, before the library asks the device anything."""
+    rec = ops.Recipe.make(8, 2)
+    args = (1 << 20, 16, 64, 32, 3 << 20, None, None, 4 << 20, 5 << 20, None, None, 0, None, ctypes.byref(rec))
+    tail = (2 << 20, None, None, None, None)
+    assert lib.moe_ffn_forward(*args, None, 1 << 30, *tail) == ops.MOE_ERR_WORKSPACE
+    assert lib.moe_ffn_forward(*args, (6 << 20) + 64, 1 << 30, *tail) == ops.MOE_ERR_WORKSPACE
+    assert lib.moe_ffn_forward(*args, 6 << 20, 4096, *tail) == ops.MOE_ERR_WORKSPACE
+    # the router: one byte short of moe_route_workspace_bytes
+    need = lib.moe_route_workspace_bytes(72, 8)
+    assert lib.moe_route(1 << 20, 72, 64, 3 << 20, None, None, ctypes.byref(rec), None, 4 << 20, 5 << 20,
+                         6 << 20, need - 1, None) == ops.MOE_ERR_WORKSPACE
+
+
+def test_route_workspace_size_does_not_depend_on_where_counters_sit(lib):
+    """The router's counters sit in a fixed header: the size grows with the
+    logits only, by 4 bytes per (token, expert) rounded to 256."""
+    base = lib.moe_route_workspace_bytes(0, 8)
+    for T, E in [(1, 8), (72, 256), (4096, 64), (65536, 1)]:
+        assert lib.moe_route_workspace_bytes(T, E) == base + -(-4 * T * E // 256) * 256
+
+
+def test_noalloc_router_checks_arguments_first(lib):
+    """moe_route_noalloc makes moe_route's checks before it touches its array:
+    an invalid recipe is INVALID_ARG (not a size refusal), sizes beyond the
+    array are UNSUPPORTED, T = 0 is OK -- none of it needs a device."""
+    x, gate, idx, w = 1 << 20, 2 << 20, 3 << 20, 4 << 20
+    e0 = ops.Recipe(0, 1, 0, 1, 1, 2, 1, 1e-20, 1.0, 0.0)
+    assert lib.moe_route_noalloc(x, 72, 64, gate, None, None, ctypes.byref(e0), None, idx, w, None) == \
+        ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_noalloc(x, 72, 64, gate, None, None, None, None, idx, w, None) == ops.MOE_ERR_INVALID_ARG
+    rec = ops.Recipe.make(8, 2)
+    assert lib.moe_route_noalloc(None, 72, 64, gate, None, None, ctypes.byref(rec), None, idx, w, None) == \
+        ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_noalloc(x + 2, 72, 64, gate, None, None, ctypes.byref(rec), None, idx, w, None) == \
+        ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_noalloc(x, 4097, 64, gate, None, None, ctypes.byref(rec), None, idx, w, None) == \
+        ops.MOE_ERR_UNSUPPORTED
+    big = ops.Recipe.make(128, 2)
+    assert lib.moe_route_noalloc(x, 4096, 64, gate, None, None, ctypes.byref(big), None, idx, w, None) == \
+        ops.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route_noalloc(None, 0, 64, None, None, None, ctypes.byref(rec), None, None, None, None) == \
+        ops.MOE_OK

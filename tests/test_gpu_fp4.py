@@ -17,7 +17,7 @@ import oracle as O
 from moe_ffn_speculative_gb300 import ops
 from moe_ffn_speculative_gb300 import synthetic as S
 from moe_ffn_speculative_gb300.build import build
-from parity_util import (Y_TOL, compare_routing, np64, oracle_recipe, output_rounding_error,
+from parity_util import (Y_TOL, compare_routing, expert_coverage, np64, oracle_recipe, output_rounding_error,
                          max_abs_over_rms, report)
 
 pytestmark = pytest.mark.gpu
@@ -115,17 +115,22 @@ FULL = [("dsv41_dspark_draft", 72), ("dsv4_flash_drafter", 72), ("dsv4_style", 5
 
 
 @pytest.mark.parametrize("name,T", FULL)
-def test_fp4_layer_full_size_sampled(name, T):
+def test_fp4_layer_full_size(name, T):
+    """Every output row against the oracle, so every touched expert's FP4
+    tiles meet it."""
     cfg = S.CONFIGS[name].with_(T=T, expert_format=F)
     d = S.make_inputs(cfg, device="cuda")
     layer, y, idx, w, counts = _run(cfg, d)
-    rows = np.unique(np.linspace(0, T - 1, 8).round().astype(int))
-    oidx, ow, margin, y_ref = _oracle(cfg, d, rows)
+    oidx, ow, margin, y_ref = _oracle(cfg, d)
     n_amb, _ = compare_routing(idx, w, oidx, ow, margin, w_tol=E2E_W_TOL, margin_tol=E2E_MARGIN_TOL)
     assert n_amb == 0
-    err = max_abs_over_rms(y[torch.as_tensor(rows, device="cuda")], y_ref)
+    gcounts = counts.cpu().numpy()
+    np.testing.assert_array_equal(gcounts, np.bincount(oidx.reshape(-1), minlength=cfg.E))
+    reached, touched = expert_coverage(oidx, gcounts)
+    err = max_abs_over_rms(y, y_ref)
     report(test="fp4_layer_full", case=f"{name}_T{T}", max_abs_over_rms=err,
-           output_rounding=output_rounding_error(y_ref), rows=len(rows))
+           output_rounding=output_rounding_error(y_ref), rows=T, experts_covered=reached, experts_touched=touched)
+    assert reached == touched
     assert err <= Y_TOL, f"max |dy| / RMS(y) = {err}"
     assert layer.ws.device_status() == (0, 0)
 

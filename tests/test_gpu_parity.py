@@ -26,7 +26,7 @@ import oracle as O
 from moe_ffn_speculative_gb300 import ops
 from moe_ffn_speculative_gb300 import synthetic as S
 from moe_ffn_speculative_gb300.build import build
-from parity_util import (MARGIN_TOL, W_ABS_TOL, Y_TOL, bf16_floor_error, compare_routing, np64,
+from parity_util import (MARGIN_TOL, W_ABS_TOL, Y_TOL, bf16_floor_error, compare_routing, expert_coverage, np64,
                          oracle_recipe, oracle_rows, output_rounding_error, max_abs_over_rms, report)
 
 pytestmark = pytest.mark.gpu
@@ -366,7 +366,7 @@ def test_automatic_schedule_choice():
 
 
 @pytest.mark.parametrize("name,T,sched", FULL)
-def test_layer_full_size_sampled(name, T, sched):
+def test_layer_full_size(name, T, sched):
     cfg = S.CONFIGS[name].with_(T=T)
     if sched is not None:
         _require(cfg, SCHEDULES[sched])
@@ -376,6 +376,9 @@ def test_layer_full_size_sampled(name, T, sched):
 
 
 def _check_full(cfg, name, T, used):
+    """Every output row against the oracle (so every touched expert's tiles
+    of both GEMMs, every span boundary and every split tile of the launch
+    meet it), plus the fp32 logits, the routing and the counts."""
     d = S.make_inputs(cfg, device="cuda")
     layer, y, idx, w, counts = _run_layer(cfg, d)
     orec, logits, oidx, ow, margin = _oracle_routing(cfg, d)
@@ -387,14 +390,16 @@ def _check_full(cfg, name, T, used):
     assert lerr <= LOGIT_TOL, f"logit error {lerr}"
     n_amb, same = compare_routing(idx, w, oidx, ow, margin, w_tol=E2E_W_TOL, margin_tol=E2E_MARGIN_TOL)
     assert n_amb == 0, f"{n_amb} ambiguous rows"
-    np.testing.assert_array_equal(counts.cpu().numpy(), np.bincount(oidx.reshape(-1), minlength=cfg.E))
-    n_s = 4 if name == "dsv3_style" else 8
-    rows = np.unique(np.linspace(0, T - 1, n_s).round().astype(int))
-    y_ref = oracle_rows(d, cfg, rows, oidx[rows], ow[rows])
-    err = max_abs_over_rms(y[torch.as_tensor(rows, device="cuda")], y_ref)
+    gcounts = counts.cpu().numpy()
+    np.testing.assert_array_equal(gcounts, np.bincount(oidx.reshape(-1), minlength=cfg.E))
+    rows = np.arange(T)
+    y_ref = oracle_rows(d, cfg, rows, oidx, ow)
+    reached, touched = expert_coverage(oidx, gcounts)
+    err = max_abs_over_rms(y, y_ref)
     out_round = output_rounding_error(y_ref)
     report(test="layer_full", case=f"{name}_T{T}", schedule=used, max_abs_over_rms=err, output_rounding=out_round,
-           logit_err=float(lerr), rows=len(rows))
+           logit_err=float(lerr), rows=len(rows), experts_covered=reached, experts_touched=touched)
+    assert reached == touched
     assert err <= Y_TOL, f"max |dy| / RMS(y) = {err} (bf16 output rounding alone: {out_round})"
     y2 = layer.forward(d["x"])
     torch.cuda.synchronize()

@@ -127,6 +127,74 @@ def test_route_writes_stay_inside_its_workspace():
     assert ws.margins_intact(), "a write outside the router's workspace"
 
 
+def _fresh_forward(cfg, d, x):
+    layer = ops.MoELayer(d, ops.Recipe.from_config(cfg), max_tokens=x.shape[0])
+    y = layer.forward(x)
+    torch.cuda.synchronize()
+    assert layer.ws.device_status() == (0, 0)
+    return y
+
+
+REUSE = {
+    # 12 experts + gated shared expert: the fused kernel at 128 tokens,
+    # stream-K with 16-column tiles at 9 and 80-column tiles at 200
+    "A": S.LayerConfig("reuse_a", T=200, H=2048, E=12, I=128, K=1, shared_I=128, shared_gated=True,
+                       router_bias_std=0.1, seed=43),
+    # another shape on the fused kernel (top-1, y written directly)
+    "B": S.LayerConfig("reuse_b", T=72, H=512, E=8, I=384, K=1, seed=44),
+    # grouped sigmoid top-8 of 64 experts on stream-K, more than 1024 tokens
+    # at the largest count (the logits GEMM)
+    "C": S.LayerConfig("reuse_c", T=1100, H=320, E=64, I=160, K=8, score_fn=1, n_group=8, topk_group=4,
+                       expert_bias_std=0.05, shared_I=96, seed=45),
+}
+SEQUENCE = [("A", 128), ("B", 72), ("A", 200), ("C", 1100), ("A", 9), ("B", 40), ("C", 17), ("C", 300),
+            ("A", 128), ("B", 72)]
+
+
+def test_one_workspace_serves_every_count_and_shape_without_reset():
+    """One workspace, zero-filled once, sized for the largest need, serves a
+    sequence of forwards that change the token count, the shape, the recipe
+    and the schedule, with no reset in between: every counter sits in the
+    fixed header and returns to zero.  Every output equals that of a fresh
+    workspace, bit for bit."""
+    data = {k: {n: (None if v is None else v.cuda()) for n, v in S.make_inputs(c).items()}
+            for k, c in REUSE.items()}
+    need = max(ops.ffn_workspace_bytes(T, REUSE[k].H, REUSE[k].I, REUSE[k].shared_I,
+                                       ops.Recipe.from_config(REUSE[k])) for k, T in SEQUENCE)
+    ws = GuardedWorkspace(need)
+    scheds = set()
+    for k, T in SEQUENCE:
+        cfg, d = REUSE[k], data[k]
+        rec = ops.Recipe.from_config(cfg)
+        x = d["x"][:T].contiguous()
+        scheds.add(ops.ffn_schedule(T, cfg.H, cfg.I, cfg.shared_I, rec, gated=cfg.shared_gated))
+        y = ops.moe_ffn_forward(x, d["gate"], d["w_gate_up"], d["w_down"], rec, ws, router_bias=d["router_bias"],
+                                expert_bias=d["expert_bias"], sh_gate_up=d["sh_gate_up"], sh_down=d["sh_down"],
+                                sh_gate=d["sh_gate"])
+        torch.cuda.synchronize()
+        assert ws.device_status() == (0, 0), (k, T)
+        assert torch.equal(y, _fresh_forward(cfg, d, x)), (k, T)
+    assert scheds == {ops.SCHEDULE_SLICE, ops.SCHEDULE_STREAM_K}
+    assert ws.margins_intact()
+
+
+def test_one_router_workspace_serves_every_count_without_reset():
+    E, H = 64, 256
+    g = torch.Generator().manual_seed(46)
+    x = torch.randn((4096, H), generator=g).to(torch.bfloat16).cuda()
+    gate = (torch.randn((E, H), generator=g) * 0.02).to(torch.bfloat16).cuda()
+    rec = ops.Recipe.make(E, 6, score_fn=ops.SCORE_SQRTSOFTPLUS, route_scale=1.5)
+    ws = GuardedWorkspace(ops.lib().moe_route_workspace_bytes(4096, E))
+    for T in (9, 4096, 72, 1100, 9):
+        xt = x[:T].contiguous()
+        i, w, _ = ops.moe_route(xt, gate, rec, ws=ws)
+        i_ref, w_ref, _ = ops.moe_route(xt, gate, rec)
+        torch.cuda.synchronize()
+        assert ws.device_status() == (0, 0), T
+        assert torch.equal(i, i_ref) and torch.equal(w, w_ref), T
+    assert ws.margins_intact()
+
+
 def test_layer_reused_across_token_counts():
     """One MoELayer serves token counts that change its schedule and token
     tile: 128 tokens take the fused kernel (12 experts and the gated shared
@@ -134,8 +202,7 @@ def test_layer_reused_across_token_counts():
     tile, 200 tokens stream-K with 80-column tiles (a smaller workspace need
     than at 128).  Every forward equals that of a layer built for exactly
     its count."""
-    cfg = S.LayerConfig("reuse", T=200, H=2048, E=12, I=128, K=1, shared_I=128, shared_gated=True,
-                        router_bias_std=0.1, seed=43)
+    cfg = REUSE["A"]
     d = {k: (None if v is None else v.cuda()) for k, v in S.make_inputs(cfg).items()}
     rec = ops.Recipe.from_config(cfg)
     layer = ops.MoELayer(d, rec, max_tokens=cfg.T)
@@ -144,6 +211,4 @@ def test_layer_reused_across_token_counts():
         y = layer.forward(x)
         torch.cuda.synchronize()
         assert layer.ws.device_status() == (0, 0)
-        y_ref = ops.MoELayer(d, rec, max_tokens=T).forward(x)
-        torch.cuda.synchronize()
-        assert torch.equal(y, y_ref), f"T={T}"
+        assert torch.equal(y, _fresh_forward(cfg, d, x)), f"T={T}"

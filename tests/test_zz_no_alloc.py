@@ -46,6 +46,38 @@ def test_noalloc_router_matches_workspace_router_on_consecutive_calls():
     _check_same(top1, *a)      # and back: nothing left over from the larger call
 
 
+def _check_same_no_logits(rec, x, gate, eb):
+    """With logits_out NULL the fp32 logits live in the library's array."""
+    i_ref, w_ref, _ = ops.moe_route(x, gate, rec, expert_bias=eb, want_logits=False)
+    i_na, w_na, l_na = ops.moe_route_noalloc(x, gate, rec, expert_bias=eb, want_logits=False)
+    torch.cuda.synchronize()
+    assert l_na is None
+    assert torch.equal(i_na, i_ref)
+    assert (w_na - w_ref).abs().max().item() <= W_ABS_TOL
+
+
+def test_noalloc_router_logits_in_its_own_array():
+    """Back-to-back calls whose logits stay inside the array: a decode-sized
+    call, one above 1024 tokens (the tiled logits GEMM, then selection on
+    8-token blocks), one that fills the array exactly (T*E equal to its
+    logits limit), then the small call again, so that leftovers of a larger
+    call would show."""
+    build()
+    ops.lib()
+    small = ops.Recipe.make(8, 2)
+    mid = ops.Recipe.make(64, 6, score_fn=ops.SCORE_SQRTSOFTPLUS, route_scale=1.5)
+    full = ops.Recipe.make(64, 4, score_fn=ops.SCORE_SIGMOID, n_group=8, topk_group=4, route_scale=2.5)
+    a = _case(72, 4096, 8, seed=11)
+    b = _case(2048, 1024, 64, seed=12, expert_bias=True)
+    c = _case(4096, 512, 64, seed=13, expert_bias=True)
+    assert 4096 * 64 == 262144  # MOE_NOALLOC_MAX_LOGITS
+    _check_same_no_logits(small, *a)
+    _check_same_no_logits(mid, *b)
+    _check_same_no_logits(full, *c)
+    _check_same_no_logits(small, *a)
+    _check_same(full, *c)  # and with the logits returned
+
+
 def test_noalloc_router_refuses_sizes_beyond_its_array():
     build()
     rec = ops.Recipe.make(512, 10)
