@@ -88,6 +88,19 @@ def bf_pair(a):
     return hi + bf(a - hi)
 
 
+def beyond_one_ulp(y_gpu, y_ref, abs_floor_rms=1e-3) -> int:
+    """Elements of the bf16 output farther from the exact output than one
+    bf16 ulp of the exact value (plus abs_floor_rms x RMS, which covers the
+    fp32 accumulation's absolute error on near-zero outputs).  An output that
+    is the exact result rounded to bf16, give or take the last bit, has
+    none."""
+    yg = y_gpu.detach().to("cpu").to(torch.float64).numpy()
+    _, ex = np.frexp(y_ref)
+    ulp = np.ldexp(1.0, ex - 8)
+    floor = abs_floor_rms * float(np.sqrt(np.mean(y_ref ** 2)))
+    return int((np.abs(yg - y_ref) > ulp + floor).sum())
+
+
 def output_rounding_error(y_ref):
     """max |dy| / RMS(y) of rounding the exact output to bf16 alone."""
     return float(np.abs(bf(y_ref) - y_ref).max() / np.sqrt(np.mean(y_ref ** 2)))

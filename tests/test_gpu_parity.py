@@ -6,11 +6,15 @@ Bars (from the routing/equivalence requirements of the MoE-FFN layer):
   where fp32 and fp64 shifted scores tie within MARGIN_TOL), weights within
   1e-6 absolute;
 * permutation: counts, offsets, sorted pairs and positions bit-exact;
-* layer output: max |y - y_oracle| / RMS(y_oracle) <= 2e-2 on the five
-  workloads; on the small test layers the bar is max(2e-2, 1.25 x the error
-  that the path's own roundings -- h as a bf16 hi+lo pair, y in bf16 --
-  produce alone), since a few heavy-tailed small-I layers (max|y| ~ 7 RMS)
-  exceed 2e-2 from the bf16 output rounding alone;
+* layer output: max |y - y_oracle| / RMS(y_oracle) <= 2e-2, or, where the
+  rounding of the exact output to bf16 alone exceeds that (a heavy-tailed
+  output: on the Qwen3.8-27B-style layer at full size the largest element is
+  about 5.5 RMS and its bf16 rounding alone is 0.0215 RMS), 1.25 x that
+  rounding floor -- on the small layers the floor also counts h's bf16 hi+lo
+  pair; the bar cannot ask for less than the output's own dtype gives;
+* full-size layers additionally: every output element within one bf16 ulp
+  (+1e-3 RMS) of the exact output, i.e. the exact result rounded to bf16
+  give or take its last bit;
 * end-to-end routing (GPU fp32 logits vs exact logits): logits within 3e-5
   (about 6x the fp32 accumulation error u*sqrt(H)*|logit| at H <= 7168,
   |logit| <= ~10), no index mismatch with a margin above 1e-4, weights within
@@ -26,7 +30,8 @@ import oracle as O
 from moe_ffn_speculative_gb300 import ops
 from moe_ffn_speculative_gb300 import synthetic as S
 from moe_ffn_speculative_gb300.build import build
-from parity_util import (MARGIN_TOL, W_ABS_TOL, Y_TOL, bf16_floor_error, compare_routing, expert_coverage, np64,
+from parity_util import (MARGIN_TOL, W_ABS_TOL, Y_TOL, beyond_one_ulp, bf16_floor_error, compare_routing,
+                         expert_coverage, np64,
                          oracle_recipe, oracle_rows, output_rounding_error, max_abs_over_rms, report)
 
 pytestmark = pytest.mark.gpu
@@ -397,10 +402,14 @@ def _check_full(cfg, name, T, used):
     reached, touched = expert_coverage(oidx, gcounts)
     err = max_abs_over_rms(y, y_ref)
     out_round = output_rounding_error(y_ref)
+    tol = max(Y_TOL, 1.25 * out_round)
+    n_ulp = beyond_one_ulp(y, y_ref)
     report(test="layer_full", case=f"{name}_T{T}", schedule=used, max_abs_over_rms=err, output_rounding=out_round,
-           logit_err=float(lerr), rows=len(rows), experts_covered=reached, experts_touched=touched)
+           tol=tol, beyond_one_ulp=n_ulp, logit_err=float(lerr), rows=len(rows), experts_covered=reached,
+           experts_touched=touched)
     assert reached == touched
-    assert err <= Y_TOL, f"max |dy| / RMS(y) = {err} (bf16 output rounding alone: {out_round})"
+    assert err <= tol, f"max |dy| / RMS(y) = {err} (bf16 output rounding alone: {out_round})"
+    assert n_ulp == 0, f"{n_ulp} outputs farther than one bf16 ulp from the exact output"
     y2 = layer.forward(d["x"])
     torch.cuda.synchronize()
     assert torch.equal(y, y2), "not deterministic"
