@@ -327,6 +327,13 @@ def run_reference(args, cfg, rank, world):
 TARGET_WORKLOADS = [("qwen38_27b_dspark", 72), ("dsv3_style", 72), ("dsv4_style", 72)]
 SWEEP_WORKLOADS = [("dsv4_style", 9), ("dsv4_style", 576), ("dsv4_style", 4096)]
 NOMINAL_HBM_GBS = 8000.0
+_T0 = time.perf_counter()
+
+
+def log(msg: str) -> None:
+    """Progress on stderr (the JSON line alone goes to stdout)."""
+    sys.stderr.write(f"[bench {time.perf_counter() - _T0:7.1f}s] {msg}\n")
+    sys.stderr.flush()
 
 
 class Workload:
@@ -371,6 +378,9 @@ class Workload:
             self.timed = {n: k for k, n in enumerate(["router", "experts", "combine"][:self.launched])}
             if cfg.T > 1024 and not self.fp4:
                 self.launched += 1
+        # inputs and the zero-filled workspace were made on torch's current
+        # stream; the layer runs on its own stream
+        torch.cuda.synchronize()
 
     def call(self, dd, xx, yy, cnt=None):
         ops, kw = self.ops, dict(router_bias=dd["router_bias"], expert_bias=dd["expert_bias"],
@@ -505,8 +515,10 @@ def workload_key(cfg, args_override: bool):
 def measure_extra(cfg, dev, rank, K, W, hbm, tflops, peak_src, sustain_s):
     """One more workload in the same process: graph replay of K layers after
     W warm-up layers, per-kernel event times, and a sustained replay."""
+    log(f"{cfg.name} T={cfg.T}: inputs")
     wl = Workload(cfg, dev, rank, "auto")
     try:
+        log(f"{cfg.name} T={cfg.T}: first forward ({wl.sched})")
         u = wl.first_forward()
         G = pick_G(K, wl.n_copies)
         g = wl.graph(G)
@@ -515,8 +527,10 @@ def measure_extra(cfg, dev, rank, K, W, hbm, tflops, peak_src, sustain_s):
         torch.cuda.synchronize()
         ms_step = wl.replay_ms(g, K // G) / K
         n_sus = max(1, int(sustain_s / (ms_step * 1e-3) / G))
+        log(f"{cfg.name} T={cfg.T}: {ms_step * 1e3:.1f} us/layer; sustained x{n_sus}")
         ms_sus = wl.replay_ms(g, n_sus) / (n_sus * G)
         del g
+        log(f"{cfg.name} T={cfg.T}: kernel times")
         per_kernel = wl.kernel_us(G, max(2, min(25, 200 // G)))
         wl.check_status("after the timed region")
         roof, layer = roofline_record(wl, u, per_kernel, ms_step, hbm, tflops, peak_src,
@@ -548,7 +562,9 @@ def run_gpu(args, cfg, rank, world):
     K = args.steps if args.steps is not None else 20000
     W = max(3, args.warmup if args.warmup is not None else 50)
     hbm, tflops, peak_src = measured_peaks()
+    log(f"{cfg.name} T={cfg.T}: inputs")
     wl = Workload(cfg, dev, rank, args.schedule)
+    log(f"{cfg.name} T={cfg.T}: first forward ({wl.sched})")
     u = wl.first_forward()
     G = pick_G(K, wl.n_copies)
     graph = wl.graph(G)
@@ -575,10 +591,13 @@ def run_gpu(args, cfg, rank, world):
     value = cfg.T * K * world / (ms_total / 1e3)
     # ---- the same graph replayed for at least `sustain` seconds
     n_sus = max(1, int(args.sustain / (ms_step * 1e-3) / G))
+    log(f"{cfg.name} T={cfg.T}: {ms_step * 1e3:.1f} us/layer; sustained x{n_sus}")
     ms_sus = max_over_ranks(wl.replay_ms(graph, n_sus), world) / (n_sus * G)
     del graph
+    log(f"{cfg.name} T={cfg.T}: kernel times")
     per_kernel = wl.kernel_us(G, max(2, min(25, 200 // G)))
     # ---- end to end through the C ABI with host buffers
+    log(f"{cfg.name} T={cfg.T}: end to end")
     n_e2e = min(K, 2000)
     ms_e2e = max_over_ranks(wl.e2e(n_e2e), world)
     e2e_value = cfg.T * n_e2e * world / (ms_e2e / 1e3)
@@ -629,7 +648,9 @@ def run_gpu(args, cfg, rank, world):
     if extra:
         line["workloads"] = extra
     if not args.no_cpu_baseline:
+        log("CPU oracle")
         line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
+    log("done")
     print(json.dumps(line), flush=True)
 
 

@@ -625,6 +625,14 @@ moe_status ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf16* g
   gp.ready = tiles + L.max_gu_tiles + L.max_dn_tiles;
   gp.I = I;
   gp.E = E;
+  gp.g_max = L.g_max;
+  gp.max_gu_tiles = L.max_gu_tiles;
+  gp.max_dn_tiles = L.max_dn_tiles;
+  {
+    const int Imax = Is > I ? Is : I;
+    gp.max_gu_iters = static_cast<long long>(L.max_gu_tiles) * ceil_div(H, kBlockK);
+    gp.max_dn_iters = static_cast<long long>(L.max_dn_tiles) * ceil_div(Imax, kBlockK);
+  }
   if (fp4) {
     gp.xh = xh;
     gp.gu_scale = fp4->scales;

@@ -57,24 +57,37 @@ struct Seg {
 // iterations, one (tile, k-range) segment at a time.
 struct Sched {
   const GroupEntry* groups;
-  int ngroups, phase, H, n_max, g;
+  int ngroups, phase, H, n_max, g, rows, idim_max;
   long long end, it;
+  bool bad;  // a group entry outside the forward's bounds: the walk stops there
 
   __device__ long long iter_of(int gi) const { return phase == 0 ? groups[gi].gu_iter : groups[gi].dn_iter; }
 
   // [b, e): the CTA's iterations; g0: the group holding iteration b
-  __device__ void init(const GroupEntry* gs, int ng, int ph, int H_, int nmax, long long b, long long e, int g0) {
-    groups = gs; ngroups = ng; phase = ph; H = H_; n_max = nmax; it = b; end = e; g = g0;
+  __device__ void init(const GemmParams& p, int ng, int ph, long long b, long long e, int g0) {
+    groups = p.groups; ngroups = ng; phase = ph; H = p.H; n_max = p.n_max; it = b; end = e; g = g0;
+    rows = p.TK + p.T;
+    idim_max = p.I_ld;
+    bad = false;
   }
 
   __device__ bool next(Seg& s) {
-    if (it >= end) return false;
+    if (it >= end || bad) return false;
     while (g + 1 < ngroups && iter_of(g + 1) <= it) ++g;
     const GroupEntry ge = groups[g];
+    const long long start = phase == 0 ? ge.gu_iter : ge.dn_iter;
+    if (g < 0 || g >= ngroups || ge.count < 1 || ge.row_base < 0 || ge.count > rows - ge.row_base ||
+        ge.idim < 1 || ge.idim > idim_max || start < 0 || start > it) {
+      bad = true;
+      return false;
+    }
     int mb, nb, kb;
     group_geometry(phase, ge.count, ge.idim, H, n_max, mb, nb, kb);
-    const long long start = phase == 0 ? ge.gu_iter : ge.dn_iter;
     const long long local = it - start;
+    if (local >= static_cast<long long>(mb) * nb * kb) {
+      bad = true;
+      return false;
+    }
     const int tile_in = static_cast<int>(local / kb);
     const int k0 = static_cast<int>(local % kb);
     const long long left = end - it;
@@ -215,8 +228,8 @@ struct WeightCursor {
 
   __device__ void init(const GemmParams& p, int ngroups, const long long (&b)[2], const long long (&e)[2],
                        const int (&g)[2]) {
-    sc0.init(p.groups, ngroups, 0, p.H, p.n_max, b[0], e[0], g[0]);
-    sc1.init(p.groups, ngroups, 1, p.H, p.n_max, b[1], e[1], g[1]);
+    sc0.init(p, ngroups, 0, b[0], e[0], g[0]);
+    sc1.init(p, ngroups, 1, b[1], e[1], g[1]);
     ph = 0;
     kk = 0;
     valid = false;
@@ -334,6 +347,10 @@ __device__ bool produce(const Smem& sm, const GemmParams& p, int ngroups, const 
     ld.step();
     ring.next(sm.S);
   }
+  if (ld.sc0.bad || ld.sc1.bad) {
+    record_failure(status, sm.abort_flag, kInfoWorkList);
+    return false;
+  }
   return true;
 }
 
@@ -342,7 +359,7 @@ template <int PHASE, bool kFp4>
 __device__ bool issue_mma(const Smem& sm, const GemmParams& p, int ngroups, long long begin, long long end, int g0,
                           uint32_t tmem_base, Ring& ring, int& seg_i, int32_t* status) {
   Sched sc;
-  sc.init(p.groups, ngroups, PHASE, p.H, p.n_max, begin, end, g0);
+  sc.init(p, ngroups, PHASE, begin, end, g0);
   Seg sg;
   while (sc.next(sg)) {
     const int buf = seg_i % p.nbuf;
@@ -385,6 +402,10 @@ __device__ bool issue_mma(const Smem& sm, const GemmParams& p, int ngroups, long
     mma_commit(&sm.accf[buf]);
     ++seg_i;
   }
+  if (sc.bad) {
+    record_failure(status, sm.abort_flag, kInfoWorkList);
+    return false;
+  }
   return true;
 }
 
@@ -411,7 +432,7 @@ __device__ bool gather(const Smem& sm, const GemmParams& p, int ngroups, long lo
     }
   }
   Sched sc;
-  sc.init(p.groups, ngroups, PHASE, p.H, p.n_max, begin, end, g0);
+  sc.init(p, ngroups, PHASE, begin, end, g0);
   constexpr int kBTiles = PHASE == 0 ? 1 : 2;
   Seg sg;
   while (sc.next(sg)) {
@@ -512,6 +533,10 @@ __device__ bool gather(const Smem& sm, const GemmParams& p, int ngroups, long lo
       }
       ring.next(sm.S);
     }
+  }
+  if (sc.bad) {
+    if (lane == 0) record_failure(status, sm.abort_flag, kInfoWorkList);
+    return false;
   }
   return true;
 }
@@ -618,6 +643,10 @@ __device__ bool convert(const Smem& sm, const GemmParams& p, int ngroups, const 
     ring.next(sm.S);
   }
   if (!range_ok) record_range(status, kInfoScaleRange);
+  if (ld.sc0.bad || ld.sc1.bad) {
+    if (r == 0) record_failure(status, sm.abort_flag, kInfoWorkList);
+    return false;
+  }
   return true;
 }
 
@@ -626,7 +655,7 @@ template <int PHASE, bool kFp4>
 __device__ bool epilogue(const Smem& sm, const GemmParams& p, int ngroups, long long begin, long long end, int g0,
                          uint32_t tmem_base, int& seg_i, int32_t* tile_counters, int32_t* status) {
   Sched sc;
-  sc.init(p.groups, ngroups, PHASE, p.H, p.n_max, begin, end, g0);
+  sc.init(p, ngroups, PHASE, begin, end, g0);
   const long long* span = sm.span + PHASE * (gridDim.x + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
@@ -761,6 +790,10 @@ __device__ bool epilogue(const Smem& sm, const GemmParams& p, int ngroups, long 
     epi_sync();
     ++seg_i;
   }
+  if (sc.bad) {
+    if (leader) record_failure(status, sm.abort_flag, kInfoWorkList);
+    return false;
+  }
   return true;
 }
 
@@ -834,10 +867,27 @@ __global__ void __launch_bounds__(kFp4 ? kGemmThreadsFp4 : kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int ng = p.header->ngroups;
+  // The router's work list, checked against the host's bounds (every thread
+  // reads the same words, so the decision is uniform): a list outside them
+  // -- a workspace that was not zero-filled, or was overwritten -- is
+  // refused instead of streamed.
+  const GemmHeader hd = *p.header;
+  const int G1 = gridDim.x + 1;
+  const long long bs[2] = {sm.span[blockIdx.x], sm.span[G1 + blockIdx.x]};
+  const long long es[2] = {sm.span[blockIdx.x + 1], sm.span[G1 + blockIdx.x + 1]};
+  const int gs[2] = {p.span_groups[blockIdx.x], p.span_groups[G1 + blockIdx.x]};
+  const bool list_ok = hd.ngroups >= 0 && hd.ngroups <= p.g_max && hd.gu_tiles >= 0 &&
+                       hd.gu_tiles <= p.max_gu_tiles && hd.dn_tiles >= 0 && hd.dn_tiles <= p.max_dn_tiles &&
+                       hd.n_eff >= 16 && hd.n_eff <= p.n_max && (hd.n_eff & 15) == 0 && hd.gu_iters >= 0 &&
+                       hd.gu_iters <= p.max_gu_iters && hd.dn_iters >= 0 && hd.dn_iters <= p.max_dn_iters &&
+                       bs[0] >= 0 && bs[0] <= es[0] && es[0] <= hd.gu_iters && bs[1] >= 0 && bs[1] <= es[1] &&
+                       es[1] <= hd.dn_iters && gs[0] >= 0 && gs[0] <= hd.ngroups && gs[1] >= 0 &&
+                       gs[1] <= hd.ngroups;
+  if (!list_ok && threadIdx.x == 0) record_failure(p.status, sm.abort_flag, kInfoWorkList);
+  const int ng = hd.ngroups;
   // Stages are sized for the widest token tile this forward actually has,
   // so narrow tiles (decode) get more stages in the same shared memory.
-  sm.b_bytes = p.header->n_eff * 128;
+  sm.b_bytes = (list_ok ? hd.n_eff : 16) * 128;
   sm.stage_bytes = 2 * kTileBytesA + 2 * sm.b_bytes;
   sm.S = min(kMaxStages, p.stage_space / static_cast<int>(sm.stage_bytes));
   if (kFp4) {
@@ -853,13 +903,9 @@ __global__ void __launch_bounds__(kFp4 ? kGemmThreadsFp4 : kGemmThreads, 1)
     sm.sbase = sm.pbase + sm.SP * kPackedBytes;
     sm.base = sm.sbase + ((sm.SP * 512 + 1023) & ~1023);
   }
-  // this CTA's cost-balanced spans of the gate_up and down iterations
-  const int G1 = gridDim.x + 1;
-  const long long bs[2] = {sm.span[blockIdx.x], sm.span[G1 + blockIdx.x]};
-  const long long es[2] = {sm.span[blockIdx.x + 1], sm.span[G1 + blockIdx.x + 1]};
-  const int gs[2] = {p.span_groups[blockIdx.x], p.span_groups[G1 + blockIdx.x]};
-
-  if (warp == 0) {
+  if (!list_ok) {
+    // nothing issued: every thread goes straight to the teardown
+  } else if (warp == 0) {
     if (lane == 0) {
       Ring ring;
       const bool ok = produce<kFp4>(sm, p, ng, bs, es, gs, &tm_gu, &tm_gu_sh, &tm_dn, &tm_dn_sh, ring, p.status);

@@ -27,7 +27,10 @@ enum : int32_t {
   // value of x or h outside the f16 range of the FP4 experts' MMAs
   kInfoScaleRange = 12, kInfoXRange = 13, kInfoHRange = 14,
   // the start gate (status word 2) stayed closed for the whole wait
-  kInfoHold = 15
+  kInfoHold = 15,
+  // the router's work list is outside the bounds the host computed (a
+  // workspace that was not zero-filled before its first use, or overwritten)
+  kInfoWorkList = 16
 };
 
 // ----------------------------------------------------------------------------
@@ -138,6 +141,9 @@ struct GemmParams {
   const uint8_t* dn_scale;     // (expert, tile, k-block), gate_up blocks first, then down
   int I, E;                    // routed experts' I, expert count
   int h_tma;                   // the down GEMM loads h rows by TMA (I, Is multiples of 64)
+  // host-computed bounds of the router's work list, checked before use
+  int g_max, max_gu_tiles, max_dn_tiles;
+  long long max_gu_iters, max_dn_iters;
 };
 
 // Routing recipe as the selection code reads it (score_fn 0 softmax,
