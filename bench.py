@@ -188,22 +188,38 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def ncu_traffic(schedule: str, workload: str):
-    """Per-launch DRAM traffic of the schedule's dominant kernel from the
-    committed ncu summary, or None when its source changed since the capture."""
-    _, prefix, src = KERNELS[schedule]
-    path = os.path.join(ROOT, "profiles", f"{prefix}_{workload}.md")
-    if not os.path.exists(path):
-        return None
+def _profile_fields(path: str, src: str):
+    """(fields, valid): the machine-readable lines of an ncu summary, and
+    whether the kernel source still hashes to what was captured."""
     with open(path) as f:
         text = f.read()
-    m = re.search(r"traffic_bytes_per_launch\s*=\s*([0-9.eE+]+)", text)
-    h = re.search(r"kernel_source_sha256\s*=\s*([0-9a-f]{64})", text)
-    if not m or not h:
-        return None
+    fields = dict(re.findall(r"^(\w+)\s*=\s*([0-9a-fA-F.eE+]+)\s*$", text, re.M))
     with open(os.path.join(CSRC, src), "rb") as f:
         cur = hashlib.sha256(f.read()).hexdigest()
-    return float(m.group(1)) if cur == h.group(1) else None
+    return fields, fields.get("kernel_source_sha256") == cur
+
+
+def ncu_traffic(schedule: str, workload: str, ex_bytes: float):
+    """(per-launch DRAM traffic of the schedule's dominant kernel, source):
+    the committed ncu summary of this exact workload, else (stream-K) a
+    summary's traffic/algorithmic ratio times this launch's algorithmic bytes
+    -- the launch reads every touched expert's k-blocks once, so its traffic
+    scales with them; (None, None) when no summary matches the current
+    kernel source."""
+    _, prefix, src = KERNELS[schedule]
+    exact = os.path.join(ROOT, "profiles", f"{prefix}_{workload}.md")
+    if os.path.exists(exact):
+        fields, ok = _profile_fields(exact, src)
+        if ok and "traffic_bytes_per_launch" in fields:
+            return float(fields["traffic_bytes_per_launch"]), "measured"
+    if schedule == "stream_k" and not workload.endswith("_fp4"):
+        pdir = os.path.join(ROOT, "profiles")
+        for fn in sorted(os.listdir(pdir)):
+            if fn.startswith(prefix + "_") and not fn.endswith("_fp4.md"):
+                fields, ok = _profile_fields(os.path.join(pdir, fn), src)
+                if ok and "traffic_ratio" in fields:
+                    return float(fields["traffic_ratio"]) * ex_bytes, "scaled"
+    return None, None
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -496,9 +512,10 @@ def roofline_record(wl, u, per_kernel, ms_step, hbm, tflops, peak_src, traffic_k
         ex_bytes = layer_bytes  # the fused launch is the whole layer
     achieved = ex_bytes / (per_kernel[kname] * 1e-6) / 1e9
     roof_layer_us = max(layer_bytes / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
-    traffic = ncu_traffic(wl.sched, traffic_key)
+    traffic, traffic_src = ncu_traffic(wl.sched, traffic_key, ex_bytes)
     roof = {"bound": "hbm", "kernel": KERNELS[wl.sched][0], "achieved": achieved, "peak": hbm, "unit": "GB/s",
             "frac": achieved / hbm, "frac_vs_nominal": achieved / NOMINAL_HBM_GBS, "traffic": traffic,
+            "traffic_source": traffic_src,
             "peak_source": peak_src, "algorithmic_bytes_per_launch": ex_bytes,
             "kernel_us": per_kernel[kname], "timing": "event nodes around the launch in graph replay"}
     layer = {"bytes": layer_bytes, "flops": flops, "roofline_us": roof_layer_us,
@@ -539,7 +556,8 @@ def measure_extra(cfg, dev, rank, K, W, hbm, tflops, peak_src, sustain_s):
                 "touched_experts": u, "us_per_layer": ms_step * 1e3, "tokens_per_s": cfg.T / (ms_step * 1e-3),
                 "steps": K, "layer_frac": layer["frac"], "kernel_frac": roof["frac"],
                 "kernel_frac_vs_nominal": roof["frac_vs_nominal"], "kernel_us": per_kernel,
-                "traffic": roof["traffic"], "algorithmic_bytes_per_launch": roof["algorithmic_bytes_per_launch"],
+                "traffic": roof["traffic"], "traffic_source": roof["traffic_source"],
+                "algorithmic_bytes_per_launch": roof["algorithmic_bytes_per_launch"],
                 "layer_bytes": layer["bytes"],
                 "sustained": {"layers": n_sus * G, "seconds": ms_sus * n_sus * G * 1e-3,
                               "us_per_layer": ms_sus * 1e3,
