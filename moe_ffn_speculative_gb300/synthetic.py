@@ -27,7 +27,9 @@ gate, router_bias, expert_bias, w_gate_up, w_down, sh_gate_up, sh_down,
 sh_gate from one torch.Generator seeded with the workload's seed.  Layers
 with FP4 routed experts draw uniform code bytes and e8m0 scale bytes uniform
 on three values around the one that gives the weights an RMS near w_std,
-in place of the bf16 expert weights.
+in place of the bf16 expert weights.  FP8 weights (routed experts, or the
+shared expert) are N(0, 1) draws cast to e4m3 codes, with one e8m0 scale per
+32 x 32 block uniform on three values around 2^round(log2(w_std)).
 """
 from __future__ import annotations
 
@@ -65,17 +67,24 @@ class LayerConfig:
     seed: int = 0
     x_std: float = 1.0
     w_std: float = 0.02
-    expert_format: str = "bf16"  # routed experts: "bf16" or "fp4" (e2m1 codes + e8m0 scales)
+    # routed experts: "bf16", "fp4" (e2m1 codes + e8m0 scale per 32 inputs) or
+    # "fp8" (e4m3 codes + e8m0 scale per 32 x 32 block)
+    expert_format: str = "bf16"
+    # shared expert: "bf16" or "fp8"
+    shared_format: str = "bf16"
 
     def with_(self, **kw) -> "LayerConfig":
         return dataclasses.replace(self, **kw)
 
     @property
     def weight_bytes(self) -> int:
-        """Bytes of all routed experts' weights."""
+        """Bytes of all routed experts' weights (codes and scales)."""
+        n = 3 * self.E * self.H * self.I
         if self.expert_format == "fp4":
-            return 3 * self.E * self.H * self.I // 2 + 3 * self.E * self.H * self.I // 32
-        return 3 * self.E * self.H * self.I * 2
+            return n // 2 + n // 32
+        if self.expert_format == "fp8":
+            return n + n // 1024
+        return n * 2
 
 
 CONFIGS: Dict[str, LayerConfig] = {
@@ -139,6 +148,27 @@ def _fp4_scale_center(w_std: float) -> int:
     return 127 + int(round(math.log2(w_std / 2.93)))
 
 
+def _fp8_codes(gen, shape, device) -> torch.Tensor:
+    """uint8 e4m3 codes of N(0, 1) draws (rounded by torch's e4m3 cast)."""
+    v = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    return v.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def _fp8_weight(gen, n: int, k: int, w_std: float, device, outer: int = 0):
+    """(codes [outer,] n x k, e8m0 scales [outer,] ceil(n/32) x ceil(k/32)):
+    block scales uniform on three values around 2^round(log2(w_std))."""
+    c = 127 + int(round(math.log2(w_std)))
+    lead = (outer,) if outer else ()
+    if outer:
+        codes = torch.empty((outer, n, k), dtype=torch.uint8, device=device)
+        for i in range(outer):
+            codes[i] = _fp8_codes(gen, (n, k), device)
+    else:
+        codes = _fp8_codes(gen, (n, k), device)
+    scales = _bytes(gen, lead + (-(-n // 32), -(-k // 32)), c - 1, c + 2, device)
+    return codes, scales
+
+
 def make_inputs(cfg: LayerConfig, device="cpu", seed: Optional[int] = None) -> Dict[str, torch.Tensor]:
     """Draw one layer's inputs and weights.  Keys: x, gate, router_bias,
     expert_bias, w_gate_up [E,2I,H], w_down [E,H,I], sh_gate_up [2Is,H],
@@ -164,12 +194,21 @@ def make_inputs(cfg: LayerConfig, device="cpu", seed: Optional[int] = None) -> D
         d["w_down_q"] = _bytes(gen, (cfg.E, cfg.H, cfg.I // 2), 0, 256, device)
         d["w_down_s"] = _bytes(gen, (cfg.E, cfg.H, cfg.I // 32), c - 1, c + 2, device)
         d["w_gate_up"] = d["w_down"] = None
+    elif cfg.expert_format == "fp8":
+        d["w_gate_up_q"], d["w_gate_up_s"] = _fp8_weight(gen, 2 * cfg.I, cfg.H, cfg.w_std, device, cfg.E)
+        d["w_down_q"], d["w_down_s"] = _fp8_weight(gen, cfg.H, cfg.I, cfg.w_std, device, cfg.E)
+        d["w_gate_up"] = d["w_down"] = None
     else:
         d["w_gate_up"] = _normal_rows(gen, cfg.E, (2 * cfg.I, cfg.H), cfg.w_std, device)
         d["w_down"] = _normal_rows(gen, cfg.E, (cfg.H, cfg.I), cfg.w_std, device)
     if cfg.shared_I > 0:
-        d["sh_gate_up"] = _normal(gen, (2 * cfg.shared_I, cfg.H), cfg.w_std, bf, device)
-        d["sh_down"] = _normal(gen, (cfg.H, cfg.shared_I), cfg.w_std, bf, device)
+        if cfg.shared_format == "fp8":
+            d["sh_gate_up_q"], d["sh_gate_up_s"] = _fp8_weight(gen, 2 * cfg.shared_I, cfg.H, cfg.w_std, device)
+            d["sh_down_q"], d["sh_down_s"] = _fp8_weight(gen, cfg.H, cfg.shared_I, cfg.w_std, device)
+            d["sh_gate_up"] = d["sh_down"] = None
+        else:
+            d["sh_gate_up"] = _normal(gen, (2 * cfg.shared_I, cfg.H), cfg.w_std, bf, device)
+            d["sh_down"] = _normal(gen, (cfg.H, cfg.shared_I), cfg.w_std, bf, device)
         d["sh_gate"] = (_normal(gen, (cfg.H,), cfg.w_std, bf, device)
                         if cfg.shared_gated else None)
     else:

@@ -30,7 +30,8 @@ Sources (web pages, cited by title and section):
   their weights), on select receiving the shifted scores, on the DeepSeek-V4 family (sqrt(softplus)
   scores, always renormalised, route_scale, clamped SwiGLU, one ungated shared
   expert), on the fused gate_up_proj / down_proj expert layout and on the
-  export formats of the official checkpoint (FP4 routed experts).
+  export formats of the official checkpoint (FP4 routed experts, FP8 linears
+  with 32 x 32 block scales).
 * [P5] MoE-Infinity PR #143 "converge DFlash spec-decode stack" -- commit note
   on the resident GPT-OSS loader (MXFP4 codes and scales, uint8,
   output-major).
@@ -395,4 +396,51 @@ def moe_layer_fp4(x, gate, gu_codes, gu_scales, dn_codes, dn_scales, recipe: Rec
     [E,2I,H/32] scales, down [E,H,I/2] codes with [E,H,I/32] scales; every
     other tensor as in moe_layer()."""
     return moe_layer(x, gate, dequant_fp4(gu_codes, gu_scales), dequant_fp4(dn_codes, dn_scales),
+                     recipe, **kw)
+
+
+# --------------------------------------------------------------------------
+# FP8 linears ([P4] commit note on the DeepSeek-V4.1 export formats: the
+# official layout keeps its linears as e4m3 with one e8m0 scale per 32 x 32
+# block of the weight).  As for FP4, the layer computes with the exactly
+# dequantized weights ([P4]: the import turns them into bf16).
+# --------------------------------------------------------------------------
+
+def e4m3_value(code: int) -> float:
+    """Value of one e4m3 byte (the OCP 8-bit floating-point format E4M3, the
+    variant without infinities): bit 7 the sign, bits 6..3 a 4-bit exponent
+    with bias 7, bits 2..0 the mantissa; exponent 0 is the subnormal range
+    (mantissa/8 x 2^-6); exponent 15 with mantissa 7 is NaN, so the largest
+    finite value is 1.75 x 2^8 = 448."""
+    sign = -1.0 if (code >> 7) & 1 else 1.0
+    e = (code >> 3) & 15
+    m = code & 7
+    if e == 15 and m == 7:
+        return float("nan")
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+E4M3_TABLE = np.array([e4m3_value(c) for c in range(256)])
+
+
+def dequant_fp8_blocks(codes: np.ndarray, scales: np.ndarray, block: int = 32) -> np.ndarray:
+    """Exact float64 weights [..., N, K] from e4m3 codes [..., N, K] (uint8)
+    and e8m0 scales [..., ceil(N/block), ceil(K/block)] (uint8), one scale for
+    every block x block tile of the weight."""
+    codes = np.asarray(codes, np.uint8)
+    scales = np.asarray(scales, np.uint8)
+    n, k = codes.shape[-2], codes.shape[-1]
+    assert scales.shape[-2] == -(-n // block) and scales.shape[-1] == -(-k // block)
+    assert scales.shape[:-2] == codes.shape[:-2]
+    s = np.repeat(np.repeat(E8M0_TABLE[scales], block, axis=-2), block, axis=-1)[..., :n, :k]
+    return E4M3_TABLE[codes] * s
+
+
+def moe_layer_fp8(x, gate, gu_codes, gu_scales, dn_codes, dn_scales, recipe: Recipe, **kw):
+    """The layer with FP8 routed experts: gate_up [E,2I,H] e4m3 codes with
+    [E,2I/32,H/32] scales, down [E,H,I] codes with [E,H/32,I/32] scales;
+    every other tensor as in moe_layer()."""
+    return moe_layer(x, gate, dequant_fp8_blocks(gu_codes, gu_scales), dequant_fp8_blocks(dn_codes, dn_scales),
                      recipe, **kw)

@@ -443,3 +443,80 @@ def test_fp4_layer_equals_layer_on_decoded_weights():
     swapped = ((gq & 15) << 4) | (gq >> 4)
     c = O.moe_layer_fp4(x, gate, swapped.astype(np.uint8), gs, dq, ds, rec)
     assert np.abs(c["y"] - a["y"]).max() > 1e-3
+
+
+# ---------------------------------------------------------------- FP8 linears
+# Format of the DeepSeek-V4.1 export (SpecForge PR #1073, commit note on the
+# official checkpoint's formats): e4m3 codes, one e8m0 scale per 32 x 32 block.
+
+# e4m3 values the OCP 8-bit floating-point specification fixes, typed here
+# from its definition (exponent bias 7, 3 mantissa bits, subnormals below
+# 2^-6, S.1111.111 NaN, no infinities), not computed from the oracle's rule.
+E4M3_LISTED = {
+    0x00: 0.0, 0x01: 0.001953125, 0x02: 0.00390625, 0x07: 0.013671875, 0x08: 0.015625, 0x0F: 0.029296875,
+    0x30: 0.5, 0x38: 1.0, 0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x48: 4.0, 0x50: 8.0, 0x70: 128.0,
+    0x77: 240.0, 0x78: 256.0, 0x7D: 416.0, 0x7E: 448.0,
+    0x80: -0.0, 0x81: -0.001953125, 0xB8: -1.0, 0xC0: -2.0, 0xFE: -448.0,
+}
+
+
+def test_e4m3_listed_values():
+    for code, v in E4M3_LISTED.items():
+        assert O.E4M3_TABLE[code] == v, hex(code)
+    assert math.copysign(1.0, O.E4M3_TABLE[0x80]) == -1.0
+    assert math.isnan(O.E4M3_TABLE[0x7F]) and math.isnan(O.E4M3_TABLE[0xFF])
+    assert np.nanmax(O.E4M3_TABLE) == 448.0 and np.nanmin(O.E4M3_TABLE) == -448.0
+
+
+def test_e4m3_matches_library_decoder():
+    torch = pytest.importorskip("torch")
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    finite = ~np.isnan(lib)
+    np.testing.assert_array_equal(O.E4M3_TABLE[finite], lib[finite])
+    np.testing.assert_array_equal(np.isnan(O.E4M3_TABLE), np.isnan(lib))
+
+
+def test_fp8_32x32_block_scales():
+    # a 64 x 96 weight of ones (code 0x38): each 32 x 32 block takes its own
+    # scale; the last column block is whole, rows and columns map as written
+    codes = np.full((64, 96), 0x38, np.uint8)
+    scales = np.array([[126, 127, 128], [129, 130, 131]], np.uint8)
+    w = O.dequant_fp8_blocks(codes, scales)
+    for bi in range(2):
+        for bj in range(3):
+            blk = w[32 * bi:32 * bi + 32, 32 * bj:32 * bj + 32]
+            assert (blk == 2.0 ** (int(scales[bi, bj]) - 127)).all()
+    # a ragged shape: 40 x 40 uses ceil(40/32) = 2 scales per dimension
+    w2 = O.dequant_fp8_blocks(np.full((40, 40), 0x40, np.uint8), np.array([[127, 128], [129, 130]], np.uint8))
+    assert w2[0, 0] == 2.0 and w2[0, 39] == 4.0 and w2[39, 0] == 8.0 and w2[39, 39] == 16.0
+
+
+def test_fp8_layer_equals_layer_on_decoded_weights():
+    # the FP8 layer is the bf16-formula layer on the decoded weights; here
+    # decoded element by element through the listed rule and the block index
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(7)
+    T, H, E, I, K = 5, 64, 4, 64, 2
+    x = rng.standard_normal((T, H))
+    gate = rng.standard_normal((E, H)) * 0.1
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    gq = rng.choice(finite, size=(E, 2 * I, H))
+    gs = rng.integers(112, 118, size=(E, 2 * I // 32, H // 32)).astype(np.uint8)
+    dq = rng.choice(finite, size=(E, H, I))
+    ds = rng.integers(112, 118, size=(E, H // 32, I // 32)).astype(np.uint8)
+
+    def decode(q, s):
+        v = torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        out = np.empty(q.shape)
+        for ix in np.ndindex(q.shape):
+            out[ix] = v[ix] * 2.0 ** (int(s[ix[:-2] + (ix[-2] // 32, ix[-1] // 32)]) - 127)
+        return out
+
+    rec = O.Recipe(num_experts=E, top_k=K, score_fn=O.SCORE_SQRTSOFTPLUS, route_scale=1.5, swiglu_limit=10.0)
+    a = O.moe_layer_fp8(x, gate, gq, gs, dq, ds, rec)
+    b = O.moe_layer(x, gate, decode(gq, gs), decode(dq, ds), rec)
+    np.testing.assert_array_equal(a["idx"], b["idx"])
+    np.testing.assert_array_equal(a["y"], b["y"])
+    # the row blocks' scales taken in the wrong order would change the result
+    c = O.moe_layer(x, gate, O.dequant_fp8_blocks(gq, gs[..., ::-1, :]), O.dequant_fp8_blocks(dq, ds), rec)
+    assert np.abs(c["y"] - a["y"]).max() > 1e-3
