@@ -302,6 +302,61 @@ MOE_API moe_status moe_ffn_forward_fp4(const moe_bf16* x, int T, int H, int I, c
                                        size_t ws_bytes, moe_bf16* y, int32_t* topk_idx_out, float* topk_w_out,
                                        int32_t* counts_out, cudaStream_t stream);
 
+/* ---- Block-scaled experts: the weights stay in the formats of DeepSeek-V4.1's
+ * official draft checkpoint (SpecForge PR #1073, commit note on its export
+ * formats) and the tensor cores' block-scaled MMA multiplies them directly.
+ *   routed_fmt MOE_FMT_FP4: the FP4 layout above (e2m1 codes, the even input
+ *       in the low nibble, one e8m0 scale per 32 inputs):
+ *         w_gate_up_q [E,2I,H/2], w_gate_up_s [E,2I,H/32],
+ *         w_down_q    [E,H,I/2],  w_down_s    [E,H,I/32]
+ *   routed_fmt MOE_FMT_FP8: e4m3 codes with one e8m0 scale per 32 x 32 block
+ *       of the weight (the checkpoint's format for its other linears):
+ *         w_gate_up_q [E,2I,H],   w_gate_up_s [E,2I/32,H/32],
+ *         w_down_q    [E,H,I],    w_down_s    [E,H/32,I/32]
+ *   shared expert, when present, always FP8 in that block format:
+ *         sh_gate_up_q [2Is,H], sh_gate_up_s [2Is/32,H/32],
+ *         sh_down_q    [H,Is],  sh_down_s    [H/32,Is/32]
+ * The layer computes with the exactly dequantized weights (code x scale), as
+ * the bf16 draft those weights import into does: the MMA applies both
+ * operands' scales per 32 products, and x and h enter as sums of e4m3 pieces
+ * (three for x, four for h, each piece with its own scale per 32 inputs) that
+ * reproduce them to within 2^-13 (x) and 2^-17 (h) of a 32-input block's
+ * largest magnitude (a bf16 x whose block spans a few binades exactly).
+ * Limits: H, I and Is multiples of 128, H <= 65536, I, Is <= 16384; FP4 code
+ * tensors 32-byte aligned, every other pointer 16-byte aligned. */
+#define MOE_FMT_FP4 1
+#define MOE_FMT_FP8 2
+
+/* Bytes of the prepared weight scales of one layer (0 for an invalid format
+ * or unsupported shape). */
+MOE_API size_t moe_mx_scales_bytes(int routed_fmt, int E, int H, int I, int Is);
+
+/* Re-lays the weight scales into the chunks the block-scaled MMA reads: for
+ * every (expert, 256-row tile, 128-input k-block) 1 KB.  Once per set of
+ * weights (load time); asynchronous on `stream`.  sh_* may be NULL when
+ * Is == 0.  scales: device buffer of >= moe_mx_scales_bytes() bytes, 16-byte
+ * aligned, owned by the caller and passed to every moe_ffn_forward_mx() with
+ * these weights.  Returns MOE_ERR_WORKSPACE when scales_bytes is too small. */
+MOE_API moe_status moe_mx_prepare_scales(int routed_fmt, const uint8_t* w_gate_up_s, const uint8_t* w_down_s, int E,
+                                         int H, int I, const uint8_t* sh_gate_up_s, const uint8_t* sh_down_s, int Is,
+                                         void* scales, size_t scales_bytes, cudaStream_t stream);
+
+/* moe_ffn_forward() with block-scaled experts: router, workspace
+ * (moe_ffn_workspace_bytes), outputs and errors as in moe_ffn_forward();
+ * always the stream-K schedule, with token tiles of up to 32 tokens.
+ *   routed_fmt   MOE_FMT_FP4 or MOE_FMT_FP8
+ *   w_gate_up_q, w_down_q   the routed experts' codes (layouts above)
+ *   sh_gate_up_q, sh_down_q the shared expert's FP8 codes, or NULL (Is = 0)
+ *   scales       from moe_mx_prepare_scales() */
+MOE_API moe_status moe_ffn_forward_mx(const moe_bf16* x, int T, int H, int I, const moe_bf16* gate,
+                                      const float* router_bias, const float* expert_bias, int routed_fmt,
+                                      const uint8_t* w_gate_up_q, const uint8_t* w_down_q,
+                                      const uint8_t* sh_gate_up_q, const uint8_t* sh_down_q, int Is,
+                                      const moe_bf16* sh_gate, const void* scales, size_t scales_bytes,
+                                      const moe_recipe* recipe, void* ws, size_t ws_bytes, moe_bf16* y,
+                                      int32_t* topk_idx_out, float* topk_w_out, int32_t* counts_out,
+                                      cudaStream_t stream);
+
 /* Synchronises `stream`, reads the device status word of a workspace used by
  * moe_route() or moe_ffn_forward(), and clears it.  Returns MOE_OK or the
  * first device-side error recorded (MOE_ERR_DEVICE_TIMEOUT, or

@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", platform.machine())
 LIB = os.path.join(PKG, "libmoe_gb300.so")
-SOURCES = ["route.cu", "gemm.cu", "slice.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["route.cu", "gemm.cu", "slice.cu", "mx.cu", "api.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -98,6 +98,24 @@ bool encode_codes_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Block-scaled weights [d2][d1][d0 inputs]: FP4 codes (two per byte; the
+// tensor map type that spaces every 16 codes over 16 bytes of shared memory,
+// the operand layout of 4-bit MMA inputs) or FP8 bytes, loaded in boxes of
+// 128 inputs x 128 rows x 1 with the 128-byte swizzle; rows past the matrix
+// read as zero.
+bool encode_mx_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, bool fp4) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t row = fp4 ? d0 / 2 : d0;  // bytes per row
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {row, row * d1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kMxK), static_cast<cuuint32_t>(kHalfRows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base),
+            dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // h [rows][2*I_ld] (16-bit: hi columns then lo columns), loaded in boxes of
 // 64 columns x 16 rows with the 128-byte swizzle; rows past the end read as
 // zero.
@@ -215,9 +233,13 @@ struct Layout {
   bool need_out;
   size_t o_status, o_cnt, o_tiles, o_logits, o_shl, o_shw, o_idx, o_w, o_counts, o_offsets, o_sp, o_pp, o_groups,
       o_header, o_spans, o_span_groups, o_partials, o_h, o_out, o_sync, o_hbuf, o_sout, o_xh, total;
+  // block-scaled path: e4m3 pieces of h and x with their scales
+  size_t o_hq, o_hs, o_xq, o_xs;
 };
 
-Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sms) {
+// mx: the layout of the block-scaled path (moe_ffn_forward_mx): token tiles
+// of up to kMxMaxTok, h and x as e4m3 pieces with their scales.
+Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sms, bool mx = false) {
   Layout L;
   L.rg = router_geometry(T, E, gated, sms);
   // Token tile width: every token of a decode-sized forward in one tile.
@@ -236,6 +258,10 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
     if (cap < nm) nm = cap;
   }
   L.n_max = nm < 16 ? 16 : (nm > 256 ? 256 : nm);
+  if (mx) {
+    const int t16 = ((T + 15) / 16) * 16;
+    L.n_max = t16 < kMxMaxTok ? (t16 < 16 ? 16 : t16) : kMxMaxTok;
+  }
   L.nbuf = (4 * L.n_max <= 512) ? 2 : 1;
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(L.nbuf * 2 * L.n_max)) cols <<= 1;
@@ -246,7 +272,7 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   L.smem = kSmemLimit;
   L.grid = sms;
   const int Imax = Is > I ? Is : I;
-  L.I_ld = ((Imax + 7) / 8) * 8;
+  L.I_ld = ((Imax + 7) / 8) * 8;  // the block-scaled path needs multiples of 128 already
   const long long TK = static_cast<long long>(T) * K;
   const long long u_max = TK < E ? TK : E;
   const long long nb_sum = u_max + TK / L.n_max;
@@ -266,7 +292,8 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   L.o_sync = kSliceSyncOffset;
   size_t o = kWsHeaderBytes;
   // stream-K arrival counters (gate_up, down) and gate_up readiness counters
-  L.o_tiles = o; o = align_up(o + 4 * static_cast<size_t>(2 * L.max_gu_tiles + L.max_dn_tiles));
+  // (+1: the block-scaled path's count of warps that cut their share of x into pieces)
+  L.o_tiles = o; o = align_up(o + 4 * static_cast<size_t>(2 * L.max_gu_tiles + L.max_dn_tiles + 1));
   L.o_logits = o; o = align_up(o + 4 * static_cast<size_t>(T) * E);
   L.o_shl = o; o = align_up(o + 4 * static_cast<size_t>(T) * (L.rg.fold_sh ? L.rg.n_eb * L.rg.hsplit : 1));
   L.o_shw = o; o = align_up(o + 4 * static_cast<size_t>(T));
@@ -281,13 +308,22 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   L.o_spans = o; o = align_up(o + 8 * 2 * static_cast<size_t>(L.grid + 1));
   L.o_span_groups = o; o = align_up(o + 4 * 2 * static_cast<size_t>(L.grid + 1));
   L.o_partials = o; o = align_up(o + 4 * static_cast<size_t>(L.grid) * 4 * 2 * L.n_max * 128);
-  L.o_h = o; o = align_up(o + 2 * 2 * rows * L.I_ld);
-  L.o_xh = o; o = align_up(o + 2 * static_cast<size_t>(T) * H);  // f16 copy of x (FP4 experts)
+  L.o_h = L.o_hq = L.o_hs = L.o_xq = L.o_xs = L.o_xh = 0;
+  if (mx) {
+    L.o_hq = o; o = align_up(o + static_cast<size_t>(kMxPh) * rows * L.I_ld);
+    L.o_hs = o; o = align_up(o + static_cast<size_t>(kMxPh) * rows * (L.I_ld / 32));
+    L.o_xq = o; o = align_up(o + static_cast<size_t>(kMxPx) * T * H);
+    L.o_xs = o; o = align_up(o + static_cast<size_t>(kMxPx) * T * (H / 32));
+  } else {
+    L.o_h = o; o = align_up(o + 2 * 2 * rows * L.I_ld);
+    L.o_xh = o; o = align_up(o + 2 * static_cast<size_t>(T) * H);  // f16 copy of x (FP4 experts)
+  }
   L.o_out = o;
   if (L.need_out) o = align_up(o + 4 * rows * H);
   // fused small-expert-count kernel: counters and the per-slice partial outputs
   L.sp = slice_plan(T, H, I, Is, E, gated, sms);
   L.o_hbuf = L.o_sout = 0;
+  if (mx) L.sp.reserve = L.sp.ok = false;
   if (L.sp.reserve) {
     // every expert's h tiles (2 per slice, each 2*n_tok rows of 128 bytes)
     // and the pair outputs for the combine; the counter sets are in the header
@@ -438,10 +474,17 @@ size_t moe_ffn_workspace_bytes(int T, int H, int I, int Is, const moe_recipe* re
   if (check_recipe(recipe) != MOE_OK || T < 0 || H < 8 || I < 8 || Is < 0) return 0;
   const int sms = device_sms();
   if (sms <= 0) return 0;
-  // the gated/ungated choice changes only the router's geometry: size for the larger
-  const Layout a = make_layout(T, H, I, Is, recipe->num_experts, recipe->top_k, false, sms);
-  const Layout b = make_layout(T, H, I, Is, recipe->num_experts, recipe->top_k, true, sms);
-  return a.total > b.total ? a.total : b.total;
+  // the gated/ungated choice changes only the router's geometry: size for the
+  // larger; where the block-scaled path takes the shape, for its layout too
+  size_t n = 0;
+  for (int mx = 0; mx < 2; ++mx) {
+    if (mx && (H % kMxK != 0 || I % kMxK != 0 || Is % kMxK != 0)) continue;
+    for (int gated = 0; gated < 2; ++gated) {
+      const Layout L = make_layout(T, H, I, Is, recipe->num_experts, recipe->top_k, gated != 0, sms, mx != 0);
+      if (L.total > n) n = L.total;
+    }
+  }
+  return n;
 }
 
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
@@ -565,7 +608,7 @@ moe_status ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf16* g
   rp.span_groups = reinterpret_cast<int32_t*>(w + L.o_span_groups);
   rp.grid = L.grid;
   rp.I = I; rp.Is = Is; rp.n_max = L.n_max;
-  rp.zero_ptr = tiles; rp.zero_count = 2 * L.max_gu_tiles + L.max_dn_tiles;
+  rp.zero_ptr = tiles; rp.zero_count = 2 * L.max_gu_tiles + L.max_dn_tiles + 1;
   uint16_t* xh = reinterpret_cast<uint16_t*>(w + L.o_xh);
   if (fp4) {
     rp.fp4 = 1;
@@ -659,6 +702,163 @@ moe_status ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf16* g
   return MOE_OK;
 }
 
+// ---- block-scaled experts (FP4 or FP8 routed, FP8 shared): router, one
+// persistent launch of both GEMMs on the block-scaled MMA, combine
+bool mx_shape_ok(int E, int H, int I, int Is) {
+  return E >= 1 && E <= 1024 && H >= kMxK && I >= kMxK && H % kMxK == 0 && I % kMxK == 0 && Is % kMxK == 0 &&
+         H <= 65536 && I <= 16384 && Is <= 16384;
+}
+
+size_t mx_scales_bytes(int E, int H, int I, int Is) {
+  return mx_scale_offset(E, H, I, Is, 1, -1, 0, 0) + static_cast<size_t>(ceil_div(H, 2 * kHalfRows)) * (Is / kMxK) * 1024;
+}
+
+inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
+moe_status ffn_forward_mx(const moe_bf16* x, int T, int H, int I, const moe_bf16* gate, const float* router_bias,
+                          const float* expert_bias, int routed_fmt, const uint8_t* w_gate_up_q,
+                          const uint8_t* w_down_q, const uint8_t* sh_gate_up_q, const uint8_t* sh_down_q, int Is,
+                          const moe_bf16* sh_gate, const void* scales, size_t scales_bytes,
+                          const moe_recipe* recipe, void* ws, size_t ws_bytes, moe_bf16* y, int32_t* topk_idx_out,
+                          float* topk_w_out, int32_t* counts_out, cudaStream_t stream) {
+  moe_status st = check_recipe(recipe);
+  if (st != MOE_OK) return st;
+  if (routed_fmt != MOE_FMT_FP4 && routed_fmt != MOE_FMT_FP8) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || H < 8 || I < 8 || Is < 0) return MOE_ERR_INVALID_ARG;
+  if (T > 65536 || !mx_shape_ok(recipe->num_experts, H, I, Is)) return MOE_ERR_UNSUPPORTED;
+  if ((sh_gate_up_q == nullptr) != (Is == 0) || (Is > 0 && sh_down_q == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (sh_gate && Is == 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !gate || !w_gate_up_q || !w_down_q || !scales || !y) return MOE_ERR_INVALID_ARG;
+  const bool fp4 = routed_fmt == MOE_FMT_FP4;
+  // FP4 codes go through the packed tensor-map type, which needs 32-byte alignment
+  const bool wq_ok = fp4 ? (aligned32(w_gate_up_q) && aligned32(w_down_q))
+                         : (aligned16(w_gate_up_q) && aligned16(w_down_q));
+  if (!aligned16(x) || !aligned16(gate) || !aligned16(y) || !aligned16(scales) || !wq_ok ||
+      (sh_gate_up_q && !aligned16(sh_gate_up_q)) || (sh_down_q && !aligned16(sh_down_q)) ||
+      (sh_gate && !aligned16(sh_gate)))
+    return MOE_ERR_INVALID_ARG;
+  const int E = recipe->num_experts, K = recipe->top_k;
+  if (scales_bytes < mx_scales_bytes(E, H, I, Is)) return MOE_ERR_INVALID_ARG;
+  const size_t xy_bytes = static_cast<size_t>(T) * H * 2;
+  if (overlaps(x, xy_bytes, y, xy_bytes)) return MOE_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0 || ws_bytes < kWsHeaderBytes) return MOE_ERR_WORKSPACE;
+  const int sms = device_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const Layout L = make_layout(T, H, I, Is, E, K, sh_gate != nullptr, sms, true);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  char* w = static_cast<char*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(w + L.o_status);
+  int32_t* idx = topk_idx_out ? topk_idx_out : reinterpret_cast<int32_t*>(w + L.o_idx);
+  float* wts = topk_w_out ? topk_w_out : reinterpret_cast<float*>(w + L.o_w);
+  int32_t* counts = counts_out ? counts_out : reinterpret_cast<int32_t*>(w + L.o_counts);
+  int32_t* sorted_pair = reinterpret_cast<int32_t*>(w + L.o_sp);
+  int32_t* pair_pos = reinterpret_cast<int32_t*>(w + L.o_pp);
+  float* sh_w = reinterpret_cast<float*>(w + L.o_shw);
+  GroupEntry* groups = reinterpret_cast<GroupEntry*>(w + L.o_groups);
+  GemmHeader* header = reinterpret_cast<GemmHeader*>(w + L.o_header);
+  int32_t* tiles = reinterpret_cast<int32_t*>(w + L.o_tiles);
+  float* out_ws = reinterpret_cast<float*>(w + L.o_out);
+
+  // ---- 1. router + permutation + work list (128-input k-blocks, 32-token tiles)
+  RouteParams rp;
+  memset(&rp, 0, sizeof(rp));
+  rp.x = x; rp.gate = gate; rp.router_bias = router_bias; rp.expert_bias = expert_bias; rp.sh_gate = sh_gate;
+  rp.T = T; rp.H = H; rp.E = E; rp.K = K;
+  rp.score_fn = recipe->score_fn; rp.n_group = recipe->n_group; rp.topk_group = recipe->topk_group;
+  rp.group_topn = recipe->group_topn; rp.renorm = recipe->norm_topk_prob; rp.eps = recipe->norm_eps;
+  rp.scale = recipe->route_scale;
+  rp.quads = L.rg.quads; rp.hsplit = L.rg.hsplit; rp.n_eb = L.rg.n_eb; rp.n_tb = L.rg.n_tb;
+  rp.fold_sh = L.rg.fold_sh ? 1 : 0;
+  rp.logits = reinterpret_cast<float*>(w + L.o_logits);
+  rp.sh_logit = reinterpret_cast<float*>(w + L.o_shl);
+  rp.idx = idx; rp.w = wts; rp.sh_w = Is > 0 ? sh_w : nullptr;
+  rp.tb_counter = reinterpret_cast<int32_t*>(w + L.o_cnt);
+  rp.glob_counter = rp.tb_counter + L.rg.n_tb;
+  rp.do_permute = 1;
+  rp.counts = counts; rp.offsets = reinterpret_cast<int32_t*>(w + L.o_offsets);
+  rp.sorted_pair = sorted_pair; rp.pair_pos = pair_pos;
+  rp.groups = groups; rp.header = header;
+  rp.spans = reinterpret_cast<int64_t*>(w + L.o_spans);
+  rp.span_groups = reinterpret_cast<int32_t*>(w + L.o_span_groups);
+  rp.grid = L.grid;
+  rp.I = I; rp.Is = Is; rp.n_max = L.n_max;
+  rp.fmt = fp4 ? kFmtMxFp4 : kFmtMxFp8;
+  rp.sh_fmt = kFmtMxFp8;
+  rp.kblk = kMxK;
+  // the tile counters, readiness counters and the x-pieces counter
+  rp.zero_ptr = tiles; rp.zero_count = 2 * L.max_gu_tiles + L.max_dn_tiles + 1;
+  record_event_on(0, stream);
+  cudaError_t e = cudaSuccess;
+  int tb = L.rg.tb;
+  if (T > 1024) {
+    e = launch_logits_gemm(x, gate, sh_gate, router_bias, T, H, E, rp.logits, rp.sh_logit, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    rp.logits_given = 1;
+    rp.fold_sh = 0;
+    rp.n_eb = 1;
+    tb = 8;
+    rp.n_tb = ceil_div(T, tb);
+  }
+  e = launch_route(rp, tb, stream);
+  record_event_on(1, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  // ---- 2. both grouped GEMMs on the block-scaled MMA, one persistent launch
+  CUtensorMap tm_gu, tm_gu_sh, tm_dn, tm_dn_sh;
+  if (!encode_mx_3d(&tm_gu, w_gate_up_q, H, I, 2ull * E, fp4) || !encode_mx_3d(&tm_dn, w_down_q, I, H, E, fp4))
+    return MOE_ERR_CUDA;
+  if (Is > 0) {
+    if (!encode_mx_3d(&tm_gu_sh, sh_gate_up_q, H, Is, 2, false) || !encode_mx_3d(&tm_dn_sh, sh_down_q, Is, H, 1, false))
+      return MOE_ERR_CUDA;
+  } else {
+    tm_gu_sh = tm_gu;
+    tm_dn_sh = tm_dn;
+  }
+  MxParams mp;
+  memset(&mp, 0, sizeof(mp));
+  mp.groups = groups; mp.header = header; mp.spans = rp.spans; mp.span_groups = rp.span_groups;
+  mp.x = x;
+  mp.xq = reinterpret_cast<uint8_t*>(w + L.o_xq);
+  mp.xs = reinterpret_cast<uint8_t*>(w + L.o_xs);
+  mp.xq_ready = tiles + 2 * L.max_gu_tiles + L.max_dn_tiles;
+  mp.sorted_pair = sorted_pair;
+  mp.T = T; mp.K = K; mp.TK = T * K; mp.H = H; mp.I_ld = Is > I ? Is : I;
+  mp.n_max = L.n_max;
+  mp.stage_space = kSmemLimit - 1024 - kCtrlBytes;
+  mp.swiglu_limit = recipe->swiglu_limit;
+  mp.hq = reinterpret_cast<uint8_t*>(w + L.o_hq);
+  mp.hs = reinterpret_cast<uint8_t*>(w + L.o_hs);
+  mp.out_ws = out_ws; mp.y = y; mp.direct_y = L.need_out ? 0 : 1;
+  mp.topk_w = wts; mp.sh_w = (Is > 0 && sh_gate) ? sh_w : nullptr;
+  mp.partials = reinterpret_cast<float*>(w + L.o_partials);
+  mp.tile_counters_gu = tiles;
+  mp.tile_counters_dn = tiles + L.max_gu_tiles;
+  mp.ready = tiles + L.max_gu_tiles + L.max_dn_tiles;
+  mp.status = status;
+  mp.scales = static_cast<const uint8_t*>(scales);
+  mp.I = I; mp.Is = Is; mp.E = E;
+  mp.routed_fp4 = fp4 ? 1 : 0;
+  mp.g_max = L.g_max;
+  mp.max_gu_tiles = L.max_gu_tiles;
+  mp.max_dn_tiles = L.max_dn_tiles;
+  mp.max_gu_iters = static_cast<long long>(L.max_gu_tiles) * ceil_div(H, kMxK);
+  mp.max_dn_iters = static_cast<long long>(L.max_dn_tiles) * ceil_div(mp.I_ld, kMxK);
+  record_event_on(2, stream);
+  e = launch_mx(tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, mp, L.grid, kSmemLimit, stream);
+  record_event_on(3, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  // ---- 3. weighted combine (+ shared expert)
+  if (L.need_out) {
+    record_event_on(4, stream);
+    e = launch_combine(out_ws, pair_pos, T, K, H, Is > 0 ? 1 : 0, y, stream);
+    record_event_on(5, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
 size_t fp4_scales_bytes(int E, int H, int I) {
   const size_t mb0 = ceil_div(I, kHalfRows), kb0 = H / kBlockK;
   const size_t mb1 = ceil_div(H, 2 * kHalfRows), kb1 = I / kBlockK;
@@ -708,6 +908,35 @@ moe_status moe_ffn_forward_fp4(const moe_bf16* x, int T, int H, int I, const moe
   return ffn_forward(x, T, H, I, gate, router_bias, expert_bias, reinterpret_cast<const moe_bf16*>(w_gate_up_q),
                      reinterpret_cast<const moe_bf16*>(w_down_q), sh_gate_up, sh_down, Is, sh_gate, recipe, ws,
                      ws_bytes, y, topk_idx_out, topk_w_out, counts_out, stream, &f);
+}
+
+size_t moe_mx_scales_bytes(int routed_fmt, int E, int H, int I, int Is) {
+  if ((routed_fmt != MOE_FMT_FP4 && routed_fmt != MOE_FMT_FP8) || Is < 0 || !mx_shape_ok(E, H, I, Is)) return 0;
+  return mx_scales_bytes(E, H, I, Is);
+}
+
+moe_status moe_mx_prepare_scales(int routed_fmt, const uint8_t* w_gate_up_s, const uint8_t* w_down_s, int E, int H,
+                                 int I, const uint8_t* sh_gate_up_s, const uint8_t* sh_down_s, int Is, void* scales,
+                                 size_t scales_bytes, cudaStream_t stream) {
+  if (routed_fmt != MOE_FMT_FP4 && routed_fmt != MOE_FMT_FP8) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || H < 1 || I < 1 || Is < 0) return MOE_ERR_INVALID_ARG;
+  if (!mx_shape_ok(E, H, I, Is)) return MOE_ERR_UNSUPPORTED;
+  if (!w_gate_up_s || !w_down_s || !scales || !aligned16(scales)) return MOE_ERR_INVALID_ARG;
+  if (Is > 0 && (!sh_gate_up_s || !sh_down_s)) return MOE_ERR_INVALID_ARG;
+  if (scales_bytes < mx_scales_bytes(E, H, I, Is)) return MOE_ERR_WORKSPACE;
+  return cuda_status(launch_mx_scales(routed_fmt == MOE_FMT_FP4 ? 1 : 0, w_gate_up_s, w_down_s, E, H, I, sh_gate_up_s,
+                                      sh_down_s, Is, static_cast<uint8_t*>(scales), stream));
+}
+
+moe_status moe_ffn_forward_mx(const moe_bf16* x, int T, int H, int I, const moe_bf16* gate, const float* router_bias,
+                              const float* expert_bias, int routed_fmt, const uint8_t* w_gate_up_q,
+                              const uint8_t* w_down_q, const uint8_t* sh_gate_up_q, const uint8_t* sh_down_q, int Is,
+                              const moe_bf16* sh_gate, const void* scales, size_t scales_bytes,
+                              const moe_recipe* recipe, void* ws, size_t ws_bytes, moe_bf16* y,
+                              int32_t* topk_idx_out, float* topk_w_out, int32_t* counts_out, cudaStream_t stream) {
+  return ffn_forward_mx(x, T, H, I, gate, router_bias, expert_bias, routed_fmt, w_gate_up_q, w_down_q, sh_gate_up_q,
+                        sh_down_q, Is, sh_gate, scales, scales_bytes, recipe, ws, ws_bytes, y, topk_idx_out,
+                        topk_w_out, counts_out, stream);
 }
 
 moe_status moe_get_device_status(void* ws, cudaStream_t stream, int32_t* info_out) {

@@ -91,23 +91,33 @@ constexpr int kGatherLag = 2;                         // cp.async groups in flig
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Weight formats of a group's k-blocks, for the work list's cost model:
+// bf16 (64 inputs, 32 KB), FP4 expanded by converter warps (64 inputs, 8.5
+// KB), and the block-scaled formats read by the MMA directly (128 inputs:
+// FP4 codes 16 KB + 1 KB of scales, FP8 codes 32 KB + 1 KB).
+enum : int { kFmtBf16 = 0, kFmtFp4Conv = 1, kFmtMxFp4 = 2, kFmtMxFp8 = 3 };
+
 // Relative cost of one k-block of a group whose tiles carry `nmma` token
 // columns, in quarters of a weight-streaming k-block: up to 16 columns a
 // k-block costs what its 32 KB of weights take to stream; wider tiles
 // (the shared expert, large token counts) add MMA, gather and epilogue
 // work, more in the down GEMM (h as hi and lo doubles its MMAs and gathers).
 // The slopes are fitted to per-CTA timings of 16- and 80-column tiles.
-// An FP4 k-block streams about a quarter of the bytes (8.5 KB).
-__host__ __device__ inline int kblock_cost(int phase, int nmma, bool fp4 = false) {
-  const int base = fp4 ? 1 : 4;
+// An FP4 k-block streams about a quarter of the bytes (8.5 KB); a
+// block-scaled FP4 k-block half (17 KB), an FP8 one about the same (33 KB).
+__host__ __device__ inline int kblock_cost(int phase, int nmma, int fmt = kFmtBf16) {
+  const int base = fmt == kFmtFp4Conv ? 1 : (fmt == kFmtMxFp4 ? 2 : 4);
   return phase == 0 ? base + ((nmma - 16) * 3 + 80) / 160 : base + ((nmma - 16) * 7 + 20) / 40;
 }
 
+// Tiles of a group: nb token blocks of up to n_max tokens, mb 256-row weight
+// tiles, kb k-blocks of `kblk` inputs (64 for bf16 operands, 128 for the
+// block-scaled 8-bit and FP4 operands).
 __host__ __device__ inline void group_geometry(int phase, int count, int idim, int H, int n_max,
-                                               int& mb, int& nb, int& kb) {
+                                               int& mb, int& nb, int& kb, int kblk = kBlockK) {
   nb = ceil_div(count, n_max);
-  if (phase == 0) { mb = ceil_div(idim, kHalfRows); kb = ceil_div(H, kBlockK); }
-  else            { mb = ceil_div(H, 2 * kHalfRows); kb = ceil_div(idim, kBlockK); }
+  if (phase == 0) { mb = ceil_div(idim, kHalfRows); kb = ceil_div(H, kblk); }
+  else            { mb = ceil_div(H, 2 * kHalfRows); kb = ceil_div(idim, kblk); }
 }
 
 struct GemmParams {
@@ -145,6 +155,67 @@ struct GemmParams {
   int g_max, max_gu_tiles, max_dn_tiles;
   long long max_gu_iters, max_dn_iters;
 };
+
+// Block-scaled expert GEMMs (mx.cu): routed experts as FP4 (e2m1 codes with
+// an e8m0 scale per 32 inputs) or FP8 (e4m3 codes with an e8m0 scale per
+// 32 x 32 block), the shared expert as FP8, both multiplied by the tensor
+// cores' block-scaled MMA (kind::mxf8f6f4) on k-blocks of 128 inputs.  The
+// activations x and h enter as sums of e4m3 pieces, each piece with its own
+// e8m0 scale per 32 inputs.
+constexpr int kMxK = 128;        // inputs per k-block
+constexpr int kMxPx = 3;         // e4m3 pieces of x
+constexpr int kMxPh = 4;         // e4m3 pieces of h
+constexpr int kMxMaxTok = 32;    // token tile: kMxPh x 32 = 128 MMA columns
+constexpr int kMxSfBytes = 512;  // one scale chunk: 128 rows x 4 inputs-chunks of 32
+constexpr int kMxThreads = 224;
+
+struct MxParams {
+  const GroupEntry* groups;
+  const GemmHeader* header;
+  const int64_t* spans;
+  const int32_t* span_groups;
+  const uint16_t* x;           // [T,H] bf16
+  uint8_t* xq;                 // [T][kMxPx][H] e4m3 pieces of x (written by the kernel's prologue)
+  uint8_t* xs;                 // [T][kMxPx][H/32] their e8m0 scales
+  int32_t* xq_ready;           // warps that finished their share of the pieces (zeroed by the router)
+  const int32_t* sorted_pair;
+  int T, K, TK, H, I_ld;       // I_ld = max(I, Is)
+  int n_max;                   // token tile width (16 or 32)
+  int stage_space;
+  float swiglu_limit;
+  uint8_t* hq;                 // [T*K + T][kMxPh][I_ld] e4m3 pieces of h
+  uint8_t* hs;                 // [T*K + T][kMxPh][I_ld/32] their scales
+  float* out_ws;               // [T*K + T, H] fp32 weighted outputs (unless direct_y)
+  uint16_t* y;
+  int direct_y;
+  const float* topk_w;
+  const float* sh_w;
+  float* partials;             // [grid][4][2][n_max][128] fp32
+  int32_t* tile_counters_gu;
+  int32_t* tile_counters_dn;
+  int32_t* ready;
+  int32_t* status;
+  const uint8_t* scales;       // prepared weight scale chunks (moe_mx_prepare_scales)
+  int I, Is, E;
+  int routed_fp4;              // routed weights are FP4 (else FP8)
+  int g_max, max_gu_tiles, max_dn_tiles;
+  long long max_gu_iters, max_dn_iters;
+};
+
+// Byte offsets of the prepared weight scales: for every (expert, 256-row
+// tile, 128-input k-block) 1 KB, the two 128-row halves' chunks; routed
+// gate_up, routed down, shared gate_up, shared down, in that order.
+__host__ __device__ inline size_t mx_scale_offset(int E, int H, int I, int Is, int phase, int e, int m, int kb) {
+  const size_t mb0 = ceil_div(I, kHalfRows), kb0 = H / kMxK, mb1 = ceil_div(H, 2 * kHalfRows), kb1 = I / kMxK;
+  const size_t r_gu = static_cast<size_t>(E) * mb0 * kb0, r_dn = static_cast<size_t>(E) * mb1 * kb1;
+  const size_t s_gu = static_cast<size_t>(ceil_div(Is, kHalfRows)) * kb0;
+  if (e >= 0) {
+    if (phase == 0) return ((static_cast<size_t>(e) * mb0 + m) * kb0 + kb) * 1024;
+    return (r_gu + (static_cast<size_t>(e) * mb1 + m) * kb1 + kb) * 1024;
+  }
+  if (phase == 0) return (r_gu + r_dn + static_cast<size_t>(m) * kb0 + kb) * 1024;
+  return (r_gu + r_dn + s_gu + static_cast<size_t>(m) * (Is / kMxK) + kb) * 1024;
+}
 
 // Routing recipe as the selection code reads it (score_fn 0 softmax,
 // 1 sigmoid, 2 sqrt(softplus); renorm = norm_topk_prob).
@@ -187,6 +258,8 @@ struct RouteParams {
   int32_t* zero_ptr;           // GEMM tile counters cleared by this launch
   int zero_count;
   int fp4;                     // routed experts are FP4: their k-blocks cost less
+  int fmt, sh_fmt;             // cost-model formats of the routed and the shared groups (kFmt*)
+  int kblk;                    // inputs per k-block of the work list (64, or 128 block-scaled)
   int logits_given;            // logits (and sh_logit) were computed by logits_gemm_kernel: route only
   uint16_t* xh;                // [T,H] f16 copy of x written for FP4 experts (nullable)
   int32_t* status;             // range errors of that copy
@@ -291,6 +364,12 @@ cudaError_t launch_slice(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, 
                          size_t smem_bytes, cudaStream_t s);
 cudaError_t launch_combine(const float* out_ws, const int32_t* pair_pos, int T, int K, int H,
                            int has_shared, uint16_t* y, cudaStream_t s);
+cudaError_t launch_mx(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, const CUtensorMap& tm_dn,
+                      const CUtensorMap& tm_dn_sh, const MxParams& p, int grid, size_t smem_bytes, cudaStream_t s);
+// Weight scales re-laid into the chunks the block-scaled MMA reads
+// (routed_fp4: one scale per 32 inputs; else one per 32 x 32 block).
+cudaError_t launch_mx_scales(int routed_fp4, const uint8_t* gu_s, const uint8_t* dn_s, int E, int H, int I,
+                             const uint8_t* sh_gu_s, const uint8_t* sh_dn_s, int Is, uint8_t* out, cudaStream_t s);
 
 // ----------------------------------------------------------------------------
 // inline PTX (device only)

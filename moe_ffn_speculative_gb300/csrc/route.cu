@@ -72,7 +72,8 @@ __device__ void block_scan_excl(const int* in, int* out, int n, int* s_warp) {
 __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* counts, int32_t* offsets,
                               int32_t* sorted_pair, int32_t* pair_pos, GroupEntry* groups, GemmHeader* header,
                               int H, int I, int Is, int n_max, int* s_cnt, int* s_cur, long long* s_buf,
-                              uint16_t* s_wc, int64_t* spans, int32_t* span_groups, int grid, bool fp4) {
+                              uint16_t* s_wc, int64_t* spans, int32_t* span_groups, int grid, int fmt,
+                              int sh_fmt, int kblk) {
   __shared__ int s_warp[kPermWarps];
   int* s_idx = reinterpret_cast<int*>(s_buf);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -229,8 +230,8 @@ __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* 
     if (lane == 0) atomicMax(&s_neff, wmax);
   }
   // geometry of a routed expert's tiles (every routed expert has the same I)
-  const int mb0 = ceil_div(I, kHalfRows), kb0 = ceil_div(H, kBlockK);
-  const int mb1 = ceil_div(H, 2 * kHalfRows), kb1 = ceil_div(I, kBlockK);
+  const int mb0 = ceil_div(I, kHalfRows), kb0 = ceil_div(H, kblk);
+  const int mb1 = ceil_div(H, 2 * kHalfRows), kb1 = ceil_div(I, kblk);
   const int per = (E + blockDim.x - 1) / blockDim.x;
   const int e0 = tid * per;
   // this thread's sums: touched experts, token blocks, gate_up cost, down cost
@@ -243,8 +244,8 @@ __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* 
       const int nmma = max(16, min(n_max, (c + 15) & ~15));
       v[0] += 1;
       v[1] += nb;
-      v[2] += static_cast<long long>(nb) * mb0 * kb0 * kblock_cost(0, nmma, fp4);
-      v[3] += static_cast<long long>(nb) * mb1 * kb1 * kblock_cost(1, nmma, fp4);
+      v[2] += static_cast<long long>(nb) * mb0 * kb0 * kblock_cost(0, nmma, fmt);
+      v[3] += static_cast<long long>(nb) * mb1 * kb1 * kblock_cost(1, nmma, fmt);
     }
   }
   long long incl[4] = {v[0], v[1], v[2], v[3]};
@@ -276,7 +277,7 @@ __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* 
       const int nb = ceil_div(c, n_max);
       const int nmma = max(16, min(n_max, (c + 15) & ~15));
       const int gi = static_cast<int>(run[0]);
-      const int w0 = kblock_cost(0, nmma, fp4), w1 = kblock_cost(1, nmma, fp4);
+      const int w0 = kblock_cost(0, nmma, fmt), w1 = kblock_cost(1, nmma, fmt);
       GroupEntry ge;
       ge.expert = e;
       ge.row_base = s_cur[e];
@@ -305,7 +306,7 @@ __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* 
     if (Is > 0) {
       int mb, nb, kb;
       const int nmma = max(16, min(n_max, (T + 15) & ~15));
-      const int w0 = kblock_cost(0, nmma), w1 = kblock_cost(1, nmma);
+      const int w0 = kblock_cost(0, nmma, sh_fmt), w1 = kblock_cost(1, nmma, sh_fmt);
       GroupEntry ge;
       ge.expert = -1;
       ge.row_base = TK;
@@ -320,11 +321,11 @@ __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* 
       groups[g] = ge;
       s_cost0[g] = gu_c;
       s_cost1[g] = dn_c;
-      group_geometry(0, T, Is, H, n_max, mb, nb, kb);
+      group_geometry(0, T, Is, H, n_max, mb, nb, kb, kblk);
       gu_t += mb * nb;
       gu_i += static_cast<long long>(mb) * nb * kb;
       gu_c += static_cast<long long>(mb) * nb * kb * w0;
-      group_geometry(1, T, Is, H, n_max, mb, nb, kb);
+      group_geometry(1, T, Is, H, n_max, mb, nb, kb, kblk);
       dn_t += mb * nb;
       dn_i += static_cast<long long>(mb) * nb * kb;
       dn_c += static_cast<long long>(mb) * nb * kb * w1;
@@ -591,7 +592,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
   if (!s_flag) return;
   __threadfence();
   permute_block(p.idx, p.T, p.K, p.E, p.counts, p.offsets, p.sorted_pair, p.pair_pos, p.groups, p.header, p.H,
-                p.I, p.Is, p.n_max, s_cnt, s_cur, s_buf, s_wc, p.spans, p.span_groups, p.grid, p.fp4 != 0);
+                p.I, p.Is, p.n_max, s_cnt, s_cur, s_buf, s_wc, p.spans, p.span_groups, p.grid,
+                p.fmt != 0 ? p.fmt : (p.fp4 ? kFmtFp4Conv : kFmtBf16), p.sh_fmt, p.kblk > 0 ? p.kblk : kBlockK);
 }
 
 // logits = x . gate^T (+ router_bias) for many tokens: a CTA computes a
@@ -686,7 +688,7 @@ __global__ void __launch_bounds__(kRouteThreads) permute_kernel(const int32_t* i
   __shared__ long long s_buf[kPermBuf];
   __shared__ uint16_t s_wc[kPermWarps * kMaxExperts];
   permute_block(idx, T, K, E, counts, offsets, sorted_pair, pair_pos, nullptr, nullptr, 0, 0, 0, 1, s_cnt, s_cur,
-                s_buf, s_wc, nullptr, nullptr, 0, false);
+                s_buf, s_wc, nullptr, nullptr, 0, kFmtBf16, kFmtBf16, kBlockK);
 }
 
 }  // namespace

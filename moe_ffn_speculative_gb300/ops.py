@@ -23,6 +23,8 @@ SCORE_SOFTMAX, SCORE_SIGMOID, SCORE_SQRTSOFTPLUS = 0, 1, 2
 # the workspace's start gate (include/moe.h) and the info word of its timeout
 WS_HOLD_OFFSET = 8
 INFO_HOLD = 15
+# routed-expert formats of the block-scaled path
+FMT_FP4, FMT_FP8 = 1, 2
 
 
 class MoeError(RuntimeError):
@@ -84,6 +86,10 @@ _SIGS = {
     "moe_fp4_prepare_scales": (_I, [_P, _P, _I, _I, _I, _P, _SZ, _P]),
     "moe_ffn_forward_fp4": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P, _I, _P,
                                  ctypes.POINTER(Recipe), _P, _SZ, _P, _P, _P, _P, _P]),
+    "moe_mx_scales_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_mx_prepare_scales": (_I, [_I, _P, _P, _I, _I, _I, _P, _P, _I, _P, _SZ, _P]),
+    "moe_ffn_forward_mx": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _SZ,
+                                ctypes.POINTER(Recipe), _P, _SZ, _P, _P, _P, _P, _P]),
 }
 
 SCHEDULE_AUTO, SCHEDULE_STREAM_K, SCHEDULE_SLICE = 0, 1, 2
@@ -316,6 +322,58 @@ def moe_ffn_forward_fp4(x, gate, w_gate_up_q, w_down_q, scales, recipe: Recipe, 
     return y
 
 
+def mx_format(t: dict) -> int:
+    """Routed-expert format of a block-scaled layer's tensors: FP4 scales
+    [E,2I,H/32] have a row per weight row, FP8 scales [E,2I/32,H/32] one per
+    32 rows."""
+    return FMT_FP4 if t["w_gate_up_s"].shape[1] == t["w_gate_up_q"].shape[1] else FMT_FP8
+
+
+def mx_dims(t: dict):
+    """(E, H, I, Is) of a block-scaled layer's tensors."""
+    q = t["w_gate_up_q"]
+    E, I = q.shape[0], q.shape[1] // 2
+    H = q.shape[2] * (2 if mx_format(t) == FMT_FP4 else 1)
+    Is = 0 if t.get("sh_gate_up_q") is None else t["sh_gate_up_q"].shape[0] // 2
+    return E, H, I, Is
+
+
+def mx_prepare_scales(t: dict, stream=None) -> torch.Tensor:
+    """The weight scales of a block-scaled layer (routed w_gate_up_s, w_down_s,
+    shared sh_gate_up_s, sh_down_s) re-laid for moe_ffn_forward_mx (once per
+    set of weights); returns the uint8 buffer."""
+    fmt = mx_format(t)
+    E, H, I, Is = mx_dims(t)
+    _need_cuda(t["w_gate_up_s"], t["w_down_s"], t.get("sh_gate_up_s"), t.get("sh_down_s"))
+    n = lib().moe_mx_scales_bytes(fmt, E, H, I, Is)
+    if n == 0:
+        raise MoeError(MOE_ERR_UNSUPPORTED, "moe_mx_scales_bytes")
+    out = torch.empty(n, dtype=torch.uint8, device=t["w_down_s"].device)
+    _check(lib().moe_mx_prepare_scales(fmt, _ptr(_u8(t["w_gate_up_s"])), _ptr(_u8(t["w_down_s"])), E, H, I,
+                                       _ptr(t.get("sh_gate_up_s")), _ptr(t.get("sh_down_s")), Is, _ptr(out), n,
+                                       _stream(stream)), "moe_mx_prepare_scales")
+    return out
+
+
+def moe_ffn_forward_mx(x, gate, routed_fmt: int, w_gate_up_q, w_down_q, scales, recipe: Recipe, ws: Workspace,
+                       I: int, router_bias=None, expert_bias=None, sh_gate_up_q=None, sh_down_q=None, sh_gate=None,
+                       y=None, topk_idx_out=None, topk_w_out=None, counts_out=None, stream=None):
+    """The whole layer with block-scaled experts (FP4 or FP8 routed, FP8
+    shared); returns y [T,H] bf16."""
+    _need_cuda(x, gate, w_gate_up_q, w_down_q, scales, router_bias, expert_bias, sh_gate_up_q, sh_down_q, sh_gate, y,
+               topk_idx_out, topk_w_out, counts_out)
+    T, H = x.shape
+    Is = 0 if sh_gate_up_q is None else sh_gate_up_q.shape[0] // 2
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _check(lib().moe_ffn_forward_mx(
+        _ptr(_u16(x)), T, H, I, _ptr(_u16(gate)), _ptr(router_bias), _ptr(expert_bias), int(routed_fmt),
+        _ptr(_u8(w_gate_up_q)), _ptr(_u8(w_down_q)), _ptr(sh_gate_up_q), _ptr(sh_down_q), Is, _ptr(sh_gate),
+        _ptr(_u8(scales)), scales.numel(), ctypes.byref(recipe), ws.ptr(), ws.nbytes, _ptr(y), _ptr(topk_idx_out),
+        _ptr(topk_w_out), _ptr(counts_out), _stream(stream)), "moe_ffn_forward_mx")
+    return y
+
+
 def set_schedule(schedule: int) -> None:
     """Expert schedule of later moe_ffn_forward calls on this thread:
     SCHEDULE_AUTO, SCHEDULE_STREAM_K or SCHEDULE_SLICE."""
@@ -349,20 +407,33 @@ _profile_keepalive = None
 class MoELayer:
     """Weights of one layer plus its workspace; ``forward(x)`` runs the layer."""
 
-    def __init__(self, tensors: dict, recipe: Recipe, max_tokens: int):
+    def __init__(self, tensors: dict, recipe: Recipe, max_tokens: int, mx: Optional[bool] = None):
+        """Routed experts as bf16 (w_gate_up, w_down), or as codes
+        (w_gate_up_q, w_down_q with scales w_gate_up_s, w_down_s, re-laid once
+        here): FP8 codes, or an FP8 shared expert (sh_gate_up_q, ...), take the
+        block-scaled path (moe_ffn_forward_mx); FP4 codes with a bf16 shared
+        expert take moe_ffn_forward_fp4 unless `mx` asks for the block-scaled
+        path."""
         self.t = tensors
         self.recipe = recipe
-        # FP4 routed experts when the codes are given (w_gate_up_q, w_down_q,
-        # and their scales w_gate_up_s, w_down_s, re-laid once here)
-        self.fp4 = tensors.get("w_down_q") is not None
-        if self.fp4:
+        coded = tensors.get("w_down_q") is not None
+        if mx is None:
+            mx = coded and (tensors.get("sh_gate_up_q") is not None or mx_format(tensors) == FMT_FP8)
+        self.mx = bool(mx)
+        self.fp4 = coded and not self.mx
+        if self.mx:
+            self.fmt = mx_format(tensors)
+            _, self.H, self.I, self.Is = mx_dims(tensors)
+            self.scales = mx_prepare_scales(tensors)
+        elif self.fp4:
             self.H = tensors["w_down_q"].shape[1]
             self.I = tensors["w_down_q"].shape[2] * 2
             self.scales = fp4_prepare_scales(tensors["w_gate_up_s"], tensors["w_down_s"])
         else:
             self.H = tensors["w_down"].shape[1]
             self.I = tensors["w_down"].shape[2]
-        self.Is = 0 if tensors.get("sh_gate_up") is None else tensors["sh_down"].shape[1]
+        if not self.mx:
+            self.Is = 0 if tensors.get("sh_gate_up") is None else tensors["sh_down"].shape[1]
         self.max_tokens = max_tokens
         # one workspace for every token count up to max_tokens: its counters
         # sit in a fixed header and return to zero after every call
@@ -374,6 +445,13 @@ class MoELayer:
         if T > self.max_tokens:
             raise ValueError("more tokens than the workspace was sized for")
         t = self.t
+        if self.mx:
+            return moe_ffn_forward_mx(x, t["gate"], self.fmt, t["w_gate_up_q"], t["w_down_q"], self.scales,
+                                      self.recipe, self.ws, self.I, router_bias=t.get("router_bias"),
+                                      expert_bias=t.get("expert_bias"), sh_gate_up_q=t.get("sh_gate_up_q"),
+                                      sh_down_q=t.get("sh_down_q"), sh_gate=t.get("sh_gate"), y=y,
+                                      topk_idx_out=topk_idx_out, topk_w_out=topk_w_out, counts_out=counts_out,
+                                      stream=stream)
         if self.fp4:
             return moe_ffn_forward_fp4(x, t["gate"], t["w_gate_up_q"], t["w_down_q"], self.scales, self.recipe,
                                        self.ws, router_bias=t.get("router_bias"), expert_bias=t.get("expert_bias"),

@@ -121,3 +121,25 @@ def test_noalloc_router_checks_arguments_first(lib):
         ops.MOE_ERR_UNSUPPORTED
     assert lib.moe_route_noalloc(None, 0, 64, None, None, None, ctypes.byref(rec), None, None, None, None) == \
         ops.MOE_OK
+
+
+def test_block_scaled_refusals_before_any_device_call(lib):
+    """moe_ffn_forward_mx / moe_mx_* refuse a bad format, a shape that is not
+    a multiple of 128 and a missing workspace on the host."""
+    rec = ops.Recipe.make(8, 2)
+    assert lib.moe_mx_scales_bytes(ops.FMT_FP4, 8, 4096, 2304, 2304) > 0
+    assert lib.moe_mx_scales_bytes(3, 8, 4096, 2304, 0) == 0
+    assert lib.moe_mx_scales_bytes(ops.FMT_FP8, 8, 4096 + 64, 2304, 0) == 0
+
+    def fwd(fmt=ops.FMT_FP4, H=256, I=256, Is=0, ws=6 << 20, ws_bytes=1 << 30):
+        return lib.moe_ffn_forward_mx(1 << 20, 16, H, I, 2 << 20, None, None, fmt, 3 << 20, 4 << 20, None, None, Is,
+                                      None, 5 << 20, 1 << 30, ctypes.byref(rec), ws, ws_bytes, 7 << 20, None, None,
+                                      None, None)
+    assert fwd(fmt=0) == ops.MOE_ERR_INVALID_ARG
+    assert fwd(H=192) == ops.MOE_ERR_UNSUPPORTED
+    assert fwd(I=320) == ops.MOE_ERR_UNSUPPORTED
+    assert fwd(Is=128) == ops.MOE_ERR_INVALID_ARG  # a shared width without shared weights
+    assert fwd(ws=None) == ops.MOE_ERR_WORKSPACE
+    assert fwd(ws_bytes=1024) == ops.MOE_ERR_WORKSPACE
+    assert lib.moe_mx_prepare_scales(ops.FMT_FP4, 1 << 20, 2 << 20, 8, 4096, 2304, None, None, 0, 3 << 20, 16,
+                                     None) == ops.MOE_ERR_WORKSPACE
