@@ -39,19 +39,47 @@ METRIC = "MoE-FFN layer tokens/s at T=72 on 1 GB300"
 UNIT = "tokens/s"
 
 
-def metric_for(cfg) -> str:
+# --weights: the routed (and shared) experts' format and the path that runs it
+WEIGHTS = {
+    "bf16": dict(expert_format="bf16", shared_format="bf16"),
+    # FP4 routed experts expanded to f16 by converter warps, bf16 shared expert
+    "fp4": dict(expert_format="fp4", shared_format="bf16"),
+    # block-scaled MMA: FP4 routed experts + FP8 shared expert (DeepSeek-V4.1's
+    # checkpoint formats), or FP8 routed + FP8 shared
+    "mx-fp4": dict(expert_format="fp4", shared_format="fp8"),
+    "mx-fp8": dict(expert_format="fp8", shared_format="fp8"),
+}
+
+
+def weights_of(cfg) -> str:
+    for k, v in WEIGHTS.items():
+        if cfg.expert_format == v["expert_format"] and (cfg.shared_format == v["shared_format"] or cfg.shared_I == 0):
+            if k == "fp4" and cfg.shared_format == "fp8":
+                continue
+            return k
+    return "mx-" + cfg.expert_format
+
+
+def is_mx(cfg) -> bool:
+    return cfg.expert_format == "fp8" or cfg.shared_format == "fp8"
+
+
+def metric_for(cfg, weights: str = None) -> str:
     """The headline metric for the headline layer, else one naming the
     workload (both arms print the same name for the same workload)."""
-    fp4 = cfg.expert_format == "fp4"
-    if cfg.name == "qwen3_8b_dspark" and cfg.T == 72 and not fp4:
+    weights = weights or weights_of(cfg)
+    if cfg.name == "qwen3_8b_dspark" and cfg.T == 72 and weights == "bf16":
         return METRIC
-    return f"MoE-FFN layer tokens/s ({cfg.name}{', FP4 experts' if fp4 else ''}, T={cfg.T})"
+    label = {"bf16": "", "fp4": ", FP4 experts", "mx-fp4": ", block-scaled FP4 experts + FP8 shared",
+             "mx-fp8": ", block-scaled FP8 experts + FP8 shared"}[weights]
+    return f"MoE-FFN layer tokens/s ({cfg.name}{label}, T={cfg.T})"
 
 
 CSRC = os.path.join(ROOT, "moe_ffn_speculative_gb300", "csrc")
 # per expert schedule: the dominant kernel, its ncu summary prefix, its source
 KERNELS = {"stream_k": ("moe_experts_kernel", "experts_kernel", "gemm.cu"),
-           "slice": ("moe_slice_kernel", "slice_kernel", "slice.cu")}
+           "slice": ("moe_slice_kernel", "slice_kernel", "slice.cu"),
+           "mx": ("moe_mx_kernel", "mx_kernel", "mx.cu")}
 
 
 def parse():
@@ -65,8 +93,10 @@ def parse():
     ap.add_argument("--experts", type=int, default=None, help="override E (small profiling cases)")
     ap.add_argument("--schedule", default="auto", choices=["auto", "stream_k", "slice"],
                     help="expert schedule (auto: the library's choice for the shape)")
-    ap.add_argument("--weights", default="bf16", choices=["bf16", "fp4"],
-                    help="routed experts' format: bf16, or FP4 (e2m1 codes + e8m0 scale per 32 inputs)")
+    ap.add_argument("--weights", default="bf16", choices=list(WEIGHTS),
+                    help="experts' format: bf16; fp4 (e2m1 codes + e8m0 scale per 32 inputs, expanded to f16, bf16 "
+                         "shared expert); mx-fp4 / mx-fp8 (block-scaled MMA: FP4 or FP8 routed experts, FP8 shared "
+                         "expert)")
     ap.add_argument("--workloads", default="targets", choices=["none", "targets", "all"],
                     help="also measure the other T=72 decode workloads (targets), plus the DeepSeek-V4-style "
                          "token sweep (all)")
@@ -158,14 +188,18 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- roofline helpers
 
+# bytes per weight: bf16; FP4 codes (half a byte) + one scale byte per 32;
+# FP8 codes + one scale byte per 32 x 32 block
+WEIGHT_BYTES = {"bf16": 2.0, "fp4": 0.5 + 1 / 32, "fp8": 1 + 1 / 1024}
+
+
 def algorithmic(cfg, counts_u: int):
     """Bytes and FLOPs of one layer forward and of its expert-GEMM launch,
     counting only the touched experts' weights (each read once)."""
     T, H, I, E, K, Is = cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cfg.shared_I
-    # routed weights: bf16, or FP4 codes (half a byte) plus one scale byte per 32
-    wb = (0.5 + 1 / 32) if cfg.expert_format == "fp4" else 2
-    gu_w = int(counts_u * 2 * I * H * wb) + 2 * Is * H * 2
-    dn_w = int(counts_u * H * I * wb) + H * Is * 2
+    wb, sb = WEIGHT_BYTES[cfg.expert_format], WEIGHT_BYTES[cfg.shared_format]
+    gu_w = int(counts_u * 2 * I * H * wb) + int(2 * Is * H * sb)
+    dn_w = int(counts_u * H * I * wb) + int(H * Is * sb)
     act = T * H * 2 * 2  # x read, y written
     gate = E * H * 2 + (H * 2 if cfg.shared_gated else 0)
     biases = E * 4 * ((cfg.router_bias_std > 0) + (cfg.expert_bias_std > 0))
@@ -174,7 +208,13 @@ def algorithmic(cfg, counts_u: int):
     # experts launch: both projections' weights once, x gathered, h (hi and lo)
     # written and read back, the weighted outputs written (fp32 rows, or bf16 y)
     out = rows * H * 4 if (K > 1 or Is) else T * H * 2
-    ex_bytes = gu_w + dn_w + T * H * 2 + 2 * rows * max(I, Is) * 2 * 2 + out
+    if is_mx(cfg):
+        # x cut into 3 e4m3 pieces (+ a scale byte per 32) written and read,
+        # h as 4 pieces written and read back
+        ex_bytes = gu_w + dn_w + T * H * 2 + 2 * int(3 * T * H * 33 / 32) + 2 * int(rows * 4 * max(I, Is) * 33 / 32) \
+            + out
+    else:
+        ex_bytes = gu_w + dn_w + T * H * 2 + 2 * rows * max(I, Is) * 2 * 2 + out
     flops = T * K * 6 * H * I + (T * 6 * H * Is if Is else 0) + 2 * T * H * E
     return layer_bytes, ex_bytes, flops
 
@@ -234,7 +274,7 @@ def cpu_oracle_pass(cfg, host, w64, tokens):
                    cfg.norm_topk_prob, cfg.norm_eps, cfg.route_scale, cfg.swiglu_limit)
     logits = O.router_logits(x, f64(host["gate"]), f64(host["router_bias"]))
     _, idx, w, _ = O.route_from_logits(logits, rec, f64(host["expert_bias"]))
-    shared = None if host["sh_gate_up"] is None else (w64["sh_gate_up"], w64["sh_down"])
+    shared = None if "sh_gate_up" not in w64 else (w64["sh_gate_up"], w64["sh_down"])
     return O.moe_combine_rows(x, idx, w, lambda e: w64[e], cfg.swiglu_limit, shared, f64(host["sh_gate"]))
 
 
@@ -246,11 +286,17 @@ def cpu_prepare(cfg):
         if cfg.expert_format == "fp4":
             w64[e] = (O.dequant_fp4(host["w_gate_up_q"][e].numpy(), host["w_gate_up_s"][e].numpy()),
                       O.dequant_fp4(host["w_down_q"][e].numpy(), host["w_down_s"][e].numpy()))
+        elif cfg.expert_format == "fp8":
+            w64[e] = (O.dequant_fp8_blocks(host["w_gate_up_q"][e].numpy(), host["w_gate_up_s"][e].numpy()),
+                      O.dequant_fp8_blocks(host["w_down_q"][e].numpy(), host["w_down_s"][e].numpy()))
         else:
             w64[e] = (host["w_gate_up"][e].double().numpy(), host["w_down"][e].double().numpy())
     if host["sh_gate_up"] is not None:
         w64["sh_gate_up"] = host["sh_gate_up"].double().numpy()
         w64["sh_down"] = host["sh_down"].double().numpy()
+    elif host.get("sh_gate_up_q") is not None:
+        w64["sh_gate_up"] = O.dequant_fp8_blocks(host["sh_gate_up_q"].numpy(), host["sh_gate_up_s"].numpy())
+        w64["sh_down"] = O.dequant_fp8_blocks(host["sh_down_q"].numpy(), host["sh_down_s"].numpy())
     return host, w64
 
 
@@ -258,7 +304,7 @@ def cpu_child(spec: dict) -> dict:
     """Runs in a child process whose BLAS thread count the parent fixed:
     full-layer oracle passes over the workload's T tokens for `seconds`."""
     torch.set_num_threads(int(spec["threads"]))
-    cfg = S.CONFIGS[spec["name"]].with_(T=int(spec["T"]), expert_format=spec["format"])
+    cfg = S.CONFIGS[spec["name"]].with_(T=int(spec["T"]), **WEIGHTS[spec["weights"]])
     host, w64 = cpu_prepare(cfg)
     t0 = time.perf_counter()
     n_tok = passes = 0
@@ -276,7 +322,7 @@ def _cpu_run(cfg, seconds: float, threads: int) -> dict:
     for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
         env[k] = str(threads)
     env["CUDA_VISIBLE_DEVICES"] = ""  # the oracle runs on the host cores only
-    spec = json.dumps({"name": cfg.name, "T": cfg.T, "format": cfg.expert_format, "seconds": seconds,
+    spec = json.dumps({"name": cfg.name, "T": cfg.T, "weights": weights_of(cfg), "seconds": seconds,
                        "threads": threads})
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", spec], capture_output=True,
                        text=True, env=env, cwd=ROOT, timeout=600)
@@ -326,8 +372,7 @@ def run_reference(args, cfg, rank, world):
             "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "I": cfg.I, "K": cfg.K,
                        "shared_I": cfg.shared_I,
-                       "routed_experts": "fp4 (e2m1 + e8m0/32)" if cfg.expert_format == "fp4" else "bf16",
-                       "tokens_per_step_sample": tok_per_step},
+                       "weights": weights_of(cfg), "tokens_per_step_sample": tok_per_step},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                              "threads": {"blas": "library default (every core)"},
                              "sample": f"{tok_per_step} of the {cfg.T} tokens per step, fp64 numpy oracle"},
@@ -340,8 +385,12 @@ def run_reference(args, cfg, rank, world):
 # The other decode workloads with a >= 70% roofline target, measured in the
 # same process and under the same clock record as the headline; with
 # --workloads all also the rest of the DeepSeek-V4-style token sweep.
-TARGET_WORKLOADS = [("qwen38_27b_dspark", 72), ("dsv3_style", 72), ("dsv4_style", 72)]
-SWEEP_WORKLOADS = [("dsv4_style", 9), ("dsv4_style", 576), ("dsv4_style", 4096)]
+TARGET_WORKLOADS = [("qwen38_27b_dspark", 72, "bf16"), ("dsv3_style", 72, "bf16"), ("dsv4_style", 72, "bf16"),
+                    # DeepSeek-V4.1's own draft layer, bf16 and in its checkpoint's formats; FP8 experts
+                    ("dsv41_dspark_draft", 72, "bf16"), ("dsv41_dspark_draft", 72, "mx-fp4"),
+                    ("dsv4_flash_drafter", 72, "mx-fp8")]
+SWEEP_WORKLOADS = [("dsv4_style", 9, "bf16"), ("dsv4_style", 576, "bf16"), ("dsv4_style", 4096, "bf16"),
+                   ("dsv41_dspark_draft", 72, "fp4")]
 NOMINAL_HBM_GBS = 8000.0
 _T0 = time.perf_counter()
 
@@ -361,24 +410,36 @@ class Workload:
         self.ops = ops
         self.cfg = cfg
         self.rec = ops.Recipe.from_config(cfg)
-        self.fp4 = cfg.expert_format == "fp4"
+        self.mx = is_mx(cfg)
+        self.fp4 = cfg.expert_format == "fp4" and not self.mx
         ops.set_schedule({"auto": ops.SCHEDULE_AUTO, "stream_k": ops.SCHEDULE_STREAM_K,
                           "slice": ops.SCHEDULE_SLICE}[schedule])
-        # FP4 routed experts always run the stream-K schedule
-        self.sched = "stream_k" if self.fp4 else ops.SCHEDULE_NAMES[ops.ffn_schedule(
-            cfg.T, cfg.H, cfg.I, cfg.shared_I, self.rec, gated=cfg.shared_gated and cfg.shared_I > 0)]
+        # coded experts always run the stream-K schedule (the block-scaled one
+        # in its own kernel)
+        if self.mx:
+            self.sched = "mx"
+        elif self.fp4:
+            self.sched = "stream_k"
+        else:
+            self.sched = ops.SCHEDULE_NAMES[ops.ffn_schedule(
+                cfg.T, cfg.H, cfg.I, cfg.shared_I, self.rec, gated=cfg.shared_gated and cfg.shared_I > 0)]
         base = S.make_inputs(cfg, device=dev, seed=cfg.seed + 1000 * rank)
         self.base = base
         self.n_copies = max(2, -(-4 * L2_BYTES // (cfg.weight_bytes + 1)))
-        wkeys = ["w_gate_up_q", "w_down_q"] if self.fp4 else ["w_gate_up", "w_down"]
+        wkeys = ["w_gate_up_q", "w_down_q"] if cfg.expert_format != "bf16" else ["w_gate_up", "w_down"]
+        if base["sh_gate_up"] is not None:
+            wkeys += ["sh_gate_up", "sh_down"]
+        if base.get("sh_gate_up_q") is not None:
+            wkeys += ["sh_gate_up_q", "sh_down_q"]
         self.layers = [base]
         for _ in range(1, self.n_copies):
             dd = dict(base)
-            for k in wkeys + (["sh_gate_up", "sh_down"] if base["sh_gate_up"] is not None else []):
+            for k in wkeys:
                 dd[k] = base[k].clone()
             self.layers.append(dd)
-        if self.fp4:
-            sc = ops.fp4_prepare_scales(base["w_gate_up_s"], base["w_down_s"])
+        if self.fp4 or self.mx:
+            sc = ops.mx_prepare_scales(base) if self.mx else ops.fp4_prepare_scales(base["w_gate_up_s"],
+                                                                                    base["w_down_s"])
             for dd in self.layers:
                 dd["scales"] = sc.clone()
         self.ws = ops.Workspace(ops.ffn_workspace_bytes(cfg.T, cfg.H, cfg.I, cfg.shared_I, self.rec), dev)
@@ -394,6 +455,7 @@ class Workload:
             self.timed = {n: k for k, n in enumerate(["router", "experts", "combine"][:self.launched])}
             if cfg.T > 1024 and not self.fp4:
                 self.launched += 1
+        self.ex_key = "fused" if self.sched == "slice" else "experts"
         # inputs and the zero-filled workspace were made on torch's current
         # stream; the layer runs on its own stream
         torch.cuda.synchronize()
@@ -402,7 +464,13 @@ class Workload:
         ops, kw = self.ops, dict(router_bias=dd["router_bias"], expert_bias=dd["expert_bias"],
                                  sh_gate_up=dd["sh_gate_up"], sh_down=dd["sh_down"], sh_gate=dd["sh_gate"], y=yy,
                                  counts_out=cnt, stream=self.stream)
-        if self.fp4:
+        if self.mx:
+            kw.pop("sh_gate_up")
+            kw.pop("sh_down")
+            ops.moe_ffn_forward_mx(xx, dd["gate"], ops.mx_format(dd), dd["w_gate_up_q"], dd["w_down_q"], dd["scales"],
+                                   self.rec, self.ws, self.cfg.I, sh_gate_up_q=dd.get("sh_gate_up_q"),
+                                   sh_down_q=dd.get("sh_down_q"), **kw)
+        elif self.fp4:
             ops.moe_ffn_forward_fp4(xx, dd["gate"], dd["w_gate_up_q"], dd["w_down_q"], dd["scales"], self.rec,
                                     self.ws, **kw)
         else:
@@ -507,7 +575,7 @@ def roofline_record(wl, u, per_kernel, ms_step, hbm, tflops, peak_src, traffic_k
     duration) and the layer's (roofline time over the step time)."""
     cfg = wl.cfg
     layer_bytes, ex_bytes, flops = algorithmic(cfg, u)
-    kname = "fused" if wl.sched == "slice" else "experts"
+    kname = wl.ex_key
     if wl.sched == "slice":
         ex_bytes = layer_bytes  # the fused launch is the whole layer
     achieved = ex_bytes / (per_kernel[kname] * 1e-6) / 1e9
@@ -526,7 +594,8 @@ def roofline_record(wl, u, per_kernel, ms_step, hbm, tflops, peak_src, traffic_k
 
 def workload_key(cfg, args_override: bool):
     wl = cfg.name if not args_override else f"{cfg.name}_T{cfg.T}_E{cfg.E}"
-    return wl + ("_fp4" if cfg.expert_format == "fp4" else "")
+    w = weights_of(cfg)
+    return wl + ("" if w == "bf16" else "_" + w.replace("-", ""))
 
 
 def measure_extra(cfg, dev, rank, K, W, hbm, tflops, peak_src, sustain_s):
@@ -552,7 +621,8 @@ def measure_extra(cfg, dev, rank, K, W, hbm, tflops, peak_src, sustain_s):
         wl.check_status("after the timed region")
         roof, layer = roofline_record(wl, u, per_kernel, ms_step, hbm, tflops, peak_src,
                                       workload_key(cfg, False))
-        return {"workload": cfg.name, "T": cfg.T, "metric": metric_for(cfg), "schedule": wl.sched,
+        return {"workload": cfg.name, "T": cfg.T, "weights": weights_of(cfg), "metric": metric_for(cfg),
+                "schedule": wl.sched,
                 "touched_experts": u, "us_per_layer": ms_step * 1e3, "tokens_per_s": cfg.T / (ms_step * 1e-3),
                 "steps": K, "layer_frac": layer["frac"], "kernel_frac": roof["frac"],
                 "kernel_frac_vs_nominal": roof["frac_vs_nominal"], "kernel_us": per_kernel,
@@ -632,26 +702,28 @@ def run_gpu(args, cfg, rank, world):
     if args.workloads != "none" and args.tokens is None and args.experts is None and args.weights == "bf16" \
             and args.schedule == "auto":
         todo = TARGET_WORKLOADS + (SWEEP_WORKLOADS if args.workloads == "all" else [])
-        for name, T in todo:
-            c = S.CONFIGS[name].with_(T=T)
-            if c.name == cfg.name and c.T == cfg.T:
+        for name, T, weights in todo:
+            c = S.CONFIGS[name].with_(T=T, **WEIGHTS[weights])
+            if c == cfg:
                 continue
             extra.append(measure_extra(c, dev, rank, K, W, hbm, tflops, peak_src, args.sustain_extra))
     clk = clocks.stop()
 
     if rank != 0:
         return
-    fp4 = cfg.expert_format == "fp4"
+    weights = weights_of(cfg)
     line = {
         "metric": metric_for(cfg),
         "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms_step,
         "us_per_layer": ms_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        # the MMA operand type: FP4 experts are expanded to f16 on chip
-        "dtype": "f16" if fp4 else "bf16", "data": "synthetic",
+        # the MMA operand types: FP4 experts are expanded to f16 on chip; the
+        # block-scaled path multiplies e2m1 or e4m3 weights by e4m3 pieces
+        "dtype": {"bf16": "bf16", "fp4": "f16", "mx-fp4": "e2m1xe4m3", "mx-fp8": "e4m3"}[weights],
+        "data": "synthetic",
         "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "I": cfg.I, "K": cfg.K,
                    "shared_I": cfg.shared_I, "touched_experts": u, "schedule": sched,
-                   "routed_experts": "fp4 (e2m1 + e8m0/32)" if fp4 else "bf16",
+                   "weights": weights,
                    "launch": f"cuda_graph_replay, {G} layer{'s' if G > 1 else ''} per graph",
                    "l2": f"weights rotate over {n_copies} copies ({n_copies * cfg.weight_bytes / 1e9:.2f} GB) > L2",
                    "parallelism": "replicas" if world > 1 else "single_gpu"},
@@ -677,9 +749,7 @@ def main():
     if args.cpu_child:
         print(json.dumps(cpu_child(json.loads(args.cpu_child))), flush=True)
         return
-    cfg = S.CONFIGS[args.config]
-    if args.weights == "fp4":
-        cfg = cfg.with_(expert_format="fp4")
+    cfg = S.CONFIGS[args.config].with_(**WEIGHTS[args.weights])
     if args.tokens is not None:
         cfg = cfg.with_(T=args.tokens)
     if args.experts is not None:

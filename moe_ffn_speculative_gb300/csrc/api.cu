@@ -233,8 +233,10 @@ struct Layout {
   bool need_out;
   size_t o_status, o_cnt, o_tiles, o_logits, o_shl, o_shw, o_idx, o_w, o_counts, o_offsets, o_sp, o_pp, o_groups,
       o_header, o_spans, o_span_groups, o_partials, o_h, o_out, o_sync, o_hbuf, o_sout, o_xh, total;
-  // block-scaled path: e4m3 pieces of h and x with their scales
-  size_t o_hq, o_hs, o_xq, o_xs;
+  // block-scaled path: the token operand images (x's for gate_up, h's for
+  // down) of every (token block, k-block), each expert's first token block
+  size_t o_img_gu, o_img_dn, o_e2d;
+  int n_dense, img_gu_rows, img_dn_rows;
 };
 
 // mx: the layout of the block-scaled path (moe_ffn_forward_mx): token tiles
@@ -308,12 +310,20 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   L.o_spans = o; o = align_up(o + 8 * 2 * static_cast<size_t>(L.grid + 1));
   L.o_span_groups = o; o = align_up(o + 4 * 2 * static_cast<size_t>(L.grid + 1));
   L.o_partials = o; o = align_up(o + 4 * static_cast<size_t>(L.grid) * 4 * 2 * L.n_max * 128);
-  L.o_h = L.o_hq = L.o_hs = L.o_xq = L.o_xs = L.o_xh = 0;
+  L.o_h = L.o_img_gu = L.o_img_dn = L.o_e2d = L.o_xh = 0;
+  L.n_dense = L.img_gu_rows = L.img_dn_rows = 0;
   if (mx) {
-    L.o_hq = o; o = align_up(o + static_cast<size_t>(kMxPh) * rows * L.I_ld);
-    L.o_hs = o; o = align_up(o + static_cast<size_t>(kMxPh) * rows * (L.I_ld / 32));
-    L.o_xq = o; o = align_up(o + static_cast<size_t>(kMxPx) * T * H);
-    L.o_xs = o; o = align_up(o + static_cast<size_t>(kMxPx) * T * (H / 32));
+    // token blocks: the routed groups' (at most u_max + TK / n_max) and the
+    // shared expert's
+    L.n_dense = static_cast<int>(u_max + TK / L.n_max) + (Is > 0 ? ceil_div(T, L.n_max) : 0);
+    L.img_gu_rows = ((kMxPx * L.n_max + 15) / 16) * 16;
+    L.img_dn_rows = ((kMxPh * L.n_max + 15) / 16) * 16;
+    const size_t slot_gu = static_cast<size_t>(L.img_gu_rows) * 128 + kMxSfBytes;
+    const size_t slot_dn = static_cast<size_t>(L.img_dn_rows) * 128 + kMxSfBytes;
+    const int Imx = Is > I ? Is : I;
+    L.o_img_gu = o; o = align_up(o + static_cast<size_t>(L.n_dense) * (H / kMxK) * slot_gu);
+    L.o_img_dn = o; o = align_up(o + static_cast<size_t>(L.n_dense) * (Imx / kMxK) * slot_dn);
+    L.o_e2d = o; o = align_up(o + 4 * static_cast<size_t>(E));
   } else {
     L.o_h = o; o = align_up(o + 2 * 2 * rows * L.I_ld);
     L.o_xh = o; o = align_up(o + 2 * static_cast<size_t>(T) * H);  // f16 copy of x (FP4 experts)
@@ -786,6 +796,7 @@ moe_status ffn_forward_mx(const moe_bf16* x, int T, int H, int I, const moe_bf16
   rp.fmt = fp4 ? kFmtMxFp4 : kFmtMxFp8;
   rp.sh_fmt = kFmtMxFp8;
   rp.kblk = kMxK;
+  rp.e2d = reinterpret_cast<int32_t*>(w + L.o_e2d);
   // the tile counters, readiness counters and the x-pieces counter
   rp.zero_ptr = tiles; rp.zero_count = 2 * L.max_gu_tiles + L.max_dn_tiles + 1;
   record_event_on(0, stream);
@@ -819,16 +830,24 @@ moe_status ffn_forward_mx(const moe_bf16* x, int T, int H, int I, const moe_bf16
   memset(&mp, 0, sizeof(mp));
   mp.groups = groups; mp.header = header; mp.spans = rp.spans; mp.span_groups = rp.span_groups;
   mp.x = x;
-  mp.xq = reinterpret_cast<uint8_t*>(w + L.o_xq);
-  mp.xs = reinterpret_cast<uint8_t*>(w + L.o_xs);
-  mp.xq_ready = tiles + 2 * L.max_gu_tiles + L.max_dn_tiles;
   mp.sorted_pair = sorted_pair;
+  mp.idx = idx;
+  mp.pair_pos = pair_pos;
+  mp.offsets = rp.offsets;
+  mp.e2d = rp.e2d;
+  mp.img_gu = reinterpret_cast<uint8_t*>(w + L.o_img_gu);
+  mp.img_dn = reinterpret_cast<uint8_t*>(w + L.o_img_dn);
+  mp.img_gu_rows = L.img_gu_rows;
+  mp.img_dn_rows = L.img_dn_rows;
+  mp.kb_gu = H / kMxK;
+  mp.kb_dn = (Is > I ? Is : I) / kMxK;
+  mp.mb0 = ceil_div(I, kHalfRows);
+  mp.n_dense = L.n_dense;
+  mp.img_ready = tiles + 2 * L.max_gu_tiles + L.max_dn_tiles;
   mp.T = T; mp.K = K; mp.TK = T * K; mp.H = H; mp.I_ld = Is > I ? Is : I;
   mp.n_max = L.n_max;
   mp.stage_space = kSmemLimit - 1024 - kCtrlBytes;
   mp.swiglu_limit = recipe->swiglu_limit;
-  mp.hq = reinterpret_cast<uint8_t*>(w + L.o_hq);
-  mp.hs = reinterpret_cast<uint8_t*>(w + L.o_hs);
   mp.out_ws = out_ws; mp.y = y; mp.direct_y = L.need_out ? 0 : 1;
   mp.topk_w = wts; mp.sh_w = (Is > 0 && sh_gate) ? sh_w : nullptr;
   mp.partials = reinterpret_cast<float*>(w + L.o_partials);

@@ -165,7 +165,7 @@ struct GemmParams {
 constexpr int kMxK = 128;        // inputs per k-block
 constexpr int kMxPx = 3;         // e4m3 pieces of x
 constexpr int kMxPh = 4;         // e4m3 pieces of h
-constexpr int kMxMaxTok = 32;    // token tile: kMxPh x 32 = 128 MMA columns
+constexpr int kMxMaxTok = 24;    // token tile: kMxPh x 24 = 96 MMA columns, two accumulator buffers in TMEM
 constexpr int kMxSfBytes = 512;  // one scale chunk: 128 rows x 4 inputs-chunks of 32
 constexpr int kMxThreads = 224;
 
@@ -175,16 +175,28 @@ struct MxParams {
   const int64_t* spans;
   const int32_t* span_groups;
   const uint16_t* x;           // [T,H] bf16
-  uint8_t* xq;                 // [T][kMxPx][H] e4m3 pieces of x (written by the kernel's prologue)
-  uint8_t* xs;                 // [T][kMxPx][H/32] their e8m0 scales
-  int32_t* xq_ready;           // warps that finished their share of the pieces (zeroed by the router)
   const int32_t* sorted_pair;
+  const int32_t* idx;          // [T*K] routing of every (token, slot)
+  const int32_t* pair_pos;     // [T*K] its row among the sorted pairs
+  const int32_t* offsets;      // [E+1] first sorted row of every expert
+  const int32_t* e2d;          // [E] first token block of every touched expert (router)
+  // Operand images: for every token block of every group (dense index: the
+  // group's first gate_up tile / mb0 + block) and every k-block, the B tile
+  // the MMA reads (rows of 128 bytes in the 128-byte-swizzled K-major layout,
+  // token j's piece p in row j*P + p) followed by its 512-byte scale chunk.
+  // The gate_up images (pieces of x) are written by the kernel's prologue,
+  // the down images (pieces of h) by the gate_up epilogue.
+  uint8_t* img_gu;
+  uint8_t* img_dn;
+  int img_gu_rows, img_dn_rows;  // rows of an image slot
+  int kb_gu, kb_dn;            // k-blocks per token block: H/128, I_ld/128
+  int mb0;                     // routed gate_up m-blocks, ceil(I/128)
+  int n_dense;                 // token blocks of all groups (bound)
+  int32_t* img_ready;          // warps that finished their share of the gate_up images (zeroed by the router)
   int T, K, TK, H, I_ld;       // I_ld = max(I, Is)
-  int n_max;                   // token tile width (16 or 32)
+  int n_max;                   // token tile width (16 or 24)
   int stage_space;
   float swiglu_limit;
-  uint8_t* hq;                 // [T*K + T][kMxPh][I_ld] e4m3 pieces of h
-  uint8_t* hs;                 // [T*K + T][kMxPh][I_ld/32] their scales
   float* out_ws;               // [T*K + T, H] fp32 weighted outputs (unless direct_y)
   uint16_t* y;
   int direct_y;
@@ -260,6 +272,7 @@ struct RouteParams {
   int fp4;                     // routed experts are FP4: their k-blocks cost less
   int fmt, sh_fmt;             // cost-model formats of the routed and the shared groups (kFmt*)
   int kblk;                    // inputs per k-block of the work list (64, or 128 block-scaled)
+  int32_t* e2d;                // [E] (nullable) each touched expert's first token block over all groups
   int logits_given;            // logits (and sh_logit) were computed by logits_gemm_kernel: route only
   uint16_t* xh;                // [T,H] f16 copy of x written for FP4 experts (nullable)
   int32_t* status;             // range errors of that copy
@@ -479,6 +492,10 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 // cp.async (16 bytes, L2 only); src_bytes == 0 zero-fills the destination.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// cp.async of 4 bytes (through L1); src_bytes == 0 zero-fills the destination.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>

@@ -16,7 +16,11 @@
 // remaining magnitude in [128, 256).  Three pieces carry a bf16 x (8
 // significant bits) and four carry h (about 16 bits, as the bf16 path's hi+lo
 // pair); each piece is one more MMA column of the token, with its own scales,
-// and the epilogue adds a token's pieces.
+// and the epilogue adds a token's pieces.  The pieces are written once,
+// straight into the shared-memory image of the B tile of every (token block,
+// k-block) -- x's by the kernel's prologue, h's by the gate_up epilogue -- so
+// a stage's token operand is two bulk copies that complete on the stage's
+// barrier: no warp waits on the L2 round trip of scattered rows.
 //
 // Layout and schedule follow the stream-K bf16 kernel (gemm.cu): swap-AB
 // tiles of 256 weight rows (two M=128 MMAs into two TMEM accumulators) by up
@@ -30,9 +34,9 @@
 // gather warp; tcgen05.cp moves the stage's scale chunks to TMEM.
 //
 // Warp roles (224 threads): warp 0 issues the weight loads, warp 1 allocates
-// TMEM and issues tcgen05.cp and the MMAs, warp 2 gathers the token pieces,
-// warps 3..6 drain TMEM; at the start warps 2..6 of every CTA cut their share
-// of x into pieces.
+// TMEM and issues tcgen05.cp and the MMAs, warp 2 issues the token images'
+// bulk copies, warps 3..6 drain TMEM; at the start warps 2..6 of every CTA
+// cut their share of x into pieces and write them into the gate_up images.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -43,13 +47,14 @@ namespace {
 
 constexpr int kHalfBytes = kHalfRows * kMxK;  // one 128-row half of a k-block in shared memory: 16 KB
 constexpr uint32_t kSfCols = 16;              // TMEM columns per stage for its scale chunks
-constexpr uint32_t kSfBase = 256;             // first TMEM column of the scale area
 constexpr int kQuantWarps = 5;                // warps 2..6 cut x into pieces
+constexpr int kImgBlocks = 16;                // 32-input blocks of one token per prologue work item
 
 struct Seg {
   int expert, row_base, count, idim;
   int m, n, k0, len, kb, tile, n_cnt;
   int ready_idx;
+  int dense;  // token block over all groups: its image slots
   long long tile_iter0;
 };
 
@@ -57,7 +62,7 @@ struct Seg {
 // of one GEMM; a group entry outside the forward's bounds stops the walk.
 struct Sched {
   const GroupEntry* groups;
-  int ngroups, phase, H, n_max, g, rows, idim_max;
+  int ngroups, phase, H, n_max, g, rows, idim_max, mb0, n_dense;
   long long end, it;
   bool bad;
 
@@ -67,6 +72,8 @@ struct Sched {
     groups = p.groups; ngroups = ng; phase = ph; H = p.H; n_max = p.n_max; it = b; end = e; g = g0;
     rows = p.TK + p.T;
     idim_max = p.I_ld;
+    mb0 = p.mb0;
+    n_dense = p.n_dense;
     bad = false;
   }
 
@@ -104,6 +111,11 @@ struct Sched {
     s.tile_iter0 = start + static_cast<long long>(tile_in) * kb;
     s.n_cnt = min(n_max, ge.count - s.n * n_max);
     s.ready_idx = ge.gu_tile + s.n;
+    s.dense = ge.gu_tile / mb0 + s.n;
+    if (ge.gu_tile % mb0 != 0 || s.dense >= n_dense) {
+      bad = true;
+      return false;
+    }
     it += len;
     return true;
   }
@@ -132,12 +144,26 @@ struct Smem {
   uint64_t *full, *empty, *accf, *acce, *drain;
   volatile int* abort_flag;
   int* s_ok;
-  long long* rowoff;  // [128] gather: byte offset of each B row's piece, or -1
-  int* rowsf;         // [128] gather: byte offset of its scale word, or -1
   long long* span;
   float* col_w;
   int* col_tok;
 };
+
+// Image slot of (token block d, k-block kb): rows x 128 bytes, then the
+// 512-byte scale chunk.
+__device__ __forceinline__ uint8_t* img_slot(uint8_t* base, int rows, int kbs, int d, int kb) {
+  return base + (static_cast<size_t>(d) * kbs + kb) * (static_cast<size_t>(rows) * 128 + kMxSfBytes);
+}
+
+// Byte of input i (0..127) in row c of a K-major 128-byte-swizzled tile.
+__device__ __forceinline__ uint32_t swz(int c, int i) {
+  return static_cast<uint32_t>(c * 128 + ((((i >> 4) ^ (c & 7)) << 4) | (i & 15)));
+}
+
+// Byte of column c's scale of input chunk j in a 512-byte scale chunk.
+__device__ __forceinline__ uint32_t sf_byte(int c, int j) {
+  return static_cast<uint32_t>(16 * (c & 31) + 4 * (c >> 5) + j);
+}
 
 // offsets within a stage
 __device__ __forceinline__ uint8_t* st_a(const Smem& sm, int s) { return sm.base + s * sm.stage_bytes; }
@@ -205,30 +231,70 @@ __device__ __forceinline__ uint8_t cut_piece(float& r, int& e_out) {
   return static_cast<uint8_t>(c);
 }
 
-// Warps 2..6 of every CTA: the CTA's share of x's 32-input blocks, cut into
-// kMxPx pieces; then one arrival per warp on the grid-wide counter.
-__device__ void quantize_x(const MxParams& p, int qw) {
+// Warps 2..6 of every CTA: the CTA's share of (token, 16 blocks of 32
+// inputs) items.  Each block of x is cut into kMxPx pieces once and written
+// into the gate_up image of every token block that holds the token (its K
+// routed experts' and the shared expert's), as row j*kMxPx + p with its
+// scale; then one arrival per warp on the grid-wide counter.
+__device__ void build_gu_images(const MxParams& p, int qw, int ngroups) {
   const int lane = threadIdx.x & 31;
   const int hb = p.H / 32;
-  const long long nblk = static_cast<long long>(p.T) * hb;
-  const long long b0 = nblk * blockIdx.x / gridDim.x, b1 = nblk * (blockIdx.x + 1) / gridDim.x;
-  for (long long b = b0 + qw; b < b1; b += kQuantWarps) {
-    const int t = static_cast<int>(b / hb), j = static_cast<int>(b % hb);
-    float r = __bfloat162float(__ushort_as_bfloat16(__ldg(p.x + static_cast<size_t>(t) * p.H + j * 32 + lane)));
+  const int per_tok = ceil_div(hb, kImgBlocks);
+  const long long items = static_cast<long long>(p.T) * per_tok;
+  const long long w0 = static_cast<long long>(blockIdx.x) * kQuantWarps + qw;
+  const long long nw = static_cast<long long>(gridDim.x) * kQuantWarps;
+  const int nd = p.K + (p.Is > 0 ? 1 : 0);  // destinations of a token (<= 33)
+  for (long long it = w0; it < items; it += nw) {
+    const int t = static_cast<int>(it / per_tok), jb0 = static_cast<int>(it % per_tok) * kImgBlocks;
+    // destination q of this token (q < K: its slot-q expert; q == K: the
+    // shared expert): token block d, row group j; lane q holds q, lane 0
+    // also q = 32
+    int dq[2] = {-1, -1}, jq[2] = {0, 0};
 #pragma unroll
-    for (int q = 0; q < kMxPx; ++q) {
-      int e;
-      const uint8_t c = cut_piece(r, e);
-      const size_t row = static_cast<size_t>(t) * kMxPx + q;
-      p.xq[row * p.H + j * 32 + lane] = c;
-      if (lane == 0) p.xs[row * hb + j] = static_cast<uint8_t>(127 + e);
+    for (int h = 0; h < 2; ++h) {
+      const int q = lane + 32 * h;
+      if (q < nd) {
+        int d = -1, j = 0;
+        if (q < p.K) {
+          const int pr = t * p.K + q;
+          const int e = __ldg(p.idx + pr);
+          if (static_cast<unsigned>(e) < static_cast<unsigned>(p.E)) {
+            const int pos = __ldg(p.pair_pos + pr) - __ldg(p.offsets + e);
+            d = __ldg(p.e2d + e) + pos / p.n_max;
+            j = pos % p.n_max;
+          }
+        } else {
+          const GroupEntry& sh = p.groups[ngroups - 1];
+          d = sh.gu_tile / p.mb0 + t / p.n_max;
+          j = t % p.n_max;
+        }
+        if (d >= 0 && d < p.n_dense && j >= 0) { dq[h] = d; jq[h] = j; }
+      }
+    }
+    for (int jb = jb0; jb < min(hb, jb0 + kImgBlocks); ++jb) {
+      float r = __bfloat162float(__ushort_as_bfloat16(__ldg(p.x + static_cast<size_t>(t) * p.H + jb * 32 + lane)));
+      const int kb = jb >> 2, ch = jb & 3, i = ch * 32 + lane;
+#pragma unroll
+      for (int pc = 0; pc < kMxPx; ++pc) {
+        int e;
+        const uint8_t c = cut_piece(r, e);
+        for (int q = 0; q < nd; ++q) {
+          const int d = __shfl_sync(0xffffffffu, q < 32 ? dq[0] : dq[1], q & 31);
+          const int j = __shfl_sync(0xffffffffu, q < 32 ? jq[0] : jq[1], q & 31);
+          if (d < 0) continue;  // warp-uniform
+          uint8_t* sl = img_slot(p.img_gu, p.img_gu_rows, p.kb_gu, d, kb);
+          const int row = j * kMxPx + pc;
+          sl[swz(row, i)] = c;
+          if (lane == 0) sl[p.img_gu_rows * 128 + sf_byte(row, ch)] = static_cast<uint8_t>(127 + e);
+        }
+      }
     }
   }
+  // the images are read by bulk copies (the async proxy)
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __threadfence();
   __syncwarp();
-  if (lane == 0) {
-    __threadfence();
-    atomicAdd(p.xq_ready, 1);
-  }
+  if (lane == 0) atomicAdd(p.img_ready, 1);
 }
 
 // ---------------------------------------------------------------- TMA producer (weights)
@@ -311,7 +377,7 @@ __device__ bool produce(const Smem& sm, const MxParams& p, int ngroups, const lo
 // ---------------------------------------------------------------- MMA issuer (one thread)
 template <int PHASE, bool kFp4>
 __device__ bool issue_mma(const Smem& sm, const MxParams& p, int ngroups, long long begin, long long end, int g0,
-                          uint32_t tmem_base, int nbuf, int n_eff_cols, Ring& ring, int& seg_i) {
+                          uint32_t tmem_base, int nbuf, int n_eff_cols, uint32_t sf_base, Ring& ring, int& seg_i) {
   Sched sc;
   sc.init(p, ngroups, PHASE, begin, end, g0);
   Seg sg;
@@ -333,7 +399,7 @@ __device__ bool issue_mma(const Smem& sm, const MxParams& p, int ngroups, long l
         return false;
       }
       tc_fence_after();
-      const uint32_t sf = tmem_base + kSfBase + static_cast<uint32_t>(ring.stage) * kSfCols;
+      const uint32_t sf = tmem_base + sf_base + static_cast<uint32_t>(ring.stage) * kSfCols;
       const uint32_t sfa = smem_u32(st_sfa(sm, ring.stage));
       sf_copy(sf, sfa);                        // weight half 0
       sf_copy(sf + 4, sfa + kMxSfBytes);       // weight half 1
@@ -361,125 +427,66 @@ __device__ bool issue_mma(const Smem& sm, const MxParams& p, int ngroups, long l
   return true;
 }
 
-// ---------------------------------------------------------------- token-piece gather (B), one warp
+// ---------------------------------------------------------------- token images (B), lane 0 of warp 2
+// Every k-block's B tile and its scale chunk are two bulk copies of the
+// (token block, k-block) image, counted on the stage's barrier.
 template <int PHASE>
 __device__ bool gather(const Smem& sm, const MxParams& p, int ngroups, long long begin, long long end, int g0,
-                       Ring& ring, int& pending, int& arr_stage, int lag) {
-  const int lane = threadIdx.x & 31;
-  constexpr int P = PHASE == 0 ? kMxPx : kMxPh;
+                       Ring& ring) {
   if (PHASE == 0) {
-    // every CTA's share of x's pieces is written before the first gather
-    int ok = 1;
-    if (lane == 0) {
-      const int target = kQuantWarps * static_cast<int>(gridDim.x);
-      const long long t0 = clock64();
-      while (ld_acquire_gpu(p.xq_ready) < target) {
-        if (*sm.abort_flag || clock64() - t0 > kWaitLimitCycles) { ok = 0; break; }
-        __nanosleep(64);
+    // every CTA's share of the gate_up images is written before the first copy
+    const int target = kQuantWarps * static_cast<int>(gridDim.x);
+    const long long t0 = clock64();
+    while (ld_acquire_gpu(p.img_ready) < target) {
+      if (*sm.abort_flag || clock64() - t0 > kWaitLimitCycles) {
+        record_failure(p.status, sm.abort_flag, kInfoReady);
+        return false;
       }
+      __nanosleep(64);
     }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok) {
-      if (lane == 0) record_failure(p.status, sm.abort_flag, kInfoReady);
-      return false;
-    }
-    (void)ld_acquire_gpu(p.xq_ready);  // every lane acquires before its reads of the pieces
+    asm volatile("fence.proxy.async.global;" ::: "memory");
   }
   Sched sc;
   sc.init(p, ngroups, PHASE, begin, end, g0);
-  const uint8_t* src = PHASE == 0 ? p.xq : p.hq;
-  const uint8_t* ssrc = PHASE == 0 ? p.xs : p.hs;
+  uint8_t* const base = PHASE == 0 ? p.img_gu : p.img_dn;
+  const int rows = PHASE == 0 ? p.img_gu_rows : p.img_dn_rows;
+  const int kbs = PHASE == 0 ? p.kb_gu : p.kb_dn;
   Seg sg;
   while (sc.next(sg)) {
     const int N = mx_cols(PHASE, sg.n_cnt);
-    const int kdim = PHASE == 0 ? p.H : p.I_ld;  // row length of a piece
-    __syncwarp();
-    for (int c = lane; c < N; c += 32) {
-      long long off = -1;
-      int soff = -1;
-      const int j = c / P, q = c - (c / P) * P;
-      if (j < sg.n_cnt) {
-        const int r = sg.n * p.n_max + j;
-        long long row;
-        if (PHASE == 0) row = sg.expert >= 0 ? __ldg(p.sorted_pair + sg.row_base + r) / p.K : r;
-        else            row = sg.row_base + r;
-        const long long prow = row * P + q;
-        off = prow * kdim;
-        soff = static_cast<int>(prow * (kdim / 32));
-      }
-      sm.rowoff[c] = off;
-      sm.rowsf[c] = soff;
-    }
     if (PHASE == 1) {
-      // h of this (expert, token block) is complete once every gate_up tile
-      // of it has signalled
+      // the down images of this token block are complete once every gate_up
+      // tile of it has signalled
       const int target = ceil_div(sg.idim, kHalfRows);
       const int32_t* rp = p.ready + sg.ready_idx;
-      int ready = lane == 0 ? (ld_acquire_gpu(rp) >= target) : 0;
-      ready = __shfl_sync(0xffffffffu, ready, 0);
-      if (!ready) {
-        // release every stage this warp holds first: the missing tiles may
-        // be this CTA's own last gate_up tiles, whose MMAs wait on them
-        cp_async_wait<0>();
-        fence_proxy_async();
-        while (pending > 0) {
-          mbar_arrive(&sm.full[arr_stage]);
-          if (++arr_stage == sm.S) arr_stage = 0;
-          --pending;
-        }
-        int okr = 1;
-        if (lane == 0) {
-          const long long t0 = clock64();
-          while (ld_acquire_gpu(rp) < target) {
-            if (*sm.abort_flag || clock64() - t0 > kWaitLimitCycles) { okr = 0; break; }
-            __nanosleep(64);
+      if (ld_acquire_gpu(rp) < target) {
+        const long long t0 = clock64();
+        while (ld_acquire_gpu(rp) < target) {
+          if (*sm.abort_flag || clock64() - t0 > kWaitLimitCycles) {
+            record_failure(p.status, sm.abort_flag, kInfoReady);
+            return false;
           }
-        }
-        okr = __shfl_sync(0xffffffffu, okr, 0);
-        if (!okr) {
-          if (lane == 0) record_failure(p.status, sm.abort_flag, kInfoReady);
-          return false;
+          __nanosleep(64);
         }
       }
-      (void)ld_acquire_gpu(rp);
+      // written by other CTAs' generic stores, read by bulk copies below
+      asm volatile("fence.proxy.async.global;" ::: "memory");
     }
-    __syncwarp();
     for (int kk = 0; kk < sg.len; ++kk) {
-      const int kb = sg.k0 + kk;
-      const bool got = mbar_wait(&sm.empty[ring.stage], ring.phase ^ 1u, sm.abort_flag);
-      if (!__all_sync(0xffffffffu, got)) {
-        if (lane == 0) record_failure(p.status, sm.abort_flag, kInfoGatherEmpty);
+      if (!mbar_wait(&sm.empty[ring.stage], ring.phase ^ 1u, sm.abort_flag)) {
+        record_failure(p.status, sm.abort_flag, kInfoGatherEmpty);
         return false;
       }
-      const uint32_t bbase = smem_u32(st_b(sm, ring.stage));
-      for (int q = lane; q < N * 8; q += 32) {
-        const int c = q >> 3, ch = q & 7;
-        const long long off = sm.rowoff[c];
-        const uint8_t* s = off >= 0 ? src + off + kb * kMxK + ch * 16 : src;
-        cp_async_16(bbase + c * 128 + ((ch ^ (c & 7)) << 4), s, off >= 0 ? 16u : 0u);
-      }
-      // the pieces' scales of the k-block's four 32-input chunks: line c % 32,
-      // word c / 32 of the chunk
-      uint32_t* sfb = reinterpret_cast<uint32_t*>(st_sfb(sm, ring.stage));
-      for (int c = lane; c < N; c += 32) {
-        const int so = sm.rowsf[c];
-        const uint32_t v = so >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(ssrc + so + kb * 4)) : 0x7F7F7F7Fu;
-        sfb[(c & 31) * 4 + (c >> 5)] = v;
-      }
-      cp_async_commit();
-      ++pending;
-      if (pending > lag) {
-        if (lag >= 2) cp_async_wait<2>(); else cp_async_wait<1>();
-        fence_proxy_async();
-        mbar_arrive(&sm.full[arr_stage]);
-        if (++arr_stage == sm.S) arr_stage = 0;
-        --pending;
-      }
+      const uint8_t* sl = img_slot(base, rows, kbs, sg.dense, sg.k0 + kk);
+      uint64_t* bar = &sm.full[ring.stage];
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(N) * 128u + kMxSfBytes);
+      bulk_load(st_b(sm, ring.stage), sl, static_cast<uint32_t>(N) * 128u, bar);
+      bulk_load(st_sfb(sm, ring.stage), sl + static_cast<size_t>(rows) * 128, kMxSfBytes, bar);
       ring.next(sm.S);
     }
   }
   if (sc.bad) {
-    if (lane == 0) record_failure(p.status, sm.abort_flag, kInfoWorkList);
+    record_failure(p.status, sm.abort_flag, kInfoWorkList);
     return false;
   }
   return true;
@@ -505,14 +512,16 @@ __device__ __forceinline__ void load_tokens4(uint32_t tacc, int j0, int n_cnt, f
   }
 }
 
-// gate_up: SwiGLU (with the clamp) into h's pieces; every lane of a warp
-// holds one of 32 consecutive rows of the intermediate dimension, i.e. one
-// 32-input block of h for each token.
+// gate_up: SwiGLU (with the clamp) into h's pieces, written into the down
+// image of k-block m (the tile's 128 rows of the intermediate dimension are
+// the down GEMM's k-block m); every lane of a warp holds one of 32
+// consecutive rows, i.e. one 32-input chunk (the warp's quarter) of h for
+// each token.
 __device__ __forceinline__ void finish_gu(const MxParams& p, const Seg& sg, int r, int j0, const float (&a)[4],
                                           const float (&b)[4]) {
   const int lane = threadIdx.x & 31;
-  const int row = sg.m * kHalfRows + r;  // < idim: I and Is are multiples of 128
   const float lim = p.swiglu_limit;
+  uint8_t* sl = img_slot(p.img_dn, p.img_dn_rows, p.kb_dn, sg.dense, sg.m);
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
     const int j = j0 + t;
@@ -523,13 +532,13 @@ __device__ __forceinline__ void finish_gu(const MxParams& p, const Seg& sg, int 
       u = fminf(fmaxf(u, -lim), lim);
     }
     float rem = g / (1.f + expf(-g)) * u;
-    const size_t hrow = static_cast<size_t>(sg.row_base + sg.n * p.n_max + j) * kMxPh;
 #pragma unroll
     for (int q = 0; q < kMxPh; ++q) {
       int e;
       const uint8_t c = cut_piece(rem, e);
-      p.hq[(hrow + q) * p.I_ld + row] = c;
-      if (lane == 0) p.hs[(hrow + q) * (p.I_ld / 32) + row / 32] = static_cast<uint8_t>(127 + e);
+      const int row = j * kMxPh + q;
+      sl[swz(row, r)] = c;
+      if (lane == 0) sl[p.img_dn_rows * 128 + sf_byte(row, r >> 5)] = static_cast<uint8_t>(127 + e);
     }
   }
 }
@@ -675,6 +684,9 @@ __device__ bool epilogue(const Smem& sm, const MxParams& p, int ngroups, long lo
       done = true;
     }
     if (PHASE == 0 && done) {
+      // this tile's k-block of the down images is written: count it towards
+      // its token block, whose images the down GEMM reads by bulk copies
+      asm volatile("fence.proxy.async.global;" ::: "memory");
       __threadfence();
       epi_sync();
       if (leader) atomicAdd(p.ready + sg.ready_idx, 1);
@@ -706,8 +718,6 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm.drain + 1);
   sm.abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   sm.s_ok = reinterpret_cast<int*>(tmem_slot + 3);
-  sm.rowoff = reinterpret_cast<long long*>(ctrl + kCtrlRowOff);
-  sm.rowsf = reinterpret_cast<int*>(ctrl + kCtrlRowOff + 128 * 8);
   sm.span = reinterpret_cast<long long*>(ctrl + kCtrlSpans);
   sm.col_w = reinterpret_cast<float*>(ctrl + kCtrlCols);
   sm.col_tok = reinterpret_cast<int*>(ctrl + kCtrlCols + 4 * 256);
@@ -715,7 +725,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
-      mbar_init(&sm.full[s], 1 + 32);
+      mbar_init(&sm.full[s], 2);  // the weight loads and the token image copies
       mbar_init(&sm.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -751,7 +761,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const int gs[2] = {p.span_groups[blockIdx.x], p.span_groups[G1 + blockIdx.x]};
   const bool list_ok = hd.ngroups >= 0 && hd.ngroups <= p.g_max && hd.gu_tiles >= 0 &&
                        hd.gu_tiles <= p.max_gu_tiles && hd.dn_tiles >= 0 && hd.dn_tiles <= p.max_dn_tiles &&
-                       hd.n_eff >= 16 && hd.n_eff <= p.n_max && (hd.n_eff & 15) == 0 && hd.gu_iters >= 0 &&
+                       hd.n_eff >= 8 && hd.n_eff <= p.n_max && (hd.n_eff & 7) == 0 && hd.gu_iters >= 0 &&
                        hd.gu_iters <= p.max_gu_iters && hd.dn_iters >= 0 && hd.dn_iters <= p.max_dn_iters &&
                        bs[0] >= 0 && bs[0] <= es[0] && es[0] <= hd.gu_iters && bs[1] >= 0 && bs[1] <= es[1] &&
                        es[1] <= hd.dn_iters && gs[0] >= 0 && gs[0] <= hd.ngroups && gs[1] >= 0 &&
@@ -759,12 +769,14 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   if (!list_ok && threadIdx.x == 0) record_failure(p.status, sm.abort_flag, kInfoWorkList);
   const int ng = hd.ngroups;
   // stages sized for the widest token tile of this forward: kMxPh pieces of
-  // n_eff tokens as B rows of 128 bytes
-  const int n_eff_cols = kMxPh * (list_ok ? hd.n_eff : 16);
+  // n_eff tokens as B rows of 128 bytes; TMEM holds two accumulator buffers
+  // (2 x 2 halves x <= 96 columns), then every stage's scale chunks
+  const int n_eff_cols = (kMxPh * (list_ok ? hd.n_eff : 16) + 15) & ~15;
   sm.b_bytes = static_cast<uint32_t>(n_eff_cols) * 128u;
   sm.stage_bytes = (2 * kHalfBytes + sm.b_bytes + 3 * kMxSfBytes + 1023u) & ~1023u;
   sm.S = min(kMaxStages, p.stage_space / static_cast<int>(sm.stage_bytes));
-  const int nbuf = n_eff_cols <= 64 ? 2 : 1;
+  const int nbuf = 2;
+  const uint32_t sf_base = static_cast<uint32_t>(nbuf * 2 * n_eff_cols);
 
   if (!list_ok) {
     // nothing issued: every thread goes straight to the teardown
@@ -780,27 +792,19 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     if (lane == 0) {
       Ring ring;
       int seg_i = 0;
-      if (issue_mma<0, kFp4>(sm, p, ng, bs[0], es[0], gs[0], tmem_base, nbuf, n_eff_cols, ring, seg_i))
-        issue_mma<1, kFp4>(sm, p, ng, bs[1], es[1], gs[1], tmem_base, nbuf, n_eff_cols, ring, seg_i);
+      if (issue_mma<0, kFp4>(sm, p, ng, bs[0], es[0], gs[0], tmem_base, nbuf, n_eff_cols, sf_base, ring, seg_i))
+        issue_mma<1, kFp4>(sm, p, ng, bs[1], es[1], gs[1], tmem_base, nbuf, n_eff_cols, sf_base, ring, seg_i);
       mma_commit(sm.drain);
       if (!mbar_wait(sm.drain, 0, nullptr)) record_failure(p.status, sm.abort_flag, kInfoDrain);
     }
   } else if (warp == 2) {
-    quantize_x(p, 0);
-    Ring ring;
-    int pending = 0, arr_stage = 0;
-    const int lag = kGatherLag < sm.S - 1 ? kGatherLag : sm.S - 1;
-    if (gather<0>(sm, p, ng, bs[0], es[0], gs[0], ring, pending, arr_stage, lag))
-      gather<1>(sm, p, ng, bs[1], es[1], gs[1], ring, pending, arr_stage, lag);
-    cp_async_wait<0>();
-    fence_proxy_async();
-    while (pending > 0) {
-      mbar_arrive(&sm.full[arr_stage]);
-      if (++arr_stage == sm.S) arr_stage = 0;
-      --pending;
+    build_gu_images(p, 0, ng);
+    if (lane == 0) {
+      Ring ring;
+      if (gather<0>(sm, p, ng, bs[0], es[0], gs[0], ring)) gather<1>(sm, p, ng, bs[1], es[1], gs[1], ring);
     }
   } else {
-    quantize_x(p, warp - 2);
+    build_gu_images(p, warp - 2, ng);
     int seg_i = 0;
     if (epilogue<0>(sm, p, ng, bs[0], es[0], gs[0], tmem_base, nbuf, n_eff_cols, seg_i, p.tile_counters_gu))
       epilogue<1>(sm, p, ng, bs[1], es[1], gs[1], tmem_base, nbuf, n_eff_cols, seg_i, p.tile_counters_dn);

@@ -73,7 +73,7 @@ __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* 
                               int32_t* sorted_pair, int32_t* pair_pos, GroupEntry* groups, GemmHeader* header,
                               int H, int I, int Is, int n_max, int* s_cnt, int* s_cur, long long* s_buf,
                               uint16_t* s_wc, int64_t* spans, int32_t* span_groups, int grid, int fmt,
-                              int sh_fmt, int kblk) {
+                              int sh_fmt, int kblk, int32_t* e2d) {
   __shared__ int s_warp[kPermWarps];
   int* s_idx = reinterpret_cast<int*>(s_buf);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -290,6 +290,7 @@ __device__ void permute_block(const int32_t* idx, int T, int K, int E, int32_t* 
       ge.gu_iter = run[1] * mb0 * kb0;
       ge.dn_iter = run[1] * mb1 * kb1;
       groups[gi] = ge;
+      if (e2d) e2d[e] = static_cast<int32_t>(run[1]);  // the expert's first token block, counted over all groups
       s_cost0[gi] = run[2];
       s_cost1[gi] = run[3];
       run[0] += 1;
@@ -593,7 +594,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
   __threadfence();
   permute_block(p.idx, p.T, p.K, p.E, p.counts, p.offsets, p.sorted_pair, p.pair_pos, p.groups, p.header, p.H,
                 p.I, p.Is, p.n_max, s_cnt, s_cur, s_buf, s_wc, p.spans, p.span_groups, p.grid,
-                p.fmt != 0 ? p.fmt : (p.fp4 ? kFmtFp4Conv : kFmtBf16), p.sh_fmt, p.kblk > 0 ? p.kblk : kBlockK);
+                p.fmt != 0 ? p.fmt : (p.fp4 ? kFmtFp4Conv : kFmtBf16), p.sh_fmt, p.kblk > 0 ? p.kblk : kBlockK, p.e2d);
 }
 
 // logits = x . gate^T (+ router_bias) for many tokens: a CTA computes a
@@ -688,7 +689,7 @@ __global__ void __launch_bounds__(kRouteThreads) permute_kernel(const int32_t* i
   __shared__ long long s_buf[kPermBuf];
   __shared__ uint16_t s_wc[kPermWarps * kMaxExperts];
   permute_block(idx, T, K, E, counts, offsets, sorted_pair, pair_pos, nullptr, nullptr, 0, 0, 0, 1, s_cnt, s_cur,
-                s_buf, s_wc, nullptr, nullptr, 0, kFmtBf16, kFmtBf16, kBlockK);
+                s_buf, s_wc, nullptr, nullptr, 0, kFmtBf16, kFmtBf16, kBlockK, nullptr);
 }
 
 }  // namespace
