@@ -271,8 +271,17 @@ __device__ void build_gu_images(const MxParams& p, int qw, int ngroups) {
         if (d >= 0 && d < p.n_dense && j >= 0) { dq[h] = d; jq[h] = j; }
       }
     }
-    for (int jb = jb0; jb < min(hb, jb0 + kImgBlocks); ++jb) {
-      float r = __bfloat162float(__ushort_as_bfloat16(__ldg(p.x + static_cast<size_t>(t) * p.H + jb * 32 + lane)));
+    // the item's inputs at once (one L2 round trip, not one per block);
+    // the blocks are then processed one at a time (a rolled loop keeps the
+    // code small for the warps that share the SM's instruction cache)
+    uint16_t xv[kImgBlocks];
+#pragma unroll
+    for (int b = 0; b < kImgBlocks; ++b)
+      xv[b] = jb0 + b < hb ? __ldg(p.x + static_cast<size_t>(t) * p.H + (jb0 + b) * 32 + lane) : 0;
+#pragma unroll 1
+    for (int b = 0; b < kImgBlocks && jb0 + b < hb; ++b) {
+      const int jb = jb0 + b;
+      float r = __bfloat162float(__ushort_as_bfloat16(xv[b]));
       const int kb = jb >> 2, ch = jb & 3, i = ch * 32 + lane;
 #pragma unroll
       for (int pc = 0; pc < kMxPx; ++pc) {
