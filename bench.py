@@ -638,6 +638,56 @@ def measure_extra(cfg, dev, rank, K, W, hbm, tflops, peak_src, sustain_s):
         wl.close()
 
 
+def measure_route_ahead(cfg, dev, rank, pairs: int = 40):
+    """Route-ahead of the routing-independent bytes: two layers (different
+    weights) back to back, each forward prefetching the other layer's router
+    gate, biases and shared expert into L2 in its expert kernel's tail, against
+    the same pair without the prefetch; and both again with an L2-evicting
+    kernel between the layers (a 256 MB copy, standing in for the attention
+    step between two MoE layers of a model).  Graph replay, microseconds per
+    layer (the evicting copies included where they run)."""
+    from moe_ffn_speculative_gb300 import ops
+    wl = Workload(cfg, dev, rank, "auto")
+    try:
+        wl.first_forward()
+        l1, l2 = wl.layers[0], wl.layers[1]
+
+        def indep(d):
+            keys = ["gate", "router_bias", "expert_bias", "sh_gate", "sh_gate_up", "sh_down", "sh_gate_up_q",
+                    "sh_down_q"]
+            return [d[k] for k in keys if d.get(k) is not None]
+        src = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+        dst = torch.empty_like(src)
+        out = {"prefetch_bytes": int(sum(t.numel() * t.element_size() for t in indep(l2)))}
+        for evict in (False, True):
+            for ahead in (False, True):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=wl.stream):
+                    for _ in range(4):
+                        for a, b in ((l1, l2), (l2, l1)):
+                            if ahead:
+                                ops.set_l2_prefetch(indep(b))
+                            wl.call(a, wl.x, wl.y)
+                            if evict:
+                                dst.copy_(src)
+                ops.set_l2_prefetch(None)
+                torch.cuda.synchronize()
+                for _ in range(3):
+                    g.replay()
+                ms = wl.replay_ms(g, pairs // 4) / (pairs * 2)
+                del g
+                out[("evict_" if evict else "") + ("ahead" if ahead else "plain")] = ms * 1e3
+        wl.check_status("after the route-ahead pairs")
+        out["gain_us"] = out["plain"] - out["ahead"]
+        out["gain_us_with_evict"] = out["evict_plain"] - out["evict_ahead"]
+        out["workload"] = cfg.name
+        out["T"] = cfg.T
+        out["unit"] = "us per layer"
+        return out
+    finally:
+        wl.close()
+
+
 def run_gpu(args, cfg, rank, world):
     from moe_ffn_speculative_gb300 import ops
     from moe_ffn_speculative_gb300.build import build
@@ -707,6 +757,11 @@ def run_gpu(args, cfg, rank, world):
             if c == cfg:
                 continue
             extra.append(measure_extra(c, dev, rank, K, W, hbm, tflops, peak_src, args.sustain_extra))
+    route_ahead = None
+    if args.workloads != "none" and args.tokens is None and args.experts is None and args.weights == "bf16" \
+            and args.schedule == "auto":
+        log("route-ahead pairs")
+        route_ahead = measure_route_ahead(S.CONFIGS["dsv4_style"].with_(T=72), dev, rank)
     clk = clocks.stop()
 
     if rank != 0:
@@ -737,6 +792,8 @@ def run_gpu(args, cfg, rank, world):
     }
     if extra:
         line["workloads"] = extra
+    if route_ahead:
+        line["route_ahead"] = route_ahead
     if not args.no_cpu_baseline:
         log("CPU oracle")
         line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)

@@ -379,6 +379,23 @@ MOE_API moe_status moe_ffn_forward_mx(const moe_bf16* x, int T, int H, int I, co
 #define MOE_INFO_HOLD 15
 MOE_API moe_status moe_get_device_status(void* ws, cudaStream_t stream, int32_t* info_out);
 
+/* Route-ahead of the routing-independent part of the next layer (MoE-Infinity
+ * PR #143 "converge DFlash spec-decode stack", route-ahead commit note:
+ * bring what the next step needs close before it runs).  Which experts the
+ * next layer touches depends on its input, but its router gate (and biases)
+ * and its shared expert do not.  The next moe_ffn_forward(),
+ * moe_ffn_forward_fp4() or moe_ffn_forward_mx() on the calling thread on the
+ * stream-K schedule takes these n <= 8 byte ranges (16-byte aligned; sizes
+ * rounded down to 16): once every CTA of its expert kernel has issued its own
+ * weight loads, it prefetches its share of them into L2, so the prefetch
+ * rides the layer's tail.  The setting is consumed by that call (also when
+ * the call runs the fused schedule, which ignores it); n = 0 clears it.
+ * Whether the bytes are still in L2 when the next layer runs depends on what
+ * runs in between (an attention step that streams more than L2 evicts them).
+ * Returns MOE_ERR_INVALID_ARG for n outside [0, 8] or a NULL / unaligned
+ * pointer. */
+MOE_API moe_status moe_set_l2_prefetch(const void* const* ptrs, const size_t* bytes, int n);
+
 /* Profiling hook: when `events` is not NULL, moe_ffn_forward() records
  * events[2*i] / events[2*i+1] (cudaEvent_t) around its i-th kernel launch,
  * for i < n_pairs, on its stream.  Per calling thread; NULL turns it off.

@@ -23,6 +23,7 @@ std::atomic<int> g_sms[kMaxDevices];  // SM count per device, filled on first us
 thread_local void* const* t_events = nullptr;
 thread_local int t_nev = 0;
 thread_local int t_schedule = MOE_SCHEDULE_AUTO;
+thread_local L2Prefetch t_prefetch = {};  // consumed by the next forward on this thread
 
 int device_sms() {
   int d = 0;
@@ -518,6 +519,9 @@ moe_status ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf16* g
                        const moe_bf16* sh_gate_up, const moe_bf16* sh_down, int Is, const moe_bf16* sh_gate,
                        const moe_recipe* recipe, void* ws, size_t ws_bytes, moe_bf16* y, int32_t* topk_idx_out,
                        float* topk_w_out, int32_t* counts_out, cudaStream_t stream, const Fp4Experts* fp4) {
+  // the next-layer prefetch setting is consumed by this call, whatever it runs
+  const L2Prefetch pf = t_prefetch;
+  t_prefetch.n = 0;
   moe_status st = check_recipe(recipe);
   if (st != MOE_OK) return st;
   if (T < 0 || H < 8 || I < 8 || Is < 0) return MOE_ERR_INVALID_ARG;
@@ -691,6 +695,7 @@ moe_status ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf16* g
     gp.gu_scale = fp4->scales;
     gp.dn_scale = fp4->scales;  // one buffer: the down blocks follow the gate_up blocks
   }
+  gp.pf = pf;
   // the down GEMM's token rows by TMA when every k-block is whole
   CUtensorMap tm_h = tm_dn;
   if (I % kBlockK == 0 && Is % kBlockK == 0) {
@@ -731,6 +736,8 @@ moe_status ffn_forward_mx(const moe_bf16* x, int T, int H, int I, const moe_bf16
                           const moe_bf16* sh_gate, const void* scales, size_t scales_bytes,
                           const moe_recipe* recipe, void* ws, size_t ws_bytes, moe_bf16* y, int32_t* topk_idx_out,
                           float* topk_w_out, int32_t* counts_out, cudaStream_t stream) {
+  const L2Prefetch pf = t_prefetch;
+  t_prefetch.n = 0;
   moe_status st = check_recipe(recipe);
   if (st != MOE_OK) return st;
   if (routed_fmt != MOE_FMT_FP4 && routed_fmt != MOE_FMT_FP8) return MOE_ERR_INVALID_ARG;
@@ -863,6 +870,7 @@ moe_status ffn_forward_mx(const moe_bf16* x, int T, int H, int I, const moe_bf16
   mp.max_dn_tiles = L.max_dn_tiles;
   mp.max_gu_iters = static_cast<long long>(L.max_gu_tiles) * ceil_div(H, kMxK);
   mp.max_dn_iters = static_cast<long long>(L.max_dn_tiles) * ceil_div(mp.I_ld, kMxK);
+  mp.pf = pf;
   record_event_on(2, stream);
   e = launch_mx(tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, mp, L.grid, kSmemLimit, stream);
   record_event_on(3, stream);
@@ -982,6 +990,20 @@ int moe_ffn_schedule(int T, int H, int I, int Is, const moe_recipe* recipe, int 
   const int E = recipe->num_experts, K = recipe->top_k;
   const Layout L = make_layout(T, H, I, Is, E, K, gated != 0 && Is > 0, sms);
   return use_slice(L, T, E, K) ? MOE_SCHEDULE_SLICE : MOE_SCHEDULE_STREAM_K;
+}
+
+moe_status moe_set_l2_prefetch(const void* const* ptrs, const size_t* bytes, int n) {
+  if (n < 0 || n > kMaxPrefetch || (n > 0 && (!ptrs || !bytes))) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i)
+    if (!ptrs[i] || !aligned16(ptrs[i])) return MOE_ERR_INVALID_ARG;
+  L2Prefetch pf = {};
+  for (int i = 0; i < n; ++i) {
+    pf.ptr[i] = static_cast<const uint8_t*>(ptrs[i]);
+    pf.bytes[i] = static_cast<long long>(bytes[i] & ~static_cast<size_t>(15));
+  }
+  pf.n = n;
+  t_prefetch = pf;
+  return MOE_OK;
 }
 
 void moe_set_profile_events(void* const* events, int n_pairs) {

@@ -120,6 +120,16 @@ __host__ __device__ inline void group_geometry(int phase, int count, int idim, i
   else            { mb = ceil_div(H, 2 * kHalfRows); kb = ceil_div(idim, kblk); }
 }
 
+// Byte ranges (16-byte aligned; sizes rounded down to 16) that an expert
+// kernel prefetches into L2 once every CTA has issued its own weight loads:
+// CTA c takes the c-th of `grid` equal shares of their concatenation.
+constexpr int kMaxPrefetch = 8;
+struct L2Prefetch {
+  const uint8_t* ptr[kMaxPrefetch];
+  long long bytes[kMaxPrefetch];
+  int n;
+};
+
 struct GemmParams {
   const GroupEntry* groups;
   const GemmHeader* header;
@@ -154,6 +164,7 @@ struct GemmParams {
   // host-computed bounds of the router's work list, checked before use
   int g_max, max_gu_tiles, max_dn_tiles;
   long long max_gu_iters, max_dn_iters;
+  L2Prefetch pf;               // byte ranges to prefetch into L2 in the launch's tail
 };
 
 // Block-scaled expert GEMMs (mx.cu): routed experts as FP4 (e2m1 codes with
@@ -212,6 +223,7 @@ struct MxParams {
   int routed_fp4;              // routed weights are FP4 (else FP8)
   int g_max, max_gu_tiles, max_dn_tiles;
   long long max_gu_iters, max_dn_iters;
+  L2Prefetch pf;
 };
 
 // Byte offsets of the prepared weight scales: for every (expert, 256-row
@@ -485,16 +497,25 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
-// L2 prefetch of a 3-D tiled box (no shared memory, no completion).
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
 // L2 prefetch of a contiguous range (16-byte aligned, a multiple of 16 bytes).
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+// This CTA's share of the ranges of `pf`, prefetched into L2 in 64 KB pieces.
+__device__ __forceinline__ void prefetch_share_l2(const L2Prefetch& pf) {
+  long long total = 0;
+  for (int i = 0; i < pf.n; ++i) total += pf.bytes[i];
+  if (total <= 0) return;
+  long long a = (total * blockIdx.x / gridDim.x) & ~15ll, b = (total * (blockIdx.x + 1) / gridDim.x) & ~15ll;
+  long long base = 0;
+  for (int i = 0; i < pf.n && a < b; ++i) {
+    const long long lo = a > base ? a : base, hi = b < base + pf.bytes[i] ? b : base + pf.bytes[i];
+    for (long long o = lo; o < hi; o += 65536) {
+      const long long n = hi - o < 65536 ? hi - o : 65536;
+      if (n >= 16) bulk_prefetch_l2(pf.ptr[i] + (o - base), static_cast<uint32_t>(n & ~15ll));
+    }
+    base += pf.bytes[i];
+  }
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -380,6 +380,9 @@ __device__ bool produce(const Smem& sm, const MxParams& p, int ngroups, const lo
     record_failure(p.status, sm.abort_flag, kInfoWorkList);
     return false;
   }
+  // every weight load of this CTA is issued: its share of the next layer's
+  // routing-independent bytes goes to L2 while the layer's tail runs
+  prefetch_share_l2(p.pf);
   return true;
 }
 

@@ -80,6 +80,7 @@ _SIGS = {
                              _P, _SZ, _P, _P, _P, _P, _P]),
     "moe_get_device_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "moe_set_profile_events": (None, [_P, _I]),
+    "moe_set_l2_prefetch": (_I, [_P, _P, _I]),
     "moe_set_schedule": (_I, [_I]),
     "moe_ffn_schedule": (_I, [_I, _I, _I, _I, ctypes.POINTER(Recipe), _I]),
     "moe_fp4_scales_bytes": (_SZ, [_I, _I, _I]),
@@ -389,6 +390,17 @@ def ffn_schedule(T: int, H: int, I: int, Is: int, recipe: Recipe, gated: bool = 
     return s
 
 
+def set_l2_prefetch(tensors) -> None:
+    """The next forward on this thread prefetches these tensors' bytes into
+    L2 in its expert kernel's tail (moe_set_l2_prefetch); None or [] clears."""
+    ts = [t for t in (tensors or []) if t is not None]
+    _need_cuda(*ts)
+    ptrs = (ctypes.c_void_p * max(1, len(ts)))(*[t.data_ptr() for t in ts])
+    sizes = (ctypes.c_size_t * max(1, len(ts)))(*[t.numel() * t.element_size() for t in ts])
+    _check(lib().moe_set_l2_prefetch(ctypes.cast(ptrs, ctypes.c_void_p), ctypes.cast(sizes, ctypes.c_void_p),
+                                     len(ts)), "moe_set_l2_prefetch")
+
+
 def set_profile_events(events) -> None:
     """events: a list of torch.cuda.Event (pairs around each launch) or None."""
     global _profile_keepalive
@@ -440,8 +452,19 @@ class MoELayer:
         self.ws = Workspace(ffn_workspace_bytes_upto(max_tokens, self.H, self.I, self.Is, recipe),
                             tensors["gate"].device)
 
-    def forward(self, x, y=None, topk_idx_out=None, topk_w_out=None, counts_out=None, stream=None):
+    def routing_independent(self):
+        """The tensors of this layer that do not depend on its routing: the
+        router gate and biases, the shared expert and its gate."""
+        t = self.t
+        keys = ["gate", "router_bias", "expert_bias", "sh_gate", "sh_gate_up", "sh_down", "sh_gate_up_q", "sh_down_q"]
+        return [t[k] for k in keys if t.get(k) is not None]
+
+    def forward(self, x, y=None, topk_idx_out=None, topk_w_out=None, counts_out=None, stream=None, ahead=None):
+        """ahead: the next MoELayer, whose routing-independent weights this
+        forward prefetches into L2 in its expert kernel's tail."""
         T = x.shape[0]
+        if ahead is not None:
+            set_l2_prefetch(ahead.routing_independent())
         if T > self.max_tokens:
             raise ValueError("more tokens than the workspace was sized for")
         t = self.t
