@@ -24,7 +24,7 @@
 //
 // Layout and schedule follow the stream-K bf16 kernel (gemm.cu): swap-AB
 // tiles of 256 weight rows (two M=128 MMAs into two TMEM accumulators) by up
-// to 32 tokens, the k-block iterations of all tiles of all touched experts
+// to 24 tokens, the k-block iterations of all tiles of all touched experts
 // cut into one contiguous span per SM, split tiles finished by the CTA that
 // holds their first k-block, both GEMMs in one persistent launch.  A k-block
 // is 128 inputs: the weight halves arrive by TMA in the MMA's K-major

@@ -416,23 +416,49 @@ def set_profile_events(events) -> None:
 _profile_keepalive = None
 
 
+def layer_path(tensors: dict, mx: Optional[bool] = None) -> str:
+    """Which entry point runs a layer with these weights: "bf16"
+    (moe_ffn_forward), "mx" (moe_ffn_forward_mx: FP4 or FP8 routed codes,
+    no shared expert or an FP8 one) or "fp4" (moe_ffn_forward_fp4: FP4
+    routed codes, no shared expert or a bf16 one).  mx=None picks the
+    block-scaled path wherever it takes the layer (H, I and the shared
+    expert's width multiples of 128, no bf16 shared expert); True / False
+    ask for it or for the converter path.  Raises ValueError for weights
+    that no path takes as asked."""
+    if tensors.get("w_down_q") is None:
+        if mx:
+            raise ValueError("the block-scaled path takes coded routed experts (w_gate_up_q, w_down_q)")
+        return "bf16"
+    bf16_shared = tensors.get("sh_gate_up") is not None
+    fp8_shared = tensors.get("sh_gate_up_q") is not None
+    if bf16_shared and fp8_shared:
+        raise ValueError("both a bf16 and an FP8 shared expert given")
+    fmt = mx_format(tensors)
+    if mx is None:
+        _, H, I, Is = mx_dims(tensors)
+        fits = H % 128 == 0 and I % 128 == 0 and Is % 128 == 0
+        mx = fmt == FMT_FP8 or fp8_shared or (fits and not bf16_shared)
+    if mx and bf16_shared:
+        raise ValueError("the block-scaled path takes an FP8 shared expert (sh_gate_up_q), not a bf16 one")
+    if not mx and (fmt == FMT_FP8 or fp8_shared):
+        raise ValueError("FP8 weights run only on the block-scaled path")
+    return "mx" if mx else "fp4"
+
+
 class MoELayer:
     """Weights of one layer plus its workspace; ``forward(x)`` runs the layer."""
 
     def __init__(self, tensors: dict, recipe: Recipe, max_tokens: int, mx: Optional[bool] = None):
         """Routed experts as bf16 (w_gate_up, w_down), or as codes
         (w_gate_up_q, w_down_q with scales w_gate_up_s, w_down_s, re-laid once
-        here): FP8 codes, or an FP8 shared expert (sh_gate_up_q, ...), take the
-        block-scaled path (moe_ffn_forward_mx); FP4 codes with a bf16 shared
-        expert take moe_ffn_forward_fp4 unless `mx` asks for the block-scaled
-        path."""
+        here).  The entry point is chosen by layer_path(tensors, mx): coded
+        weights take the block-scaled path (moe_ffn_forward_mx) wherever it
+        takes the layer, else FP4 codes take moe_ffn_forward_fp4."""
         self.t = tensors
         self.recipe = recipe
-        coded = tensors.get("w_down_q") is not None
-        if mx is None:
-            mx = coded and (tensors.get("sh_gate_up_q") is not None or mx_format(tensors) == FMT_FP8)
-        self.mx = bool(mx)
-        self.fp4 = coded and not self.mx
+        path = layer_path(tensors, mx)
+        self.mx = path == "mx"
+        self.fp4 = path == "fp4"
         if self.mx:
             self.fmt = mx_format(tensors)
             _, self.H, self.I, self.Is = mx_dims(tensors)

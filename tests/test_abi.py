@@ -143,3 +143,35 @@ def test_block_scaled_refusals_before_any_device_call(lib):
     assert fwd(ws_bytes=1024) == ops.MOE_ERR_WORKSPACE
     assert lib.moe_mx_prepare_scales(ops.FMT_FP4, 1 << 20, 2 << 20, 8, 4096, 2304, None, None, 0, 3 << 20, 16,
                                      None) == ops.MOE_ERR_WORKSPACE
+
+
+def test_layer_path_selection():
+    """Which entry point a layer's weights take, decided on the host from the
+    tensors' presence and shapes (CPU tensors: no library call is made)."""
+    from moe_ffn_speculative_gb300 import synthetic as S
+
+    def t(**kw):
+        return S.make_inputs(S.LayerConfig("sel", T=2, H=256, E=2, I=256, K=1, seed=3, **kw))
+
+    assert ops.layer_path(t()) == "bf16"
+    assert ops.layer_path(t(shared_I=128)) == "bf16"
+    # FP4 codes: block-scaled by default, the converter when asked
+    assert ops.layer_path(t(expert_format="fp4")) == "mx"
+    assert ops.layer_path(t(expert_format="fp4"), mx=False) == "fp4"
+    # a bf16 shared expert keeps FP4 on the converter; asking otherwise is refused
+    assert ops.layer_path(t(expert_format="fp4", shared_I=128)) == "fp4"
+    with pytest.raises(ValueError):
+        ops.layer_path(t(expert_format="fp4", shared_I=128), mx=True)
+    # an FP8 shared expert or FP8 routed experts: block-scaled only
+    assert ops.layer_path(t(expert_format="fp4", shared_I=128, shared_format="fp8")) == "mx"
+    assert ops.layer_path(t(expert_format="fp8")) == "mx"
+    with pytest.raises(ValueError):
+        ops.layer_path(t(expert_format="fp8"), mx=False)
+    with pytest.raises(ValueError):
+        ops.layer_path(t(expert_format="fp8", shared_I=128))
+    # widths the block-scaled path does not take (I = 192) stay on the converter
+    d = S.make_inputs(S.LayerConfig("sel", T=2, H=256, E=2, I=192, K=1, expert_format="fp4", seed=3))
+    assert ops.layer_path(d) == "fp4"
+    # bf16 experts cannot take the block-scaled path
+    with pytest.raises(ValueError):
+        ops.layer_path(t(), mx=True)

@@ -83,7 +83,7 @@ def _oracle(cfg, d, rows=None):
 
 
 def _run(cfg, d):
-    layer = ops.MoELayer(d, ops.Recipe.from_config(cfg), cfg.T)
+    layer = ops.MoELayer(d, ops.Recipe.from_config(cfg), cfg.T, mx=False)
     assert layer.fp4
     idx = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device="cuda")
     w = torch.empty((cfg.T, cfg.K), dtype=torch.float32, device="cuda")

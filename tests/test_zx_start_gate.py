@@ -18,13 +18,17 @@ pytestmark = pytest.mark.gpu
 CASES = {
     # the fused one-launch kernel (units wait at the gate after the
     # prologue's loads are issued; helpers and combine tasks see the status)
-    "slice": (S.LayerConfig("gate_slice", T=72, H=512, E=8, I=384, K=1, seed=51), ops.SCHEDULE_SLICE),
+    "slice": (S.LayerConfig("gate_slice", T=72, H=512, E=8, I=384, K=1, seed=51), ops.SCHEDULE_SLICE, None),
     # router launch, then the stream-K expert kernel (every CTA waits)
     "stream_k": (S.LayerConfig("gate_sk", T=64, H=320, E=16, I=160, K=4, shared_I=96, shared_gated=True,
-                               seed=52), ops.SCHEDULE_STREAM_K),
+                               seed=52), ops.SCHEDULE_STREAM_K, None),
     # the FP4 expert kernel (converter warps too)
     "fp4": (S.LayerConfig("gate_fp4", T=16, H=128, E=8, I=128, K=2, expert_format="fp4", seed=53),
-            ops.SCHEDULE_AUTO),
+            ops.SCHEDULE_AUTO, False),
+    # the block-scaled kernel (its prologue's image writers and the image
+    # gather too), FP4 routed experts and an FP8 shared expert
+    "mx": (S.LayerConfig("gate_mx", T=40, H=256, E=8, I=256, K=2, shared_I=128, expert_format="fp4",
+                         shared_format="fp8", seed=54), ops.SCHEDULE_AUTO, True),
 }
 
 
@@ -37,11 +41,12 @@ def _library():
 
 @pytest.mark.parametrize("name", list(CASES))
 def test_closed_start_gate_times_out_and_the_next_forward_is_correct(name):
-    cfg, sched = CASES[name]
+    cfg, sched, mx = CASES[name]
     d = {k: (None if v is None else v.cuda()) for k, v in S.make_inputs(cfg).items()}
     ops.set_schedule(sched)
     try:
-        layer = ops.MoELayer(d, ops.Recipe.from_config(cfg), cfg.T)
+        layer = ops.MoELayer(d, ops.Recipe.from_config(cfg), cfg.T, mx=mx)
+        assert layer.mx == bool(mx)
         used = ops.ffn_schedule(cfg.T, cfg.H, cfg.I, cfg.shared_I, layer.recipe, gated=cfg.shared_gated)
         if cfg.expert_format != "fp4":
             assert used == sched
