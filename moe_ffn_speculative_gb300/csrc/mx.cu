@@ -214,9 +214,9 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t
 // an all-zero block), the value's e4m3 code at that scale, and the remainder
 // for the next piece.
 __device__ __forceinline__ uint8_t cut_piece(float& r, int& e_out) {
-  float m = fabsf(r);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  // the block's largest magnitude in one warp reduction: the bits of a
+  // non-negative float order as the unsigned integers they spell
+  const float m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(r))));
   int e = 0;
   if (m > 0.f) {
     int k;
@@ -272,29 +272,45 @@ __device__ void build_gu_images(const MxParams& p, int qw, int ngroups) {
       }
     }
     // the item's inputs at once (one L2 round trip, not one per block);
-    // the blocks are then processed one at a time (a rolled loop keeps the
-    // code small for the warps that share the SM's instruction cache)
+    // then one k-block (four blocks) at a time: the four blocks' pieces are
+    // cut side by side, so their warp reductions overlap, and each
+    // destination is visited once per k-block (a rolled outer loop keeps
+    // the code small for the warps that share the SM's instruction cache)
     uint16_t xv[kImgBlocks];
 #pragma unroll
     for (int b = 0; b < kImgBlocks; ++b)
       xv[b] = jb0 + b < hb ? __ldg(p.x + static_cast<size_t>(t) * p.H + (jb0 + b) * 32 + lane) : 0;
 #pragma unroll 1
-    for (int b = 0; b < kImgBlocks && jb0 + b < hb; ++b) {
-      const int jb = jb0 + b;
-      float r = __bfloat162float(__ushort_as_bfloat16(xv[b]));
-      const int kb = jb >> 2, ch = jb & 3, i = ch * 32 + lane;
+    for (int b0 = 0; b0 < kImgBlocks && jb0 + b0 < hb; b0 += 4) {
+      const int kb = (jb0 + b0) >> 2;  // H is a multiple of 128: the k-block's four blocks are all here
+      float r[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) r[u] = __bfloat162float(__ushort_as_bfloat16(xv[b0 + u]));
+      uint8_t c[kMxPx][4];
+      uint32_t sfw[kMxPx];  // the four blocks' scale bytes of each piece, block u in byte u
 #pragma unroll
       for (int pc = 0; pc < kMxPx; ++pc) {
-        int e;
-        const uint8_t c = cut_piece(r, e);
-        for (int q = 0; q < nd; ++q) {
-          const int d = __shfl_sync(0xffffffffu, q < 32 ? dq[0] : dq[1], q & 31);
-          const int j = __shfl_sync(0xffffffffu, q < 32 ? jq[0] : jq[1], q & 31);
-          if (d < 0) continue;  // warp-uniform
-          uint8_t* sl = img_slot(p.img_gu, p.img_gu_rows, p.kb_gu, d, kb);
+        sfw[pc] = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          int e;
+          c[pc][u] = cut_piece(r[u], e);
+          sfw[pc] |= static_cast<uint32_t>(127 + e) << (8 * u);
+        }
+      }
+      for (int q = 0; q < nd; ++q) {
+        const int d = __shfl_sync(0xffffffffu, q < 32 ? dq[0] : dq[1], q & 31);
+        const int j = __shfl_sync(0xffffffffu, q < 32 ? jq[0] : jq[1], q & 31);
+        if (d < 0) continue;  // warp-uniform
+        uint8_t* sl = img_slot(p.img_gu, p.img_gu_rows, p.kb_gu, d, kb);
+#pragma unroll
+        for (int pc = 0; pc < kMxPx; ++pc) {
           const int row = j * kMxPx + pc;
-          sl[swz(row, i)] = c;
-          if (lane == 0) sl[p.img_gu_rows * 128 + sf_byte(row, ch)] = static_cast<uint8_t>(127 + e);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) sl[swz(row, u * 32 + lane)] = c[pc][u];
+          // the row's four scale bytes are adjacent: one aligned word
+          if (lane == 0)
+            *reinterpret_cast<uint32_t*>(sl + p.img_gu_rows * 128 + sf_byte(row, 0)) = sfw[pc];
         }
       }
     }
@@ -534,23 +550,30 @@ __device__ __forceinline__ void finish_gu(const MxParams& p, const Seg& sg, int 
   const int lane = threadIdx.x & 31;
   const float lim = p.swiglu_limit;
   uint8_t* sl = img_slot(p.img_dn, p.img_dn_rows, p.kb_dn, sg.dense, sg.m);
+  // the four tokens' h values, cut into pieces side by side so that their
+  // warp reductions overlap (columns past the tile's tokens cut zeros and
+  // store nothing; the count is uniform over the warp)
+  float rem[4];
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
-    const int j = j0 + t;
-    if (j >= sg.n_cnt) break;  // uniform over the warp
     float g = a[t], u = b[t];
     if (lim > 0.f) {
       g = fminf(g, lim);
       u = fminf(fmaxf(u, -lim), lim);
     }
-    float rem = g / (1.f + expf(-g)) * u;
+    rem[t] = j0 + t < sg.n_cnt ? g / (1.f + expf(-g)) * u : 0.f;
+  }
 #pragma unroll
-    for (int q = 0; q < kMxPh; ++q) {
+  for (int q = 0; q < kMxPh; ++q) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
       int e;
-      const uint8_t c = cut_piece(rem, e);
-      const int row = j * kMxPh + q;
-      sl[swz(row, r)] = c;
-      if (lane == 0) sl[p.img_dn_rows * 128 + sf_byte(row, r >> 5)] = static_cast<uint8_t>(127 + e);
+      const uint8_t c = cut_piece(rem[t], e);
+      if (j0 + t < sg.n_cnt) {
+        const int row = (j0 + t) * kMxPh + q;
+        sl[swz(row, r)] = c;
+        if (lane == 0) sl[p.img_dn_rows * 128 + sf_byte(row, r >> 5)] = static_cast<uint8_t>(127 + e);
+      }
     }
   }
 }
