@@ -536,6 +536,40 @@ class Workload:
         del g
         return {n: float(np.mean(v)) for n, v in acc.items()}
 
+    def event_overhead(self, G, replays):
+        """What event nodes add to a launch they bracket in graph replay: the
+        mean event-pair time around an empty launch (torch's spin kernel with
+        no cycles) minus that launch's own period back to back without
+        events.  A kernel's event-timed duration minus this is its duration
+        as it runs inside a graph of consecutive launches."""
+        try:  # event record nodes that keep their timestamps under capture
+            evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)] for _ in range(G)]
+        except TypeError:
+            return {"event_pair_us": None, "empty_launch_period_us": None, "overhead_us": 0.0}
+        with torch.cuda.stream(self.stream):
+            for row in evs:
+                for e in row:
+                    e.record(self.stream)
+            torch.cuda.synchronize()
+            g_ev, g_plain = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_ev, stream=self.stream):
+                for row in evs:
+                    row[0].record(self.stream)
+                    torch.cuda._sleep(0)
+                    row[1].record(self.stream)
+            with torch.cuda.graph(g_plain, stream=self.stream):
+                for _ in range(G):
+                    torch.cuda._sleep(0)
+        pairs = []
+        for _ in range(replays):
+            g_ev.replay()
+            torch.cuda.synchronize()
+            pairs += [row[0].elapsed_time(row[1]) * 1e3 for row in evs]
+        period = self.replay_ms(g_plain, replays) * 1e3 / (replays * G)
+        del g_ev, g_plain
+        pair = float(np.median(pairs))
+        return {"event_pair_us": pair, "empty_launch_period_us": period, "overhead_us": pair - period}
+
     def e2e(self, n):
         """Through the C ABI with host buffers: pinned x -> device, forward,
         device y -> pinned host, every step (eager launches)."""
@@ -570,22 +604,32 @@ def pick_G(K, n_copies):
     return next((g for g in (8, 6, 4, 2) if K % g == 0 and g % n_copies == 0), 1)
 
 
-def roofline_record(wl, u, per_kernel, ms_step, hbm, tflops, peak_src, traffic_key):
-    """The dominant kernel's roofline (algorithmic bytes over its event-timed
-    duration) and the layer's (roofline time over the step time)."""
+def roofline_record(wl, u, per_kernel, ms_step, hbm, tflops, peak_src, traffic_key, ev_over):
+    """The dominant kernel's roofline (algorithmic bytes over its duration)
+    and the layer's (roofline time over the step time).  The duration of a
+    layer that is one launch is the timed region's time per launch (CUDA
+    events around the whole region, inter-launch gaps included); otherwise
+    the kernel's event-node time in graph replay minus what event nodes add
+    to an empty launch (measured in the same process).  Both raw figures are
+    kept in the record."""
     cfg = wl.cfg
     layer_bytes, ex_bytes, flops = algorithmic(cfg, u)
     kname = wl.ex_key
+    raw = per_kernel[kname]
     if wl.sched == "slice":
         ex_bytes = layer_bytes  # the fused launch is the whole layer
-    achieved = ex_bytes / (per_kernel[kname] * 1e-6) / 1e9
+        dur, how = ms_step * 1e3, "timed region / launches (one launch per layer, back to back in graph replay)"
+    else:
+        dur, how = raw - ev_over["overhead_us"], "event nodes around the launch in graph replay, minus their overhead"
+    achieved = ex_bytes / (dur * 1e-6) / 1e9
     roof_layer_us = max(layer_bytes / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
     traffic, traffic_src = ncu_traffic(wl.sched, traffic_key, ex_bytes)
     roof = {"bound": "hbm", "kernel": KERNELS[wl.sched][0], "achieved": achieved, "peak": hbm, "unit": "GB/s",
             "frac": achieved / hbm, "frac_vs_nominal": achieved / NOMINAL_HBM_GBS, "traffic": traffic,
             "traffic_source": traffic_src,
             "peak_source": peak_src, "algorithmic_bytes_per_launch": ex_bytes,
-            "kernel_us": per_kernel[kname], "timing": "event nodes around the launch in graph replay"}
+            "kernel_us": dur, "timing": how, "kernel_us_event_nodes": raw,
+            "frac_event_nodes": ex_bytes / (raw * 1e-6) / 1e9 / hbm, "event_overhead": ev_over}
     layer = {"bytes": layer_bytes, "flops": flops, "roofline_us": roof_layer_us,
              "achieved_gbs": layer_bytes / (ms_step * 1e-3) / 1e9, "frac": roof_layer_us / (ms_step * 1e3),
              "frac_vs_nominal": layer_bytes / (NOMINAL_HBM_GBS * 1e9) * 1e6 / (ms_step * 1e3)}
@@ -618,14 +662,17 @@ def measure_extra(cfg, dev, rank, K, W, hbm, tflops, peak_src, sustain_s):
         del g
         log(f"{cfg.name} T={cfg.T}: kernel times")
         per_kernel = wl.kernel_us(G, max(2, min(25, 200 // G)))
+        ev_over = wl.event_overhead(8, 10)
         wl.check_status("after the timed region")
         roof, layer = roofline_record(wl, u, per_kernel, ms_step, hbm, tflops, peak_src,
-                                      workload_key(cfg, False))
+                                      workload_key(cfg, False), ev_over)
         return {"workload": cfg.name, "T": cfg.T, "weights": weights_of(cfg), "metric": metric_for(cfg),
                 "schedule": wl.sched,
                 "touched_experts": u, "us_per_layer": ms_step * 1e3, "tokens_per_s": cfg.T / (ms_step * 1e-3),
                 "steps": K, "layer_frac": layer["frac"], "kernel_frac": roof["frac"],
-                "kernel_frac_vs_nominal": roof["frac_vs_nominal"], "kernel_us": per_kernel,
+                "kernel_frac_vs_nominal": roof["frac_vs_nominal"], "kernel_frac_event_nodes": roof["frac_event_nodes"],
+                "kernel_us": {k: v - ev_over["overhead_us"] for k, v in per_kernel.items()},
+                "kernel_us_event_nodes": per_kernel, "event_overhead_us": ev_over["overhead_us"],
                 "traffic": roof["traffic"], "traffic_source": roof["traffic_source"],
                 "algorithmic_bytes_per_launch": roof["algorithmic_bytes_per_launch"],
                 "layer_bytes": layer["bytes"],
@@ -742,6 +789,7 @@ def run_gpu(args, cfg, rank, world):
     del graph
     log(f"{cfg.name} T={cfg.T}: kernel times")
     per_kernel = wl.kernel_us(G, max(2, min(25, 200 // G)))
+    ev_over = wl.event_overhead(8, 10)
     # ---- end to end through the C ABI with host buffers
     log(f"{cfg.name} T={cfg.T}: end to end")
     n_e2e = min(K, 2000)
@@ -749,7 +797,8 @@ def run_gpu(args, cfg, rank, world):
     e2e_value = cfg.T * n_e2e * world / (ms_e2e / 1e3)
     wl.check_status("after the timed region")
     override = args.tokens is not None or args.experts is not None
-    roof, layer = roofline_record(wl, u, per_kernel, ms_step, hbm, tflops, peak_src, workload_key(cfg, override))
+    roof, layer = roofline_record(wl, u, per_kernel, ms_step, hbm, tflops, peak_src, workload_key(cfg, override),
+                                  ev_over)
     layer["sustained"] = {"layers": n_sus * G, "seconds": ms_sus * n_sus * G * 1e-3, "us_per_layer": ms_sus * 1e3,
                           "frac": layer["roofline_us"] / (ms_sus * 1e3)}
     sched, n_copies, launched = wl.sched, wl.n_copies, wl.launched
@@ -792,7 +841,8 @@ def run_gpu(args, cfg, rank, world):
                    "parallelism": "replicas" if world > 1 else "single_gpu"},
         "roofline": roof,
         "layer_roofline": layer,
-        "kernel_us": per_kernel,
+        "kernel_us": {k: v - ev_over["overhead_us"] for k, v in per_kernel.items()},
+        "kernel_us_event_nodes": per_kernel,
         "gpu_launches": launched * K,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cfg.T * cfg.H * 2,
                 "d2h_bytes_per_step": cfg.T * cfg.H * 2, "steps": n_e2e, "launch": "eager"},
