@@ -252,13 +252,20 @@ def ncu_traffic(schedule: str, workload: str, ex_bytes: float):
         fields, ok = _profile_fields(exact, src)
         if ok and "traffic_bytes_per_launch" in fields:
             return float(fields["traffic_bytes_per_launch"]), "measured"
-    if schedule == "stream_k" and not workload.endswith("_fp4"):
+    # the same kernel and weight format captured on a smaller layer: its
+    # traffic / algorithmic ratio (bf16 stream-K, or the block-scaled kernel
+    # with the same routed-expert format)
+    fmt = next((f for f in ("_mxfp4", "_mxfp8") if workload.endswith(f)), "")
+    if (schedule == "stream_k" and not workload.endswith("_fp4")) or (schedule == "mx" and fmt):
         pdir = os.path.join(ROOT, "profiles")
         for fn in sorted(os.listdir(pdir)):
-            if fn.startswith(prefix + "_") and not fn.endswith("_fp4.md"):
-                fields, ok = _profile_fields(os.path.join(pdir, fn), src)
-                if ok and "traffic_ratio" in fields:
-                    return float(fields["traffic_ratio"]) * ex_bytes, "scaled"
+            if not fn.startswith(prefix + "_") or fn.endswith("_fp4.md"):
+                continue
+            if schedule == "mx" and not fn.endswith(fmt + ".md"):
+                continue
+            fields, ok = _profile_fields(os.path.join(pdir, fn), src)
+            if ok and "traffic_ratio" in fields:
+                return float(fields["traffic_ratio"]) * ex_bytes, "scaled"
     return None, None
 
 
@@ -506,6 +513,8 @@ class Workload:
         return g
 
     def replay_ms(self, graph, n):
+        """Milliseconds of n replays on the workload's stream (synchronised on
+        return: replays that share the workspace never overlap)."""
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(self.stream):
             e0.record(self.stream)
@@ -721,9 +730,11 @@ def measure_route_ahead(cfg, dev, rank, pairs: int = 40):
                 ops.set_l2_prefetch(None)
                 graphs[("evict_" if evict else "") + ("ahead" if ahead else "plain")] = g
         torch.cuda.synchronize()
+        # warm-up replays on the workload's stream, finished before the timed
+        # ones: the layers share one workspace, so two replays must never
+        # overlap (a replay runs on the stream current at the call)
         for g in graphs.values():
-            for _ in range(3):
-                g.replay()
+            wl.replay_ms(g, 3)
         # the variants in turn, three rounds, the best of each: a drift of the
         # box's speed over the run does not decide the comparison
         best = {k: float("inf") for k in graphs}
