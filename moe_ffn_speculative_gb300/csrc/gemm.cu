@@ -323,8 +323,8 @@ __device__ bool produce(const Smem& sm, const GemmParams& p, int ngroups, const 
         tma_load_3d_hint(sm.pbase + pring.stage * kPackedBytes + h * (kPackedBytes / 2), tm, bar, c0, c1, c2, pol);
       }
       const uint8_t* sc = ld.ph == 0 ? p.gu_scale : p.dn_scale;
-      bulk_load(sm.sbase + pring.stage * 512, sc + fp4_scale_offset(p, ld.ph, ld.sg.expert, ld.sg.m, ld.sg.k0 + ld.kk),
-                512, bar);
+      bulk_load_hint(sm.sbase + pring.stage * 512,
+                     sc + fp4_scale_offset(p, ld.ph, ld.sg.expert, ld.sg.m, ld.sg.k0 + ld.kk), 512, bar, pol);
       last_ps = pring.stage;
       last_pphase = pring.phase;
       pring.next(sm.SP);

@@ -387,8 +387,12 @@ __device__ bool produce(const Smem& sm, const MxParams& p, int ngroups, const lo
       else            { c1 = sg.m * 2 * kHalfRows + h * kHalfRows; c2 = plane; }
       tma_load_3d_hint(a + h * kHalfBytes, tm, bar, kb * kMxK, c1, c2, pol);
     }
-    bulk_load(st_sfa(sm, ring.stage), p.scales + mx_scale_offset(p.E, p.H, p.I, p.Is, ld.ph, sg.expert, sg.m, kb),
-              2 * kMxSfBytes, bar);
+    // the weights' scale chunks are streamed once too: evict-first, like the
+    // codes, so that they do not push the router's and the next layer's
+    // operands out of L2
+    bulk_load_hint(st_sfa(sm, ring.stage),
+                   p.scales + mx_scale_offset(p.E, p.H, p.I, p.Is, ld.ph, sg.expert, sg.m, kb), 2 * kMxSfBytes,
+                   bar, pol);
     ld.step();
     ring.next(sm.S);
   }
