@@ -343,8 +343,11 @@ __device__ __forceinline__ void unit_load_gu(const SliceParams& p, const SliceSm
   uint8_t* st = sm.base + stage * 2 * kTileBytesA;
   uint64_t* bar = &sm.full[stage];
   mbar_arrive_expect_tx(bar, 2 * kTileBytesA + sm.b_bytes);
-  tma_load_3d(st, gu, bar, kb * kBlockK, u.s * kHalfRows, zg);                    // gate rows of the slice
-  tma_load_3d(st + kTileBytesA, gu, bar, kb * kBlockK, u.s * kHalfRows, zg + 1);  // up rows
+  // weights are streamed once: evict-first, so that L2 keeps x, h and the
+  // router's operands
+  const uint64_t pol = l2_evict_first_policy();
+  tma_load_3d_hint(st, gu, bar, kb * kBlockK, u.s * kHalfRows, zg, pol);                    // gate rows
+  tma_load_3d_hint(st + kTileBytesA, gu, bar, kb * kBlockK, u.s * kHalfRows, zg + 1, pol);  // up rows
   tma_load_2d(sm.bbase + stage * sm.b_bytes, tm_x, bar, kb * kBlockK, 0);         // every token
 }
 
@@ -390,6 +393,7 @@ __device__ void unit_produce(const SliceParams& p, const SliceSmem& sm, const Un
   const DownGeom g = down_geom(p, u, n);
   const CUtensorMap* dn = u.shared ? tm_dn_sh : tm_dn;
   const int zd = u.shared ? 0 : u.e;
+  const uint64_t pol = l2_evict_first_policy();
   Ring rb;
   const int np = n_passes(p, u, g);
   for (int pi = 0; pi < np; ++pi) {
@@ -404,7 +408,7 @@ __device__ void unit_produce(const SliceParams& p, const SliceSmem& sm, const Un
       uint64_t* bar = &sm.fullB[rb.stage];
       mbar_arrive_expect_tx(bar, static_cast<uint32_t>(ps.cj) * kTileBytesA);
       for (int jj = 0; jj < ps.cj; ++jj)
-        tma_load_3d(st + jj * kTileBytesA, dn, bar, kbd * kBlockK, (ps.j0 + jj) * kHalfRows, zd);
+        tma_load_3d_hint(st + jj * kTileBytesA, dn, bar, kbd * kBlockK, (ps.j0 + jj) * kHalfRows, zd, pol);
       rb.next(g.S);
     }
   }
