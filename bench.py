@@ -228,15 +228,25 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def kernel_source_hash(src: str) -> str:
+    """sha256 over the kernel's .cu file and every shared header it builds
+    with (csrc/*.cuh, include/moe.h), in a fixed order."""
+    h = hashlib.sha256()
+    names = [os.path.join(CSRC, src)] + sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh"))
+    names.append(os.path.join(ROOT, "include", "moe.h"))
+    for n in names:
+        with open(n, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def _profile_fields(path: str, src: str):
     """(fields, valid): the machine-readable lines of an ncu summary, and
-    whether the kernel source still hashes to what was captured."""
+    whether the kernel's sources still hash to what was captured."""
     with open(path) as f:
         text = f.read()
     fields = dict(re.findall(r"^(\w+)\s*=\s*([0-9a-fA-F.eE+]+)\s*$", text, re.M))
-    with open(os.path.join(CSRC, src), "rb") as f:
-        cur = hashlib.sha256(f.read()).hexdigest()
-    return fields, fields.get("kernel_source_sha256") == cur
+    return fields, fields.get("kernel_source_sha256") == kernel_source_hash(src)
 
 
 def ncu_traffic(schedule: str, workload: str, ex_bytes: float):

@@ -87,7 +87,7 @@ constexpr int kCtrlRowOff = 256;
 constexpr int kCtrlSpans = 256 + 256 * 8;
 constexpr int kCtrlCols = 6144;
 constexpr int kMaxGrid = (kCtrlCols - kCtrlSpans) / 16 - 1;
-constexpr int kGatherLag = 2;                         // cp.async groups in flight (<= stages - 1)
+constexpr int kGatherLag = 1;                         // cp.async groups in flight (<= stages - 1)
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
