@@ -72,11 +72,13 @@ __device__ __forceinline__ void warp_argmax(float& v, int& ix, float& carry) {
 template <int NJ, bool kShared>
 __device__ void select_token(const float* lrow, const SelCfg& c, int32_t* idx_out, float* w_out) {
   const int lane = threadIdx.x & 31;
-  float l[NJ], s[NJ], key[NJ];
+  float l[NJ], s[NJ], key[NJ], eb[NJ];
+  // the logits and the expert bias are loaded together, before any scoring
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
     const int e = lane + 32 * j;
     l[j] = e < c.E ? (kShared ? lrow[e] : __ldcg(lrow + e)) : kNegInf;
+    eb[j] = (c.expert_bias && e < c.E) ? __ldg(c.expert_bias + e) : 0.f;
   }
   // ---- score (fp32)
   if (c.score_fn == 0) {  // softmax
@@ -115,7 +117,7 @@ __device__ void select_token(const float* lrow, const SelCfg& c, int32_t* idx_ou
     float v;
     if (e >= c.E) v = kNegInf;
     else if (on_logits) v = l[j];
-    else v = c.expert_bias ? s[j] + __ldg(c.expert_bias + e) : s[j];
+    else v = c.expert_bias ? s[j] + eb[j] : s[j];
     key[j] = (v != v) ? -FLT_MAX : v;
   }
   // ---- group-limited select: keep the topk_group groups with the best sum
