@@ -59,6 +59,11 @@ SMALL = {
                        shared_format="fp8", seed=65),
     # top-1 FP8 experts without a shared expert: y written by the down epilogue
     "fp8_top1_direct": _cfg("mx_fp8_top1", T=72, H=256, E=8, I=256, K=1, expert_format="fp8", seed=66),
+    # one token: one piece row group per token block, every other row zero
+    "fp4_one_token": _cfg("mx_fp4_one", T=1, H=128, E=8, I=128, K=2, shared_I=128, expert_format="fp4",
+                          shared_format="fp8", seed=70),
+    # every expert selected by every token (K = E)
+    "fp8_all_experts": _cfg("mx_fp8_all", T=30, H=128, E=4, I=128, K=4, expert_format="fp8", seed=69),
     # more than 1024 tokens: the router's logits GEMM, then select and permute
     "fp4_many_tokens": _cfg("mx_fp4_many", T=1100, H=128, E=12, I=128, K=2, shared_I=128, shared_gated=True,
                             expert_format="fp4", shared_format="fp8", seed=67),

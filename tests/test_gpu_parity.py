@@ -176,6 +176,8 @@ SMALL = {
                                                shared_I=128, seed=9),
     "single_expert_dense": S.LayerConfig("r6", T=20, H=128, E=1, I=64, K=1, route_scale=2.0, seed=10),
     "one_token": S.LayerConfig("r7", T=1, H=64, E=8, I=32, K=2, shared_I=32, seed=11),
+    # every expert selected by every token (K = E): no expert is skipped
+    "all_experts_selected": S.LayerConfig("r10", T=24, H=128, E=4, I=64, K=4, shared_I=64, seed=15),
     # > 1024 tokens (the tiled logits GEMM) with H not a multiple of its
     # 32-wide chunks, router bias and the shared-expert gate as one more
     # GEMM column
