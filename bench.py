@@ -229,11 +229,10 @@ def measured_peaks():
 
 
 def kernel_source_hash(src: str) -> str:
-    """sha256 over the kernel's .cu file and every shared header it builds
-    with (csrc/*.cuh, include/moe.h), in a fixed order."""
+    """sha256 over the kernel's .cu file and the library's internal headers
+    it builds with (csrc/*.cuh), in a fixed order."""
     h = hashlib.sha256()
     names = [os.path.join(CSRC, src)] + sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh"))
-    names.append(os.path.join(ROOT, "include", "moe.h"))
     for n in names:
         with open(n, "rb") as f:
             h.update(f.read())

@@ -343,7 +343,8 @@ MOE_API moe_status moe_mx_prepare_scales(int routed_fmt, const uint8_t* w_gate_u
 
 /* moe_ffn_forward() with block-scaled experts: router, workspace
  * (moe_ffn_workspace_bytes), outputs and errors as in moe_ffn_forward();
- * always the stream-K schedule, with token tiles of up to 32 tokens.
+ * always the stream-K schedule, with token tiles of up to 24 tokens (an
+ * expert with more tokens streams its weights once per tile).
  *   routed_fmt   MOE_FMT_FP4 or MOE_FMT_FP8
  *   w_gate_up_q, w_down_q   the routed experts' codes (layouts above)
  *   sh_gate_up_q, sh_down_q the shared expert's FP8 codes, or NULL (Is = 0)
@@ -365,8 +366,9 @@ MOE_API moe_status moe_ffn_forward_mx(const moe_bf16* x, int T, int H, int I, co
  * ran out; MOE_INFO_HOLD for the start gate below).
  *
  * Start gate: the int32 at byte offset MOE_WS_HOLD_OFFSET of a workspace.
- * While it is non-zero, the expert kernels of moe_ffn_forward() and
- * moe_ffn_forward_fp4() wait at their start; once it is zero they go on.  A
+ * While it is non-zero, the expert kernels of moe_ffn_forward(),
+ * moe_ffn_forward_fp4() and moe_ffn_forward_mx() wait at their start; once it
+ * is zero they go on.  A
  * wait that lasts past a quarter of the device wait limit (about a quarter
  * second of SM clocks; every other device wait gives up after about one
  * second) ends the forward with MOE_ERR_DEVICE_TIMEOUT / MOE_INFO_HOLD: every CTA
