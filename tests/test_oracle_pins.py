@@ -520,3 +520,43 @@ def test_fp8_layer_equals_layer_on_decoded_weights():
     # the row blocks' scales taken in the wrong order would change the result
     c = O.moe_layer(x, gate, O.dequant_fp8_blocks(gq, gs[..., ::-1, :]), O.dequant_fp8_blocks(dq, ds), rec)
     assert np.abs(c["y"] - a["y"]).max() > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# selection margin: perturbations below it keep the selection, and for plain
+# top-k one of its size flips it (brute force on small random scores)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n_group,topk_group", [(1, 1), (4, 2), (8, 3)])
+def test_selection_margin_bounds_the_perturbations_that_keep_the_selection(n_group, topk_group):
+    rng = np.random.default_rng(31 + n_group)
+    E, K, T = 16 if n_group < 8 else 32, 4, 40
+    rec = O.Recipe(num_experts=E, top_k=K, n_group=n_group, topk_group=topk_group)
+    choice = rng.standard_normal((T, E))
+    idx = O.select(choice, rec)
+    m = O.selection_margin(choice, idx, rec)
+    assert (m > 0).all()
+    # every shifted score moved by at most m/4.01: a group score (a sum of
+    # two scores) by at most m/2.005, so no gap of size >= m can close
+    for _ in range(200):
+        d = rng.uniform(-1.0, 1.0, (T, E)) * (m[:, None] / 4.01)
+        np.testing.assert_array_equal(O.select(choice + d, rec), idx)
+    if n_group == 1:
+        # the two scores across the smallest gap, moved by 0.51 m towards each
+        # other, swap (two picks change order, or a pick leaves the set)
+        rows = np.arange(T)
+        picked = choice[rows[:, None], idx]
+        rest = choice.copy()
+        rest[rows[:, None], idx] = -np.inf
+        flipped = 0
+        for t in range(T):
+            gaps = list(picked[t, :-1] - picked[t, 1:]) + [picked[t, -1] - rest[t].max()]
+            j = int(np.argmin(gaps))
+            assert gaps[j] == pytest.approx(m[t])
+            hi = idx[t, j]
+            lo = idx[t, j + 1] if j < K - 1 else int(np.argmax(rest[t]))
+            c = choice[t].copy()
+            c[hi] -= 0.51 * m[t]
+            c[lo] += 0.51 * m[t]
+            flipped += not np.array_equal(O.select(c[None, :], rec)[0], idx[t])
+        assert flipped == T
