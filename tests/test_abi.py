@@ -175,3 +175,20 @@ def test_layer_path_selection():
     # bf16 experts cannot take the block-scaled path
     with pytest.raises(ValueError):
         ops.layer_path(t(), mx=True)
+
+
+def test_l2_prefetch_refusals(lib):
+    """moe_set_l2_prefetch only records ranges (no device access): more than
+    eight ranges, missing arrays, a null or misaligned pointer are refused;
+    an empty list clears."""
+    P = ctypes.c_void_p
+    arr = (P * 9)(*([P(0x1000)] * 9))
+    sizes = (ctypes.c_size_t * 9)(*([4096] * 9))
+    assert lib.moe_set_l2_prefetch(ctypes.cast(arr, P), ctypes.cast(sizes, P), 9) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_l2_prefetch(None, None, 1) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_l2_prefetch(None, None, -1) == ops.MOE_ERR_INVALID_ARG
+    bad = (P * 1)(P(0x1008))
+    assert lib.moe_set_l2_prefetch(ctypes.cast(bad, P), ctypes.cast(sizes, P), 1) == ops.MOE_ERR_INVALID_ARG
+    null = (P * 1)(P(0))
+    assert lib.moe_set_l2_prefetch(ctypes.cast(null, P), ctypes.cast(sizes, P), 1) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_l2_prefetch(None, None, 0) == 0
