@@ -231,6 +231,14 @@ MOE_API moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I,
  *       per-slice partial outputs.  An expert no token picked stops streaming
  *       once the routing is known.  Shape limits: T <= 128, E (+1 with
  *       sh_gate) <= 16, E*ceil(I/128) + ceil(Is/128) + ceil(T/7) <= SMs.
+ *       The launch is made with programmatic stream serialization: its
+ *       CTAs may start on the SMs that the previous kernel on the stream
+ *       leaves (when that kernel allows it, as this one does) and stream
+ *       their first weights into shared memory and L2 there; everything
+ *       they read that a kernel writes (x, the workspace) waits until the
+ *       previous kernel has completed.  So a CTA of the launch may wait for
+ *       another to be placed (bounded, MOE_ERR_DEVICE_TIMEOUT on expiry): the
+ *       grid assumes the SMs are not held by other work for long.
  *   MOE_SCHEDULE_AUTO      SLICE where the shape fits, the expected number
  *       of untouched experts under uniform routing, E*(1-K/E)^T, is at most
  *       0.25, and the down GEMM's work items (128-row output tiles, each cut

@@ -529,6 +529,21 @@ __device__ __forceinline__ void prefetch_share_l2(const L2Prefetch& pf) {
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+// L2 prefetch of one tile box of a 3-D tensor map.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+// Programmatic dependent launch: let the next launch on the stream (made
+// with the programmatic-serialization attribute) start its CTAs, and wait
+// until the previous launch on the stream has completed with its memory
+// visible (a no-op when the launch does not depend on one programmatically).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // cp.async (16 bytes, L2 only); src_bytes == 0 zero-fills the destination.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {

@@ -33,6 +33,12 @@
 // without other work, wait until every expert has finished the tile and sum
 // the pair outputs in slot order: the result does not depend on timing.
 //
+// Consecutive forwards on a stream overlap: a launch lets the next one place
+// its CTAs on the SMs it leaves (programmatic dependent launch); those CTAs
+// load their first ring-full of gate/up weights and prefetch the next
+// weights into L2 while the previous forward's last output tiles are being
+// computed, and read x and the workspace only once it has completed.
+//
 // Unit CTA warp roles (224 threads): warp 0 issues the weight TMA loads,
 // warp 1 allocates TMEM and issues the MMAs, warp 2 builds the unit's token
 // list, then fetches the down GEMM's h tiles and publishes finished output
@@ -47,6 +53,12 @@ namespace {
 
 constexpr int kSliceThreads = 224;  // 7 warps
 constexpr uint32_t kSliceTmemCols = 512;
+// L2 prefetch at the start of a launch, while the previous launch on the
+// stream ends: a unit's gate/up k-blocks after its first ring-full, a
+// helper's first down k-blocks (up to 16 per output tile, 32 boxes of 16 KB).
+constexpr int kSlicePrefetchGu = 6;
+constexpr int kSlicePrefetchDnKb = 16;
+constexpr int kSlicePrefetchDnBoxes = 32;
 
 static_assert(kSliceTokPerTask == kSliceThreads / 32, "one combine token per warp");
 
@@ -334,10 +346,11 @@ __device__ __forceinline__ int pass_kb(const Pass& ps, int q) {
 }
 
 // The loads of gate_up k-block kb into its (free) stage: the slice's gate and
-// up rows and every token's x.
+// up rows and (with_x) every token's x; without x, the caller loads the
+// x tile later on the same barrier.
 __device__ __forceinline__ void unit_load_gu(const SliceParams& p, const SliceSmem& sm, const Unit& u,
                                              const CUtensorMap* tm_gu, const CUtensorMap* tm_gu_sh,
-                                             const CUtensorMap* tm_x, int kb, int stage) {
+                                             const CUtensorMap* tm_x, int kb, int stage, bool with_x = true) {
   const CUtensorMap* gu = u.shared ? tm_gu_sh : tm_gu;
   const int zg = u.shared ? 0 : 2 * u.e;
   uint8_t* st = sm.base + stage * 2 * kTileBytesA;
@@ -348,7 +361,42 @@ __device__ __forceinline__ void unit_load_gu(const SliceParams& p, const SliceSm
   const uint64_t pol = l2_evict_first_policy();
   tma_load_3d_hint(st, gu, bar, kb * kBlockK, u.s * kHalfRows, zg, pol);                    // gate rows
   tma_load_3d_hint(st + kTileBytesA, gu, bar, kb * kBlockK, u.s * kHalfRows, zg + 1, pol);  // up rows
-  tma_load_2d(sm.bbase + stage * sm.b_bytes, tm_x, bar, kb * kBlockK, 0);         // every token
+  if (with_x) tma_load_2d(sm.bbase + stage * sm.b_bytes, tm_x, bar, kb * kBlockK, 0);       // every token
+}
+
+// L2 prefetch of the weights the CTA streams first after its ring-full: a
+// unit's next gate/up k-blocks; a helper's first down k-blocks, in the order
+// its passes take them (its output tiles are fixed before the routing is
+// known, only the tokens it multiplies are not).
+__device__ void prefetch_first_weights(const SliceParams& p, const Unit& u, const CUtensorMap* tm_gu,
+                                       const CUtensorMap* tm_gu_sh, const CUtensorMap* tm_dn,
+                                       const CUtensorMap* tm_dn_sh, int kb_first) {
+  if (u.has_a) {
+    const CUtensorMap* gu = u.shared ? tm_gu_sh : tm_gu;
+    const int zg = u.shared ? 0 : 2 * u.e;
+    for (int kb = kb_first; kb < min(u.nkb, kb_first + kSlicePrefetchGu); ++kb) {
+      tma_prefetch_l2_3d(gu, kb * kBlockK, u.s * kHalfRows, zg);
+      tma_prefetch_l2_3d(gu, kb * kBlockK, u.s * kHalfRows, zg + 1);
+    }
+    return;
+  }
+  if (u.ni == 0) return;
+  const CUtensorMap* dn = u.shared ? tm_dn_sh : tm_dn;
+  const int zd = u.shared ? 0 : u.e;
+  if (p.parts == 1) {
+    const int kq = min(u.nkb_d, min(kSlicePrefetchDnKb, kSlicePrefetchDnBoxes / u.ni));
+    for (int q = 0; q < kq; ++q) {
+      const int kbd = (q + u.kstart) % u.nkb_d;
+      for (int jj = 0; jj < u.ni; ++jj) tma_prefetch_l2_3d(dn, kbd * kBlockK, (u.i0 + jj) * kHalfRows, zd);
+    }
+  } else {
+    int boxes = kSlicePrefetchDnBoxes;
+    for (int it = u.i0; it < u.i0 + u.ni && boxes > 0; ++it) {
+      const int j = it / p.parts, part = it - j * p.parts;
+      const int ka = u.nkb_d * part / p.parts, kn = u.nkb_d * (part + 1) / p.parts - ka;
+      for (int q = 0; q < kn && boxes > 0; ++q, --boxes) tma_prefetch_l2_3d(dn, (ka + q) * kBlockK, j * kHalfRows, zd);
+    }
+  }
 }
 
 // k-blocks [0, kb_first) were issued into the fresh ring by the prologue.
@@ -838,21 +886,13 @@ __global__ void __launch_bounds__(kSliceThreads, 1)
     fence_barrier_init();
     fence_proxy_async();
     if (is_unit) {
-      // the first ring-full of weight loads goes out before the rest of the
-      // prologue (the counter-set read, TMEM allocation, the block barrier)
+      // the first ring-full of gate/up weights goes out before the rest of
+      // the prologue, and before the previous launch on the stream has
+      // ended (a forward never writes weights); their x tiles once it has
       kb_first = min(sm.S, u.nkb);
-      for (int kb = 0; kb < kb_first; ++kb) unit_load_gu(p, sm, u, &tm_gu, &tm_gu_sh, &tm_x, kb, kb);
+      for (int kb = 0; kb < kb_first; ++kb) unit_load_gu(p, sm, u, &tm_gu, &tm_gu_sh, &tm_x, kb, kb, false);
     }
-  }
-  // Counter sets alternate between forwards: the previous forward flipped
-  // the parity word as it ended; this one clears the set the previous one
-  // used, which the next one will use.
-  const int par = *reinterpret_cast<const volatile int32_t*>(p.sync) & 1;
-  sm.ss = p.sync + 1 + par * p.set_words;
-  sm.ready = sm.ss + kSliceSyncWords + p.n_mt;
-  if (bid == static_cast<int>(gridDim.x) - 1) {
-    int32_t* other = p.sync + 1 + (par ^ 1) * p.set_words;
-    for (int i = threadIdx.x; i < p.set_words; i += blockDim.x) other[i] = 0;
+    prefetch_first_weights(p, u, &tm_gu, &tm_gu_sh, &tm_dn, &tm_dn_sh, kb_first);
   }
   const bool works = is_unit || u.ni > 0;
   if (works && warp == 0 && lane == 0) {
@@ -867,6 +907,24 @@ __global__ void __launch_bounds__(kSliceThreads, 1)
   if (works && warp == 1) {
     tmem_alloc(sm.tmem_slot, kSliceTmemCols);
     tmem_relinquish();
+  }
+  // The next forward on the stream may place its CTAs on the SMs this one
+  // leaves and start streaming its weights; everything that reads what the
+  // previous launch wrote (x, the workspace, the counter sets) waits until
+  // that launch has completed.
+  griddep_launch_dependents();
+  griddep_wait();
+  if (threadIdx.x == 0)
+    for (int kb = 0; kb < kb_first; ++kb) tma_load_2d(sm.bbase + kb * sm.b_bytes, &tm_x, &sm.full[kb], kb * kBlockK, 0);
+  // Counter sets alternate between forwards: the previous forward flipped
+  // the parity word as it ended; this one clears the set the previous one
+  // used, which the next one will use.
+  const int par = *reinterpret_cast<const volatile int32_t*>(p.sync) & 1;
+  sm.ss = p.sync + 1 + par * p.set_words;
+  sm.ready = sm.ss + kSliceSyncWords + p.n_mt;
+  if (bid == static_cast<int>(gridDim.x) - 1) {
+    int32_t* other = p.sync + 1 + (par ^ 1) * p.set_words;
+    for (int i = threadIdx.x; i < p.set_words; i += blockDim.x) other[i] = 0;
   }
   tc_fence_before();
   __syncthreads();
@@ -920,9 +978,14 @@ cudaError_t launch_slice(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, 
   cfg.blockDim = dim3(kSliceThreads);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = s;
+  // Not a cooperative launch: the grid is one CTA per SM and every CTA takes
+  // an SM's whole shared memory, so once the previous launch on the stream
+  // has ended every CTA is resident (and every cross-CTA wait is bounded in
+  // any case).  Programmatic serialization lets this launch's CTAs start on
+  // the SMs the previous forward leaves, overlapping its tail.
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, moe_slice_kernel, tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, tm_x, p);
