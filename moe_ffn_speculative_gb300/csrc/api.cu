@@ -176,6 +176,14 @@ RouterGeom router_geometry(int T, int E, bool gated, int sms) {
   if (static_cast<long long>(ceil_div(T, 8)) * g.n_eb < sms && static_cast<long long>(ceil_div(T, 4)) * g.n_eb <= sms)
     g.tb = 4;
   g.n_tb = ceil_div(T, g.tb);
+  // With several expert blocks, fewer rows per block and H split over more
+  // warps while the grid still fits in one wave: each warp's chain of
+  // dependent gate loads gets shorter (the GEMV is bound by that latency).
+  if (g.n_eb > 1) {
+    while (g.quads > 1 && static_cast<long long>(g.n_tb) * ceil_div(qn, g.quads / 2) <= sms) g.quads >>= 1;
+    g.hsplit = 8 / g.quads;
+    g.n_eb = ceil_div(qn, g.quads);
+  }
   return g;
 }
 
