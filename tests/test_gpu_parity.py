@@ -439,3 +439,53 @@ def test_repeated_forwards_bit_identical(sched):
             torch.cuda.synchronize()
             assert torch.equal(y, y_ref), f"forward {it} differs"
         assert layer.ws.device_status()[0] == 0
+
+
+@pytest.mark.parametrize("sched", list(SCHEDULES))
+def test_chained_forwards_back_to_back(sched):
+    """Layers chained on one stream (each forward's input is the previous
+    forward's output), launched back to back without a host synchronisation,
+    eagerly and from a replayed CUDA graph, give the bits of the same chain
+    synchronised after every forward: a launch that starts before the
+    previous one has ended (the fused schedule's CTAs start on the SMs the
+    previous forward leaves) reads x only once that forward has written it."""
+    cfg = S.CONFIGS["qwen3_8b_dspark"]
+    _require(cfg, SCHEDULES[sched])
+    d = S.make_inputs(cfg, device="cuda")
+    rec = ops.Recipe.from_config(cfg)
+    n = 8
+    with _schedule(SCHEDULES[sched]):
+        layer = ops.MoELayer(d, rec, cfg.T)
+        ref, x = [], d["x"]
+        for _ in range(n):
+            x = layer.forward(x).clone()
+            torch.cuda.synchronize()
+            ref.append(x)
+        assert all(torch.isfinite(r.float()).all() for r in ref)
+        s = torch.cuda.Stream()
+        outs = [torch.empty_like(d["x"]) for _ in range(n)]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            x = d["x"]
+            for i in range(n):
+                layer.forward(x, y=outs[i], stream=s)
+                x = outs[i]
+        torch.cuda.synchronize()
+        for i in range(n):
+            assert torch.equal(outs[i], ref[i]), f"eager forward {i} differs"
+        outs2 = [torch.empty_like(d["x"]) for _ in range(n)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            x = d["x"]
+            for i in range(n):
+                layer.forward(x, y=outs2[i], stream=s)
+                x = outs2[i]
+        for rep in range(3):
+            for o in outs2:
+                o.zero_()
+            torch.cuda.synchronize()
+            g.replay()
+            torch.cuda.synchronize()
+            for i in range(n):
+                assert torch.equal(outs2[i], ref[i]), f"graph replay {rep}, forward {i} differs"
+        assert layer.ws.device_status()[0] == 0
