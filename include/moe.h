@@ -238,7 +238,8 @@ MOE_API moe_status moe_ffn_forward(const moe_bf16* x, int T, int H, int I,
  *       they read that a kernel writes (x, the workspace) waits until the
  *       previous kernel has completed.  So a CTA of the launch may wait for
  *       another to be placed (bounded, MOE_ERR_DEVICE_TIMEOUT on expiry): the
- *       grid assumes the SMs are not held by other work for long.
+ *       grid assumes the SMs are not held by other work for long, and
+ *       moe_set_launch_overlap(0) makes it a cooperative launch instead.
  *   MOE_SCHEDULE_AUTO      SLICE where the shape fits, the expected number
  *       of untouched experts under uniform routing, E*(1-K/E)^T, is at most
  *       0.25, and the down GEMM's work items (128-row output tiles, each cut
@@ -256,6 +257,15 @@ typedef enum {
  * forced MOE_SCHEDULE_SLICE still runs STREAM_K where the shape does not fit.
  * Returns MOE_ERR_INVALID_ARG for an unknown value. */
 MOE_API moe_status moe_set_schedule(int schedule);
+
+/* Per calling thread: how later MOE_SCHEDULE_SLICE launches start.  1 (the
+ * default): with programmatic stream serialization, overlapping the end of
+ * the previous kernel on the stream (see MOE_SCHEDULE_SLICE above).  0: as
+ * cooperative launches, which start once every CTA of the grid can be
+ * resident -- for streams whose kernels may run beside other work that holds
+ * SMs.  Both compute the same bits.  Returns MOE_ERR_INVALID_ARG for a value
+ * other than 0 or 1. */
+MOE_API moe_status moe_set_launch_overlap(int enable);
 
 /* The schedule moe_ffn_forward() would run for this shape on the current
  * device under the calling thread's setting: MOE_SCHEDULE_STREAM_K or

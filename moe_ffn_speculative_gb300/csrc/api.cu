@@ -23,6 +23,7 @@ std::atomic<int> g_sms[kMaxDevices];  // SM count per device, filled on first us
 thread_local void* const* t_events = nullptr;
 thread_local int t_nev = 0;
 thread_local int t_schedule = MOE_SCHEDULE_AUTO;
+thread_local int t_overlap = 1;  // slice launches overlap the previous kernel on the stream
 thread_local L2Prefetch t_prefetch = {};  // consumed by the next forward on this thread
 
 int device_sms() {
@@ -602,7 +603,8 @@ moe_status ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf16* g
     record_event_on(0, stream);
     record_event_on(1, stream);
     record_event_on(2, stream);
-    const cudaError_t e = launch_slice(tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, tm_x, sp, L.grid, kSmemLimit, stream);
+    const cudaError_t e =
+        launch_slice(tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, tm_x, sp, L.grid, kSmemLimit, t_overlap != 0, stream);
     record_event_on(3, stream);
     return cuda_status(e);
   }
@@ -988,6 +990,12 @@ moe_status moe_set_schedule(int schedule) {
   if (schedule != MOE_SCHEDULE_AUTO && schedule != MOE_SCHEDULE_STREAM_K && schedule != MOE_SCHEDULE_SLICE)
     return MOE_ERR_INVALID_ARG;
   t_schedule = schedule;
+  return MOE_OK;
+}
+
+moe_status moe_set_launch_overlap(int enable) {
+  if (enable != 0 && enable != 1) return MOE_ERR_INVALID_ARG;
+  t_overlap = enable;
   return MOE_OK;
 }
 

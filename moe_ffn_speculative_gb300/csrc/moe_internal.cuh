@@ -384,9 +384,10 @@ cudaError_t launch_experts(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh
 // FP4 block scales re-laid into 512-byte (expert, tile, k-block) blocks.
 cudaError_t launch_fp4_scales(const uint8_t* gu_s, const uint8_t* dn_s, int E, int H, int I, uint8_t* out,
                               cudaStream_t s);
+// overlap: programmatic stream serialization, else a cooperative launch
 cudaError_t launch_slice(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, const CUtensorMap& tm_dn,
                          const CUtensorMap& tm_dn_sh, const CUtensorMap& tm_x, const SliceParams& p, int grid,
-                         size_t smem_bytes, cudaStream_t s);
+                         size_t smem_bytes, bool overlap, cudaStream_t s);
 cudaError_t launch_combine(const float* out_ws, const int32_t* pair_pos, int T, int K, int H,
                            int has_shared, uint16_t* y, cudaStream_t s);
 cudaError_t launch_mx(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, const CUtensorMap& tm_dn,

@@ -969,7 +969,7 @@ __global__ void __launch_bounds__(kSliceThreads, 1)
 
 cudaError_t launch_slice(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, const CUtensorMap& tm_dn,
                          const CUtensorMap& tm_dn_sh, const CUtensorMap& tm_x, const SliceParams& p, int grid,
-                         size_t smem_bytes, cudaStream_t s) {
+                         size_t smem_bytes, bool overlap, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(moe_slice_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem_bytes));
   if (e != cudaSuccess) return e;
@@ -978,14 +978,20 @@ cudaError_t launch_slice(const CUtensorMap& tm_gu, const CUtensorMap& tm_gu_sh, 
   cfg.blockDim = dim3(kSliceThreads);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = s;
-  // Not a cooperative launch: the grid is one CTA per SM and every CTA takes
-  // an SM's whole shared memory, so once the previous launch on the stream
-  // has ended every CTA is resident (and every cross-CTA wait is bounded in
-  // any case).  Programmatic serialization lets this launch's CTAs start on
-  // the SMs the previous forward leaves, overlapping its tail.
+  // With overlap, not a cooperative launch: the grid is one CTA per SM and
+  // every CTA takes an SM's whole shared memory, so once the previous launch
+  // on the stream has ended every CTA is resident (and every cross-CTA wait
+  // is bounded in any case).  Programmatic serialization lets this launch's
+  // CTAs start on the SMs the previous forward leaves, overlapping its tail.
+  // Without, a cooperative launch (griddepcontrol.wait is then a no-op).
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  if (overlap) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, moe_slice_kernel, tm_gu, tm_gu_sh, tm_dn, tm_dn_sh, tm_x, p);

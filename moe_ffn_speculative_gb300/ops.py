@@ -82,6 +82,7 @@ _SIGS = {
     "moe_set_profile_events": (None, [_P, _I]),
     "moe_set_l2_prefetch": (_I, [_P, _P, _I]),
     "moe_set_schedule": (_I, [_I]),
+    "moe_set_launch_overlap": (_I, [_I]),
     "moe_ffn_schedule": (_I, [_I, _I, _I, _I, ctypes.POINTER(Recipe), _I]),
     "moe_fp4_scales_bytes": (_SZ, [_I, _I, _I]),
     "moe_fp4_prepare_scales": (_I, [_P, _P, _I, _I, _I, _P, _SZ, _P]),
@@ -379,6 +380,13 @@ def set_schedule(schedule: int) -> None:
     """Expert schedule of later moe_ffn_forward calls on this thread:
     SCHEDULE_AUTO, SCHEDULE_STREAM_K or SCHEDULE_SLICE."""
     _check(lib().moe_set_schedule(int(schedule)), "moe_set_schedule")
+
+
+def set_launch_overlap(enable: bool) -> None:
+    """Whether later fused-schedule launches on this thread overlap the
+    previous kernel on their stream (True, the default) or are cooperative
+    launches (False); both compute the same bits."""
+    _check(lib().moe_set_launch_overlap(1 if enable else 0), "moe_set_launch_overlap")
 
 
 def ffn_schedule(T: int, H: int, I: int, Is: int, recipe: Recipe, gated: bool = False) -> int:

@@ -192,3 +192,14 @@ def test_l2_prefetch_refusals(lib):
     null = (P * 1)(P(0))
     assert lib.moe_set_l2_prefetch(ctypes.cast(null, P), ctypes.cast(sizes, P), 1) == ops.MOE_ERR_INVALID_ARG
     assert lib.moe_set_l2_prefetch(None, None, 0) == 0
+
+
+def test_launch_overlap_setting(lib):
+    """The per-thread launch-overlap switch takes 0 or 1 and refuses the rest,
+    without touching a device."""
+    assert lib.moe_set_launch_overlap(2) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_launch_overlap(-1) == ops.MOE_ERR_INVALID_ARG
+    assert lib.moe_set_launch_overlap(0) == ops.MOE_OK
+    assert lib.moe_set_launch_overlap(1) == ops.MOE_OK
+    ops.set_launch_overlap(False)
+    ops.set_launch_overlap(True)

@@ -51,6 +51,8 @@ int main(void) {
                         NULL, NULL, NULL, (cudaStream_t)0) == MOE_OK);
   CHECK(moe_route_from_logits(NULL, 0, NULL, &ok, NULL, NULL, (cudaStream_t)0) == MOE_OK);
   CHECK(moe_set_schedule(7) == MOE_ERR_INVALID_ARG);
+  CHECK(moe_set_launch_overlap(2) == MOE_ERR_INVALID_ARG);
+  CHECK(moe_set_launch_overlap(1) == MOE_OK);
   printf("c abi ok\n");
   return 0;
 }

@@ -441,6 +441,31 @@ def test_repeated_forwards_bit_identical(sched):
         assert layer.ws.device_status()[0] == 0
 
 
+def test_slice_launch_overlap_off_gives_the_same_bits():
+    """The fused layer launched cooperatively (no overlap with the previous
+    kernel) and with programmatic serialization computes the same bits,
+    alone and chained back to back."""
+    cfg = S.CONFIGS["qwen3_8b_dspark"]
+    _require(cfg, ops.SCHEDULE_SLICE)
+    d = S.make_inputs(cfg, device="cuda")
+    rec = ops.Recipe.from_config(cfg)
+    outs = {}
+    with _schedule(ops.SCHEDULE_SLICE):
+        layer = ops.MoELayer(d, rec, cfg.T)
+        try:
+            for overlap in (True, False):
+                ops.set_launch_overlap(overlap)
+                y1 = layer.forward(d["x"])
+                y2 = layer.forward(y1)
+                torch.cuda.synchronize()
+                outs[overlap] = (y1.clone(), y2.clone())
+        finally:
+            ops.set_launch_overlap(True)
+        assert layer.ws.device_status()[0] == 0
+    assert torch.equal(outs[True][0], outs[False][0])
+    assert torch.equal(outs[True][1], outs[False][1])
+
+
 @pytest.mark.parametrize("sched", list(SCHEDULES))
 def test_chained_forwards_back_to_back(sched):
     """Layers chained on one stream (each forward's input is the previous
