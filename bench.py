@@ -103,6 +103,8 @@ def parse():
     ap.add_argument("--sustain", type=float, default=1.0, help="seconds of the sustained replay (headline)")
     ap.add_argument("--sustain-extra", type=float, default=0.5, help="seconds of the sustained replay (others)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--route-only", action="store_true",
+                    help="time the routing entry point (moe_route) alone on the workload's x and gate")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-child", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -808,6 +810,62 @@ def measure_route_ahead(cfg, dev, rank, pairs: int = 40):
         wl.close()
 
 
+def run_route_only(args, cfg, rank, world):
+    """moe_route alone (router logits, score, select, weights) on the
+    workload's x, gate and biases, in graph replay of 8 calls per graph:
+    one JSON line with its time per call.  Its operands (x and the gate, a
+    few MB) stay in L2 across calls."""
+    from moe_ffn_speculative_gb300 import ops
+    from moe_ffn_speculative_gb300.build import build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = S.make_router_inputs(cfg, device=dev)
+    rec = ops.Recipe.from_config(cfg)
+    ws = ops.Workspace(ops.lib().moe_route_workspace_bytes(cfg.T, cfg.E), dev)
+    stream = torch.cuda.Stream(device=dev)
+    out = {}
+
+    def call():
+        out["r"] = ops.moe_route(d["x"], d["gate"], rec, router_bias=d["router_bias"],
+                                 expert_bias=d["expert_bias"], ws=ws, want_logits=False, stream=stream)
+
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    G = 8
+    K = (args.steps if args.steps is not None else 4000) // G * G or G
+    W = max(3, args.warmup if args.warmup is not None else 50)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(G):
+            call()
+    with torch.cuda.stream(stream):
+        for _ in range(-(-W // G)):
+            g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K // G):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    st, info = ws.device_status(stream)
+    if st != 0:
+        raise SystemExit(f"moe_route: device status {st} ({info})")
+    us = e0.elapsed_time(e1) / K * 1e3
+    gate_bytes = cfg.E * cfg.H * 2 + cfg.T * cfg.H * 2
+    print(json.dumps({"metric": "moe_route time per call", "value": us, "unit": "us", "higher_is_better": False,
+                      "calls": K, "warmup": W, "tokens_per_s": cfg.T / (us * 1e-6),
+                      "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "K": cfg.K,
+                                 "launch": f"cuda_graph_replay, {G} calls per graph",
+                                 "operands": f"x and gate ({gate_bytes / 1e6:.2f} MB) L2-resident"}}),
+          flush=True)
+
+
 def run_gpu(args, cfg, rank, world):
     from moe_ffn_speculative_gb300 import ops
     from moe_ffn_speculative_gb300.build import build
@@ -940,6 +998,8 @@ def main():
     rank, world = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, cfg, rank, world)
+    elif args.route_only:
+        run_route_only(args, cfg, rank, world)
     else:
         run_gpu(args, cfg, rank, world)
     if world > 1:

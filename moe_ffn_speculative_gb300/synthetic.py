@@ -216,6 +216,22 @@ def make_inputs(cfg: LayerConfig, device="cpu", seed: Optional[int] = None) -> D
     return d
 
 
+def make_router_inputs(cfg: LayerConfig, device="cpu", seed: Optional[int] = None) -> Dict[str, torch.Tensor]:
+    """Only x, gate, router_bias and expert_bias, drawn as make_inputs draws
+    them first (the same values), without the experts' weights."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(cfg.seed if seed is None else seed)
+    d: Dict[str, Optional[torch.Tensor]] = {}
+    d["x"] = _normal(gen, (cfg.T, cfg.H), cfg.x_std, torch.bfloat16, device)
+    d["gate"] = _normal(gen, (cfg.E, cfg.H), cfg.w_std, torch.bfloat16, device)
+    d["router_bias"] = (_normal(gen, (cfg.E,), cfg.router_bias_std, torch.float32, device)
+                        if cfg.router_bias_std > 0 else None)
+    d["expert_bias"] = (_normal(gen, (cfg.E,), cfg.expert_bias_std, torch.float32, device)
+                        if cfg.expert_bias_std > 0 else None)
+    return d
+
+
 def make_x(cfg: LayerConfig, T: int, device="cpu", seed: int = 0) -> torch.Tensor:
     """Only the activations, for sweeps over the token count."""
     gen = torch.Generator(device=torch.device(device))

@@ -87,3 +87,14 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert len(lines) == 1
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+
+
+@pytest.mark.parametrize("name", ["qwen38_27b_dspark", "dsv3_style", "dsv4_style"])
+def test_router_only_inputs_are_the_layers_own(name):
+    """bench.py --route-only draws x, the gate and the biases as the full
+    layer draws them first: the router it times sees the layer's operands."""
+    import torch
+    cfg = S.CONFIGS[name].with_(T=5, E=16, I=32, H=64, shared_I=32 if S.CONFIGS[name].shared_I else 0)
+    full, router = S.make_inputs(cfg), S.make_router_inputs(cfg)
+    for k in ("x", "gate", "router_bias", "expert_bias"):
+        assert (full[k] is None and router[k] is None) or torch.equal(full[k], router[k]), k
