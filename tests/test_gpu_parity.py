@@ -466,15 +466,23 @@ def test_slice_launch_overlap_off_gives_the_same_bits():
     assert torch.equal(outs[True][1], outs[False][1])
 
 
+CHAINED = {"qwen3_8b_dspark": S.CONFIGS["qwen3_8b_dspark"],
+           "ragged_gated_shared_router_bias": SMALL["ragged_gated_shared_router_bias"],
+           "sqrtsoftplus_clamp_shared": SMALL["sqrtsoftplus_clamp_shared"]}
+
+
 @pytest.mark.parametrize("sched", list(SCHEDULES))
-def test_chained_forwards_back_to_back(sched):
+@pytest.mark.parametrize("name", list(CHAINED))
+def test_chained_forwards_back_to_back(name, sched):
     """Layers chained on one stream (each forward's input is the previous
     forward's output), launched back to back without a host synchronisation,
     eagerly and from a replayed CUDA graph, give the bits of the same chain
     synchronised after every forward: a launch that starts before the
     previous one has ended (the fused schedule's CTAs start on the SMs the
-    previous forward leaves) reads x only once that forward has written it."""
-    cfg = S.CONFIGS["qwen3_8b_dspark"]
+    previous forward leaves) reads x only once that forward has written it.
+    The small layers take the fused schedule's combine tasks (top-2 with a
+    gated shared expert; top-6 with an ungated one)."""
+    cfg = CHAINED[name]
     _require(cfg, SCHEDULES[sched])
     d = S.make_inputs(cfg, device="cuda")
     rec = ops.Recipe.from_config(cfg)
