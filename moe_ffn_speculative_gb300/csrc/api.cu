@@ -17,6 +17,10 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr size_t kAlign = 256;
 constexpr int kSmemLimit = 232448;  // 227 KB of dynamic shared memory per CTA
+// Above this many tokens a layer's router takes its logits from the tiled
+// CUDA-core GEMM (split over H to fill the SMs) instead of the GEMV, whose
+// grid no longer fits one wave there.
+constexpr int kLogitsGemmMinTokens = 384;
 
 std::atomic<int> g_sms[kMaxDevices];  // SM count per device, filled on first use (0: not yet)
 
@@ -241,6 +245,8 @@ struct Layout {
   size_t smem;
   int max_gu_tiles, max_dn_tiles, g_max;
   bool need_out;
+  int lsplit;  // H ranges of the logits GEMM (layers above kLogitsGemmMinTokens tokens)
+  size_t o_lpart;
   size_t o_status, o_cnt, o_tiles, o_logits, o_shl, o_shw, o_idx, o_w, o_counts, o_offsets, o_sp, o_pp, o_groups,
       o_header, o_spans, o_span_groups, o_partials, o_h, o_out, o_sync, o_hbuf, o_sout, o_xh, total;
   // block-scaled path: the token operand images (x's for gate_up, h's for
@@ -308,6 +314,11 @@ Layout make_layout(int T, int H, int I, int Is, int E, int K, bool gated, int sm
   L.o_tiles = o; o = align_up(o + 4 * static_cast<size_t>(2 * L.max_gu_tiles + L.max_dn_tiles + 1));
   L.o_logits = o; o = align_up(o + 4 * static_cast<size_t>(T) * E);
   L.o_shl = o; o = align_up(o + 4 * static_cast<size_t>(T) * (L.rg.fold_sh ? L.rg.n_eb * L.rg.hsplit : 1));
+  // the logits GEMM's partial sums over its ranges of H
+  const int E_tot = E + (gated ? 1 : 0);
+  L.lsplit = T > kLogitsGemmMinTokens ? logits_gemm_split(T, H, E_tot, sms) : 1;
+  L.o_lpart = o;
+  if (L.lsplit > 1) o = align_up(o + 4 * static_cast<size_t>(L.lsplit) * T * E_tot);
   L.o_shw = o; o = align_up(o + 4 * static_cast<size_t>(T));
   L.o_idx = o; o = align_up(o + 4 * static_cast<size_t>(TK));
   L.o_w = o; o = align_up(o + 4 * static_cast<size_t>(TK));
@@ -454,7 +465,7 @@ moe_status moe_route(const moe_bf16* x, int T, int H, const moe_bf16* gate, cons
   p.do_permute = 0;
   if (T > 1024) {
     // many tokens: the logits by the tiled CUDA-core GEMM, then selection only
-    const cudaError_t e = launch_logits_gemm(x, gate, nullptr, router_bias, T, H, E, p.logits, nullptr, stream);
+    const cudaError_t e = launch_logits_gemm(x, gate, nullptr, router_bias, T, H, E, p.logits, nullptr, 1, nullptr, stream);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     p.logits_given = 1;
     p.n_eb = 1;
@@ -642,14 +653,17 @@ moe_status ffn_forward(const moe_bf16* x, int T, int H, int I, const moe_bf16* g
   record_event_on(0, stream);
   cudaError_t e = cudaSuccess;
   int tb = L.rg.tb;
-  if (T > 1024 && !fp4) {
-    // many tokens: the logits by a tiled CUDA-core GEMM (enough 64 x 64
-    // tiles to fill the SMs only from about a thousand tokens on), then the
-    // router launch only selects, permutes and builds the work list (one
-    // CTA per 8 tokens)
-    e = launch_logits_gemm(x, gate, sh_gate, router_bias, T, H, E, rp.logits, rp.sh_logit, stream);
+  if (T > kLogitsGemmMinTokens && !fp4) {
+    // many tokens: the logits by a tiled CUDA-core GEMM, H cut into enough
+    // ranges (partial sums the router launch adds in order) that its 128 x
+    // 64 tiles fill the SMs, then the router launch only selects, permutes
+    // and builds the work list (one CTA per 8 tokens)
+    e = launch_logits_gemm(x, gate, sh_gate, router_bias, T, H, E, rp.logits, rp.sh_logit, L.lsplit,
+                           reinterpret_cast<float*>(w + L.o_lpart), stream);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     rp.logits_given = 1;
+    rp.lsplit = L.lsplit;
+    rp.lpart = reinterpret_cast<const float*>(w + L.o_lpart);
     rp.fold_sh = 0;
     rp.n_eb = 1;
     tb = 8;
@@ -819,10 +833,13 @@ moe_status ffn_forward_mx(const moe_bf16* x, int T, int H, int I, const moe_bf16
   record_event_on(0, stream);
   cudaError_t e = cudaSuccess;
   int tb = L.rg.tb;
-  if (T > 1024) {
-    e = launch_logits_gemm(x, gate, sh_gate, router_bias, T, H, E, rp.logits, rp.sh_logit, stream);
+  if (T > kLogitsGemmMinTokens) {
+    e = launch_logits_gemm(x, gate, sh_gate, router_bias, T, H, E, rp.logits, rp.sh_logit, L.lsplit,
+                           reinterpret_cast<float*>(w + L.o_lpart), stream);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     rp.logits_given = 1;
+    rp.lsplit = L.lsplit;
+    rp.lpart = reinterpret_cast<const float*>(w + L.o_lpart);
     rp.fold_sh = 0;
     rp.n_eb = 1;
     tb = 8;

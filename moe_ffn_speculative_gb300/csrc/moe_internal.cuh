@@ -286,6 +286,8 @@ struct RouteParams {
   int kblk;                    // inputs per k-block of the work list (64, or 128 block-scaled)
   int32_t* e2d;                // [E] (nullable) each touched expert's first token block over all groups
   int logits_given;            // logits (and sh_logit) were computed by logits_gemm_kernel: route only
+  int lsplit;                  // > 1: the GEMM left lsplit partial sums over ranges of H in lpart
+  const float* lpart;          // [lsplit][T][E (+1 with sh_gate)] fp32, summed in split order
   uint16_t* xh;                // [T,H] f16 copy of x written for FP4 experts (nullable)
   int32_t* status;             // range errors of that copy
 };
@@ -369,9 +371,15 @@ moe_status route_check_args(const uint16_t* x, int T, int H, const uint16_t* gat
 // launchers (route.cu, gemm.cu, combine.cu); return cudaError_t
 cudaError_t launch_route(const RouteParams& p, int tb, cudaStream_t s);
 // Tiled CUDA-core logits GEMM for many tokens (the router's first step).
+// split > 1: H is cut into split ranges of 32-input chunks, one grid slice
+// each, which write their partial sums (no router bias) to part
+// [split][T][E (+1)]; the router launch adds them in split order.
 cudaError_t launch_logits_gemm(const uint16_t* x, const uint16_t* gate, const uint16_t* sh_gate,
                                const float* router_bias, int T, int H, int E, float* logits, float* sh_logit,
-                               cudaStream_t s);
+                               int split, float* part, cudaStream_t s);
+// H ranges of the logits GEMM for a layer's router with T tokens: enough
+// slices to fill the SMs about three times, each at least 8 chunks of 32.
+int logits_gemm_split(int T, int H, int E_tot, int sms);
 cudaError_t launch_select_from_logits(const float* logits, int T, int E, int K, const float* expert_bias,
                                       int score_fn, int n_group, int topk_group, int group_topn,
                                       int renorm, float eps, float scale, int32_t* idx, float* w,

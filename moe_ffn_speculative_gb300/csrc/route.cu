@@ -418,6 +418,22 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
     // warp w routes token t0 + w
     if (warp < TB && t0 + warp < p.T) {
       const int tok = t0 + warp;
+      if (p.lsplit > 1) {
+        // the GEMM's partial sums of this token's logits, added in split order
+        const int E_tot = p.E + (p.sh_gate ? 1 : 0);
+        for (int e = lane; e < E_tot; e += 32) {
+          float v = 0.f;
+          for (int zz = 0; zz < p.lsplit; ++zz)
+            v += __ldcg(p.lpart + (static_cast<size_t>(zz) * p.T + tok) * E_tot + e);
+          if (e < p.E) {
+            if (p.router_bias) v += __ldg(p.router_bias + e);
+            p.logits[static_cast<size_t>(tok) * p.E + e] = v;
+          } else {
+            p.sh_logit[tok] = v;
+          }
+        }
+        __syncwarp();
+      }
       select_token<NJ, false>(p.logits + static_cast<size_t>(tok) * p.E, sel,
                               p.idx + static_cast<size_t>(tok) * p.K, p.w + static_cast<size_t>(tok) * p.K);
       if (lane == 0 && p.sh_w) p.sh_w[tok] = p.sh_gate ? 1.f / (1.f + expf(-__ldcg(p.sh_logit + tok))) : 1.f;
@@ -608,12 +624,16 @@ __global__ void __launch_bounds__(256) logits_gemm_kernel(const uint16_t* __rest
                                                           const uint16_t* __restrict__ gate,
                                                           const uint16_t* __restrict__ sh_gate,
                                                           const float* __restrict__ router_bias, int T, int H, int E,
-                                                          float* __restrict__ logits, float* __restrict__ sh_logit) {
+                                                          float* __restrict__ logits, float* __restrict__ sh_logit,
+                                                          int split, float* __restrict__ part) {
   __shared__ __align__(16) float As[kLgBK][kLgBM + 4];
   __shared__ __align__(16) float Bs[kLgBK][kLgBN + 4];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int t0 = blockIdx.x * kLgBM, e0 = blockIdx.y * kLgBN;
   const int E_tot = E + (sh_gate ? 1 : 0);
+  // this slice's range of H: chunks [nch*z/split, nch*(z+1)/split) of 32 inputs
+  const int nch = ceil_div(H, kLgBK), z = blockIdx.z;
+  const int h_lo = nch * z / split * kLgBK, h_hi = min(H, nch * (z + 1) / split * kLgBK);
   // loader: x rows lr and lr + 64, gate row lr; 8 consecutive h at lc
   const int lr = tid >> 2, lc = (tid & 3) * 8;
   const uint16_t* xrow0 = t0 + lr < T ? x + static_cast<size_t>(t0 + lr) * H : nullptr;
@@ -626,10 +646,10 @@ __global__ void __launch_bounds__(256) logits_gemm_kernel(const uint16_t* __rest
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
   const uint4 zero = make_uint4(0, 0, 0, 0);
-  uint4 xv0 = (xrow0 && lc < H) ? ldg128(xrow0 + lc) : zero;
-  uint4 xv1 = (xrow1 && lc < H) ? ldg128(xrow1 + lc) : zero;
-  uint4 gv = (grow && lc < H) ? ldg128(grow + lc) : zero;
-  for (int h0 = 0; h0 < H; h0 += kLgBK) {
+  uint4 xv0 = (xrow0 && h_lo + lc < h_hi) ? ldg128(xrow0 + h_lo + lc) : zero;
+  uint4 xv1 = (xrow1 && h_lo + lc < h_hi) ? ldg128(xrow1 + h_lo + lc) : zero;
+  uint4 gv = (grow && h_lo + lc < h_hi) ? ldg128(grow + h_lo + lc) : zero;
+  for (int h0 = h_lo; h0 < h_hi; h0 += kLgBK) {
     __syncthreads();  // the previous chunk is read
     const uint32_t x0w[4] = {xv0.x, xv0.y, xv0.z, xv0.w}, x1w[4] = {xv1.x, xv1.y, xv1.z, xv1.w};
     const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
@@ -644,9 +664,9 @@ __global__ void __launch_bounds__(256) logits_gemm_kernel(const uint16_t* __rest
     }
     __syncthreads();
     const int hn = h0 + kLgBK + lc;  // the next chunk's loads overlap this chunk's products
-    xv0 = (xrow0 && hn < H) ? ldg128(xrow0 + hn) : zero;
-    xv1 = (xrow1 && hn < H) ? ldg128(xrow1 + hn) : zero;
-    gv = (grow && hn < H) ? ldg128(grow + hn) : zero;
+    xv0 = (xrow0 && hn < h_hi) ? ldg128(xrow0 + hn) : zero;
+    xv1 = (xrow1 && hn < h_hi) ? ldg128(xrow1 + hn) : zero;
+    gv = (grow && hn < h_hi) ? ldg128(grow + hn) : zero;
 #pragma unroll
     for (int k = 0; k < kLgBK; ++k) {
       const float4 a0 = *reinterpret_cast<const float4*>(&As[k][ty * 8]);
@@ -666,8 +686,13 @@ __global__ void __launch_bounds__(256) logits_gemm_kernel(const uint16_t* __rest
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e = e0 + tx * 4 + j;
-      if (e < E) logits[static_cast<size_t>(t) * E + e] = acc[i][j] + (router_bias ? __ldg(router_bias + e) : 0.f);
-      else if (e < E_tot) sh_logit[t] = acc[i][j];
+      if (split > 1) {
+        if (e < E_tot) part[(static_cast<size_t>(z) * T + t) * E_tot + e] = acc[i][j];
+      } else if (e < E) {
+        logits[static_cast<size_t>(t) * E + e] = acc[i][j] + (router_bias ? __ldg(router_bias + e) : 0.f);
+      } else if (e < E_tot) {
+        sh_logit[t] = acc[i][j];
+      }
     }
   }
 }
@@ -696,11 +721,18 @@ __global__ void __launch_bounds__(kRouteThreads) permute_kernel(const int32_t* i
 
 cudaError_t launch_logits_gemm(const uint16_t* x, const uint16_t* gate, const uint16_t* sh_gate,
                                const float* router_bias, int T, int H, int E, float* logits, float* sh_logit,
-                               cudaStream_t s) {
+                               int split, float* part, cudaStream_t s) {
   const int E_tot = E + (sh_gate ? 1 : 0);
-  dim3 grid(ceil_div(T, kLgBM), ceil_div(E_tot, kLgBN));
-  logits_gemm_kernel<<<grid, 256, 0, s>>>(x, gate, sh_gate, router_bias, T, H, E, logits, sh_logit);
+  dim3 grid(ceil_div(T, kLgBM), ceil_div(E_tot, kLgBN), split);
+  logits_gemm_kernel<<<grid, 256, 0, s>>>(x, gate, sh_gate, router_bias, T, H, E, logits, sh_logit, split, part);
   return cudaGetLastError();
+}
+
+int logits_gemm_split(int T, int H, int E_tot, int sms) {
+  const int tiles = ceil_div(T, kLgBM) * ceil_div(E_tot, kLgBN);
+  const int by_sm = 3 * sms / tiles, by_h = ceil_div(H, kLgBK) / 8;
+  const int s = by_sm < by_h ? by_sm : by_h;
+  return s < 1 ? 1 : s;
 }
 
 namespace {
