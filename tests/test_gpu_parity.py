@@ -185,6 +185,10 @@ SMALL = {
                                                 shared_gated=True, router_bias_std=0.1, seed=14),
     "wide_tokens_K8": S.LayerConfig("r8", T=300, H=320, E=64, I=160, K=8, score_fn=1, n_group=8, topk_group=4,
                                     expert_bias_std=0.05, shared_I=96, seed=12),
+    # > 384 tokens: the layer's logits by the GEMM split over two ranges of H,
+    # summed by the router launch with the router bias and the shared-gate column
+    "split_logits_gated_bias": S.LayerConfig("r11", T=400, H=512, E=16, I=64, K=2, shared_I=64, shared_gated=True,
+                                             router_bias_std=0.1, expert_bias_std=0.05, seed=16),
 }
 
 
