@@ -626,8 +626,13 @@ __global__ void __launch_bounds__(256) logits_gemm_kernel(const uint16_t* __rest
                                                           const float* __restrict__ router_bias, int T, int H, int E,
                                                           float* __restrict__ logits, float* __restrict__ sh_logit,
                                                           int split, float* __restrict__ part) {
-  __shared__ __align__(16) float As[kLgBK][kLgBM + 4];
-  __shared__ __align__(16) float Bs[kLgBK][kLgBN + 4];
+  // x and gate chunks as fp32, k-major; row k starts 8*(k/8) words further
+  // than its stride alone would place it, so that the four lanes storing one
+  // token's (or gate row's) 8 inputs hit four different banks
+  __shared__ __align__(16) float As[kLgBK * (kLgBM + 4) + 24];
+  __shared__ __align__(16) float Bs[kLgBK * (kLgBN + 4) + 24];
+  auto a_at = [](int k, int t) { return k * (kLgBM + 4) + ((k >> 3) << 3) + t; };
+  auto b_at = [](int k, int e) { return k * (kLgBN + 4) + ((k >> 3) << 3) + e; };
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int t0 = blockIdx.x * kLgBM, e0 = blockIdx.y * kLgBN;
   const int E_tot = E + (sh_gate ? 1 : 0);
@@ -655,12 +660,12 @@ __global__ void __launch_bounds__(256) logits_gemm_kernel(const uint16_t* __rest
     const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      As[lc + 2 * i][lr] = bf_lo(x0w[i]);
-      As[lc + 2 * i + 1][lr] = bf_hi(x0w[i]);
-      As[lc + 2 * i][lr + 64] = bf_lo(x1w[i]);
-      As[lc + 2 * i + 1][lr + 64] = bf_hi(x1w[i]);
-      Bs[lc + 2 * i][lr] = bf_lo(gw[i]);
-      Bs[lc + 2 * i + 1][lr] = bf_hi(gw[i]);
+      As[a_at(lc + 2 * i, lr)] = bf_lo(x0w[i]);
+      As[a_at(lc + 2 * i + 1, lr)] = bf_hi(x0w[i]);
+      As[a_at(lc + 2 * i, lr + 64)] = bf_lo(x1w[i]);
+      As[a_at(lc + 2 * i + 1, lr + 64)] = bf_hi(x1w[i]);
+      Bs[b_at(lc + 2 * i, lr)] = bf_lo(gw[i]);
+      Bs[b_at(lc + 2 * i + 1, lr)] = bf_hi(gw[i]);
     }
     __syncthreads();
     const int hn = h0 + kLgBK + lc;  // the next chunk's loads overlap this chunk's products
@@ -669,9 +674,9 @@ __global__ void __launch_bounds__(256) logits_gemm_kernel(const uint16_t* __rest
     gv = (grow && hn < h_hi) ? ldg128(grow + hn) : zero;
 #pragma unroll
     for (int k = 0; k < kLgBK; ++k) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&As[k][ty * 8]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&As[k][ty * 8 + 4]);
-      const float4 b = *reinterpret_cast<const float4*>(&Bs[k][tx * 4]);
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[a_at(k, ty * 8)]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[a_at(k, ty * 8 + 4)]);
+      const float4 b = *reinterpret_cast<const float4*>(&Bs[b_at(k, tx * 4)]);
       const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i)
