@@ -615,9 +615,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteParams 
 
 // logits = x . gate^T (+ router_bias) for many tokens: a CTA computes a
 // 128-token x 64-expert tile with x and gate staged through shared memory as
-// fp32, each thread an 8 x 4 block accumulated over H in increasing order
-// (fp32 fused multiply-adds of the exact bf16 products).  Column E is the
-// shared-expert gate when sh_gate is given (-> sh_logit).
+// fp32, each thread an 8 x 4 block accumulated over its range of H in
+// increasing order (fp32 fused multiply-adds of the exact bf16 products);
+// with one range the tile is the logits, with several each range's partial
+// sums go to `part` for the router launch to add in range order.  Column E
+// is the shared-expert gate when sh_gate is given (-> sh_logit).
 constexpr int kLgBM = 128, kLgBN = 64, kLgBK = 32;
 
 __global__ void __launch_bounds__(256) logits_gemm_kernel(const uint16_t* __restrict__ x,
