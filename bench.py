@@ -818,6 +818,8 @@ def run_route_only(args, cfg, rank, world):
     from moe_ffn_speculative_gb300 import ops
     from moe_ffn_speculative_gb300.build import build
 
+    if rank != 0:  # one line, from rank 0, as the other modes print
+        return
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
     build()
