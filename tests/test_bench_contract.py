@@ -98,3 +98,28 @@ def test_router_only_inputs_are_the_layers_own(name):
     full, router = S.make_inputs(cfg), S.make_router_inputs(cfg)
     for k in ("x", "gate", "router_bias", "expert_bias"):
         assert (full[k] is None and router[k] is None) or torch.equal(full[k], router[k]), k
+
+
+def test_fused_layer_reports_back_to_back_and_isolated_launch_times():
+    """The fused schedule's layer is one launch: its kernel time is the timed
+    region's time per launch (consecutive launches overlap), and the launch on
+    its own -- event nodes around it, their measured overhead taken off -- is
+    reported beside it; other schedules report the event-node time minus the
+    overhead."""
+    from types import SimpleNamespace
+    cfg = S.CONFIGS["qwen3_8b_dspark"]
+    ev = {"event_pair_us": 5.0, "empty_launch_period_us": 1.1, "overhead_us": 3.9}
+    wl = SimpleNamespace(cfg=cfg, sched="slice", ex_key="fused")
+    roof, layer = bench.roofline_record(wl, 8, {"fused": 57.9}, 0.0499, 6780.0, 1942.5, "measured",
+                                        "qwen3_8b_dspark", ev)
+    assert roof["kernel_us"] == pytest.approx(49.9)
+    assert roof["kernel_us_isolated"] == pytest.approx(54.0)
+    assert roof["frac"] == pytest.approx(roof["algorithmic_bytes_per_launch"] / 49.9e-6 / 1e9 / 6780.0)
+    assert roof["frac_isolated"] == pytest.approx(roof["algorithmic_bytes_per_launch"] / 54.0e-6 / 1e9 / 6780.0)
+    assert layer["frac"] == pytest.approx(layer["roofline_us"] / 49.9)
+    cfg4 = S.CONFIGS["dsv4_style"]
+    wl4 = SimpleNamespace(cfg=cfg4, sched="stream_k", ex_key="experts")
+    roof4, _ = bench.roofline_record(wl4, 210, {"router": 30.0, "experts": 752.0, "combine": 7.5}, 0.78, 6780.0,
+                                     1942.5, "measured", "dsv4_style", ev)
+    assert roof4["kernel_us"] == pytest.approx(748.1)
+    assert "kernel_us_isolated" not in roof4
